@@ -1,0 +1,327 @@
+"""Benchmark of the fused LM-head + cross-entropy micro-step library on GB300.
+
+One step = one optimizer step of the GPT-2 124M LM-head workload: G micro-steps of
+lmce_microstep (logits tiles -> online logsumexp and loss, dlogits -> dW and dh) and
+one lmce_finalize, on synthetic seeded inputs already resident in device memory.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lmce|reference]
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU oracle on
+bounded samples of the same workload instead.  Under torchrun every rank runs its
+own micro-steps (weak scaling); the valid count and dW are SUM-reduced over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tokens/s fused LM-head+CE fwd+bwd (1×GB300); % of dense BF16 tensor peak"
+UNIT = "tokens/s"
+FP32_LANES_PER_SM = 128
+N_SM = 152
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=5)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="lmce", choices=["lmce", "reference"])
+    p.add_argument("--workload", default="gpt2_124m_head")
+    p.add_argument("--path", default="auto", choices=["auto", "simt", "tcgen05"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample-rows", type=int, default=2048)
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}, \
+        "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_sample_rate(w, rows: int):
+    """Float64 oracle tokens/s on one micro-step of ``rows`` rows (full C and V)."""
+    from oracle import lmce_oracle as O
+
+    h, y = w.micro[0]
+    h = h[:rows]
+    y = y[:rows]
+    t0 = time.perf_counter()
+    O.step([(h, y)], w.W)
+    dt = time.perf_counter() - t0
+    return rows / dt, dt
+
+
+def run_reference(args, rank, world):
+    from grad_lmce_microstep_gb300 import inputs as I
+
+    if rank != 0:
+        return
+    w = I.make(args.workload)
+    rows = args.cpu_sample_rows
+    for _ in range(args.warmup):
+        oracle_sample_rate(w, rows)
+    rates = []
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        r, _ = oracle_sample_rate(w, rows)
+        rates.append(r)
+    wall = time.perf_counter() - t_all
+    value = rows * args.steps / wall
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "C": w.C, "V": w.V,
+                   "sample": f"one micro-step of {rows} rows of micro-batch 0 per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{rows} rows x full V x full C per step, float64 numpy/BLAS"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_lmce(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from grad_lmce_microstep_gb300 import dp
+    from grad_lmce_microstep_gb300 import inputs as I
+    from grad_lmce_microstep_gb300 import lmce as M
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = I.make(args.workload, seed=rank)
+    W = w.W.to(dev)
+    mbs = [(h.to(dev), y.to(dev)) for h, y in w.micro]
+    dhs = [torch.empty_like(h) for h, _ in mbs]
+    dW = torch.empty(w.V, w.C, dtype=torch.float32, device=dev)
+    max_N = max(int(y.numel()) for _, y in mbs)
+    L = M.Lmce(w.C, w.V, max_N, dW, w.dtype, norm="global", grad_accum_steps=w.G, path=args.path)
+    gv = dp.global_valid_count(sum(w.valid_counts()), device=dev if world > 1 else None)
+    stream = torch.cuda.current_stream(dev)
+    tokens_rank = w.tokens
+
+    def step():
+        for (h, y), dh in zip(mbs, dhs):
+            L.microstep(h, W, y, gv, dh, stream=stream)
+        res = L.finalize(stream=stream)
+        if world > 1:
+            dp.reduce_step(dW, res[0], res[1])
+        return res
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        res = step()
+    barrier()
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    L.profile(True)
+    launches0 = L.launches
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        res = step()
+    ev1.record(stream)
+    barrier()
+    launches = L.launches - launches0
+    L.profile(False)
+    prof = L.profile_read()
+    clocks = sampler.stop() if sampler else None
+    ms = ev0.elapsed_time(ev1)
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    value = tokens_rank * world * args.steps / (ms_max / 1e3)
+
+    # end to end through the public API: pinned host inputs copied every step, loss read back
+    e2e = None
+    if not args.no_e2e:
+        hs_host = [h.cpu().pin_memory() for h, _ in w.micro]
+        ys_host = [y.cpu().pin_memory() for _, y in w.micro]
+        h_dev = [torch.empty_like(h) for h, _ in mbs]
+        y_dev = [torch.empty_like(y) for _, y in mbs]
+
+        def step_e2e():
+            for hh, yh, hd, yd, dh in zip(hs_host, ys_host, h_dev, y_dev, dhs):
+                hd.copy_(hh, non_blocking=True)
+                yd.copy_(yh, non_blocking=True)
+                L.microstep(hd, W, yd, gv, dh, stream=stream)
+            return L.finalize(stream=stream)
+
+        for _ in range(max(1, args.warmup)):
+            step_e2e()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            step_e2e()
+        barrier()
+        dt = time.perf_counter() - t0
+        t = torch.tensor([dt], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        h2d = sum(h.numel() * h.element_size() + y.numel() * y.element_size() for h, y in w.micro)
+        e2e = {"value": tokens_rank * world * args.steps / float(t.item()), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 48}
+
+    if rank != 0:
+        return
+
+    pk, pk_kind = peaks()
+    # algorithmic work: 6 C V flops per token for the whole path, 2 C V for each of the three
+    # contractions (logits, dW, dh); the recomputed logits of the gradient passes are not counted.
+    flop_tok = 6.0 * w.C * w.V
+    kinds = {k: v for k, v in prof.items() if v[1] > 0}
+    dom = max(kinds, key=lambda k: kinds[k][0])
+    dom_ms, dom_n = kinds[dom]
+    tok_per_launch = tokens_rank / w.G
+    alg_flop_launch = {"lse": 2.0, "dW": 2.0, "dh": 2.0, "finish": 0.0}[dom] * w.C * w.V * tok_per_launch
+    achieved = alg_flop_launch / (dom_ms / dom_n / 1e3) / 1e12
+    if L.path == "tcgen05":
+        peak = pk["bf16_tflops_sustained"] if "bf16_tflops_sustained" in pk else pk["bf16_tflops"]
+        bound = "tensor"
+    else:
+        clk = (clocks or {}).get("sm_max_mhz") or pk.get("sm_max_mhz", 2070.0)
+        peak = N_SM * FP32_LANES_PER_SM * 2 * clk * 1e6 / 1e12
+        bound = "alu"
+    total_frac = value / world * flop_tok / 1e12 / (pk.get("bf16_tflops_sustained") or pk["bf16_tflops"])
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        rate, secs = oracle_sample_rate(w, args.cpu_sample_rows)
+        cpu = {"value": rate, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"one micro-step of {args.cpu_sample_rows} rows (full C={w.C}, V={w.V}), "
+                         f"float64 numpy/BLAS, {secs:.1f} s"}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "fp32",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "tokens_per_step": tokens_rank * world, "micro_steps": w.G,
+                   "micro_batch_tokens": int(tok_per_launch), "C": w.C, "V": w.V, "path": L.path,
+                   "parallelism": f"dp{world}",
+                   "l2": "no flush: inputs larger than L2 (per step %d distinct h buffers of %.0f MB, "
+                         "W %.0f MB, fp32 dW %.0f MB)" % (w.G, mbs[0][0].numel() * 2 / 1e6,
+                                                         W.numel() * W.element_size() / 1e6,
+                                                         dW.numel() * 4 / 1e6)},
+        "frac_of_peak": {"value": total_frac, "flop_per_token": flop_tok,
+                         "peak_tflops": pk.get("bf16_tflops_sustained") or pk["bf16_tflops"],
+                         "peak": f"bf16 sustained, {pk_kind}"},
+        "roofline": {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": ("bf16_tflops_sustained of " + pk_kind) if bound == "tensor"
+                     else "fp32 FFMA: 152 SMs x 128 lanes x 2 flop x max SM clock"},
+        "kernels_ms": {k: {"total_ms": v[0], "launches": v[1], "avg_ms": v[0] / v[1]} for k, v in kinds.items()},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "check": {"loss_mean": res[2], "valid": res[1]},
+    }
+    print(json.dumps(line), flush=True)
+    L.close()
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus == 1 else 1)))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_lmce(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,301 @@
+// C-ABI of the lmce library: handle, argument checks, status codes, dispatch, and the
+// fixed-order loss/count reduction shared by both compute paths.
+#include <stdlib.h>
+#include <string.h>
+#include <math.h>
+
+#include <new>
+
+#include "lmce.h"
+#include "lmce_internal.cuh"
+
+namespace lmce {
+namespace {
+
+constexpr int FIN_T = 256;
+
+// One block sums the per-block partials of a micro-step in a fixed order (each thread a
+// fixed strided subset, then a fixed tree), then updates the step accumulators.
+// The gradient scale of this micro-step is set here:
+//   global norm    : s = 1 / global_valid
+//   micro-mean norm: s = 1 / (valid_k * G), 0 for a micro-step without valid targets
+// ("Multi-GPU calculation of gradients for accelerated training", section "Gradient
+// accumulation averages across micro-steps").
+__global__ void __launch_bounds__(FIN_T) finish_kernel(const double* __restrict__ part_loss,
+                                                       const int* __restrict__ part_cnt,
+                                                       const unsigned* __restrict__ part_err,
+                                                       int64_t nparts, int norm, int G,
+                                                       long long global_valid, DevAcc* acc) {
+  __shared__ double sl[FIN_T];
+  __shared__ long long sc[FIN_T];
+  __shared__ unsigned se[FIN_T];
+  const int t = threadIdx.x;
+  double l = 0.0;
+  long long c = 0;
+  unsigned e = 0;
+  for (int64_t i = t; i < nparts; i += FIN_T) {
+    l += part_loss[i];
+    c += part_cnt[i];
+    e |= part_err[i];
+  }
+  sl[t] = l;
+  sc[t] = c;
+  se[t] = e;
+  __syncthreads();
+  for (int o = FIN_T / 2; o > 0; o >>= 1) {
+    if (t < o) {
+      sl[t] += sl[t + o];
+      sc[t] += sc[t + o];
+      se[t] |= se[t + o];
+    }
+    __syncthreads();
+  }
+  if (t == 0) {
+    double loss_k = sl[0];
+    long long cnt_k = sc[0];
+    double s;
+    if (norm == LMCE_NORM_GLOBAL) s = global_valid > 0 ? 1.0 / (double)global_valid : 0.0;
+    else s = cnt_k > 0 ? 1.0 / ((double)cnt_k * (double)G) : 0.0;
+    acc->scale = (float)s;
+    acc->loss_sum += loss_k;
+    acc->objective += s * loss_k;
+    acc->count += cnt_k;
+    acc->err |= se[0];
+    if (!isfinite(loss_k)) acc->err |= ERR_BIT_NONFINITE;
+    acc->micro += 1;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_finish(const StepArgs& a, const Scratch& s, int64_t nparts, Launch& L) {
+  L.begin(K_FINISH);
+  finish_kernel<<<1, FIN_T, 0, L.st>>>(s.part_loss, s.part_cnt, s.part_err, nparts, a.norm, a.G,
+                                       (long long)a.global_valid, s.acc);
+  L.end();
+  return cudaGetLastError();
+}
+
+}  // namespace lmce
+
+using namespace lmce;
+
+struct lmce_handle {
+  lmce_config cfg;
+  float* dW;
+  int device;
+  int path;            // resolved: LMCE_PATH_SIMT or LMCE_PATH_TCGEN05
+  Scratch sc;
+  DevAcc* host_acc;    // pinned
+  bool first;          // next micro-step writes dW instead of adding
+  int attempted;       // micro-steps accepted since create/finalize
+  int64_t launches;
+  Prof prof;
+};
+
+static int check_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) return LMCE_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev) != cudaSuccess)
+    return LMCE_ERR_CUDA;
+  if (major != 10 || minor != 3) return LMCE_ERR_ARCH;
+  return LMCE_OK;
+}
+
+static void free_scratch(lmce_handle* h) {
+  cudaFree(h->sc.lse);
+  cudaFree(h->sc.part_loss);
+  cudaFree(h->sc.part_cnt);
+  cudaFree(h->sc.part_err);
+  cudaFree(h->sc.acc);
+  if (h->host_acc) cudaFreeHost(h->host_acc);
+  memset(&h->sc, 0, sizeof(h->sc));
+  h->host_acc = nullptr;
+}
+
+extern "C" int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out) {
+  if (!cfg || !dW || !out) return LMCE_ERR_ARG;
+  *out = nullptr;
+  if (cfg->C <= 0 || cfg->V <= 0 || cfg->max_N < 0 || cfg->grad_accum_steps < 1) return LMCE_ERR_ARG;
+  if (cfg->C > (1 << 20) || cfg->V > (1LL << 31) || cfg->max_N > (1LL << 31)) return LMCE_ERR_ARG;
+  if (cfg->dtype != LMCE_BF16 && cfg->dtype != LMCE_FP32) return LMCE_ERR_ARG;
+  if (cfg->norm != LMCE_NORM_GLOBAL && cfg->norm != LMCE_NORM_MICRO_MEAN) return LMCE_ERR_ARG;
+  if (cfg->path < LMCE_PATH_AUTO || cfg->path > LMCE_PATH_TCGEN05 || cfg->reserved != 0) return LMCE_ERR_ARG;
+  const bool tc_ok = tc_supported(cfg->C, cfg->V, cfg->dtype == LMCE_BF16);
+  const bool simt_ok = cfg->C <= 2048;
+  int path;
+  if (cfg->path == LMCE_PATH_TCGEN05) {
+    if (!tc_ok) return LMCE_ERR_ARG;
+    path = LMCE_PATH_TCGEN05;
+  } else if (cfg->path == LMCE_PATH_SIMT) {
+    if (!simt_ok) return LMCE_ERR_ARG;
+    path = LMCE_PATH_SIMT;
+  } else {
+    if (tc_ok) path = LMCE_PATH_TCGEN05;
+    else if (simt_ok) path = LMCE_PATH_SIMT;
+    else return LMCE_ERR_ARG;
+  }
+  int dev = 0;
+  int st = check_device(&dev);
+  if (st != LMCE_OK) return st;
+  lmce_handle* h = new (std::nothrow) lmce_handle();
+  if (!h) return LMCE_ERR_CUDA;
+  h->cfg = *cfg;
+  h->dW = dW;
+  h->device = dev;
+  h->path = path;
+  h->first = true;
+  const int64_t maxN = cfg->max_N > 0 ? cfg->max_N : 1;
+  int64_t parts = simt_parts(maxN);
+  int64_t tp = tc_parts(maxN);
+  if (tp > parts) parts = tp;
+  h->sc.max_parts = parts;
+  bool ok = cudaMalloc(&h->sc.lse, sizeof(float) * maxN) == cudaSuccess &&
+            cudaMalloc(&h->sc.part_loss, sizeof(double) * parts) == cudaSuccess &&
+            cudaMalloc(&h->sc.part_cnt, sizeof(int) * parts) == cudaSuccess &&
+            cudaMalloc(&h->sc.part_err, sizeof(unsigned) * parts) == cudaSuccess &&
+            cudaMalloc(&h->sc.acc, sizeof(DevAcc)) == cudaSuccess &&
+            cudaMallocHost(&h->host_acc, sizeof(DevAcc)) == cudaSuccess &&
+            cudaMemset(h->sc.acc, 0, sizeof(DevAcc)) == cudaSuccess &&
+            cudaDeviceSynchronize() == cudaSuccess;
+  if (!ok) {
+    free_scratch(h);
+    delete h;
+    return LMCE_ERR_CUDA;
+  }
+  *out = h;
+  return LMCE_OK;
+}
+
+extern "C" int lmce_microstep(lmce_handle* h, const void* hidden, const void* W, const int32_t* targets,
+                              int64_t N, int64_t global_valid, void* dh, float* row_loss, void* stream) {
+  if (!h) return LMCE_ERR_ARG;
+  const lmce_config& c = h->cfg;
+  if (N < 0 || N > c.max_N) return LMCE_ERR_ARG;
+  if (N > 0 && (!hidden || !W || !targets || !dh)) return LMCE_ERR_ARG;
+  if (h->path == LMCE_PATH_TCGEN05 && N > 0) {
+    if (((uintptr_t)hidden | (uintptr_t)W | (uintptr_t)dh | (uintptr_t)h->dW) & 15) return LMCE_ERR_ARG;
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t esz = c.dtype == LMCE_BF16 ? 2 : 4;
+  if (c.norm == LMCE_NORM_GLOBAL && global_valid <= 0) {
+    if (N > 0 && cudaMemsetAsync(dh, 0, (size_t)N * c.C * esz, st) != cudaSuccess) return LMCE_ERR_CUDA;
+    if (N > 0 && row_loss && cudaMemsetAsync(row_loss, 0, (size_t)N * sizeof(float), st) != cudaSuccess)
+      return LMCE_ERR_CUDA;
+    h->attempted += 1;  // dW untouched: the next micro-step with valid rows still writes it
+    return LMCE_ERR_NO_VALID;
+  }
+  StepArgs a;
+  a.hidden = hidden;
+  a.W = W;
+  a.targets = targets;
+  a.dh = dh;
+  a.dW = h->dW;
+  a.row_loss = row_loss;
+  a.N = N;
+  a.C = c.C;
+  a.V = c.V;
+  a.ignore_id = c.ignore_id;
+  a.norm = c.norm;
+  a.G = c.grad_accum_steps;
+  a.global_valid = global_valid;
+  a.beta = h->first ? 0 : 1;
+  a.bf16 = c.dtype == LMCE_BF16;
+  if (N == 0) {
+    // An empty micro-step still counts; the first one of a step leaves dW = 0.
+    if (h->first && cudaMemsetAsync(h->dW, 0, sizeof(float) * (size_t)c.V * c.C, st) != cudaSuccess)
+      return LMCE_ERR_CUDA;
+    h->first = false;
+    h->attempted += 1;
+    return LMCE_OK;
+  }
+  Launch L;
+  L.st = st;
+  L.prof = &h->prof;
+  cudaError_t e = h->path == LMCE_PATH_TCGEN05 ? tc_microstep(a, h->sc, L) : simt_microstep(a, h->sc, L);
+  h->launches += L.n;
+  if (e != cudaSuccess) return LMCE_ERR_CUDA;
+  h->first = false;
+  h->attempted += 1;
+  return LMCE_OK;
+}
+
+extern "C" int lmce_finalize(lmce_handle* h, double* loss_sum, int64_t* valid_count, double* loss_mean,
+                             void* stream) {
+  if (!h) return LMCE_ERR_ARG;
+  if (h->attempted == 0) return LMCE_ERR_STATE;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(h->host_acc, h->sc.acc, sizeof(DevAcc), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return LMCE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return LMCE_ERR_CUDA;
+  const DevAcc r = *h->host_acc;
+  if (loss_sum) *loss_sum = r.loss_sum;
+  if (valid_count) *valid_count = (int64_t)r.count;
+  if (loss_mean) *loss_mean = r.count > 0 ? r.objective : NAN;
+  h->first = true;
+  h->attempted = 0;
+  if (cudaMemsetAsync(h->sc.acc, 0, sizeof(DevAcc), st) != cudaSuccess) return LMCE_ERR_CUDA;
+  if (r.err & ERR_BIT_BAD_TARGET) return LMCE_ERR_BAD_TARGET;
+  if ((r.err & ERR_BIT_NONFINITE) || !isfinite(r.loss_sum)) return LMCE_ERR_NONFINITE;
+  if (r.count == 0) return LMCE_ERR_NO_VALID;
+  return LMCE_OK;
+}
+
+extern "C" int lmce_destroy(lmce_handle* h) {
+  if (!h) return LMCE_OK;
+  int cur = 0;
+  cudaGetDevice(&cur);
+  if (cur != h->device) cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
+  free_scratch(h);
+  for (cudaEvent_t e : h->prof.pool) cudaEventDestroy(e);
+  if (cur != h->device) cudaSetDevice(cur);
+  delete h;
+  return LMCE_OK;
+}
+
+extern "C" const char* lmce_status_string(int s) {
+  switch (s) {
+    case LMCE_OK: return "ok";
+    case LMCE_ERR_ARG: return "invalid argument";
+    case LMCE_ERR_ARCH: return "device is not compute capability 10.3 (sm_103)";
+    case LMCE_ERR_CUDA: return "CUDA error";
+    case LMCE_ERR_BAD_TARGET: return "target outside [0, V) that is not the ignore id";
+    case LMCE_ERR_NO_VALID: return "no valid target in the step";
+    case LMCE_ERR_NONFINITE: return "loss is not finite";
+    case LMCE_ERR_STATE: return "call out of order";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int64_t lmce_launch_count(const lmce_handle* h) { return h ? h->launches : 0; }
+
+extern "C" int lmce_selected_path(const lmce_handle* h) { return h ? h->path : -1; }
+
+extern "C" int lmce_profile(lmce_handle* h, int enable) {
+  if (!h) return LMCE_ERR_ARG;
+  if (enable) {
+    h->prof.recs.clear();
+    h->prof.used = 0;
+  }
+  h->prof.on = enable != 0;
+  return LMCE_OK;
+}
+
+extern "C" int lmce_profile_read(lmce_handle* h, int kind, double* total_ms, int64_t* launches) {
+  if (!h || !total_ms || !launches || kind < 0 || kind >= K_COUNT) return LMCE_ERR_ARG;
+  double t = 0.0;
+  int64_t n = 0;
+  for (const Prof::Rec& r : h->prof.recs) {
+    if (r.kind != kind) continue;
+    if (cudaEventSynchronize(r.b) != cudaSuccess) return LMCE_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) return LMCE_ERR_CUDA;
+    t += ms;
+    ++n;
+  }
+  *total_ms = t;
+  *launches = n;
+  return LMCE_OK;
+}

@@ -1,0 +1,114 @@
+// Internal declarations shared by the lmce translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include <vector>
+
+namespace lmce {
+
+// Kernel kinds for the timing records (same values as LMCE_KIND_* in lmce.h).
+enum Kind { K_LSE = 0, K_FINISH = 1, K_DW = 2, K_DH = 3, K_COUNT = 4 };
+
+// Optional CUDA-event records around every kernel launch.
+struct Prof {
+  bool on = false;
+  std::vector<cudaEvent_t> pool;
+  size_t used = 0;
+  struct Rec { int kind; cudaEvent_t a, b; };
+  std::vector<Rec> recs;
+  cudaEvent_t next() {
+    if (used == pool.size()) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+      pool.push_back(e);
+    }
+    return pool[used++];
+  }
+};
+
+// Launch context of one micro-step: stream, timing records, launch counter.
+struct Launch {
+  cudaStream_t st;
+  Prof* prof;
+  int n = 0;
+  cudaEvent_t pending = nullptr;
+  int pending_kind = 0;
+  void begin(int kind) {
+    ++n;
+    if (prof && prof->on) {
+      pending = prof->next();
+      pending_kind = kind;
+      if (pending) cudaEventRecord(pending, st);
+    }
+  }
+  void end() {
+    if (prof && prof->on && pending) {
+      cudaEvent_t b = prof->next();
+      if (b) {
+        cudaEventRecord(b, st);
+        prof->recs.push_back({pending_kind, pending, b});
+      }
+      pending = nullptr;
+    }
+  }
+};
+
+// Step accumulators kept on the device between micro-steps of one optimizer step.
+struct DevAcc {
+  double loss_sum;    // sum of valid row losses over the step
+  double objective;   // sum_k s_k * loss_sum_k
+  long long count;    // valid targets over the step
+  unsigned int err;   // ERR_BIT_* flags
+  unsigned int micro; // micro-steps that ran
+  float scale;        // s of the micro-step being processed (read by the gradient kernels)
+  float pad_;
+};
+
+constexpr unsigned ERR_BIT_BAD_TARGET = 1u;
+constexpr unsigned ERR_BIT_NONFINITE = 2u;
+
+// Arguments of one micro-step as the kernels see them.
+struct StepArgs {
+  const void* hidden;     // [N, C] dtype
+  const void* W;          // [V, C] dtype
+  const int32_t* targets; // [N]
+  void* dh;               // [N, C] dtype
+  float* dW;              // [V, C] fp32
+  float* row_loss;        // [N] or nullptr
+  int64_t N, C, V;
+  int32_t ignore_id;
+  int32_t norm;           // 0 global, 1 micro mean
+  int32_t G;
+  int64_t global_valid;
+  int32_t beta;           // 0: dW = grad, 1: dW += grad
+  int32_t bf16;           // 1: dtype bf16, 0: fp32
+};
+
+// Library-owned device scratch.
+struct Scratch {
+  float* lse;          // [max_N] per-row logsumexp
+  double* part_loss;   // [max_parts] per-block loss partials
+  int* part_cnt;       // [max_parts] per-block valid counts
+  unsigned* part_err;  // [max_parts] per-block error flags
+  DevAcc* acc;         // step accumulators
+  int64_t max_parts;
+};
+
+// Fixed-order reduction of the per-block partials of one micro-step into the step
+// accumulators; also computes this micro-step's gradient scale.  One launch.
+cudaError_t launch_finish(const StepArgs& a, const Scratch& s, int64_t nparts, Launch& L);
+
+// SIMT path (fp32 FFMA).
+int64_t simt_parts(int64_t N);
+size_t simt_grad_smem(int64_t C);
+cudaError_t simt_microstep(const StepArgs& a, const Scratch& s, Launch& L);
+
+// Tensor-core path (tcgen05 + TMA).
+bool tc_supported(int64_t C, int64_t V, int bf16);
+int64_t tc_parts(int64_t N);
+cudaError_t tc_microstep(const StepArgs& a, const Scratch& s, Launch& L);
+
+}  // namespace lmce

@@ -1,0 +1,167 @@
+/*
+ * lmce -- fused LM-head + token-level softmax cross-entropy, forward and backward,
+ * with gradient-accumulation micro-steps, for GB300 (sm_103a).
+ *
+ * What one optimizer step computes (GPT-2 124M training pages):
+ *   logits z = h . W^T with the tied, bias-free output projection W[V, C]
+ *     ("How I trained my own GPT-2 124M on FineWeb-Edu", section 4, weight tying);
+ *   per-row loss  l_n = logsumexp_v(z[n, :]) - z[n, y_n]  for y_n != ignore_id
+ *     (same page, section 4: softmax, pick the target's probability, negative log);
+ *   the gradient of  sum_k s_k * sum_n l_n  over the micro-steps k of one step,
+ *     accumulated into an fp32 dW  (section 8.1, gradient accumulation);
+ *   s_k = 1 / (valid targets over the whole step)  -- the global token mean -- or the
+ *     pages' 1 / (valid targets of micro-step k * G)  ("Multi-GPU calculation of
+ *     gradients for accelerated training", sections "Gradient accumulation averages
+ *     across micro-steps" and "DDP averages gradients across processes").
+ *   Pad targets are ignored by the loss (zerotofrontier "GPT", section "Document
+ *   boundaries, packing and masking"); the ignore id is configurable, -100 by default.
+ *
+ * The N x V logits never reach device memory: every pass recomputes its logit
+ * tiles on chip.
+ *
+ * Conventions for every function below:
+ *   - Device pointers are CUDA device addresses on the current device; host pointers
+ *     are ordinary host memory.  Rows are C-contiguous (row-major), no padding.
+ *   - Every call returns an int status (LMCE_OK or an LMCE_ERR_* code) and never
+ *     throws; no device code traps or asserts.
+ *   - Calls on one handle must be issued from one host thread and enqueue on one
+ *     stream (or on streams the caller orders).  Only lmce_finalize blocks the host.
+ */
+#ifndef LMCE_H_
+#define LMCE_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LMCE_API __attribute__((visibility("default")))
+#else
+#define LMCE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------------------- */
+#define LMCE_OK              0
+#define LMCE_ERR_ARG         1  /* null pointer, bad size or dtype, unaligned pointer      */
+#define LMCE_ERR_ARCH        2  /* the current device is not compute capability 10.3       */
+#define LMCE_ERR_CUDA        3  /* a CUDA runtime call or kernel launch failed              */
+#define LMCE_ERR_BAD_TARGET  4  /* a target was outside [0, V) and not ignore_id (finalize) */
+#define LMCE_ERR_NO_VALID    5  /* the step has no valid target                             */
+#define LMCE_ERR_NONFINITE   6  /* the summed loss is not finite (finalize)                 */
+#define LMCE_ERR_STATE       7  /* call out of order (e.g. finalize before any micro-step)  */
+
+/* ---- configuration ----------------------------------------------------------------- */
+typedef enum { LMCE_BF16 = 0, LMCE_FP32 = 1 } lmce_dtype;
+
+typedef enum {
+  LMCE_NORM_GLOBAL = 0,     /* s = 1 / global_valid  (global token-weighted mean, default) */
+  LMCE_NORM_MICRO_MEAN = 1  /* s = 1 / (valid targets of this micro-step * grad_accum_steps) */
+} lmce_norm;
+
+typedef enum {
+  LMCE_PATH_AUTO = 0,       /* tensor-core path when the shape allows it, else SIMT      */
+  LMCE_PATH_SIMT = 1,       /* fp32 FFMA kernels (any C <= 2048, any V, either dtype)    */
+  LMCE_PATH_TCGEN05 = 2     /* tcgen05/TMA kernels: bf16, C % 64 == 0, 64 <= C <= 1024    */
+} lmce_path;
+
+typedef struct lmce_config {
+  int64_t C;                /* hidden size (columns of h and W)                              */
+  int64_t V;                /* rows of W, padded vocabulary entries included                 */
+  int64_t max_N;            /* most rows any micro-step will pass; sizes the library scratch */
+  int32_t dtype;            /* lmce_dtype of hidden, W and dh                                */
+  int32_t ignore_id;        /* target value that carries no loss (usually -100)              */
+  int32_t norm;             /* lmce_norm                                                     */
+  int32_t grad_accum_steps; /* G >= 1; used by LMCE_NORM_MICRO_MEAN                          */
+  int32_t path;             /* lmce_path                                                     */
+  int32_t reserved;         /* must be 0                                                     */
+} lmce_config;
+
+typedef struct lmce_handle lmce_handle;
+
+/*
+ * lmce_create -- validate cfg, check the device, allocate the library scratch
+ * (per-row logsumexp, per-block loss/count partials, the step accumulators and the
+ * error word: about 12 * max_N + 64 KB of device memory) and return a handle in *out.
+ *   dW : device, fp32 [V, C], owned by the caller and kept by the handle until
+ *        lmce_destroy.  The first lmce_microstep after create or finalize WRITES it
+ *        (dW = this micro-step's gradient); later ones ADD to it.
+ * Errors: LMCE_ERR_ARG (null cfg/dW/out, C or V <= 0, max_N < 0, unknown dtype/norm/path,
+ *         G < 1, a forced path the shape does not allow), LMCE_ERR_ARCH, LMCE_ERR_CUDA.
+ */
+LMCE_API int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out);
+
+/*
+ * lmce_microstep -- enqueue one micro-step on `stream` (a cudaStream_t; NULL = legacy
+ * default stream) and return without waiting.
+ *   hidden      : device, dtype [N, C]  -- h, the final hidden states of N rows
+ *   W           : device, dtype [V, C]  -- the tied wte / lm_head weight
+ *   targets     : device, int32 [N]     -- next-token ids, or ignore_id
+ *   N           : rows in this micro-step, 0 <= N <= max_N (N == 0 is a no-op micro-step)
+ *   global_valid: LMCE_NORM_GLOBAL: valid targets over the whole optimizer step (all
+ *                 micro-steps, all data-parallel ranks); ignored for MICRO_MEAN
+ *   dh          : device, dtype [N, C], written (not accumulated): d(objective)/dh,
+ *                 rounded to nearest-even from fp32 for bf16
+ *   row_loss    : device, fp32 [N] or NULL; when given, receives every row's loss
+ *                 (0 on ignored rows)
+ * Out-of-range targets are treated as ignored and reported by lmce_finalize.
+ * The tensor-core path needs hidden, W, dh and dW 16-byte aligned.
+ * Errors: LMCE_ERR_ARG, LMCE_ERR_NO_VALID (GLOBAL norm with global_valid <= 0: dh is
+ *         zeroed, dW untouched, nothing else is enqueued), LMCE_ERR_CUDA.
+ */
+LMCE_API int lmce_microstep(lmce_handle* h, const void* hidden, const void* W, const int32_t* targets,
+                   int64_t N, int64_t global_valid, void* dh, float* row_loss, void* stream);
+
+/*
+ * lmce_finalize -- synchronise `stream`, read the step's results and reset the handle
+ * for the next optimizer step (the next micro-step writes dW again).
+ *   loss_sum    : host, may be NULL -- sum of the valid rows' losses over the step
+ *   valid_count : host, may be NULL -- valid targets seen over the step
+ *   loss_mean   : host, may be NULL -- sum_k s_k * loss_sum_k, the objective whose gradient
+ *                 dW holds: the token mean for GLOBAL norm on one rank, the pages'
+ *                 sum_k mean_k / G for MICRO_MEAN; NaN when no target was valid
+ * Errors: LMCE_ERR_STATE (no micro-step since create/finalize), LMCE_ERR_BAD_TARGET,
+ *         LMCE_ERR_NONFINITE, LMCE_ERR_NO_VALID, LMCE_ERR_CUDA.  Results are written
+ *         whenever the device values could be read, errors included.
+ */
+LMCE_API int lmce_finalize(lmce_handle* h, double* loss_sum, int64_t* valid_count, double* loss_mean,
+                  void* stream);
+
+/* lmce_destroy -- free the library scratch (not dW) and the handle.  NULL is allowed. */
+LMCE_API int lmce_destroy(lmce_handle* h);
+
+/* lmce_status_string -- static description of a status code. */
+LMCE_API const char* lmce_status_string(int status);
+
+/* lmce_launch_count -- kernels this handle has launched since create (host counter). */
+LMCE_API int64_t lmce_launch_count(const lmce_handle* h);
+
+/* lmce_selected_path -- LMCE_PATH_SIMT or LMCE_PATH_TCGEN05: the path micro-steps run. */
+LMCE_API int lmce_selected_path(const lmce_handle* h);
+
+/* ---- kernel timing (benchmark instrumentation) --------------------------------------
+ * When enabled, the library records a CUDA event pair around every kernel it launches
+ * (on the stream the kernel runs on) so that per-kernel device time can be read back.
+ * Kinds: */
+#define LMCE_KIND_LSE     0  /* logits tiles + online logsumexp + per-row loss           */
+#define LMCE_KIND_FINISH  1  /* fixed-order loss / count reduction, gradient scale        */
+#define LMCE_KIND_DW      2  /* recomputed logits -> dlogits -> dW accumulation           */
+#define LMCE_KIND_DH      3  /* recomputed logits -> dlogits -> dh                        */
+#define LMCE_KIND_COUNT   4
+
+/* lmce_profile -- enable (1: clears earlier records) or disable (0) the event records. */
+LMCE_API int lmce_profile(lmce_handle* h, int enable);
+
+/*
+ * lmce_profile_read -- synchronise the recorded events and return, for one kind, the
+ * summed device time in milliseconds and the number of launches recorded.
+ * Errors: LMCE_ERR_ARG (null handle or outputs, unknown kind), LMCE_ERR_CUDA.
+ */
+LMCE_API int lmce_profile_read(lmce_handle* h, int kind, double* total_ms, int64_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LMCE_H_ */

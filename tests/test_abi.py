@@ -1,0 +1,63 @@
+"""The C-ABI library loads and exports every function include/lmce.h declares.
+
+No compute call is made: only entry points that reject their arguments before
+touching a device are exercised, so this runs without a GPU.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from grad_lmce_microstep_gb300 import build as B
+from grad_lmce_microstep_gb300 import lmce as M
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "lmce.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(M.LIB_PATH):
+        B.build()
+    return M.load()
+
+
+def declared():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"LMCE_API\s+[\w\s\*]+?\b(lmce_\w+)\s*\(", txt)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared() == sorted(M.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared():
+        assert hasattr(lib, name), name
+        assert isinstance(getattr(lib, name), ctypes._CFuncPtr)
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert M.status_string(code) and M.status_string(code) != "unknown status"
+    assert M.status_string(99) == "unknown status"
+
+
+def test_argument_errors_before_any_device_call(lib):
+    cfg = M.Config(768, 50304, 1024, 0, -100, 0, 1, 0, 0)
+    h = ctypes.c_void_p()
+    # null dW / null cfg / null out
+    assert lib.lmce_create(ctypes.byref(cfg), None, ctypes.byref(h)) == M.ERR_ARG
+    assert lib.lmce_create(None, ctypes.c_void_p(16), ctypes.byref(h)) == M.ERR_ARG
+    for bad in (dict(C=0), dict(V=-1), dict(max_N=-5), dict(dtype=7), dict(norm=3), dict(path=9),
+                dict(grad_accum_steps=0), dict(reserved=1), dict(C=4096, path=1)):
+        c = M.Config(768, 50304, 1024, 0, -100, 0, 1, 0, 0)
+        for k, v in bad.items():
+            setattr(c, k, v)
+        assert lib.lmce_create(ctypes.byref(c), ctypes.c_void_p(16), ctypes.byref(h)) == M.ERR_ARG, bad
+    assert lib.lmce_microstep(None, None, None, None, 0, 0, None, None, None) == M.ERR_ARG
+    assert lib.lmce_finalize(None, None, None, None, None) == M.ERR_ARG
+    assert lib.lmce_destroy(None) == M.OK
+    assert lib.lmce_profile(None, 1) == M.ERR_ARG
+    assert lib.lmce_launch_count(None) == 0
