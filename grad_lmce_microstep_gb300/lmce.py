@@ -31,7 +31,10 @@ PATH_NAMES = {v: k for k, v in PATHS.items()}
 TORCH_DTYPES = {"bf16": torch.bfloat16, "fp32": torch.float32}
 
 EXPORTS = ("lmce_create", "lmce_microstep", "lmce_finalize", "lmce_destroy", "lmce_status_string",
-           "lmce_launch_count", "lmce_selected_path", "lmce_profile", "lmce_profile_read")
+           "lmce_launch_count", "lmce_selected_path", "lmce_profile", "lmce_profile_read",
+           "lmce_microstep_noalloc")
+
+NOALLOC_MAX_N = 65536
 
 KINDS = {"lse": 0, "finish": 1, "dW": 2, "dh": 3}
 
@@ -80,6 +83,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.lmce_profile.restype = i32
     L.lmce_profile_read.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]
     L.lmce_profile_read.restype = i32
+    L.lmce_microstep_noalloc.argtypes = [ctypes.POINTER(Config), vp, vp, vp, i64, i64, vp, vp, i32, vp, vp, vp, vp]
+    L.lmce_microstep_noalloc.restype = i32
     _lib = L
     return L
 

@@ -160,6 +160,39 @@ LMCE_API int lmce_profile(lmce_handle* h, int enable);
  */
 LMCE_API int lmce_profile_read(lmce_handle* h, int kind, double* total_ms, int64_t* launches);
 
+/* ---- allocation-free micro-step --------------------------------------------------------
+ * No counterpart on the GPT-2 training pages: this entry point exists for callers that
+ * cannot call cudaMalloc -- a host runtime that hands out all device memory from its own
+ * pool or arena and does not let a library allocate behind its back, or a code path that
+ * must not stall (cudaFree synchronises the whole device, and cudaMalloc may too).
+ *
+ * lmce_microstep_noalloc -- enqueue one self-contained micro-step on `stream` with the
+ * SIMT kernels, without any allocation: no cudaMalloc, no cudaFree, no allocating library
+ * routine.  Its scratch (per-row logsumexp, per-block partials, accumulators) is a fixed
+ * array of about 360 KB compiled into the library, which every GPU that loads the library
+ * holds until the process exits.
+ *   cfg             : as for lmce_create; max_N is ignored, path must be AUTO or SIMT,
+ *                     C <= 2048
+ *   hidden, W, targets, N, global_valid, dh, row_loss : as for lmce_microstep
+ *   dW              : device, fp32 [V, C]; written (accumulate_dW == 0) or added to (!= 0)
+ *   loss_sum_out    : device double, or NULL: this micro-step's summed loss
+ *   valid_count_out : device int64, or NULL: this micro-step's valid targets
+ * Limits: N <= LMCE_NOALLOC_MAX_N; a larger N returns LMCE_ERR_ARG before anything is
+ * enqueued.  Out-of-range targets are treated as ignored but not reported here.
+ * The first call on a device sets up that device (looks up the array's device address
+ * with that device current), so make it before any stream capture.  Every call on a device
+ * shares the one array and it keeps the last call's contents (the accumulators are cleared
+ * by each call); calls whose work overlaps on the GPU -- on different streams, or from
+ * different host threads -- race on it and must be serialised by the caller.
+ * Errors: LMCE_ERR_ARG, LMCE_ERR_ARCH, LMCE_ERR_NO_VALID (GLOBAL norm with
+ *         global_valid <= 0: dh zeroed, dW untouched), LMCE_ERR_CUDA.
+ */
+#define LMCE_NOALLOC_MAX_N 65536
+LMCE_API int lmce_microstep_noalloc(const lmce_config* cfg, const void* hidden, const void* W,
+                                    const int32_t* targets, int64_t N, int64_t global_valid, void* dh,
+                                    float* dW, int accumulate_dW, float* row_loss, double* loss_sum_out,
+                                    int64_t* valid_count_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
