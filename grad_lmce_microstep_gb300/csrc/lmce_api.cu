@@ -109,6 +109,9 @@ static void free_scratch(lmce_handle* h) {
   cudaFree(h->sc.part_cnt);
   cudaFree(h->sc.part_err);
   cudaFree(h->sc.acc);
+  cudaFree(h->sc.tc_part_m);
+  cudaFree(h->sc.tc_part_l);
+  cudaFree(h->sc.tc_zt);
   if (h->host_acc) cudaFreeHost(h->host_acc);
   memset(&h->sc, 0, sizeof(h->sc));
   h->host_acc = nullptr;
@@ -157,8 +160,13 @@ extern "C" int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out)
             cudaMalloc(&h->sc.part_err, sizeof(unsigned) * parts) == cudaSuccess &&
             cudaMalloc(&h->sc.acc, sizeof(DevAcc)) == cudaSuccess &&
             cudaMallocHost(&h->host_acc, sizeof(DevAcc)) == cudaSuccess &&
-            cudaMemset(h->sc.acc, 0, sizeof(DevAcc)) == cudaSuccess &&
-            cudaDeviceSynchronize() == cudaSuccess;
+            cudaMemset(h->sc.acc, 0, sizeof(DevAcc)) == cudaSuccess;
+  if (ok && path == LMCE_PATH_TCGEN05) {
+    const size_t slices = sizeof(float) * (size_t)TC_MAX_SPLIT * (size_t)maxN;
+    ok = cudaMalloc(&h->sc.tc_part_m, slices) == cudaSuccess && cudaMalloc(&h->sc.tc_part_l, slices) == cudaSuccess &&
+         cudaMalloc(&h->sc.tc_zt, sizeof(float) * maxN) == cudaSuccess;
+  }
+  ok = ok && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
     free_scratch(h);
     delete h;
@@ -236,6 +244,7 @@ extern "C" int lmce_finalize(lmce_handle* h, double* loss_sum, int64_t* valid_co
   h->first = true;
   h->attempted = 0;
   if (cudaMemsetAsync(h->sc.acc, 0, sizeof(DevAcc), st) != cudaSuccess) return LMCE_ERR_CUDA;
+  if (r.err & ERR_BIT_TIMEOUT) return LMCE_ERR_CUDA;  // a bounded device wait ran out
   if (r.err & ERR_BIT_BAD_TARGET) return LMCE_ERR_BAD_TARGET;
   if ((r.err & ERR_BIT_NONFINITE) || !isfinite(r.loss_sum)) return LMCE_ERR_NONFINITE;
   if (r.count == 0) return LMCE_ERR_NO_VALID;

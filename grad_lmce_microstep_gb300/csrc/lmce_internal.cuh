@@ -69,6 +69,8 @@ struct DevAcc {
 
 constexpr unsigned ERR_BIT_BAD_TARGET = 1u;
 constexpr unsigned ERR_BIT_NONFINITE = 2u;
+// A bounded device wait ran out (tensor-core path); bits 8..15 say which wait.
+constexpr unsigned ERR_BIT_TIMEOUT = 4u;
 
 // Arguments of one micro-step as the kernels see them.
 struct StepArgs {
@@ -95,7 +97,13 @@ struct Scratch {
   unsigned* part_err;  // [max_parts] per-block error flags
   DevAcc* acc;         // step accumulators
   int64_t max_parts;
+  // tensor-core path only
+  float* tc_part_m;    // [TC_MAX_SPLIT][max_N] per-slice base-2 row max
+  float* tc_part_l;    // [TC_MAX_SPLIT][max_N] per-slice sum of 2^(x - max)
+  float* tc_zt;        // [max_N] target logit
 };
+
+constexpr int TC_MAX_SPLIT = 32;
 
 // Fixed-order reduction of the per-block partials of one micro-step into the step
 // accumulators; also computes this micro-step's gradient scale.  One launch.
@@ -105,6 +113,8 @@ cudaError_t launch_finish(const StepArgs& a, const Scratch& s, int64_t nparts, L
 int64_t simt_parts(int64_t N);
 size_t simt_grad_smem(int64_t C);
 cudaError_t simt_microstep(const StepArgs& a, const Scratch& s, Launch& L);
+// The two gradient passes alone (lse and the scale already on the device).
+cudaError_t simt_grads(const StepArgs& a, const Scratch& s, Launch& L);
 
 // Tensor-core path (tcgen05 + TMA).
 bool tc_supported(int64_t C, int64_t V, int bf16);

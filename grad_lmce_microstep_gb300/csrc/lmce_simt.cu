@@ -227,15 +227,7 @@ int64_t simt_parts(int64_t N) { return (N + R - 1) / R; }
 size_t simt_grad_smem(int64_t C) { return (size_t)R * (size_t)C * sizeof(float); }
 
 template <typename T>
-static cudaError_t simt_run(const StepArgs& a, const Scratch& sc, Launch& L) {
-  const int64_t nb = simt_parts(a.N);
-  L.begin(K_LSE);
-  simt_lse_kernel<T><<<(unsigned)nb, NT, 0, L.st>>>(a, sc.lse, sc.part_loss, sc.part_cnt, sc.part_err);
-  L.end();
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  e = launch_finish(a, sc, nb, L);
-  if (e != cudaSuccess) return e;
+static cudaError_t simt_grads_t(const StepArgs& a, const Scratch& sc, Launch& L) {
   const size_t smem = simt_grad_smem(a.C);
   auto kdw = simt_grad_kernel<T, true>;
   auto kdh = simt_grad_kernel<T, false>;
@@ -245,16 +237,33 @@ static cudaError_t simt_run(const StepArgs& a, const Scratch& sc, Launch& L) {
   L.begin(K_DW);
   kdw<<<(unsigned)((a.V + R - 1) / R), NT, smem, L.st>>>(a, sc.lse, sc.acc);
   L.end();
-  e = cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   L.begin(K_DH);
-  kdh<<<(unsigned)nb, NT, smem, L.st>>>(a, sc.lse, sc.acc);
+  kdh<<<(unsigned)simt_parts(a.N), NT, smem, L.st>>>(a, sc.lse, sc.acc);
   L.end();
   return cudaGetLastError();
 }
 
+template <typename T>
+static cudaError_t simt_run(const StepArgs& a, const Scratch& sc, Launch& L) {
+  const int64_t nb = simt_parts(a.N);
+  L.begin(K_LSE);
+  simt_lse_kernel<T><<<(unsigned)nb, NT, 0, L.st>>>(a, sc.lse, sc.part_loss, sc.part_cnt, sc.part_err);
+  L.end();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_finish(a, sc, nb, L);
+  if (e != cudaSuccess) return e;
+  return simt_grads_t<T>(a, sc, L);
+}
+
 cudaError_t simt_microstep(const StepArgs& a, const Scratch& sc, Launch& L) {
   return a.bf16 ? simt_run<__nv_bfloat16>(a, sc, L) : simt_run<float>(a, sc, L);
+}
+
+cudaError_t simt_grads(const StepArgs& a, const Scratch& sc, Launch& L) {
+  return a.bf16 ? simt_grads_t<__nv_bfloat16>(a, sc, L) : simt_grads_t<float>(a, sc, L);
 }
 
 }  // namespace lmce

@@ -63,7 +63,7 @@ typedef enum {
 typedef enum {
   LMCE_PATH_AUTO = 0,       /* tensor-core path when the shape allows it, else SIMT      */
   LMCE_PATH_SIMT = 1,       /* fp32 FFMA kernels (any C <= 2048, any V, either dtype)    */
-  LMCE_PATH_TCGEN05 = 2     /* tcgen05/TMA kernels: bf16, C % 64 == 0, 64 <= C <= 1024    */
+  LMCE_PATH_TCGEN05 = 2     /* tcgen05/TMA kernels: bf16, C % 256 == 0, 256 <= C <= 1024 */
 } lmce_path;
 
 typedef struct lmce_config {

@@ -45,7 +45,7 @@ def test_tiny_char_fp32():
 
 @pytest.mark.parametrize("path", PATHS_BF16)
 def test_micro_mean_unequal_counts(path):
-    w = I.custom([256, 256, 129], 128, 777, "bf16", seed=2)
+    w = I.custom([256, 256, 129], 256, 777, "bf16", seed=2)
     w.micro[1][1][50:] = I.IGNORE_ID
     _need_path(path, w.C, w.V, w.dtype)
     for norm in ("global", "micro_mean"):
@@ -68,7 +68,7 @@ def test_logit_stress_small(path):
 
 @pytest.mark.parametrize("path", PATHS_BF16)
 def test_bitwise_reproducible(path):
-    w = I.custom([384, 200], 192, 1500, "bf16", seed=4)
+    w = I.custom([384, 200], 256, 1500, "bf16", seed=4)
     _need_path(path, w.C, w.V, w.dtype)
     a = run_lib(w, path=path)
     b = run_lib(w, path=path)
