@@ -289,6 +289,380 @@ __global__ void __launch_bounds__(256) tc_combine_kernel(const float* __restrict
   }
 }
 
+// ---- pass 2: gradients ----------------------------------------------------------------
+// One kernel shape serves both contractions of the backward pass.  A CTA pair owns 128
+// "X" rows and streams the other operand "Y" in blocks of 256 rows:
+//   dW pass: X = W (vocabulary rows), Y = h (tokens);  acc^T[c][v] = sum_n h[n][c] dz[n][v]
+//   dh pass: X = h (tokens), Y = W (vocabulary rows);   acc^T[c][n] = sum_v W[v][c] dz[n][v]
+// Per block: S^T = Y_blk . X^T (cta_group::2, M = 256 stream rows, N = 128, K = C) lands in
+// TMEM; each epilogue thread owns one stream row, forms dz = s (exp(z - lse) - onehot) with
+// the logsumexp of pass 1 (0 on ignored rows), rounds it to bf16 and writes it, already in
+// the 128-byte-swizzled MN-major operand layout, half into its own CTA's shared memory
+// and half into the peer's (the N half each CTA supplies).  Then
+// acc^T[C x 128] += Y_blk^T . dz (cta_group::2, M = 256 C rows per chunk, K = 256 stream
+// rows) accumulates in TMEM for the whole stream.  The S tile of block j+1 is computed
+// while the epilogue turns block j into dz, and the accumulation of block j runs while the
+// epilogue works on block j+1.  Every output element has one owner: deterministic.
+constexpr int G_XT = 128;                  // X rows per pair (64 per CTA)
+constexpr int G_YB = 256;                  // stream rows per block (128 per CTA)
+constexpr int G_ST = 4;                    // Y stages of 16 KB
+constexpr int G_STAGE = 16384;
+constexpr int G_DZ = G_YB * 128;           // one dz buffer: 256 K-rows x 64 bf16 = 32 KB
+constexpr int G_THREADS = 192;
+
+struct GradParams {
+  const int32_t* targets;
+  const float* lse;
+  const DevAcc* acc;     // scale of this micro-step
+  unsigned* err;
+  float* dW;             // dW pass output (fp32 [V, C])
+  __nv_bfloat16* dh;     // dh pass output (bf16 [N, C])
+  int N, V, C;
+  int beta;              // dW pass: 0 writes, 1 adds
+};
+
+__host__ __device__ constexpr int grad_smem_bytes(int C) {
+  return (G_XT / 2) * C * 2 + G_ST * G_STAGE + 2 * G_DZ + 1024;
+}
+
+template <bool DW>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
+    tc_grad_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmYs,
+                   const __grid_constant__ CUtensorMap tmYa, GradParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int KC = p.C / 64;                  // 64-wide C chunks (S phase stages per block)
+  const int NCH = p.C / 256;                // 256-row C chunks of acc^T
+  uint8_t* sX = smem;                       // [KC][64 rows][128 B]
+  uint8_t* sY = smem + (G_XT / 2) * p.C * 2;
+  uint8_t* sDZ = sY + G_ST * G_STAGE;       // [2][256 rows][128 B]
+  __shared__ __align__(8) uint64_t full[G_ST], pfull[G_ST], empty[G_ST];
+  __shared__ __align__(8) uint64_t x_full, x_pfull, s_full, s_empty, dz_full[2], dz_empty[2], acc_full, drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ volatile int epi_abort;
+  __shared__ float col_lse2[G_XT];          // dh pass: per-column (token) lse * log2(e)
+  __shared__ int col_y[G_XT];               // dh pass: per-column target (or -1: no gradient)
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int x0 = (blockIdx.x >> 1) * G_XT;
+  const int nX = DW ? p.V : p.N;
+  const int nY = DW ? p.N : p.V;
+  const int nblk = (nY + G_YB - 1) / G_YB;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < G_ST; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&pfull[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    mbar_init(smem_u32(&x_full), 1);
+    mbar_init(smem_u32(&x_pfull), 1);
+    mbar_init(smem_u32(&s_full), 1);
+    mbar_init(smem_u32(&s_empty), 2);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&dz_full[b]), 2 * 128);
+      mbar_init(smem_u32(&dz_empty[b]), 1);
+    }
+    mbar_init(smem_u32(&acc_full), 1);
+    mbar_init(smem_u32(&drain_bar), 1);
+    epi_abort = 0;
+    fence_mbar_init();
+  }
+  if (!DW && threadIdx.x < G_XT) {
+    const int n = x0 + threadIdx.x;
+    int y = -1;
+    float l2 = 0.f;
+    if (n < p.N) {
+      const int t = p.targets[n];
+      if (t >= 0 && t < p.V) {
+        y = t;
+        l2 = p.lse[n] * LOG2E;
+      }
+    }
+    col_y[threadIdx.x] = y;
+    col_lse2[threadIdx.x] = l2;
+  }
+  if (warp == 1) {
+    tmem_alloc<2>(smem_u32(&tmem_base_sh), 512);
+    tmem_relinquish<2>();
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const uint32_t tS = tmem + NCH * 128;     // S^T columns after the accumulator chunks
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmX);
+      tma_prefetch_desc(&tmYs);
+      tma_prefetch_desc(&tmYa);
+      mbar_expect_tx(smem_u32(&x_full), (G_XT / 2) * p.C * 2);
+      for (int kc = 0; kc < KC; ++kc)
+        tma_load_2d(smem_u32(sX) + kc * 8192, &tmX, smem_u32(&x_full), kc * 64, x0 + (int)rank * 64);
+      int it = 0;
+      bool ok = true;
+      for (int j = 0; j <= nblk && ok; ++j) {
+        const int nst = (j < nblk ? KC : 0) + (j >= 1 ? NCH * 4 : 0);
+        for (int u = 0; u < nst; ++u, ++it) {
+          const int s = it % G_ST;
+          if (!mbar_wait(smem_u32(&empty[s]), ((it / G_ST) & 1) ^ 1, WAIT_NS)) {
+            record_timeout(p.err, 17);
+            ok = false;
+            break;
+          }
+          const uint32_t dst = smem_u32(sY) + s * G_STAGE;
+          const uint32_t bar = smem_u32(&full[s]);
+          mbar_expect_tx(bar, G_STAGE);
+          if (j < nblk && u < KC) {
+            // S phase of block j: my 128 stream rows x C chunk u
+            tma_load_2d(dst, &tmYs, bar, u * 64, j * G_YB + (int)rank * 128);
+          } else {
+            // accumulation phase of block j-1: 64 stream rows (sub-step q) x my 128 C of chunk i
+            const int v = u - (j < nblk ? KC : 0);
+            const int i = v >> 2, q = v & 3;
+            const int row = (j - 1) * G_YB + q * 64;
+            const int col = i * 256 + (int)rank * 128;
+            tma_load_2d(dst, &tmYa, bar, col, row);
+            tma_load_2d(dst + 8192, &tmYa, bar, col + 64, row);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (rank == 1) {
+      // ---------------- forwarder (peer CTA) ----------------
+      if (lane == 0) {
+        const uint32_t lp = mapa(smem_u32(&pfull[0]), 0);
+        bool ok = mbar_wait(smem_u32(&x_full), 0, WAIT_NS);
+        if (!ok) record_timeout(p.err, 18);
+        else mbar_arrive_cluster(mapa(smem_u32(&x_pfull), 0));
+        int it = 0;
+        for (int j = 0; j <= nblk && ok; ++j) {
+          const int nst = (j < nblk ? KC : 0) + (j >= 1 ? NCH * 4 : 0);
+          for (int u = 0; u < nst; ++u, ++it) {
+            const int s = it % G_ST;
+            if (!mbar_wait(smem_u32(&full[s]), (it / G_ST) & 1, WAIT_NS)) {
+              record_timeout(p.err, 19);
+              ok = false;
+              break;
+            }
+            mbar_arrive_cluster(lp + s * 8);
+          }
+        }
+      }
+    } else if (lane == 0) {
+      // ---------------- MMA issuer (leader CTA) ----------------
+      const uint32_t idS = idesc_bf16(256, G_XT, 0, 0);
+      const uint32_t idA = idesc_bf16(256, G_XT, 1, 1);
+      bool ok = mbar_wait(smem_u32(&x_full), 0, WAIT_NS) && mbar_wait_cluster(smem_u32(&x_pfull), 0, WAIT_NS);
+      if (!ok) record_timeout(p.err, 20);
+      int it = 0;
+      for (int j = 0; j <= nblk && ok; ++j) {
+        if (j < nblk) {
+          // S^T of block j (the epilogue must have read block j-1's)
+          if (!mbar_wait_cluster(smem_u32(&s_empty), (j & 1) ^ 1, WAIT_NS)) {
+            record_timeout(p.err, 21);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int kc = 0; kc < KC; ++kc, ++it) {
+            const int s = it % G_ST;
+            const uint32_t ph = (it / G_ST) & 1;
+            if (!mbar_wait(smem_u32(&full[s]), ph, WAIT_NS) || !mbar_wait_cluster(smem_u32(&pfull[s]), ph, WAIT_NS)) {
+              record_timeout(p.err, 22);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a = smem_u32(sY) + s * G_STAGE;
+            const uint32_t b = smem_u32(sX) + kc * 8192;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ss<2>(tS, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(b + k * 32, 16, 1024), idS,
+                        (kc | k) != 0);
+            mma_commit_mc2(smem_u32(&empty[s]), 3);
+          }
+          if (!ok) break;
+          mma_commit_mc2(smem_u32(&s_full), 3);
+        }
+        if (j >= 1) {
+          // accumulation of block j-1 with its dz
+          const int jb = j - 1, db = jb & 1;
+          if (!mbar_wait_cluster(smem_u32(&dz_full[db]), (jb >> 1) & 1, WAIT_NS)) {
+            record_timeout(p.err, 23);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t dzb = smem_u32(sDZ) + db * G_DZ;
+          for (int i = 0; i < NCH && ok; ++i)
+            for (int q = 0; q < 4; ++q, ++it) {
+              const int s = it % G_ST;
+              const uint32_t ph = (it / G_ST) & 1;
+              if (!mbar_wait(smem_u32(&full[s]), ph, WAIT_NS) ||
+                  !mbar_wait_cluster(smem_u32(&pfull[s]), ph, WAIT_NS)) {
+                record_timeout(p.err, 24);
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t a = smem_u32(sY) + s * G_STAGE;
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_ss<2>(tmem + i * 128, sdesc_sw128(a + k * 2048, 8192, 1024),
+                          sdesc_sw128(dzb + q * 8192 + k * 2048, 32768, 1024), idA, (jb | q | k) != 0);
+              mma_commit_mc2(smem_u32(&empty[s]), 3);
+            }
+          if (!ok) break;
+          mma_commit_mc2(smem_u32(&dz_empty[db]), 3);
+          if (jb == nblk - 1) mma_commit_mc2(smem_u32(&acc_full), 3);
+        }
+      }
+      if (!ok) {
+        mma_commit<2>(smem_u32(&drain_bar));
+        mbar_wait(smem_u32(&drain_bar), 0, WAIT_NS);
+      }
+    }
+  } else {
+    // ---------------- epilogue: warps 2..5, one stream row per thread ----------------
+    const int q = warp & 3;
+    const int kl = q * 32 + lane;                 // TMEM lane = my stream row in this CTA
+    const int kb = (int)rank * 128 + kl;          // row within the 256-row block
+    const float s = p.acc->scale;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const uint32_t leader_s_empty = mapa(smem_u32(&s_empty), 0);
+    const uint32_t leader_dz_full = mapa(smem_u32(&dz_full[0]), 0);
+    const uint32_t dz_local = smem_u32(sDZ);
+    const uint32_t dz_peer = mapa(dz_local, rank ^ 1);
+    bool alive = true;
+    for (int j = 0; j < nblk; ++j) {
+      if (!mbar_wait(smem_u32(&s_full), j & 1, WAIT_NS)) {
+        record_timeout(p.err, 25);
+        epi_abort = 1;
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (epi_abort) { alive = false; break; }
+      tc_fence_after();
+      float z[G_XT];
+#pragma unroll
+      for (int c = 0; c < G_XT / 32; ++c) {
+        float v[32];
+        tmem_ld32(tS + lane_off + c * 32, v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) z[c * 32 + e] = v[e];
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (warp == 2 && lane == 0) {
+        if (rank == 0) mbar_arrive(smem_u32(&s_empty));
+        else mbar_arrive_cluster(leader_s_empty);
+      }
+      // dz for my stream row
+      const int ys = j * G_YB + kb;                 // stream row index
+      int yrow = -1;                                // dW pass: my token's target
+      float lrow2 = 0.f;
+      if (DW) {
+        if (ys < p.N) {
+          const int t = p.targets[ys];
+          if (t >= 0 && t < p.V) {
+            yrow = t;
+            lrow2 = p.lse[ys] * LOG2E;
+          }
+        }
+      }
+      const bool row_ok = DW ? (yrow >= 0) : (ys < p.V);
+      uint32_t packed[G_XT / 2];
+#pragma unroll
+      for (int x = 0; x < G_XT; x += 2) {
+        float d0 = 0.f, d1 = 0.f;
+        if (row_ok) {
+          if (DW) {
+            const int v0 = x0 + x;
+            if (v0 < p.V) d0 = s * (exp2f(fmaf(z[x], LOG2E, -lrow2)) - (v0 == yrow ? 1.f : 0.f));
+            if (v0 + 1 < p.V) d1 = s * (exp2f(fmaf(z[x + 1], LOG2E, -lrow2)) - (v0 + 1 == yrow ? 1.f : 0.f));
+          } else {
+            if (col_y[x] >= 0) d0 = s * (exp2f(fmaf(z[x], LOG2E, -col_lse2[x])) - (ys == col_y[x] ? 1.f : 0.f));
+            if (col_y[x + 1] >= 0)
+              d1 = s * (exp2f(fmaf(z[x + 1], LOG2E, -col_lse2[x + 1])) - (ys == col_y[x + 1] ? 1.f : 0.f));
+          }
+        }
+        __nv_bfloat162 pr = __floats2bfloat162_rn(d0, d1);
+        packed[x / 2] = *reinterpret_cast<uint32_t*>(&pr);
+      }
+      const int db = j & 1;
+      if (!mbar_wait(smem_u32(&dz_empty[db]), ((j >> 1) & 1) ^ 1, WAIT_NS)) {
+        record_timeout(p.err, 26);
+        epi_abort = 1;
+      }
+      // columns [64d, 64d + 64) go to CTA d, at K-row kb of dz buffer db
+#pragma unroll
+      for (int d = 0; d < 2; ++d) {
+        const uint32_t base = (d == (int)rank ? dz_local : dz_peer) + db * G_DZ;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t addr = base + sw128_offset(kb, c * 16);
+          const uint32_t* w = packed + d * 32 + c * 4;
+          if (d == (int)rank)
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                         "r"(w[3])
+                         : "memory");
+          else
+            asm volatile("st.shared::cluster.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
+                         "r"(w[2]), "r"(w[3])
+                         : "memory");
+        }
+      }
+      fence_proxy_async();
+      mbar_arrive_cluster(leader_dz_full + db * 8);
+    }
+    // accumulator -> output
+    if (alive) {
+      if (!mbar_wait(smem_u32(&acc_full), 0, WAIT_NS)) {
+        record_timeout(p.err, 27);
+        epi_abort = 1;
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (!epi_abort) {
+        tc_fence_after();
+        for (int i = 0; i < NCH; ++i) {
+          const int c = i * 256 + (int)rank * 128 + kl;   // my C row of the accumulator
+#pragma unroll 1
+          for (int cc = 0; cc < G_XT / 32; ++cc) {
+            float v[32];
+            tmem_ld32(tmem + i * 128 + lane_off + cc * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int x = x0 + cc * 32 + e;
+              if (x < nX) {
+                if (DW) {
+                  float* o = p.dW + (size_t)x * p.C + c;
+                  *o = p.beta ? (*o + v[e]) : v[e];
+                } else {
+                  p.dh[(size_t)x * p.C + c] = __float2bfloat16_rn(v[e]);
+                }
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<2>(tmem, 512);
+  }
+}
+
 // ---- host side ------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -380,7 +754,7 @@ cudaError_t tc_lse(const StepArgs& a, const Scratch& sc, Launch& L) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t nparts = tc_parts(a.N);
-  L.begin(K_LSE);
+  L.begin(K_FINISH);
   tc_combine_kernel<<<(unsigned)nparts, 256, 0, L.st>>>(sc.tc_part_m, sc.tc_part_l, sc.tc_zt, nsplit, a, sc.lse,
                                                         sc.part_loss, sc.part_cnt, sc.part_err);
   L.end();
@@ -389,10 +763,44 @@ cudaError_t tc_lse(const StepArgs& a, const Scratch& sc, Launch& L) {
   return launch_finish(a, sc, nparts, L);
 }
 
+bool tc_grad_supported(int64_t C) { return C % 256 == 0 && C >= 256 && C <= 768; }
+
+template <bool DW>
+cudaError_t tc_grad(const StepArgs& a, const Scratch& sc, Launch& L) {
+  const void* X = DW ? a.W : a.hidden;
+  const void* Y = DW ? a.hidden : a.W;
+  const int64_t nX = DW ? a.V : a.N, nY = DW ? a.N : a.V;
+  CUtensorMap mx, mys, mya;
+  if (!make_map(&mx, X, (uint64_t)nX, (uint64_t)a.C, G_XT / 2) ||
+      !make_map(&mys, Y, (uint64_t)nY, (uint64_t)a.C, 128) || !make_map(&mya, Y, (uint64_t)nY, (uint64_t)a.C, 64))
+    return cudaErrorInvalidValue;
+  GradParams p;
+  p.targets = a.targets;
+  p.lse = sc.lse;
+  p.acc = sc.acc;
+  p.err = &sc.acc->err;
+  p.dW = a.dW;
+  p.dh = static_cast<__nv_bfloat16*>(a.dh);
+  p.N = (int)a.N;
+  p.V = (int)a.V;
+  p.C = (int)a.C;
+  p.beta = a.beta;
+  const int smem = grad_smem_bytes((int)a.C);
+  cudaFuncSetAttribute(tc_grad_kernel<DW>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const unsigned pairs = (unsigned)((nX + G_XT - 1) / G_XT);
+  L.begin(DW ? K_DW : K_DH);
+  tc_grad_kernel<DW><<<2 * pairs, G_THREADS, smem, L.st>>>(mx, mys, mya, p);
+  L.end();
+  return cudaGetLastError();
+}
+
 cudaError_t tc_microstep(const StepArgs& a, const Scratch& sc, Launch& L) {
   cudaError_t e = tc_lse(a, sc, L);
   if (e != cudaSuccess) return e;
-  return simt_grads(a, sc, L);
+  if (!tc_grad_supported(a.C)) return simt_grads(a, sc, L);
+  e = tc_grad<true>(a, sc, L);
+  if (e != cudaSuccess) return e;
+  return tc_grad<false>(a, sc, L);
 }
 
 }  // namespace lmce

@@ -66,6 +66,14 @@ def test_logit_stress_small(path):
     assert_parity(got, ref, "bf16")
 
 
+def test_wide_hidden_c1024():
+    # C = 1024: tensor-core logsumexp, SIMT gradients (the tensor-core gradient pass takes C <= 768)
+    w = I.custom([300, 140], 1024, 900, "bf16", seed=9, ignore_frac=0.05)
+    got = run_lib(w, path="tcgen05")
+    assert got["status"] == M.OK
+    assert_parity(got, run_oracle(w), "bf16")
+
+
 @pytest.mark.parametrize("path", PATHS_BF16)
 def test_bitwise_reproducible(path):
     w = I.custom([384, 200], 256, 1500, "bf16", seed=4)
