@@ -59,7 +59,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(L_THREADS, 1)
     tc_lse_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW, LseParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full[L_ST], pfull[L_ST], empty[L_ST], acc_full[2], acc_empty[2];
+  __shared__ __align__(8) uint64_t full[L_ST], empty[L_ST], acc_full[2], acc_empty[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ volatile int epi_abort;
@@ -76,7 +76,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(L_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < L_ST; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&pfull[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -102,6 +101,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(L_THREADS, 1)
       tma_prefetch_desc(&tmH);
       tma_prefetch_desc(&tmW);
       const int hrow = nb * 256 + (int)rank * L_BM;
+      const uint32_t lead_full = mapa(smem_u32(&full[0]), 0);  // both halves land on the leader's barrier
       int it = 0;
       bool ok = true;
       for (int t = 0; t < ntiles && ok; ++t) {
@@ -111,29 +111,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(L_THREADS, 1)
           const uint32_t ph = ((it / L_ST) & 1) ^ 1;
           if (!mbar_wait(smem_u32(&empty[s]), ph, WAIT_NS)) { record_timeout(p.err, 1); ok = false; break; }
           const uint32_t a = smem_u32(smem + s * L_STAGE), b = a + L_STAGE_A;
-          mbar_expect_tx(smem_u32(&full[s]), L_STAGE);
-          tma_load_2d(a, &tmH, smem_u32(&full[s]), kc * L_BK, hrow);
-          tma_load_2d(b, &tmW, smem_u32(&full[s]), kc * L_BK, wrow);
+          if (rank == 0) mbar_expect_tx(smem_u32(&full[s]), 2 * L_STAGE);
+          tma_load_2d_cg2(a, &tmH, lead_full + s * 8, kc * L_BK, hrow);
+          tma_load_2d_cg2(b, &tmW, lead_full + s * 8, kc * L_BK, wrow);
         }
       }
     }
   } else if (warp == 1) {
     if (rank == 1) {
-      // ---------------- forwarder: tell the leader when this CTA's stage landed ------------
-      if (lane == 0) {
-        const uint32_t leader_pfull = mapa(smem_u32(&pfull[0]), 0);
-        int it = 0;
-        for (int t = 0; t < ntiles; ++t)
-          for (int kc = 0; kc < kchunks; ++kc, ++it) {
-            const int s = it % L_ST;
-            if (!mbar_wait(smem_u32(&full[s]), (it / L_ST) & 1, WAIT_NS)) {
-              record_timeout(p.err, 2);
-              t = ntiles;
-              break;
-            }
-            mbar_arrive_cluster(leader_pfull + s * 8);
-          }
-      }
+      // the peer CTA issues nothing: its TMA loads complete on the leader's barriers
     } else if (lane == 0) {
       // ---------------- MMA issuer (leader CTA) ----------------
       const uint32_t idesc = idesc_bf16(256, 256, 0, 0);
@@ -151,7 +137,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(L_THREADS, 1)
         for (int kc = 0; kc < kchunks; ++kc, ++it) {
           const int s = it % L_ST;
           const uint32_t ph = (it / L_ST) & 1;
-          if (!mbar_wait(smem_u32(&full[s]), ph, WAIT_NS) || !mbar_wait_cluster(smem_u32(&pfull[s]), ph, WAIT_NS)) {
+          if (!mbar_wait(smem_u32(&full[s]), ph, WAIT_NS)) {
             record_timeout(p.err, 4);
             ok = false;
             break;
@@ -305,9 +291,9 @@ __global__ void __launch_bounds__(256) tc_combine_kernel(const float* __restrict
 // epilogue works on block j+1.  Every output element has one owner: deterministic.
 constexpr int G_XT = 128;                  // X rows per pair (64 per CTA)
 constexpr int G_YB = 256;                  // stream rows per block (128 per CTA)
-constexpr int G_ST = 4;                    // Y stages of 16 KB
+constexpr int G_ST = 6;                    // Y stages of 16 KB
 constexpr int G_STAGE = 16384;
-constexpr int G_DZ = G_YB * 128;           // one dz buffer: 256 K-rows x 64 bf16 = 32 KB
+constexpr int G_DZ = G_YB * 128;           // the dz buffer: 256 K-rows x 64 bf16 = 32 KB
 constexpr int G_THREADS = 192;
 
 struct GradParams {
@@ -322,7 +308,7 @@ struct GradParams {
 };
 
 __host__ __device__ constexpr int grad_smem_bytes(int C) {
-  return (G_XT / 2) * C * 2 + G_ST * G_STAGE + 2 * G_DZ + 1024;
+  return (G_XT / 2) * C * 2 + G_ST * G_STAGE + G_DZ + 1024;
 }
 
 template <bool DW>
@@ -335,9 +321,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
   const int NCH = p.C / 256;                // 256-row C chunks of acc^T
   uint8_t* sX = smem;                       // [KC][64 rows][128 B]
   uint8_t* sY = smem + (G_XT / 2) * p.C * 2;
-  uint8_t* sDZ = sY + G_ST * G_STAGE;       // [2][256 rows][128 B]
-  __shared__ __align__(8) uint64_t full[G_ST], pfull[G_ST], empty[G_ST];
-  __shared__ __align__(8) uint64_t x_full, x_pfull, s_full, s_empty, dz_full[2], dz_empty[2], acc_full, drain_bar;
+  uint8_t* sDZ = sY + G_ST * G_STAGE;       // [256 rows][128 B]
+  __shared__ __align__(8) uint64_t full[G_ST], empty[G_ST];
+  __shared__ __align__(8) uint64_t x_full, s_full, s_empty, dz_full, dz_empty, acc_full, drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int epi_abort;
   __shared__ float col_lse2[G_XT];          // dh pass: per-column (token) lse * log2(e)
@@ -353,17 +339,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < G_ST; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&pfull[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
     mbar_init(smem_u32(&x_full), 1);
-    mbar_init(smem_u32(&x_pfull), 1);
     mbar_init(smem_u32(&s_full), 1);
     mbar_init(smem_u32(&s_empty), 2);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&dz_full[b]), 2 * 128);
-      mbar_init(smem_u32(&dz_empty[b]), 1);
-    }
+    mbar_init(smem_u32(&dz_full), 2 * 128);
+    mbar_init(smem_u32(&dz_empty), 1);
     mbar_init(smem_u32(&acc_full), 1);
     mbar_init(smem_u32(&drain_bar), 1);
     epi_abort = 0;
@@ -399,9 +381,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       tma_prefetch_desc(&tmX);
       tma_prefetch_desc(&tmYs);
       tma_prefetch_desc(&tmYa);
-      mbar_expect_tx(smem_u32(&x_full), (G_XT / 2) * p.C * 2);
+      // both CTAs' loads complete on the leader's barriers, which expect both halves' bytes
+      const uint32_t lead_x = mapa(smem_u32(&x_full), 0);
+      const uint32_t lead_full = mapa(smem_u32(&full[0]), 0);
+      if (rank == 0) mbar_expect_tx(smem_u32(&x_full), 2 * (G_XT / 2) * p.C * 2);
       for (int kc = 0; kc < KC; ++kc)
-        tma_load_2d(smem_u32(sX) + kc * 8192, &tmX, smem_u32(&x_full), kc * 64, x0 + (int)rank * 64);
+        tma_load_2d_cg2(smem_u32(sX) + kc * 8192, &tmX, lead_x, kc * 64, x0 + (int)rank * 64);
       int it = 0;
       bool ok = true;
       for (int j = 0; j <= nblk && ok; ++j) {
@@ -414,50 +399,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             break;
           }
           const uint32_t dst = smem_u32(sY) + s * G_STAGE;
-          const uint32_t bar = smem_u32(&full[s]);
-          mbar_expect_tx(bar, G_STAGE);
+          const uint32_t bar = lead_full + s * 8;
+          if (rank == 0) mbar_expect_tx(smem_u32(&full[s]), 2 * G_STAGE);
           if (j < nblk && u < KC) {
             // S phase of block j: my 128 stream rows x C chunk u
-            tma_load_2d(dst, &tmYs, bar, u * 64, j * G_YB + (int)rank * 128);
+            tma_load_2d_cg2(dst, &tmYs, bar, u * 64, j * G_YB + (int)rank * 128);
           } else {
             // accumulation phase of block j-1: 64 stream rows (sub-step q) x my 128 C of chunk i
             const int v = u - (j < nblk ? KC : 0);
             const int i = v >> 2, q = v & 3;
             const int row = (j - 1) * G_YB + q * 64;
             const int col = i * 256 + (int)rank * 128;
-            tma_load_2d(dst, &tmYa, bar, col, row);
-            tma_load_2d(dst + 8192, &tmYa, bar, col + 64, row);
+            tma_load_2d_cg2(dst, &tmYa, bar, col, row);
+            tma_load_2d_cg2(dst + 8192, &tmYa, bar, col + 64, row);
           }
         }
       }
     }
   } else if (warp == 1) {
     if (rank == 1) {
-      // ---------------- forwarder (peer CTA) ----------------
-      if (lane == 0) {
-        const uint32_t lp = mapa(smem_u32(&pfull[0]), 0);
-        bool ok = mbar_wait(smem_u32(&x_full), 0, WAIT_NS);
-        if (!ok) record_timeout(p.err, 18);
-        else mbar_arrive_cluster(mapa(smem_u32(&x_pfull), 0));
-        int it = 0;
-        for (int j = 0; j <= nblk && ok; ++j) {
-          const int nst = (j < nblk ? KC : 0) + (j >= 1 ? NCH * 4 : 0);
-          for (int u = 0; u < nst; ++u, ++it) {
-            const int s = it % G_ST;
-            if (!mbar_wait(smem_u32(&full[s]), (it / G_ST) & 1, WAIT_NS)) {
-              record_timeout(p.err, 19);
-              ok = false;
-              break;
-            }
-            mbar_arrive_cluster(lp + s * 8);
-          }
-        }
-      }
+      // the peer CTA issues nothing: its TMA loads complete on the leader's barriers
     } else if (lane == 0) {
       // ---------------- MMA issuer (leader CTA) ----------------
       const uint32_t idS = idesc_bf16(256, G_XT, 0, 0);
       const uint32_t idA = idesc_bf16(256, G_XT, 1, 1);
-      bool ok = mbar_wait(smem_u32(&x_full), 0, WAIT_NS) && mbar_wait_cluster(smem_u32(&x_pfull), 0, WAIT_NS);
+      bool ok = mbar_wait(smem_u32(&x_full), 0, WAIT_NS);
       if (!ok) record_timeout(p.err, 20);
       int it = 0;
       for (int j = 0; j <= nblk && ok; ++j) {
@@ -472,7 +438,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           for (int kc = 0; kc < KC; ++kc, ++it) {
             const int s = it % G_ST;
             const uint32_t ph = (it / G_ST) & 1;
-            if (!mbar_wait(smem_u32(&full[s]), ph, WAIT_NS) || !mbar_wait_cluster(smem_u32(&pfull[s]), ph, WAIT_NS)) {
+            if (!mbar_wait(smem_u32(&full[s]), ph, WAIT_NS)) {
               record_timeout(p.err, 22);
               ok = false;
               break;
@@ -491,20 +457,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         }
         if (j >= 1) {
           // accumulation of block j-1 with its dz
-          const int jb = j - 1, db = jb & 1;
-          if (!mbar_wait_cluster(smem_u32(&dz_full[db]), (jb >> 1) & 1, WAIT_NS)) {
+          const int jb = j - 1;
+          if (!mbar_wait_cluster(smem_u32(&dz_full), jb & 1, WAIT_NS)) {
             record_timeout(p.err, 23);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t dzb = smem_u32(sDZ) + db * G_DZ;
+          const uint32_t dzb = smem_u32(sDZ);
           for (int i = 0; i < NCH && ok; ++i)
             for (int q = 0; q < 4; ++q, ++it) {
               const int s = it % G_ST;
               const uint32_t ph = (it / G_ST) & 1;
-              if (!mbar_wait(smem_u32(&full[s]), ph, WAIT_NS) ||
-                  !mbar_wait_cluster(smem_u32(&pfull[s]), ph, WAIT_NS)) {
+              if (!mbar_wait(smem_u32(&full[s]), ph, WAIT_NS)) {
                 record_timeout(p.err, 24);
                 ok = false;
                 break;
@@ -518,7 +483,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
               mma_commit_mc2(smem_u32(&empty[s]), 3);
             }
           if (!ok) break;
-          mma_commit_mc2(smem_u32(&dz_empty[db]), 3);
+          mma_commit_mc2(smem_u32(&dz_empty), 3);
           if (jb == nblk - 1) mma_commit_mc2(smem_u32(&acc_full), 3);
         }
       }
@@ -535,7 +500,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     const float s = p.acc->scale;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const uint32_t leader_s_empty = mapa(smem_u32(&s_empty), 0);
-    const uint32_t leader_dz_full = mapa(smem_u32(&dz_full[0]), 0);
+    const uint32_t leader_dz_full = mapa(smem_u32(&dz_full), 0);
     const uint32_t dz_local = smem_u32(sDZ);
     const uint32_t dz_peer = mapa(dz_local, rank ^ 1);
     bool alive = true;
@@ -594,15 +559,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         __nv_bfloat162 pr = __floats2bfloat162_rn(d0, d1);
         packed[x / 2] = *reinterpret_cast<uint32_t*>(&pr);
       }
-      const int db = j & 1;
-      if (!mbar_wait(smem_u32(&dz_empty[db]), ((j >> 1) & 1) ^ 1, WAIT_NS)) {
+      // the single dz buffer is free once the accumulation of block j-1 has completed
+      if (!mbar_wait(smem_u32(&dz_empty), (j & 1) ^ 1, WAIT_NS)) {
         record_timeout(p.err, 26);
         epi_abort = 1;
       }
-      // columns [64d, 64d + 64) go to CTA d, at K-row kb of dz buffer db
+      // columns [64d, 64d + 64) go to CTA d, at K-row kb of the dz buffer
 #pragma unroll
       for (int d = 0; d < 2; ++d) {
-        const uint32_t base = (d == (int)rank ? dz_local : dz_peer) + db * G_DZ;
+        const uint32_t base = (d == (int)rank ? dz_local : dz_peer);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const uint32_t addr = base + sw128_offset(kb, c * 16);
@@ -618,7 +583,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         }
       }
       fence_proxy_async();
-      mbar_arrive_cluster(leader_dz_full + db * 8);
+      mbar_arrive_cluster(leader_dz_full);
     }
     // accumulator -> output
     if (alive) {

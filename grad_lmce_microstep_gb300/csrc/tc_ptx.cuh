@@ -118,6 +118,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, uint3
       : "memory");
 }
 
+// Pair form: the load lands in this CTA's shared memory but completes its bytes on an
+// mbarrier that may live in the peer CTA (shared::cluster address, e.g. from mapa), so both
+// CTAs of a pair can feed one barrier in the leader.
+__device__ __forceinline__ void tma_load_2d_cg2(uint32_t dst, const void* map, uint32_t bar_cluster, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+
 // ---- tcgen05 ----------------------------------------------------------------------------
 template <int CG>
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
