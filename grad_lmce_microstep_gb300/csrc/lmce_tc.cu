@@ -280,35 +280,48 @@ __global__ void __launch_bounds__(256) tc_combine_kernel(const float* __restrict
 // "X" rows and streams the other operand "Y" in blocks of 256 rows:
 //   dW pass: X = W (vocabulary rows), Y = h (tokens);  acc^T[c][v] = sum_n h[n][c] dz[n][v]
 //   dh pass: X = h (tokens), Y = W (vocabulary rows);   acc^T[c][n] = sum_v W[v][c] dz[n][v]
+// with dz[n][v] = s (softmax(z_n)[v] - [v == y_n]) ("How I trained my own GPT-2 124M",
+// section 4, differentiated; s from the gradient-accumulation normalisation).
 // Per block: S^T = Y_blk . X^T (cta_group::2, M = 256 stream rows, N = 128, K = C) lands in
-// TMEM; each epilogue thread owns one stream row, forms dz = s (exp(z - lse) - onehot) with
-// the logsumexp of pass 1 (0 on ignored rows), rounds it to bf16 and writes it, already in
-// the 128-byte-swizzled MN-major operand layout, half into its own CTA's shared memory
-// and half into the peer's (the N half each CTA supplies).  Then
+// TMEM; eight epilogue warps (two per TMEM lane quarter, one per half of the 128 columns)
+// form s*softmax = 2^(z log2 e + log2 s - lse log2 e) with one FFMA and one ex2 per
+// element, round to bf16 and write it, already in the 128-byte-swizzled MN-major operand
+// layout, into the CTA that supplies that half of N (its own or the peer's, over DSMEM).
+// The one-hot part is applied once per row: the dW pass fixes the target's element of its
+// row (from the target logit pass 1 kept), the dh pass subtracts s*W[y_n] when it writes dh.
 // acc^T[C x 128] += Y_blk^T . dz (cta_group::2, M = 256 C rows per chunk, K = 256 stream
-// rows) accumulates in TMEM for the whole stream.  The S tile of block j+1 is computed
-// while the epilogue turns block j into dz, and the accumulation of block j runs while the
-// epilogue works on block j+1.  Every output element has one owner: deterministic.
+// rows) accumulates in TMEM for the whole stream, one 64-row quarter of dz at a time as
+// soon as that quarter is written.  The S tile of block j+1 is computed while the epilogue
+// works on block j.  Every output element has one owner: deterministic.
 constexpr int G_XT = 128;                  // X rows per pair (64 per CTA)
 constexpr int G_YB = 256;                  // stream rows per block (128 per CTA)
-constexpr int G_ST = 6;                    // Y stages of 16 KB
-constexpr int G_STAGE = 16384;
+constexpr int G_ST = 8;                    // ring slots
+constexpr int G_SLOT = 24576;              // S stage: Y 128x64 (16 KB) + X 64x64 (8 KB); acc stage: Y 16 KB
+constexpr int G_SLOT_X = 16384;            // offset of the X chunk inside an S-stage slot
 constexpr int G_DZ = G_YB * 128;           // the dz buffer: 256 K-rows x 64 bf16 = 32 KB
-constexpr int G_THREADS = 192;
+constexpr int G_EPI_WARPS = 8;
+constexpr int G_THREADS = 64 + 32 * G_EPI_WARPS;
 
 struct GradParams {
   const int32_t* targets;
   const float* lse;
+  const float* zt;       // target logits (pass 1)
   const DevAcc* acc;     // scale of this micro-step
   unsigned* err;
   float* dW;             // dW pass output (fp32 [V, C])
   __nv_bfloat16* dh;     // dh pass output (bf16 [N, C])
+  const __nv_bfloat16* Wt;  // dh pass: W, for the one-hot term
   int N, V, C;
   int beta;              // dW pass: 0 writes, 1 adds
 };
 
 __host__ __device__ constexpr int grad_smem_bytes(int C) {
-  return (G_XT / 2) * C * 2 + G_ST * G_STAGE + G_DZ + 1024;
+  return G_ST * G_SLOT + G_DZ + 1024 + 0 * C;
+}
+
+__device__ __forceinline__ void st_shared_b16(uint32_t addr, uint16_t v, bool remote) {
+  if (remote) asm volatile("st.shared::cluster.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+  else asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
 template <bool DW>
@@ -319,14 +332,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int KC = p.C / 64;                  // 64-wide C chunks (S phase stages per block)
   const int NCH = p.C / 256;                // 256-row C chunks of acc^T
-  uint8_t* sX = smem;                       // [KC][64 rows][128 B]
-  uint8_t* sY = smem + (G_XT / 2) * p.C * 2;
-  uint8_t* sDZ = sY + G_ST * G_STAGE;       // [256 rows][128 B]
+  uint8_t* sY = smem;                       // ring of G_ST slots
+  uint8_t* sDZ = sY + G_ST * G_SLOT;        // [256 rows][128 B]
   __shared__ __align__(8) uint64_t full[G_ST], empty[G_ST];
-  __shared__ __align__(8) uint64_t x_full, s_full, s_empty, dz_full, dz_empty, acc_full, drain_bar;
+  __shared__ __align__(8) uint64_t s_full, s_empty, dz_full[4], dz_empty, acc_full, drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int epi_abort;
-  __shared__ float col_lse2[G_XT];          // dh pass: per-column (token) lse * log2(e)
+  __shared__ float col_c[G_XT];             // dh pass: per-column log2(s) - lse log2(e), or -inf
   __shared__ int col_y[G_XT];               // dh pass: per-column target (or -1: no gradient)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -335,16 +347,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
   const int nX = DW ? p.V : p.N;
   const int nY = DW ? p.N : p.V;
   const int nblk = (nY + G_YB - 1) / G_YB;
+  const float s = p.acc->scale;
+  const float log2s = log2f(s);             // -inf when s == 0: every dz is then 0
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < G_ST; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
+    for (int i = 0; i < G_ST; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), 1);
     }
-    mbar_init(smem_u32(&x_full), 1);
     mbar_init(smem_u32(&s_full), 1);
     mbar_init(smem_u32(&s_empty), 2);
-    mbar_init(smem_u32(&dz_full), 2 * 128);
+    for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&dz_full[q]), 4);
     mbar_init(smem_u32(&dz_empty), 1);
     mbar_init(smem_u32(&acc_full), 1);
     mbar_init(smem_u32(&drain_bar), 1);
@@ -354,16 +367,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
   if (!DW && threadIdx.x < G_XT) {
     const int n = x0 + threadIdx.x;
     int y = -1;
-    float l2 = 0.f;
+    float c = -INFINITY;
     if (n < p.N) {
       const int t = p.targets[n];
       if (t >= 0 && t < p.V) {
         y = t;
-        l2 = p.lse[n] * LOG2E;
+        c = log2s - p.lse[n] * LOG2E;
       }
     }
     col_y[threadIdx.x] = y;
-    col_lse2[threadIdx.x] = l2;
+    col_c[threadIdx.x] = c;
   }
   if (warp == 1) {
     tmem_alloc<2>(smem_u32(&tmem_base_sh), 512);
@@ -382,32 +395,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       tma_prefetch_desc(&tmYs);
       tma_prefetch_desc(&tmYa);
       // both CTAs' loads complete on the leader's barriers, which expect both halves' bytes
-      const uint32_t lead_x = mapa(smem_u32(&x_full), 0);
       const uint32_t lead_full = mapa(smem_u32(&full[0]), 0);
-      if (rank == 0) mbar_expect_tx(smem_u32(&x_full), 2 * (G_XT / 2) * p.C * 2);
-      for (int kc = 0; kc < KC; ++kc)
-        tma_load_2d_cg2(smem_u32(sX) + kc * 8192, &tmX, lead_x, kc * 64, x0 + (int)rank * 64);
       int it = 0;
       bool ok = true;
       for (int j = 0; j <= nblk && ok; ++j) {
         const int nst = (j < nblk ? KC : 0) + (j >= 1 ? NCH * 4 : 0);
         for (int u = 0; u < nst; ++u, ++it) {
-          const int s = it % G_ST;
-          if (!mbar_wait(smem_u32(&empty[s]), ((it / G_ST) & 1) ^ 1, WAIT_NS)) {
+          const int st = it % G_ST;
+          if (!mbar_wait(smem_u32(&empty[st]), ((it / G_ST) & 1) ^ 1, WAIT_NS)) {
             record_timeout(p.err, 17);
             ok = false;
             break;
           }
-          const uint32_t dst = smem_u32(sY) + s * G_STAGE;
-          const uint32_t bar = lead_full + s * 8;
-          if (rank == 0) mbar_expect_tx(smem_u32(&full[s]), 2 * G_STAGE);
+          const uint32_t dst = smem_u32(sY) + st * G_SLOT;
+          const uint32_t bar = lead_full + st * 8;
           if (j < nblk && u < KC) {
-            // S phase of block j: my 128 stream rows x C chunk u
+            // S phase of block j: my 128 stream rows and my 64 X rows, C chunk u
+            if (rank == 0) mbar_expect_tx(smem_u32(&full[st]), 2 * (16384 + 8192));
             tma_load_2d_cg2(dst, &tmYs, bar, u * 64, j * G_YB + (int)rank * 128);
+            tma_load_2d_cg2(dst + G_SLOT_X, &tmX, bar, u * 64, x0 + (int)rank * 64);
           } else {
-            // accumulation phase of block j-1: 64 stream rows (sub-step q) x my 128 C of chunk i
+            // accumulation phase of block j-1, quarter q (64 stream rows), my 128 C of chunk i
+            if (rank == 0) mbar_expect_tx(smem_u32(&full[st]), 2 * 16384);
             const int v = u - (j < nblk ? KC : 0);
-            const int i = v >> 2, q = v & 3;
+            const int q = v / NCH, i = v % NCH;
             const int row = (j - 1) * G_YB + q * 64;
             const int col = i * 256 + (int)rank * 128;
             tma_load_2d_cg2(dst, &tmYa, bar, col, row);
@@ -417,14 +428,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    if (rank == 1) {
-      // the peer CTA issues nothing: its TMA loads complete on the leader's barriers
-    } else if (lane == 0) {
-      // ---------------- MMA issuer (leader CTA) ----------------
+    if (rank == 0 && lane == 0) {
+      // ---------------- MMA issuer (leader CTA; the peer issues nothing) ----------------
       const uint32_t idS = idesc_bf16(256, G_XT, 0, 0);
       const uint32_t idA = idesc_bf16(256, G_XT, 1, 1);
-      bool ok = mbar_wait(smem_u32(&x_full), 0, WAIT_NS);
-      if (!ok) record_timeout(p.err, 20);
+      bool ok = true;
       int it = 0;
       for (int j = 0; j <= nblk && ok; ++j) {
         if (j < nblk) {
@@ -436,52 +444,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           }
           tc_fence_after();
           for (int kc = 0; kc < KC; ++kc, ++it) {
-            const int s = it % G_ST;
-            const uint32_t ph = (it / G_ST) & 1;
-            if (!mbar_wait(smem_u32(&full[s]), ph, WAIT_NS)) {
+            const int st = it % G_ST;
+            if (!mbar_wait(smem_u32(&full[st]), (it / G_ST) & 1, WAIT_NS)) {
               record_timeout(p.err, 22);
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t a = smem_u32(sY) + s * G_STAGE;
-            const uint32_t b = smem_u32(sX) + kc * 8192;
+            const uint32_t a = smem_u32(sY) + st * G_SLOT;
+            const uint32_t b = a + G_SLOT_X;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               mma_ss<2>(tS, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(b + k * 32, 16, 1024), idS,
                         (kc | k) != 0);
-            mma_commit_mc2(smem_u32(&empty[s]), 3);
+            mma_commit_mc2(smem_u32(&empty[st]), 3);
           }
           if (!ok) break;
           mma_commit_mc2(smem_u32(&s_full), 3);
         }
         if (j >= 1) {
-          // accumulation of block j-1 with its dz
+          // accumulation of block j-1, one 64-row quarter of dz at a time
           const int jb = j - 1;
-          if (!mbar_wait_cluster(smem_u32(&dz_full), jb & 1, WAIT_NS)) {
-            record_timeout(p.err, 23);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
           const uint32_t dzb = smem_u32(sDZ);
-          for (int i = 0; i < NCH && ok; ++i)
-            for (int q = 0; q < 4; ++q, ++it) {
-              const int s = it % G_ST;
-              const uint32_t ph = (it / G_ST) & 1;
-              if (!mbar_wait(smem_u32(&full[s]), ph, WAIT_NS)) {
+          for (int q = 0; q < 4 && ok; ++q) {
+            if (!mbar_wait_cluster(smem_u32(&dz_full[q]), jb & 1, WAIT_NS)) {
+              record_timeout(p.err, 23);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            for (int i = 0; i < NCH; ++i, ++it) {
+              const int st = it % G_ST;
+              if (!mbar_wait(smem_u32(&full[st]), (it / G_ST) & 1, WAIT_NS)) {
                 record_timeout(p.err, 24);
                 ok = false;
                 break;
               }
               tc_fence_after();
-              const uint32_t a = smem_u32(sY) + s * G_STAGE;
+              const uint32_t a = smem_u32(sY) + st * G_SLOT;
 #pragma unroll
               for (int k = 0; k < 4; ++k)
                 mma_ss<2>(tmem + i * 128, sdesc_sw128(a + k * 2048, 8192, 1024),
                           sdesc_sw128(dzb + q * 8192 + k * 2048, 32768, 1024), idA, (jb | q | k) != 0);
-              mma_commit_mc2(smem_u32(&empty[s]), 3);
+              mma_commit_mc2(smem_u32(&empty[st]), 3);
             }
+          }
           if (!ok) break;
           mma_commit_mc2(smem_u32(&dz_empty), 3);
           if (jb == nblk - 1) mma_commit_mc2(smem_u32(&acc_full), 3);
@@ -493,97 +500,101 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       }
     }
   } else {
-    // ---------------- epilogue: warps 2..5, one stream row per thread ----------------
+    // ---------------- epilogue: warps 2..9 ----------------
+    // warp -> (TMEM lane quarter q = warp % 4, column half hf); thread = one stream row
     const int q = warp & 3;
+    const int hf = (warp - 2) >> 2;
     const int kl = q * 32 + lane;                 // TMEM lane = my stream row in this CTA
     const int kb = (int)rank * 128 + kl;          // row within the 256-row block
-    const float s = p.acc->scale;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const uint32_t leader_s_empty = mapa(smem_u32(&s_empty), 0);
-    const uint32_t leader_dz_full = mapa(smem_u32(&dz_full), 0);
-    const uint32_t dz_local = smem_u32(sDZ);
-    const uint32_t dz_peer = mapa(dz_local, rank ^ 1);
+    const uint32_t leader_dz_full = mapa(smem_u32(&dz_full[0]), 0) + (uint32_t)(kb >> 6) * 8;
+    const bool remote = hf != (int)rank;         // column half hf is supplied by CTA hf
+    const uint32_t dz_dst = remote ? mapa(smem_u32(sDZ), (uint32_t)hf) : smem_u32(sDZ);
     bool alive = true;
     for (int j = 0; j < nblk; ++j) {
+      const int ys = j * G_YB + kb;               // my stream row
+      // dW pass: my token's target, logsumexp and target logit, loaded while S is computed
+      float crow = -INFINITY;                     // log2(s) - lse log2(e), -inf: no gradient
+      int xt = -1;                                // my target's column in this X tile
+      float fix = 0.f;                            // dz of that element: s (p_t - 1)
+      if (DW && ys < p.N) {
+        const int t = p.targets[ys];
+        if (t >= 0 && t < p.V) {
+          const float l2 = p.lse[ys] * LOG2E;
+          crow = log2s - l2;
+          if (t >= x0 && t < x0 + G_XT) {
+            xt = t - x0;
+            fix = s * (ex2_approx(fmaf(p.zt[ys], LOG2E, -l2)) - 1.f);
+          }
+        }
+      }
       if (!mbar_wait(smem_u32(&s_full), j & 1, WAIT_NS)) {
         record_timeout(p.err, 25);
         epi_abort = 1;
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      asm volatile("bar.sync 1, 256;" ::: "memory");
       if (epi_abort) { alive = false; break; }
       tc_fence_after();
-      float z[G_XT];
-#pragma unroll
-      for (int c = 0; c < G_XT / 32; ++c) {
+      float z[64];
+      {
         float v[32];
-        tmem_ld32(tS + lane_off + c * 32, v);
+        tmem_ld32(tS + lane_off + hf * 64, v);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) z[c * 32 + e] = v[e];
+        for (int e = 0; e < 32; ++e) z[e] = v[e];
+        tmem_ld32(tS + lane_off + hf * 64 + 32, v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) z[32 + e] = v[e];
       }
-      tmem_ld_wait();
       tc_fence_before();
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      asm volatile("bar.sync 1, 256;" ::: "memory");
       if (warp == 2 && lane == 0) {
         if (rank == 0) mbar_arrive(smem_u32(&s_empty));
         else mbar_arrive_cluster(leader_s_empty);
       }
-      // dz for my stream row
-      const int ys = j * G_YB + kb;                 // stream row index
-      int yrow = -1;                                // dW pass: my token's target
-      float lrow2 = 0.f;
-      if (DW) {
-        if (ys < p.N) {
-          const int t = p.targets[ys];
-          if (t >= 0 && t < p.V) {
-            yrow = t;
-            lrow2 = p.lse[ys] * LOG2E;
-          }
-        }
-      }
-      const bool row_ok = DW ? (yrow >= 0) : (ys < p.V);
-      uint32_t packed[G_XT / 2];
+      // s * softmax for my row and column half; rows past the stream end get 0 (dh pass:
+      // their W rows are zero-filled and contribute nothing)
+      uint32_t packed[32];
 #pragma unroll
-      for (int x = 0; x < G_XT; x += 2) {
-        float d0 = 0.f, d1 = 0.f;
-        if (row_ok) {
-          if (DW) {
-            const int v0 = x0 + x;
-            if (v0 < p.V) d0 = s * (exp2f(fmaf(z[x], LOG2E, -lrow2)) - (v0 == yrow ? 1.f : 0.f));
-            if (v0 + 1 < p.V) d1 = s * (exp2f(fmaf(z[x + 1], LOG2E, -lrow2)) - (v0 + 1 == yrow ? 1.f : 0.f));
-          } else {
-            if (col_y[x] >= 0) d0 = s * (exp2f(fmaf(z[x], LOG2E, -col_lse2[x])) - (ys == col_y[x] ? 1.f : 0.f));
-            if (col_y[x + 1] >= 0)
-              d1 = s * (exp2f(fmaf(z[x + 1], LOG2E, -col_lse2[x + 1])) - (ys == col_y[x + 1] ? 1.f : 0.f));
-          }
+      for (int e = 0; e < 64; e += 2) {
+        float c0, c1;
+        if (DW) {
+          c0 = crow;
+          c1 = crow;
+        } else {
+          c0 = col_c[hf * 64 + e];
+          c1 = col_c[hf * 64 + e + 1];
         }
+        const float d0 = ex2_approx(fmaf(z[e], LOG2E, c0));
+        const float d1 = ex2_approx(fmaf(z[e + 1], LOG2E, c1));
         __nv_bfloat162 pr = __floats2bfloat162_rn(d0, d1);
-        packed[x / 2] = *reinterpret_cast<uint32_t*>(&pr);
+        packed[e / 2] = *reinterpret_cast<uint32_t*>(&pr);
       }
-      // the single dz buffer is free once the accumulation of block j-1 has completed
+      // the dz buffer is free once the accumulation of block j-1 has completed
       if (!mbar_wait(smem_u32(&dz_empty), (j & 1) ^ 1, WAIT_NS)) {
         record_timeout(p.err, 26);
         epi_abort = 1;
       }
-      // columns [64d, 64d + 64) go to CTA d, at K-row kb of the dz buffer
 #pragma unroll
-      for (int d = 0; d < 2; ++d) {
-        const uint32_t base = (d == (int)rank ? dz_local : dz_peer);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t addr = base + sw128_offset(kb, c * 16);
-          const uint32_t* w = packed + d * 32 + c * 4;
-          if (d == (int)rank)
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-                         "r"(w[3])
-                         : "memory");
-          else
-            asm volatile("st.shared::cluster.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
-                         "r"(w[2]), "r"(w[3])
-                         : "memory");
-        }
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t addr = dz_dst + sw128_offset(kb, c * 16);
+        const uint32_t* w = packed + c * 4;
+        if (remote)
+          asm volatile("st.shared::cluster.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
+                       "r"(w[2]), "r"(w[3])
+                       : "memory");
+        else
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                       "r"(w[3])
+                       : "memory");
+      }
+      if (DW && xt >= hf * 64 && xt < hf * 64 + 64) {
+        __nv_bfloat16 fb = __float2bfloat16_rn(fix);
+        st_shared_b16(dz_dst + sw128_offset(kb, (xt - hf * 64) * 2), *reinterpret_cast<uint16_t*>(&fb), remote);
       }
       fence_proxy_async();
-      mbar_arrive_cluster(leader_dz_full);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(leader_dz_full);
     }
     // accumulator -> output
     if (alive) {
@@ -591,25 +602,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         record_timeout(p.err, 27);
         epi_abort = 1;
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      asm volatile("bar.sync 1, 256;" ::: "memory");
       if (!epi_abort) {
         tc_fence_after();
         for (int i = 0; i < NCH; ++i) {
           const int c = i * 256 + (int)rank * 128 + kl;   // my C row of the accumulator
 #pragma unroll 1
-          for (int cc = 0; cc < G_XT / 32; ++cc) {
+          for (int cc = 0; cc < 2; ++cc) {
             float v[32];
-            tmem_ld32(tmem + i * 128 + lane_off + cc * 32, v);
-            tmem_ld_wait();
+            tmem_ld32(tmem + i * 128 + lane_off + hf * 64 + cc * 32, v);
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              const int x = x0 + cc * 32 + e;
+              const int xl = hf * 64 + cc * 32 + e;
+              const int x = x0 + xl;
               if (x < nX) {
                 if (DW) {
                   float* o = p.dW + (size_t)x * p.C + c;
                   *o = p.beta ? (*o + v[e]) : v[e];
                 } else {
-                  p.dh[(size_t)x * p.C + c] = __float2bfloat16_rn(v[e]);
+                  float val = v[e];
+                  const int y = col_y[xl];
+                  if (y >= 0) val -= s * __bfloat162float(p.Wt[(size_t)y * p.C + c]);
+                  p.dh[(size_t)x * p.C + c] = __float2bfloat16_rn(val);
                 }
               }
             }
@@ -742,8 +756,10 @@ cudaError_t tc_grad(const StepArgs& a, const Scratch& sc, Launch& L) {
   GradParams p;
   p.targets = a.targets;
   p.lse = sc.lse;
+  p.zt = sc.tc_zt;
   p.acc = sc.acc;
   p.err = &sc.acc->err;
+  p.Wt = static_cast<const __nv_bfloat16*>(a.W);
   p.dW = a.dW;
   p.dh = static_cast<__nv_bfloat16*>(a.dh);
   p.N = (int)a.N;

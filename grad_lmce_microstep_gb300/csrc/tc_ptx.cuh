@@ -208,6 +208,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 2^x with the hardware approximation (ex2.approx.ftz: relative error ~2^-22, -inf -> +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---- descriptors ------------------------------------------------------------------------
 // Shared-memory matrix descriptor, 128-byte swizzle.  K-major operands: rows of 128 B
 // (64 bf16 along K), 8-row groups `sbo` bytes apart, `lbo` unused.  MN-major operands:
