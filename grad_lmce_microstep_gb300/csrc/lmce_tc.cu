@@ -30,10 +30,10 @@ constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s: any wait longer than this i
 // ---- pass 1 geometry -----------------------------------------------------------------
 constexpr int L_BM = 128;            // token rows per CTA (256 per pair)
 constexpr int L_BN = 128;            // vocab rows per CTA (256 per pair tile)
-constexpr int L_BK = 64;             // C per stage (one 128-byte swizzle atom)
-constexpr int L_ST = 6;              // stages
-constexpr int L_STAGE_A = L_BM * L_BK * 2;  // 16 KB
-constexpr int L_STAGE_B = L_BN * L_BK * 2;  // 16 KB
+constexpr int L_BK = 128;            // C per stage: two 64-column swizzle atoms, one 3D TMA box each side
+constexpr int L_ST = 3;              // stages
+constexpr int L_STAGE_A = L_BM * L_BK * 2;  // 32 KB
+constexpr int L_STAGE_B = L_BN * L_BK * 2;  // 32 KB
 constexpr int L_STAGE = L_STAGE_A + L_STAGE_B;
 constexpr int L_THREADS = 192;       // warp 0 TMA, warp 1 MMA / forwarder, warps 2-5 epilogue
 constexpr int L_SMEM = L_ST * L_STAGE + 1024;
@@ -112,8 +112,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(L_THREADS, 1)
           if (!mbar_wait(smem_u32(&empty[s]), ph, WAIT_NS)) { record_timeout(p.err, 1); ok = false; break; }
           const uint32_t a = smem_u32(smem + s * L_STAGE), b = a + L_STAGE_A;
           if (rank == 0) mbar_expect_tx(smem_u32(&full[s]), 2 * L_STAGE);
-          tma_load_2d_cg2(a, &tmH, lead_full + s * 8, kc * L_BK, hrow);
-          tma_load_2d_cg2(b, &tmW, lead_full + s * 8, kc * L_BK, wrow);
+          tma_load_3d_cg2(a, &tmH, lead_full + s * 8, 0, hrow, kc * 2);
+          tma_load_3d_cg2(b, &tmW, lead_full + s * 8, 0, wrow, kc * 2);
         }
       }
     }
@@ -145,9 +145,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(L_THREADS, 1)
           tc_fence_after();
           const uint32_t a = smem_u32(smem + s * L_STAGE), bb = a + L_STAGE_A;
 #pragma unroll
-          for (int k = 0; k < L_BK / 16; ++k)
-            mma_ss<2>(d, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(bb + k * 32, 16, 1024), idesc,
-                      (kc | k) != 0);
+          for (int k = 0; k < L_BK / 16; ++k) {
+            const uint32_t off = (k >> 2) * (L_BM * 128) + (k & 3) * 32;  // atom (64 columns), then 16-column step
+            mma_ss<2>(d, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(bb + off, 16, 1024), idesc, (kc | k) != 0);
+          }
           mma_commit_mc2(smem_u32(&empty[s]), 3);
         }
         if (ok) mma_commit_mc2(smem_u32(&acc_full[b]), 3);
@@ -295,10 +296,11 @@ __global__ void __launch_bounds__(256) tc_combine_kernel(const float* __restrict
 // works on block j.  Every output element has one owner: deterministic.
 constexpr int G_XT = 128;                  // X rows per pair (64 per CTA)
 constexpr int G_YB = 256;                  // stream rows per block (128 per CTA)
-constexpr int G_ST = 8;                    // ring slots
-constexpr int G_SLOT = 24576;              // S stage: Y 128x64 (16 KB) + X 64x64 (8 KB); acc stage: Y 16 KB
-constexpr int G_SLOT_X = 16384;            // offset of the X chunk inside an S-stage slot
-constexpr int G_DZ = G_YB * 128;           // the dz buffer: 256 K-rows x 64 bf16 = 32 KB
+constexpr int G_ST = 3;                    // ring slots
+constexpr int G_SLOT = 49152;              // S stage: Y 128 rows x 128 C (32 KB) + X 64 x 128 (16 KB);
+                                           // accumulation stage: Y 64 rows x 128 C for every chunk (<= 48 KB)
+constexpr int G_SLOT_X = 32768;            // offset of the X box inside an S-stage slot
+constexpr int G_DZ = G_YB * 128;           // one dz buffer: 256 K-rows x 64 bf16 = 32 KB (two of them)
 constexpr int G_EPI_WARPS = 8;
 constexpr int G_THREADS = 64 + 32 * G_EPI_WARPS;
 
@@ -316,7 +318,7 @@ struct GradParams {
 };
 
 __host__ __device__ constexpr int grad_smem_bytes(int C) {
-  return G_ST * G_SLOT + G_DZ + 1024 + 0 * C;
+  return G_ST * G_SLOT + 2 * G_DZ + 1024 + 0 * C;
 }
 
 __device__ __forceinline__ void st_shared_b16(uint32_t addr, uint16_t v, bool remote) {
@@ -330,12 +332,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
                    const __grid_constant__ CUtensorMap tmYa, GradParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int KC = p.C / 64;                  // 64-wide C chunks (S phase stages per block)
+  const int KC = p.C / 128;                 // S phase stages per block (128 C each)
   const int NCH = p.C / 256;                // 256-row C chunks of acc^T
   uint8_t* sY = smem;                       // ring of G_ST slots
-  uint8_t* sDZ = sY + G_ST * G_SLOT;        // [256 rows][128 B]
+  uint8_t* sDZ = sY + G_ST * G_SLOT;        // [2][256 rows][128 B]
   __shared__ __align__(8) uint64_t full[G_ST], empty[G_ST];
-  __shared__ __align__(8) uint64_t s_full, s_empty, dz_full[4], dz_empty, acc_full, drain_bar;
+  __shared__ __align__(8) uint64_t s_full, s_empty, dz_full[2][4], dz_empty[2], acc_full, drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int epi_abort;
   __shared__ float col_c[G_XT];             // dh pass: per-column log2(s) - lse log2(e), or -inf
@@ -357,8 +359,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     }
     mbar_init(smem_u32(&s_full), 1);
     mbar_init(smem_u32(&s_empty), 2);
-    for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&dz_full[q]), 4);
-    mbar_init(smem_u32(&dz_empty), 1);
+    for (int b = 0; b < 2; ++b) {
+      for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&dz_full[b][q]), 4);
+      mbar_init(smem_u32(&dz_empty[b]), 1);
+    }
     mbar_init(smem_u32(&acc_full), 1);
     mbar_init(smem_u32(&drain_bar), 1);
     epi_abort = 0;
@@ -399,7 +403,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       int it = 0;
       bool ok = true;
       for (int j = 0; j <= nblk && ok; ++j) {
-        const int nst = (j < nblk ? KC : 0) + (j >= 1 ? NCH * 4 : 0);
+        const int nst = (j < nblk ? KC : 0) + (j >= 1 ? 4 : 0);
         for (int u = 0; u < nst; ++u, ++it) {
           const int st = it % G_ST;
           if (!mbar_wait(smem_u32(&empty[st]), ((it / G_ST) & 1) ^ 1, WAIT_NS)) {
@@ -410,19 +414,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           const uint32_t dst = smem_u32(sY) + st * G_SLOT;
           const uint32_t bar = lead_full + st * 8;
           if (j < nblk && u < KC) {
-            // S phase of block j: my 128 stream rows and my 64 X rows, C chunk u
-            if (rank == 0) mbar_expect_tx(smem_u32(&full[st]), 2 * (16384 + 8192));
-            tma_load_2d_cg2(dst, &tmYs, bar, u * 64, j * G_YB + (int)rank * 128);
-            tma_load_2d_cg2(dst + G_SLOT_X, &tmX, bar, u * 64, x0 + (int)rank * 64);
+            // S phase of block j: my 128 stream rows and my 64 X rows, C columns [128u, 128u + 128)
+            if (rank == 0) mbar_expect_tx(smem_u32(&full[st]), 2 * (32768 + 16384));
+            tma_load_3d_cg2(dst, &tmYs, bar, 0, j * G_YB + (int)rank * 128, u * 2);
+            tma_load_3d_cg2(dst + G_SLOT_X, &tmX, bar, 0, x0 + (int)rank * 64, u * 2);
           } else {
-            // accumulation phase of block j-1, quarter q (64 stream rows), my 128 C of chunk i
-            if (rank == 0) mbar_expect_tx(smem_u32(&full[st]), 2 * 16384);
-            const int v = u - (j < nblk ? KC : 0);
-            const int q = v / NCH, i = v % NCH;
+            // accumulation phase of block j-1, quarter q (64 stream rows): my 128 C of every chunk
+            if (rank == 0) mbar_expect_tx(smem_u32(&full[st]), 2 * 16384 * NCH);
+            const int q = u - (j < nblk ? KC : 0);
             const int row = (j - 1) * G_YB + q * 64;
-            const int col = i * 256 + (int)rank * 128;
-            tma_load_2d_cg2(dst, &tmYa, bar, col, row);
-            tma_load_2d_cg2(dst + 8192, &tmYa, bar, col + 64, row);
+            for (int i = 0; i < NCH; ++i)
+              tma_load_3d_cg2(dst + i * 16384, &tmYa, bar, 0, row, (i * 256 + (int)rank * 128) / 64);
           }
         }
       }
@@ -454,9 +456,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             const uint32_t a = smem_u32(sY) + st * G_SLOT;
             const uint32_t b = a + G_SLOT_X;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_ss<2>(tS, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(b + k * 32, 16, 1024), idS,
-                        (kc | k) != 0);
+            for (int k = 0; k < 8; ++k)
+              mma_ss<2>(tS, sdesc_sw128(a + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
+                        sdesc_sw128(b + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), idS, (kc | k) != 0);
             mma_commit_mc2(smem_u32(&empty[st]), 3);
           }
           if (!ok) break;
@@ -464,33 +466,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         }
         if (j >= 1) {
           // accumulation of block j-1, one 64-row quarter of dz at a time
-          const int jb = j - 1;
-          const uint32_t dzb = smem_u32(sDZ);
+          const int jb = j - 1, db = jb & 1;
+          const uint32_t dzb = smem_u32(sDZ) + db * G_DZ;
           for (int q = 0; q < 4 && ok; ++q) {
-            if (!mbar_wait_cluster(smem_u32(&dz_full[q]), jb & 1, WAIT_NS)) {
+            if (!mbar_wait_cluster(smem_u32(&dz_full[db][q]), (jb >> 1) & 1, WAIT_NS)) {
               record_timeout(p.err, 23);
               ok = false;
               break;
             }
+            const int st = it % G_ST;
+            if (!mbar_wait(smem_u32(&full[st]), (it / G_ST) & 1, WAIT_NS)) {
+              record_timeout(p.err, 24);
+              ok = false;
+              break;
+            }
+            ++it;
             tc_fence_after();
-            for (int i = 0; i < NCH; ++i, ++it) {
-              const int st = it % G_ST;
-              if (!mbar_wait(smem_u32(&full[st]), (it / G_ST) & 1, WAIT_NS)) {
-                record_timeout(p.err, 24);
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              const uint32_t a = smem_u32(sY) + st * G_SLOT;
+            const uint32_t a = smem_u32(sY) + st * G_SLOT;
+            for (int i = 0; i < NCH; ++i) {
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                mma_ss<2>(tmem + i * 128, sdesc_sw128(a + k * 2048, 8192, 1024),
+                mma_ss<2>(tmem + i * 128, sdesc_sw128(a + i * 16384 + k * 2048, 8192, 1024),
                           sdesc_sw128(dzb + q * 8192 + k * 2048, 32768, 1024), idA, (jb | q | k) != 0);
-              mma_commit_mc2(smem_u32(&empty[st]), 3);
             }
+            mma_commit_mc2(smem_u32(&empty[st]), 3);
           }
           if (!ok) break;
-          mma_commit_mc2(smem_u32(&dz_empty), 3);
+          mma_commit_mc2(smem_u32(&dz_empty[db]), 3);
           if (jb == nblk - 1) mma_commit_mc2(smem_u32(&acc_full), 3);
         }
       }
@@ -508,7 +510,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     const int kb = (int)rank * 128 + kl;          // row within the 256-row block
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const uint32_t leader_s_empty = mapa(smem_u32(&s_empty), 0);
-    const uint32_t leader_dz_full = mapa(smem_u32(&dz_full[0]), 0) + (uint32_t)(kb >> 6) * 8;
+    const uint32_t leader_dz_full = mapa(smem_u32(&dz_full[0][0]), 0) + (uint32_t)(kb >> 6) * 8;
     const bool remote = hf != (int)rank;         // column half hf is supplied by CTA hf
     const uint32_t dz_dst = remote ? mapa(smem_u32(sDZ), (uint32_t)hf) : smem_u32(sDZ);
     bool alive = true;
@@ -570,14 +572,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         __nv_bfloat162 pr = __floats2bfloat162_rn(d0, d1);
         packed[e / 2] = *reinterpret_cast<uint32_t*>(&pr);
       }
-      // the dz buffer is free once the accumulation of block j-1 has completed
-      if (!mbar_wait(smem_u32(&dz_empty), (j & 1) ^ 1, WAIT_NS)) {
+      // dz buffer j&1 is free once the accumulation of block j-2 has completed
+      const int db = j & 1;
+      if (!mbar_wait(smem_u32(&dz_empty[db]), ((j >> 1) & 1) ^ 1, WAIT_NS)) {
         record_timeout(p.err, 26);
         epi_abort = 1;
       }
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const uint32_t addr = dz_dst + sw128_offset(kb, c * 16);
+        const uint32_t addr = dz_dst + db * G_DZ + sw128_offset(kb, c * 16);
         const uint32_t* w = packed + c * 4;
         if (remote)
           asm volatile("st.shared::cluster.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
@@ -590,11 +593,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       }
       if (DW && xt >= hf * 64 && xt < hf * 64 + 64) {
         __nv_bfloat16 fb = __float2bfloat16_rn(fix);
-        st_shared_b16(dz_dst + sw128_offset(kb, (xt - hf * 64) * 2), *reinterpret_cast<uint16_t*>(&fb), remote);
+        st_shared_b16(dz_dst + db * G_DZ + sw128_offset(kb, (xt - hf * 64) * 2), *reinterpret_cast<uint16_t*>(&fb),
+                      remote);
       }
-      fence_proxy_async();
+      if (remote) fence_proxy_async();
+      else fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(leader_dz_full);
+      if (lane == 0) mbar_arrive_cluster(leader_dz_full + db * 32);
     }
     // accumulator -> output
     if (alive) {
@@ -656,15 +661,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 matrix [rows, cols] row-major; box {64 cols, box_rows}, 128-byte swizzle, zero fill.
-bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// The same matrix seen as [cols/64][rows][64]: box {64, box_rows, box_chunks} loads box_chunks
+// consecutive 64-column swizzle atoms of box_rows rows in one instruction.
+bool make_map3(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_chunks) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+  cuuint64_t dims[3] = {64, rows, cols / 64};
+  cuuint64_t strides[2] = {cols * 2, 128};
+  cuuint32_t box[3] = {64, box_rows, box_chunks};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -708,8 +714,8 @@ int64_t tc_parts(int64_t N) { return (N + 255) / 256; }
 
 cudaError_t tc_lse(const StepArgs& a, const Scratch& sc, Launch& L) {
   CUtensorMap mh, mw;
-  if (!make_map(&mh, a.hidden, (uint64_t)a.N, (uint64_t)a.C, L_BM) ||
-      !make_map(&mw, a.W, (uint64_t)a.V, (uint64_t)a.C, L_BN))
+  if (!make_map3(&mh, a.hidden, (uint64_t)a.N, (uint64_t)a.C, L_BM, 2) ||
+      !make_map3(&mw, a.W, (uint64_t)a.V, (uint64_t)a.C, L_BN, 2))
     return cudaErrorInvalidValue;
   const int nblocks = (int)((a.N + 255) / 256);
   const int vtiles = (int)((a.V + 255) / 256);
@@ -750,8 +756,8 @@ cudaError_t tc_grad(const StepArgs& a, const Scratch& sc, Launch& L) {
   const void* Y = DW ? a.hidden : a.W;
   const int64_t nX = DW ? a.V : a.N, nY = DW ? a.N : a.V;
   CUtensorMap mx, mys, mya;
-  if (!make_map(&mx, X, (uint64_t)nX, (uint64_t)a.C, G_XT / 2) ||
-      !make_map(&mys, Y, (uint64_t)nY, (uint64_t)a.C, 128) || !make_map(&mya, Y, (uint64_t)nY, (uint64_t)a.C, 64))
+  if (!make_map3(&mx, X, (uint64_t)nX, (uint64_t)a.C, G_XT / 2, 2) ||
+      !make_map3(&mys, Y, (uint64_t)nY, (uint64_t)a.C, 128, 2) || !make_map3(&mya, Y, (uint64_t)nY, (uint64_t)a.C, 64, 2))
     return cudaErrorInvalidValue;
   GradParams p;
   p.targets = a.targets;

@@ -128,6 +128,14 @@ __device__ __forceinline__ void tma_load_2d_cg2(uint32_t dst, const void* map, u
       : "memory");
 }
 
+// 3D form of the pair load (box {64 columns, rows, chunks} of a [chunks][rows][64] view).
+__device__ __forceinline__ void tma_load_3d_cg2(uint32_t dst, const void* map, uint32_t bar_cluster, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 // ---- tcgen05 ----------------------------------------------------------------------------
 template <int CG>
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
