@@ -35,7 +35,7 @@ constexpr int L_ST = 3;              // stages
 constexpr int L_STAGE_A = L_BM * L_BK * 2;  // 32 KB
 constexpr int L_STAGE_B = L_BN * L_BK * 2;  // 32 KB
 constexpr int L_STAGE = L_STAGE_A + L_STAGE_B;
-constexpr int L_THREADS = 192;       // warp 0 TMA, warp 1 MMA / forwarder, warps 2-5 epilogue
+constexpr int L_THREADS = 320;       // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue (two per lane quarter)
 constexpr int L_SMEM = L_ST * L_STAGE + 1024;
 
 struct LseParams {
@@ -63,6 +63,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(L_THREADS, 1)
   __shared__ uint32_t tmem_base_sh;
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ volatile int epi_abort;
+  __shared__ float half_m[L_BM], half_l[L_BM];   // second column half's (max, sum) per row
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -96,25 +97,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(L_THREADS, 1)
   const uint32_t tmem = tmem_base_sh;
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer: lane 0 waits and arms the barrier, lanes 0 and 1 each
+    // issue one 32 KB box (separate lanes overlap their issue cost) ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tmH);
       tma_prefetch_desc(&tmW);
-      const int hrow = nb * 256 + (int)rank * L_BM;
-      const uint32_t lead_full = mapa(smem_u32(&full[0]), 0);  // both halves land on the leader's barrier
-      int it = 0;
-      bool ok = true;
-      for (int t = 0; t < ntiles && ok; ++t) {
-        const int wrow = (t_begin + t) * 256 + (int)rank * L_BN;
-        for (int kc = 0; kc < kchunks; ++kc, ++it) {
-          const int s = it % L_ST;
-          const uint32_t ph = ((it / L_ST) & 1) ^ 1;
-          if (!mbar_wait(smem_u32(&empty[s]), ph, WAIT_NS)) { record_timeout(p.err, 1); ok = false; break; }
-          const uint32_t a = smem_u32(smem + s * L_STAGE), b = a + L_STAGE_A;
-          if (rank == 0) mbar_expect_tx(smem_u32(&full[s]), 2 * L_STAGE);
-          tma_load_3d_cg2(a, &tmH, lead_full + s * 8, 0, hrow, kc * 2);
-          tma_load_3d_cg2(b, &tmW, lead_full + s * 8, 0, wrow, kc * 2);
+    }
+    const int hrow = nb * 256 + (int)rank * L_BM;
+    const uint32_t lead_full = mapa(smem_u32(&full[0]), 0);  // both halves land on the leader's barrier
+    int it = 0;
+    bool ok = true;
+    for (int t = 0; t < ntiles && ok; ++t) {
+      const int wrow = (t_begin + t) * 256 + (int)rank * L_BN;
+      for (int kc = 0; kc < kchunks; ++kc, ++it) {
+        const int s = it % L_ST;
+        const uint32_t ph = ((it / L_ST) & 1) ^ 1;
+        bool w = true;
+        if (lane == 0) {
+          w = mbar_wait(smem_u32(&empty[s]), ph, WAIT_NS);
+          if (!w) record_timeout(p.err, 1);
+          else if (rank == 0) mbar_expect_tx(smem_u32(&full[s]), 2 * L_STAGE);
         }
+        if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+        const uint32_t a = smem_u32(smem + s * L_STAGE);
+        if (lane == 0) tma_load_3d_cg2(a, &tmH, lead_full + s * 8, 0, hrow, kc * 2);
+        else if (lane == 1) tma_load_3d_cg2(a + L_STAGE_A, &tmW, lead_full + s * 8, 0, wrow, kc * 2);
+        __syncwarp();
       }
     }
   } else if (warp == 1) {
@@ -160,9 +168,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(L_THREADS, 1)
       }
     }
   } else {
-    // ---------------- epilogue: warps 2..5, one token row per thread ----------------
+    // ---------------- epilogue: warps 2..9 ----------------
+    // warp -> TMEM lane quarter q (its token rows) and column half hf of every tile; each
+    // thread keeps a base-2 running (max, sum) of its row over its half of the columns.
     const int q = warp & 3;
-    const int row = (int)rank * L_BM + q * 32 + lane;
+    const int hf = (warp - 2) >> 2;
+    const int kl = q * 32 + lane;
+    const int row = (int)rank * L_BM + kl;
     const int n = nb * 256 + row;
     const int y = (n < p.N) ? p.targets[n] : p.ignore_id;
     float m2 = -INFINITY, l = 0.f;
@@ -173,42 +185,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(L_THREADS, 1)
         record_timeout(p.err, 5);
         epi_abort = 1;
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      asm volatile("bar.sync 1, 256;" ::: "memory");
       if (epi_abort) break;  // the same decision in every epilogue thread
       tc_fence_after();
-      const int v0 = (t_begin + t) * 256;
-      const uint32_t taddr = tmem + b * 256 + ((uint32_t)(q * 32) << 16);
+      const int c0 = (t_begin + t) * 256 + hf * 128;      // first vocabulary column of my half
+      const int tcol = y - c0;                            // my target's column in my half, if any
+      const bool full_half = c0 + 128 <= p.V;
+      const uint32_t taddr = tmem + b * 256 + hf * 128 + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         float v[32];
         tmem_ld32(taddr + c * 32, v);
-        tmem_ld_wait();
-        const int vb = v0 + c * 32;
-        float cm = -INFINITY;
+        if (tcol >= c * 32 && tcol < c * 32 + 32) {
+          float zv = 0.f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (vb + j < p.V) cm = fmaxf(cm, v[j]);
-          if (vb + j == y) p.zt[n] = v[j];
+          for (int j = 0; j < 32; ++j) zv = (tcol - c * 32 == j) ? v[j] : zv;
+          p.zt[n] = zv;
         }
+        if (!full_half) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (c0 + c * 32 + j >= p.V) v[j] = -INFINITY;
+        }
+        float cm = v[0];
+#pragma unroll
+        for (int j = 1; j < 32; ++j) cm = fmaxf(cm, v[j]);
         if (cm == -INFINITY) continue;
         const float mn = fmaxf(m2, cm * LOG2E);
-        float s = 0.f;
+        float sum = 0.f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (vb + j < p.V) s += exp2f(fmaf(v[j], LOG2E, -mn));
-        l = l * exp2f(m2 - mn) + s;
+        for (int j = 0; j < 32; ++j) sum += ex2_approx(fmaf(v[j], LOG2E, -mn));
+        l = l * ex2_approx(m2 - mn) + sum;
         m2 = mn;
       }
       tc_fence_before();
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      asm volatile("bar.sync 1, 256;" ::: "memory");
       if (warp == 2 && lane == 0) {
         if (rank == 0) mbar_arrive(smem_u32(&acc_empty[b]));
         else mbar_arrive_cluster(leader_acc_empty + b * 8);
       }
     }
-    if (n < p.N) {
-      p.part_m[(size_t)split * p.N + n] = m2;
-      p.part_l[(size_t)split * p.N + n] = l;
+    // merge the two column halves of every row, then write this slice's partial
+    if (hf == 1) {
+      half_m[kl] = m2;
+      half_l[kl] = l;
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (hf == 0 && n < p.N) {
+      const float mo = half_m[kl], lo = half_l[kl];
+      const float M = fmaxf(m2, mo);
+      const float L = (M == -INFINITY) ? 0.f : l * ex2_approx(m2 - M) + lo * ex2_approx(mo - M);
+      p.part_m[(size_t)split * p.N + n] = M;
+      p.part_l[(size_t)split * p.N + n] = L;
     }
   }
 
@@ -393,40 +421,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
   const uint32_t tS = tmem + NCH * 128;     // S^T columns after the accumulator chunks
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer: lane 0 waits and arms the barrier; each box of a
+    // stage is issued by its own lane so their issue costs overlap ----------------
     if (lane == 0) {
       tma_prefetch_desc(&tmX);
       tma_prefetch_desc(&tmYs);
       tma_prefetch_desc(&tmYa);
-      // both CTAs' loads complete on the leader's barriers, which expect both halves' bytes
-      const uint32_t lead_full = mapa(smem_u32(&full[0]), 0);
-      int it = 0;
-      bool ok = true;
-      for (int j = 0; j <= nblk && ok; ++j) {
-        const int nst = (j < nblk ? KC : 0) + (j >= 1 ? 4 : 0);
-        for (int u = 0; u < nst; ++u, ++it) {
-          const int st = it % G_ST;
-          if (!mbar_wait(smem_u32(&empty[st]), ((it / G_ST) & 1) ^ 1, WAIT_NS)) {
-            record_timeout(p.err, 17);
-            ok = false;
-            break;
-          }
-          const uint32_t dst = smem_u32(sY) + st * G_SLOT;
-          const uint32_t bar = lead_full + st * 8;
-          if (j < nblk && u < KC) {
-            // S phase of block j: my 128 stream rows and my 64 X rows, C columns [128u, 128u + 128)
-            if (rank == 0) mbar_expect_tx(smem_u32(&full[st]), 2 * (32768 + 16384));
-            tma_load_3d_cg2(dst, &tmYs, bar, 0, j * G_YB + (int)rank * 128, u * 2);
-            tma_load_3d_cg2(dst + G_SLOT_X, &tmX, bar, 0, x0 + (int)rank * 64, u * 2);
-          } else {
-            // accumulation phase of block j-1, quarter q (64 stream rows): my 128 C of every chunk
-            if (rank == 0) mbar_expect_tx(smem_u32(&full[st]), 2 * 16384 * NCH);
-            const int q = u - (j < nblk ? KC : 0);
-            const int row = (j - 1) * G_YB + q * 64;
-            for (int i = 0; i < NCH; ++i)
-              tma_load_3d_cg2(dst + i * 16384, &tmYa, bar, 0, row, (i * 256 + (int)rank * 128) / 64);
-          }
+    }
+    // both CTAs' loads complete on the leader's barriers, which expect both halves' bytes
+    const uint32_t lead_full = mapa(smem_u32(&full[0]), 0);
+    int it = 0;
+    bool ok = true;
+    for (int j = 0; j <= nblk && ok; ++j) {
+      const int nst = (j < nblk ? KC : 0) + (j >= 1 ? 4 : 0);
+      for (int u = 0; u < nst; ++u, ++it) {
+        const int st = it % G_ST;
+        const bool sphase = j < nblk && u < KC;
+        bool w = true;
+        if (lane == 0) {
+          w = mbar_wait(smem_u32(&empty[st]), ((it / G_ST) & 1) ^ 1, WAIT_NS);
+          if (!w) record_timeout(p.err, 17);
+          else if (rank == 0) mbar_expect_tx(smem_u32(&full[st]), sphase ? 2 * (32768 + 16384) : 2 * 16384 * NCH);
         }
+        if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+        const uint32_t dst = smem_u32(sY) + st * G_SLOT;
+        const uint32_t bar = lead_full + st * 8;
+        if (sphase) {
+          // S phase of block j: my 128 stream rows and my 64 X rows, C columns [128u, 128u + 128)
+          if (lane == 0) tma_load_3d_cg2(dst, &tmYs, bar, 0, j * G_YB + (int)rank * 128, u * 2);
+          else if (lane == 1) tma_load_3d_cg2(dst + G_SLOT_X, &tmX, bar, 0, x0 + (int)rank * 64, u * 2);
+        } else if (lane < NCH) {
+          // accumulation phase of block j-1, quarter q (64 stream rows): my 128 C of chunk `lane`
+          const int q = u - (j < nblk ? KC : 0);
+          const int row = (j - 1) * G_YB + q * 64;
+          tma_load_3d_cg2(dst + lane * 16384, &tmYa, bar, 0, row, (lane * 256 + (int)rank * 128) / 64);
+        }
+        __syncwarp();
       }
     }
   } else if (warp == 1) {
