@@ -45,6 +45,28 @@ def parse():
     return p.parse_args()
 
 
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the ncu summaries under profiles/, or None when the
+    kernel source changed since the counters were taken."""
+    import glob
+    import hashlib
+    import re
+
+    src = os.path.join(ROOT, "grad_lmce_microstep_gb300", "csrc", "lmce_tc.cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for f in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        txt = open(f).read()
+        m = re.search(r"traffic_bytes_per_launch:(.*)", txt)
+        h = re.search(r"sha256\[:16\] = ([0-9a-f]{16})", txt)
+        if not m or not h or h.group(1) != sha:
+            continue
+        for kv in m.group(1).split():
+            k, v = kv.split("=")
+            if k == kernel:
+                return int(v)
+    return None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -286,7 +308,7 @@ def run_lmce(args, rank, world, local_rank):
                          "peak_tflops": pk.get("bf16_tflops_sustained") or pk["bf16_tflops"],
                          "peak": f"bf16 sustained, {pk_kind}"},
         "roofline": {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": ncu_traffic(dom) if L.path == "tcgen05" else None,
                      "peak_source": ("bf16_tflops_sustained of " + pk_kind) if bound == "tensor"
                      else "fp32 FFMA: 152 SMs x 128 lanes x 2 flop x max SM clock"},
         "kernels_ms": {k: {"total_ms": v[0], "launches": v[1], "avg_ms": v[0] / v[1]} for k, v in kinds.items()},

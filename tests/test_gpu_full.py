@@ -1,0 +1,144 @@
+"""Parity at the full workload sizes, in the launch configuration bench.py times.
+
+The float64 oracle cannot run these workloads whole in seconds, so each test compares
+outputs it can compute one by one -- sampled rows of dh and of the per-row loss (each needs
+only that row's logits), sampled rows of dW (given the oracle's logsumexp of every row) --
+or uses special inputs with a closed form at full size (W = 0).  Tolerances are the
+method's: loss relative error <= 1e-3; dh, dW max abs error <= 2e-2 x max|oracle| (bf16).
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from grad_lmce_microstep_gb300 import inputs as I
+from grad_lmce_microstep_gb300 import lmce as M
+from oracle import lmce_oracle as O
+
+from gpu_util import GRAD_REL, LOSS_REL
+
+pytestmark = pytest.mark.gpu
+
+ROWS_PER_MICRO = 48
+DW_ROWS = 24
+
+
+def _run(w, W=None):
+    """Whole optimizer step on the GPU, keeping outputs on the device."""
+    Wd = (w.W if W is None else W).cuda()
+    mbs = [(h.cuda(), y.cuda()) for h, y in w.micro]
+    dW, dhs, rls, res = M.run_step(Wd, mbs, w.dtype, row_loss=True)
+    torch.cuda.synchronize()
+    return dW, dhs, rls, res
+
+
+def _sample_rows(w, k, rng, extra=()):
+    n = w.micro[k][1].numel()
+    rows = set(rng.choice(n, size=min(ROWS_PER_MICRO, n), replace=False).tolist())
+    rows.update(int(r) for r in extra if r < n)
+    return np.array(sorted(rows))
+
+
+def _check_rows(w, dhs, rls, scales, rng, extra=lambda k: ()):
+    Wf = O.f64(w.W)
+    for k, (h, y) in enumerate(w.micro):
+        rows = _sample_rows(w, k, rng, extra(k))
+        ti = torch.as_tensor(rows)
+        lse, rl, dh = O.row_outputs(h[ti], Wf, y[ti], scales[k], w.ignore_id)
+        got_dh = dhs[k][torch.as_tensor(rows, device="cuda")].double().cpu().numpy()
+        got_rl = rls[k][torch.as_tensor(rows, device="cuda")].double().cpu().numpy()
+        tol = GRAD_REL[w.dtype] * max(np.abs(dh).max(), 1e-30)
+        assert np.abs(got_dh - dh).max() <= tol, (k, np.abs(got_dh - dh).max() / max(np.abs(dh).max(), 1e-30))
+        assert np.abs(got_rl - rl).max() <= LOSS_REL * max(1.0, np.abs(rl).max())
+
+
+def _check_dW_rows(w, dW, scales, rng, lses, extra=()):
+    vs = sorted(set(rng.choice(w.V, size=DW_ROWS, replace=False).tolist()) | set(extra))
+    want = O.dW_rows(w.micro, w.W, lses, scales, vs, w.ignore_id)
+    got = dW[torch.as_tensor(vs, device="cuda")].double().cpu().numpy()
+    tol = GRAD_REL[w.dtype] * np.abs(want).max()
+    assert np.abs(got - want).max() <= tol, np.abs(got - want).max() / np.abs(want).max()
+
+
+def _oracle_totals(w):
+    lses = [O.lse_all(h, w.W) for h, _ in w.micro]
+    loss = 0.0
+    for (h, y), lse in zip(w.micro, lses):
+        valid, _ = O.target_status(y, w.V, w.ignore_id)
+        yy = O.i64(y)[valid]
+        z_t = np.einsum("nc,nc->n", O.f64(h)[valid], O.f64(w.W)[yy])
+        loss += float((lse[valid] - z_t).sum())
+    return lses, loss
+
+
+@pytest.mark.parametrize("name", ["gpt2_124m_head", "masked_unequal"])
+def test_full_size_head(name):
+    w = I.make(name)
+    rng = np.random.default_rng(7)
+    dW, dhs, rls, (ls, cnt, mean, st) = _run(w)
+    assert st == M.OK
+    counts = w.valid_counts()
+    assert cnt == sum(counts)
+    scales = O.micro_scales(counts, "global", w.G)
+    lses, loss = _oracle_totals(w)
+    assert abs(ls - loss) <= LOSS_REL * abs(loss)
+    assert abs(mean - loss / sum(counts)) <= LOSS_REL * abs(loss / sum(counts))
+    # rows from each micro-step, incl. the masked tail of the masked workload
+    extra = (lambda k: [16383, 1023, 1024 * 16 - 1]) if name == "masked_unequal" else (lambda k: [0])
+    _check_rows(w, dhs, rls, scales, rng, extra)
+    # dW rows: random ones, the padded vocabulary tail and frequent targets
+    ys = np.concatenate([O.i64(y) for _, y in w.micro])
+    top = np.bincount(ys[ys >= 0], minlength=w.V).argsort()[-4:].tolist()
+    _check_dW_rows(w, dW, scales, rng, lses, extra=top + [w.V - 1, 50257])
+
+
+def test_full_batch_524k_sampled_and_closed_form():
+    w = I.make("gpt2_124m_full_batch")
+    rng = np.random.default_rng(8)
+    dW, dhs, rls, (ls, cnt, mean, st) = _run(w)
+    assert st == M.OK and cnt == 524288
+    scales = O.micro_scales(w.valid_counts(), "global", w.G)
+    _check_rows(w, dhs, rls, scales, rng)
+    # the summed loss equals the sum of the per-row losses the library returned
+    assert abs(ls - sum(float(r.double().sum()) for r in rls)) <= 1e-6 * abs(ls)
+    del dhs, rls
+    # W = 0 at the same shape: every softmax is uniform, so
+    #   dW[v] = s * (sum_n h_n / V - sum_{n: y_n = v} h_n), dh = 0, loss = log V per row
+    Wz = torch.zeros_like(w.W)
+    dW0, dhs0, _, (ls0, cnt0, mean0, st0) = _run(w, Wz)
+    assert st0 == M.OK
+    assert abs(mean0 - math.log(w.V)) <= 1e-6 * math.log(w.V)
+    assert all(float(d.abs().max()) == 0.0 for d in dhs0)
+    s = 1.0 / 524288
+    hsum = np.zeros(w.C)
+    for h, _ in w.micro:
+        hsum += h.double().sum(0).numpy()
+    vs = np.array(sorted(set(rng.choice(w.V, 64, replace=False).tolist())))
+    want = np.tile(s * hsum / w.V, (len(vs), 1))
+    for h, y in w.micro:
+        yy = O.i64(y)
+        for i, v in enumerate(vs):
+            sel = np.nonzero(yy == v)[0]
+            if len(sel):
+                want[i] -= s * h[torch.as_tensor(sel)].double().sum(0).numpy()
+    got = dW0[torch.as_tensor(vs, device="cuda")].double().cpu().numpy()
+    assert np.abs(got - want).max() <= GRAD_REL["bf16"] * np.abs(want).max()
+
+
+def test_full_logit_stress():
+    w = I.make("logit_stress")
+    rng = np.random.default_rng(9)
+    dW, dhs, rls, (ls, cnt, mean, st) = _run(w)
+    assert st == M.OK
+    counts = w.valid_counts()
+    scales = O.micro_scales(counts, "global", w.G)
+    lses, loss = _oracle_totals(w)
+    assert max(float(l.max()) for l in lses) > 60.0
+    assert abs(ls - loss) <= LOSS_REL * abs(loss)
+    # include the x40 rows (largest norms) of every micro-step
+    norms = [h.float().norm(dim=1) for h, _ in w.micro]
+    big = [n.argsort(descending=True)[:8].tolist() for n in norms]
+    _check_rows(w, dhs, rls, scales, rng, extra=lambda k: big[k])
+    _check_dW_rows(w, dW, scales, rng, lses)
