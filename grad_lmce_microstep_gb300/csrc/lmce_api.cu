@@ -112,6 +112,7 @@ static void free_scratch(lmce_handle* h) {
   cudaFree(h->sc.tc_part_m);
   cudaFree(h->sc.tc_part_l);
   cudaFree(h->sc.tc_zt);
+  cudaFree(h->sc.tc_part);
   if (h->host_acc) cudaFreeHost(h->host_acc);
   memset(&h->sc, 0, sizeof(h->sc));
   h->host_acc = nullptr;
@@ -164,7 +165,8 @@ extern "C" int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out)
   if (ok && path == LMCE_PATH_TCGEN05) {
     const size_t slices = sizeof(float) * (size_t)TC_MAX_SPLIT * (size_t)maxN;
     ok = cudaMalloc(&h->sc.tc_part_m, slices) == cudaSuccess && cudaMalloc(&h->sc.tc_part_l, slices) == cudaSuccess &&
-         cudaMalloc(&h->sc.tc_zt, sizeof(float) * maxN) == cudaSuccess;
+         cudaMalloc(&h->sc.tc_zt, sizeof(float) * maxN) == cudaSuccess &&
+         cudaMalloc(&h->sc.tc_part, tc_part_bytes(cfg->C)) == cudaSuccess;
   }
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {

@@ -101,6 +101,7 @@ struct Scratch {
   float* tc_part_m;    // [TC_MAX_SPLIT][max_N] per-slice base-2 row max
   float* tc_part_l;    // [TC_MAX_SPLIT][max_N] per-slice sum of 2^(x - max)
   float* tc_zt;        // [max_N] target logit
+  float* tc_part;      // gradient passes: fp32 partial sums of split tiles, [2 * pairs][128][C]
 };
 
 constexpr int TC_MAX_SPLIT = 32;
@@ -119,6 +120,8 @@ cudaError_t simt_grads(const StepArgs& a, const Scratch& s, Launch& L);
 // Tensor-core path (tcgen05 + TMA).
 bool tc_supported(int64_t C, int64_t V, int bf16);
 int64_t tc_parts(int64_t N);
+int64_t tc_pairs();
+size_t tc_part_bytes(int64_t C);
 cudaError_t tc_microstep(const StepArgs& a, const Scratch& s, Launch& L);
 
 }  // namespace lmce

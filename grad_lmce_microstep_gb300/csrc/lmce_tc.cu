@@ -35,7 +35,7 @@ constexpr int L_ST = 3;              // stages
 constexpr int L_STAGE_A = L_BM * L_BK * 2;  // 32 KB
 constexpr int L_STAGE_B = L_BN * L_BK * 2;  // 32 KB
 constexpr int L_STAGE = L_STAGE_A + L_STAGE_B;
-constexpr int L_THREADS = 320;       // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue (two per lane quarter)
+constexpr int L_THREADS = 352;       // warps 0 and 10 TMA, warp 1 MMA, warps 2-9 epilogue (two per lane quarter)
 constexpr int L_SMEM = L_ST * L_STAGE + 1024;
 
 struct LseParams {
@@ -96,10 +96,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(L_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
-  if (warp == 0) {
-    // ---------------- TMA producer: lane 0 waits and arms the barrier, lanes 0 and 1 each
-    // issue one 32 KB box (separate lanes overlap their issue cost) ----------------
-    if (lane == 0) {
+  if (warp == 0 || warp == 10) {
+    // ---------------- TMA producers: two warps take alternate stages (a warp's TMA issue
+    // has a fixed cost, so two warps double the rate); in each, lane 0 waits and arms the
+    // barrier and lanes 0 and 1 each issue one 32 KB box ----------------
+    const int pw = warp == 0 ? 0 : 1;
+    if (lane == 0 && pw == 0) {
       tma_prefetch_desc(&tmH);
       tma_prefetch_desc(&tmW);
     }
@@ -110,6 +112,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(L_THREADS, 1)
     for (int t = 0; t < ntiles && ok; ++t) {
       const int wrow = (t_begin + t) * 256 + (int)rank * L_BN;
       for (int kc = 0; kc < kchunks; ++kc, ++it) {
+        if ((it & 1) != pw) continue;
         const int s = it % L_ST;
         const uint32_t ph = ((it / L_ST) & 1) ^ 1;
         bool w = true;
@@ -167,7 +170,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(L_THREADS, 1)
         mbar_wait(smem_u32(&drain_bar), 0, WAIT_NS);
       }
     }
-  } else {
+  } else if (warp <= 9) {
     // ---------------- epilogue: warps 2..9 ----------------
     // warp -> TMEM lane quarter q (its token rows) and column half hf of every tile; each
     // thread keeps a base-2 running (max, sum) of its row over its half of the columns.
@@ -330,7 +333,7 @@ constexpr int G_SLOT = 49152;              // S stage: Y 128 rows x 128 C (32 KB
 constexpr int G_SLOT_X = 32768;            // offset of the X box inside an S-stage slot
 constexpr int G_DZ = G_YB * 128;           // one dz buffer: 256 K-rows x 64 bf16 = 32 KB (two of them)
 constexpr int G_EPI_WARPS = 8;
-constexpr int G_THREADS = 64 + 32 * G_EPI_WARPS;
+constexpr int G_THREADS = 96 + 32 * G_EPI_WARPS;   // warps 0 and 10 TMA, 1 MMA, 2-9 epilogue
 
 struct GradParams {
   const int32_t* targets;
@@ -341,8 +344,27 @@ struct GradParams {
   float* dW;             // dW pass output (fp32 [V, C])
   __nv_bfloat16* dh;     // dh pass output (bf16 [N, C])
   const __nv_bfloat16* Wt;  // dh pass: W, for the one-hot term
+  float* part;           // [2 * pairs][128][C] fp32 partial sums of split tiles
   int N, V, C;
   int beta;              // dW pass: 0 writes, 1 adds
+};
+
+// Balanced persistent schedule.  Work units are (X tile t, stream block j), t-major; pair pi
+// of P takes units [U pi / P, U (pi + 1) / P).  Its range crosses X tiles in segments; a segment
+// that covers a whole tile writes the output directly, a segment that covers part of a tile
+// (at most the pair's first and last) writes fp32 partial sums to slot 2 pi (first segment) or
+// 2 pi + 1, and tc_split_combine_kernel adds the partials of each split tile in pair order.
+struct Sched {
+  long long U;  // tiles * blocks per tile
+  int P;        // pairs
+  int nblk;     // stream blocks per tile
+  __host__ __device__ long long u0(int p) const { return U * p / P; }
+  __host__ __device__ int pair_of(long long u) const {
+    int p = (int)((u * P) / U);
+    while (p + 1 < P && u0(p + 1) <= u) ++p;
+    while (p > 0 && u0(p) > u) --p;
+    return p;
+  }
 };
 
 __host__ __device__ constexpr int grad_smem_bytes(int C) {
@@ -365,7 +387,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
   uint8_t* sY = smem;                       // ring of G_ST slots
   uint8_t* sDZ = sY + G_ST * G_SLOT;        // [2][256 rows][128 B]
   __shared__ __align__(8) uint64_t full[G_ST], empty[G_ST];
-  __shared__ __align__(8) uint64_t s_full, s_empty, dz_full[2][4], dz_empty[2], acc_full, drain_bar;
+  __shared__ __align__(8) uint64_t s_full, s_empty, dz_full[2][4], dz_empty[2], acc_full, acc_empty, drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int epi_abort;
   __shared__ float col_c[G_XT];             // dh pass: per-column log2(s) - lse log2(e), or -inf
@@ -373,10 +395,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
-  const int x0 = (blockIdx.x >> 1) * G_XT;
   const int nX = DW ? p.V : p.N;
   const int nY = DW ? p.N : p.V;
   const int nblk = (nY + G_YB - 1) / G_YB;
+  const int T = (nX + G_XT - 1) / G_XT;
+  const Sched sch{(long long)T * nblk, (int)(gridDim.x >> 1), nblk};
+  const int pi = blockIdx.x >> 1;
+  const long long ub = sch.u0(pi), ue = sch.u0(pi + 1);
+  const int t_first = (int)(ub / nblk), t_last = (int)((ue - 1) / nblk);
   const float s = p.acc->scale;
   const float log2s = log2f(s);             // -inf when s == 0: every dz is then 0
 
@@ -392,23 +418,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       mbar_init(smem_u32(&dz_empty[b]), 1);
     }
     mbar_init(smem_u32(&acc_full), 1);
+    mbar_init(smem_u32(&acc_empty), 2);
     mbar_init(smem_u32(&drain_bar), 1);
     epi_abort = 0;
     fence_mbar_init();
-  }
-  if (!DW && threadIdx.x < G_XT) {
-    const int n = x0 + threadIdx.x;
-    int y = -1;
-    float c = -INFINITY;
-    if (n < p.N) {
-      const int t = p.targets[n];
-      if (t >= 0 && t < p.V) {
-        y = t;
-        c = log2s - p.lse[n] * LOG2E;
-      }
-    }
-    col_y[threadIdx.x] = y;
-    col_c[threadIdx.x] = c;
   }
   if (warp == 1) {
     tmem_alloc<2>(smem_u32(&tmem_base_sh), 512);
@@ -420,10 +433,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
   const uint32_t tmem = tmem_base_sh;
   const uint32_t tS = tmem + NCH * 128;     // S^T columns after the accumulator chunks
 
-  if (warp == 0) {
-    // ---------------- TMA producer: lane 0 waits and arms the barrier; each box of a
-    // stage is issued by its own lane so their issue costs overlap ----------------
-    if (lane == 0) {
+  if (warp == 0 || warp == 10) {
+    // ---------------- TMA producers: two warps take alternate stages; in each, lane 0 waits
+    // and arms the barrier and each box of the stage is issued by its own lane ----------------
+    const int pw = warp == 0 ? 0 : 1;
+    if (lane == 0 && pw == 0) {
       tma_prefetch_desc(&tmX);
       tma_prefetch_desc(&tmYs);
       tma_prefetch_desc(&tmYa);
@@ -432,31 +446,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     const uint32_t lead_full = mapa(smem_u32(&full[0]), 0);
     int it = 0;
     bool ok = true;
-    for (int j = 0; j <= nblk && ok; ++j) {
-      const int nst = (j < nblk ? KC : 0) + (j >= 1 ? 4 : 0);
-      for (int u = 0; u < nst; ++u, ++it) {
-        const int st = it % G_ST;
-        const bool sphase = j < nblk && u < KC;
-        bool w = true;
-        if (lane == 0) {
-          w = mbar_wait(smem_u32(&empty[st]), ((it / G_ST) & 1) ^ 1, WAIT_NS);
-          if (!w) record_timeout(p.err, 17);
-          else if (rank == 0) mbar_expect_tx(smem_u32(&full[st]), sphase ? 2 * (32768 + 16384) : 2 * 16384 * NCH);
+    for (int t = t_first; t <= t_last && ok; ++t) {
+      const int b0 = (int)(max(ub, (long long)t * nblk) - (long long)t * nblk);
+      const int nb = (int)(min(ue, (long long)(t + 1) * nblk) - (long long)t * nblk) - b0;
+      const int x0 = t * G_XT;
+      for (int j = 0; j <= nb && ok; ++j) {
+        const int nst = (j < nb ? KC : 0) + (j >= 1 ? 4 : 0);
+        for (int u = 0; u < nst; ++u, ++it) {
+          if ((it & 1) != pw) continue;
+          const int st = it % G_ST;
+          const bool sphase = j < nb && u < KC;
+          bool w = true;
+          if (lane == 0) {
+            w = mbar_wait(smem_u32(&empty[st]), ((it / G_ST) & 1) ^ 1, WAIT_NS);
+            if (!w) record_timeout(p.err, 17);
+            else if (rank == 0) mbar_expect_tx(smem_u32(&full[st]), sphase ? 2 * (32768 + 16384) : 2 * 16384 * NCH);
+          }
+          if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+          const uint32_t dst = smem_u32(sY) + st * G_SLOT;
+          const uint32_t bar = lead_full + st * 8;
+          if (sphase) {
+            // S phase of block b0+j: my 128 stream rows and my 64 X rows, C columns [128u, 128u + 128)
+            if (lane == 0) tma_load_3d_cg2(dst, &tmYs, bar, 0, (b0 + j) * G_YB + (int)rank * 128, u * 2);
+            else if (lane == 1) tma_load_3d_cg2(dst + G_SLOT_X, &tmX, bar, 0, x0 + (int)rank * 64, u * 2);
+          } else if (lane == 0) {
+            // accumulation phase of block b0+j-1, quarter q (64 stream rows): my 128 C of every
+            // chunk, one 4D box [chunk][atom][64 rows][64]
+            const int q = u - (j < nb ? KC : 0);
+            const int row = (b0 + j - 1) * G_YB + q * 64;
+            tma_load_4d_cg2(dst, &tmYa, bar, 0, row, 2 * (int)rank, 0);
+          }
+          __syncwarp();
         }
-        if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
-        const uint32_t dst = smem_u32(sY) + st * G_SLOT;
-        const uint32_t bar = lead_full + st * 8;
-        if (sphase) {
-          // S phase of block j: my 128 stream rows and my 64 X rows, C columns [128u, 128u + 128)
-          if (lane == 0) tma_load_3d_cg2(dst, &tmYs, bar, 0, j * G_YB + (int)rank * 128, u * 2);
-          else if (lane == 1) tma_load_3d_cg2(dst + G_SLOT_X, &tmX, bar, 0, x0 + (int)rank * 64, u * 2);
-        } else if (lane < NCH) {
-          // accumulation phase of block j-1, quarter q (64 stream rows): my 128 C of chunk `lane`
-          const int q = u - (j < nblk ? KC : 0);
-          const int row = (j - 1) * G_YB + q * 64;
-          tma_load_3d_cg2(dst + lane * 16384, &tmYa, bar, 0, row, (lane * 256 + (int)rank * 128) / 64);
-        }
-        __syncwarp();
       }
     }
   } else if (warp == 1) {
@@ -465,206 +486,256 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       const uint32_t idS = idesc_bf16(256, G_XT, 0, 0);
       const uint32_t idA = idesc_bf16(256, G_XT, 1, 1);
       bool ok = true;
-      int it = 0;
-      for (int j = 0; j <= nblk && ok; ++j) {
-        if (j < nblk) {
-          // S^T of block j (the epilogue must have read block j-1's)
-          if (!mbar_wait_cluster(smem_u32(&s_empty), (j & 1) ^ 1, WAIT_NS)) {
-            record_timeout(p.err, 21);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          for (int kc = 0; kc < KC; ++kc, ++it) {
-            const int st = it % G_ST;
-            if (!mbar_wait(smem_u32(&full[st]), (it / G_ST) & 1, WAIT_NS)) {
-              record_timeout(p.err, 22);
+      int it = 0, g = 0, sg = 0;              // stage counter, global block counter, segment counter
+      for (int t = t_first; t <= t_last && ok; ++t, ++sg) {
+        const int b0 = (int)(max(ub, (long long)t * nblk) - (long long)t * nblk);
+        const int nb = (int)(min(ue, (long long)(t + 1) * nblk) - (long long)t * nblk) - b0;
+        for (int j = 0; j <= nb && ok; ++j) {
+          if (j < nb) {
+            // S^T of block j (the epilogue must have read the previous block's)
+            const int gb = g + j;
+            if (!mbar_wait_cluster(smem_u32(&s_empty), (gb & 1) ^ 1, WAIT_NS)) {
+              record_timeout(p.err, 21);
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t a = smem_u32(sY) + st * G_SLOT;
-            const uint32_t b = a + G_SLOT_X;
+            for (int kc = 0; kc < KC; ++kc, ++it) {
+              const int st = it % G_ST;
+              if (!mbar_wait(smem_u32(&full[st]), (it / G_ST) & 1, WAIT_NS)) {
+                record_timeout(p.err, 22);
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t a = smem_u32(sY) + st * G_SLOT;
+              const uint32_t b = a + G_SLOT_X;
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              mma_ss<2>(tS, sdesc_sw128(a + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-                        sdesc_sw128(b + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), idS, (kc | k) != 0);
-            mma_commit_mc2(smem_u32(&empty[st]), 3);
+              for (int k = 0; k < 8; ++k)
+                mma_ss<2>(tS, sdesc_sw128(a + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
+                          sdesc_sw128(b + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), idS, (kc | k) != 0);
+              mma_commit_mc2(smem_u32(&empty[st]), 3);
+            }
+            if (!ok) break;
+            mma_commit_mc2(smem_u32(&s_full), 3);
           }
-          if (!ok) break;
-          mma_commit_mc2(smem_u32(&s_full), 3);
-        }
-        if (j >= 1) {
-          // accumulation of block j-1, one 64-row quarter of dz at a time
-          const int jb = j - 1, db = jb & 1;
-          const uint32_t dzb = smem_u32(sDZ) + db * G_DZ;
-          for (int q = 0; q < 4 && ok; ++q) {
-            if (!mbar_wait_cluster(smem_u32(&dz_full[db][q]), (jb >> 1) & 1, WAIT_NS)) {
-              record_timeout(p.err, 23);
-              ok = false;
-              break;
+          if (j >= 1) {
+            // accumulation of block j-1, one 64-row quarter of dz at a time
+            const int jb = j - 1, gb = g + jb, db = gb & 1;
+            if (jb == 0) {
+              // the epilogue must have drained the previous segment's accumulator
+              if (!mbar_wait_cluster(smem_u32(&acc_empty), (sg & 1) ^ 1, WAIT_NS)) {
+                record_timeout(p.err, 28);
+                ok = false;
+                break;
+              }
+              tc_fence_after();
             }
-            const int st = it % G_ST;
-            if (!mbar_wait(smem_u32(&full[st]), (it / G_ST) & 1, WAIT_NS)) {
-              record_timeout(p.err, 24);
-              ok = false;
-              break;
-            }
-            ++it;
-            tc_fence_after();
-            const uint32_t a = smem_u32(sY) + st * G_SLOT;
-            for (int i = 0; i < NCH; ++i) {
+            const uint32_t dzb = smem_u32(sDZ) + db * G_DZ;
+            for (int q = 0; q < 4 && ok; ++q) {
+              if (!mbar_wait_cluster(smem_u32(&dz_full[db][q]), (gb >> 1) & 1, WAIT_NS)) {
+                record_timeout(p.err, 23);
+                ok = false;
+                break;
+              }
+              const int st = it % G_ST;
+              if (!mbar_wait(smem_u32(&full[st]), (it / G_ST) & 1, WAIT_NS)) {
+                record_timeout(p.err, 24);
+                ok = false;
+                break;
+              }
+              ++it;
+              tc_fence_after();
+              const uint32_t a = smem_u32(sY) + st * G_SLOT;
+              for (int i = 0; i < NCH; ++i) {
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                mma_ss<2>(tmem + i * 128, sdesc_sw128(a + i * 16384 + k * 2048, 8192, 1024),
-                          sdesc_sw128(dzb + q * 8192 + k * 2048, 32768, 1024), idA, (jb | q | k) != 0);
+                for (int k = 0; k < 4; ++k)
+                  mma_ss<2>(tmem + i * 128, sdesc_sw128(a + i * 16384 + k * 2048, 8192, 1024),
+                            sdesc_sw128(dzb + q * 8192 + k * 2048, 32768, 1024), idA, (jb | q | k) != 0);
+              }
+              mma_commit_mc2(smem_u32(&empty[st]), 3);
             }
-            mma_commit_mc2(smem_u32(&empty[st]), 3);
+            if (!ok) break;
+            mma_commit_mc2(smem_u32(&dz_empty[db]), 3);
+            if (jb == nb - 1) mma_commit_mc2(smem_u32(&acc_full), 3);
           }
-          if (!ok) break;
-          mma_commit_mc2(smem_u32(&dz_empty[db]), 3);
-          if (jb == nblk - 1) mma_commit_mc2(smem_u32(&acc_full), 3);
         }
+        g += nb;
       }
       if (!ok) {
         mma_commit<2>(smem_u32(&drain_bar));
         mbar_wait(smem_u32(&drain_bar), 0, WAIT_NS);
       }
     }
-  } else {
+  } else if (warp <= 9) {
     // ---------------- epilogue: warps 2..9 ----------------
     // warp -> (TMEM lane quarter q = warp % 4, column half hf); thread = one stream row
     const int q = warp & 3;
     const int hf = (warp - 2) >> 2;
+    const int et = (warp - 2) * 32 + lane;        // 0..255 within the epilogue warps
     const int kl = q * 32 + lane;                 // TMEM lane = my stream row in this CTA
     const int kb = (int)rank * 128 + kl;          // row within the 256-row block
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const uint32_t leader_s_empty = mapa(smem_u32(&s_empty), 0);
+    const uint32_t leader_acc_empty = mapa(smem_u32(&acc_empty), 0);
     const uint32_t leader_dz_full = mapa(smem_u32(&dz_full[0][0]), 0) + (uint32_t)(kb >> 6) * 8;
     const bool remote = hf != (int)rank;         // column half hf is supplied by CTA hf
     const uint32_t dz_dst = remote ? mapa(smem_u32(sDZ), (uint32_t)hf) : smem_u32(sDZ);
-    bool alive = true;
-    for (int j = 0; j < nblk; ++j) {
-      const int ys = j * G_YB + kb;               // my stream row
-      // dW pass: my token's target, logsumexp and target logit, loaded while S is computed
-      float crow = -INFINITY;                     // log2(s) - lse log2(e), -inf: no gradient
-      int xt = -1;                                // my target's column in this X tile
-      float fix = 0.f;                            // dz of that element: s (p_t - 1)
-      if (DW && ys < p.N) {
-        const int t = p.targets[ys];
-        if (t >= 0 && t < p.V) {
-          const float l2 = p.lse[ys] * LOG2E;
-          crow = log2s - l2;
-          if (t >= x0 && t < x0 + G_XT) {
-            xt = t - x0;
-            fix = s * (ex2_approx(fmaf(p.zt[ys], LOG2E, -l2)) - 1.f);
+    int g = 0, sg = 0;
+    for (int t = t_first; t <= t_last; ++t, ++sg) {
+      const int b0 = (int)(max(ub, (long long)t * nblk) - (long long)t * nblk);
+      const int nb = (int)(min(ue, (long long)(t + 1) * nblk) - (long long)t * nblk) - b0;
+      const int x0 = t * G_XT;
+      if (!DW) {
+        // per-column constants of this X tile (tokens): target and log2(s) - lse log2(e)
+        if (et < G_XT) {
+          const int n = x0 + et;
+          int y = -1;
+          float c = -INFINITY;
+          if (n < p.N) {
+            const int tg = p.targets[n];
+            if (tg >= 0 && tg < p.V) {
+              y = tg;
+              c = log2s - p.lse[n] * LOG2E;
+            }
+          }
+          col_y[et] = y;
+          col_c[et] = c;
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+      }
+      for (int j = 0; j < nb; ++j) {
+        const int gb = g + j;
+        const int ys = (b0 + j) * G_YB + kb;        // my stream row
+        // dW pass: my token's target, logsumexp and target logit, loaded while S is computed
+        float crow = -INFINITY;                     // log2(s) - lse log2(e), -inf: no gradient
+        int xt = -1;                                // my target's column in this X tile
+        float fix = 0.f;                            // dz of that element: s (p_t - 1)
+        if (DW && ys < p.N) {
+          const int tg = p.targets[ys];
+          if (tg >= 0 && tg < p.V) {
+            const float l2 = p.lse[ys] * LOG2E;
+            crow = log2s - l2;
+            if (tg >= x0 && tg < x0 + G_XT) {
+              xt = tg - x0;
+              fix = s * (ex2_approx(fmaf(p.zt[ys], LOG2E, -l2)) - 1.f);
+            }
           }
         }
-      }
-      if (!mbar_wait(smem_u32(&s_full), j & 1, WAIT_NS)) {
-        record_timeout(p.err, 25);
-        epi_abort = 1;
-      }
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-      if (epi_abort) { alive = false; break; }
-      tc_fence_after();
-      float z[64];
-      {
-        float v[32];
-        tmem_ld32(tS + lane_off + hf * 64, v);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) z[e] = v[e];
-        tmem_ld32(tS + lane_off + hf * 64 + 32, v);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) z[32 + e] = v[e];
-      }
-      tc_fence_before();
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-      if (warp == 2 && lane == 0) {
-        if (rank == 0) mbar_arrive(smem_u32(&s_empty));
-        else mbar_arrive_cluster(leader_s_empty);
-      }
-      // s * softmax for my row and column half; rows past the stream end get 0 (dh pass:
-      // their W rows are zero-filled and contribute nothing)
-      uint32_t packed[32];
-#pragma unroll
-      for (int e = 0; e < 64; e += 2) {
-        float c0, c1;
-        if (DW) {
-          c0 = crow;
-          c1 = crow;
-        } else {
-          c0 = col_c[hf * 64 + e];
-          c1 = col_c[hf * 64 + e + 1];
+        if (!mbar_wait(smem_u32(&s_full), gb & 1, WAIT_NS)) {
+          record_timeout(p.err, 25);
+          epi_abort = 1;
         }
-        const float d0 = ex2_approx(fmaf(z[e], LOG2E, c0));
-        const float d1 = ex2_approx(fmaf(z[e + 1], LOG2E, c1));
-        __nv_bfloat162 pr = __floats2bfloat162_rn(d0, d1);
-        packed[e / 2] = *reinterpret_cast<uint32_t*>(&pr);
-      }
-      // dz buffer j&1 is free once the accumulation of block j-2 has completed
-      const int db = j & 1;
-      if (!mbar_wait(smem_u32(&dz_empty[db]), ((j >> 1) & 1) ^ 1, WAIT_NS)) {
-        record_timeout(p.err, 26);
-        epi_abort = 1;
-      }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (epi_abort) break;
+        tc_fence_after();
+        float z[64];
+        {
+          float v[32];
+          tmem_ld32(tS + lane_off + hf * 64, v);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t addr = dz_dst + db * G_DZ + sw128_offset(kb, c * 16);
-        const uint32_t* w = packed + c * 4;
-        if (remote)
-          asm volatile("st.shared::cluster.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
-                       "r"(w[2]), "r"(w[3])
-                       : "memory");
-        else
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-                       "r"(w[3])
-                       : "memory");
+          for (int e = 0; e < 32; ++e) z[e] = v[e];
+          tmem_ld32(tS + lane_off + hf * 64 + 32, v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) z[32 + e] = v[e];
+        }
+        tc_fence_before();
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (warp == 2 && lane == 0) {
+          if (rank == 0) mbar_arrive(smem_u32(&s_empty));
+          else mbar_arrive_cluster(leader_s_empty);
+        }
+        // s * softmax for my row and column half; rows past the stream end get 0 (dh pass:
+        // their W rows are zero-filled and contribute nothing)
+        uint32_t packed[32];
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {
+          float c0, c1;
+          if (DW) {
+            c0 = crow;
+            c1 = crow;
+          } else {
+            c0 = col_c[hf * 64 + e];
+            c1 = col_c[hf * 64 + e + 1];
+          }
+          const float d0 = ex2_approx(fmaf(z[e], LOG2E, c0));
+          const float d1 = ex2_approx(fmaf(z[e + 1], LOG2E, c1));
+          __nv_bfloat162 pr = __floats2bfloat162_rn(d0, d1);
+          packed[e / 2] = *reinterpret_cast<uint32_t*>(&pr);
+        }
+        // dz buffer gb&1 is free once the accumulation two blocks back has completed
+        const int db = gb & 1;
+        if (!mbar_wait(smem_u32(&dz_empty[db]), ((gb >> 1) & 1) ^ 1, WAIT_NS)) {
+          record_timeout(p.err, 26);
+          epi_abort = 1;
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t addr = dz_dst + db * G_DZ + sw128_offset(kb, c * 16);
+          const uint32_t* w = packed + c * 4;
+          if (remote)
+            asm volatile("st.shared::cluster.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
+                         "r"(w[2]), "r"(w[3])
+                         : "memory");
+          else
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                         "r"(w[3])
+                         : "memory");
+        }
+        if (DW && xt >= hf * 64 && xt < hf * 64 + 64) {
+          __nv_bfloat16 fb = __float2bfloat16_rn(fix);
+          st_shared_b16(dz_dst + db * G_DZ + sw128_offset(kb, (xt - hf * 64) * 2), *reinterpret_cast<uint16_t*>(&fb),
+                        remote);
+        }
+        if (remote) fence_proxy_async();
+        else fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(leader_dz_full + db * 32);
       }
-      if (DW && xt >= hf * 64 && xt < hf * 64 + 64) {
-        __nv_bfloat16 fb = __float2bfloat16_rn(fix);
-        st_shared_b16(dz_dst + db * G_DZ + sw128_offset(kb, (xt - hf * 64) * 2), *reinterpret_cast<uint16_t*>(&fb),
-                      remote);
-      }
-      if (remote) fence_proxy_async();
-      else fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(leader_dz_full + db * 32);
-    }
-    // accumulator -> output
-    if (alive) {
-      if (!mbar_wait(smem_u32(&acc_full), 0, WAIT_NS)) {
+      // accumulator -> output (whole tile) or partial slot (part of a tile); an abort is
+      // acted on only right after a barrier, so every epilogue thread takes the same branch
+      if (!mbar_wait(smem_u32(&acc_full), sg & 1, WAIT_NS)) {
         record_timeout(p.err, 27);
         epi_abort = 1;
       }
       asm volatile("bar.sync 1, 256;" ::: "memory");
-      if (!epi_abort) {
-        tc_fence_after();
-        for (int i = 0; i < NCH; ++i) {
-          const int c = i * 256 + (int)rank * 128 + kl;   // my C row of the accumulator
+      if (epi_abort) break;
+      tc_fence_after();
+      const bool whole = b0 == 0 && nb == nblk;
+      float* part = p.part + (size_t)(2 * pi + (sg == 0 ? 0 : 1)) * G_XT * p.C;
+      for (int i = 0; i < NCH; ++i) {
+        const int c = i * 256 + (int)rank * 128 + kl;   // my C row of the accumulator
 #pragma unroll 1
-          for (int cc = 0; cc < 2; ++cc) {
-            float v[32];
-            tmem_ld32(tmem + i * 128 + lane_off + hf * 64 + cc * 32, v);
+        for (int cc = 0; cc < 2; ++cc) {
+          float v[32];
+          tmem_ld32(tmem + i * 128 + lane_off + hf * 64 + cc * 32, v);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int xl = hf * 64 + cc * 32 + e;
-              const int x = x0 + xl;
-              if (x < nX) {
-                if (DW) {
-                  float* o = p.dW + (size_t)x * p.C + c;
-                  *o = p.beta ? (*o + v[e]) : v[e];
-                } else {
-                  float val = v[e];
-                  const int y = col_y[xl];
-                  if (y >= 0) val -= s * __bfloat162float(p.Wt[(size_t)y * p.C + c]);
-                  p.dh[(size_t)x * p.C + c] = __float2bfloat16_rn(val);
-                }
+          for (int e = 0; e < 32; ++e) {
+            const int xl = hf * 64 + cc * 32 + e;
+            const int x = x0 + xl;
+            if (!whole) {
+              part[(size_t)xl * p.C + c] = v[e];
+            } else if (x < nX) {
+              if (DW) {
+                float* o = p.dW + (size_t)x * p.C + c;
+                *o = p.beta ? (*o + v[e]) : v[e];
+              } else {
+                float val = v[e];
+                const int y = col_y[xl];
+                if (y >= 0) val -= s * __bfloat162float(p.Wt[(size_t)y * p.C + c]);
+                p.dh[(size_t)x * p.C + c] = __float2bfloat16_rn(val);
               }
             }
           }
         }
       }
+      tc_fence_before();
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (warp == 2 && lane == 0) {
+        if (rank == 0) mbar_arrive(smem_u32(&acc_empty));
+        else mbar_arrive_cluster(leader_acc_empty);
+      }
+      g += nb;
     }
   }
 
@@ -674,6 +745,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc<2>(tmem, 512);
+  }
+}
+
+// The X tiles the schedule split between pairs: those holding a pair boundary.
+constexpr int MAX_SPLIT_TILES = 160;
+struct SplitTiles {
+  int n;
+  int t[MAX_SPLIT_TILES];
+};
+
+// Adds the partial sums of every split X tile in pair order and writes the output exactly as
+// the gradient kernel does for whole tiles.  grid: (split tiles, ceil(128 * C / 1024)); each
+// thread handles four consecutive C columns of one row.
+template <bool DW>
+__global__ void __launch_bounds__(256) tc_split_combine_kernel(GradParams p, Sched sch, const __grid_constant__ SplitTiles sp) {
+  __shared__ int slots[16];
+  __shared__ int nslots;
+  const int t = sp.t[blockIdx.x];
+  if (threadIdx.x == 0) {
+    const long long tb = (long long)t * sch.nblk, te = tb + sch.nblk;
+    const int pa = sch.pair_of(tb), pz = sch.pair_of(te - 1);
+    int n = 0;
+    for (int q = pa; q <= pz && n < 16; ++q) slots[n++] = 2 * q + ((long long)t == sch.u0(q) / sch.nblk ? 0 : 1);
+    nslots = n;
+  }
+  __syncthreads();
+  const int idx4 = blockIdx.y * 256 + threadIdx.x;       // index of a group of 4 columns
+  const int per_row = p.C / 4;
+  if (idx4 >= G_XT * per_row) return;
+  const int xl = idx4 / per_row, c = (idx4 % per_row) * 4;
+  const int x = t * G_XT + xl;
+  const int nX = DW ? p.V : p.N;
+  if (x >= nX) return;
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < nslots; ++k) {
+    const float4 w = *reinterpret_cast<const float4*>(p.part + ((size_t)slots[k] * G_XT + xl) * p.C + c);
+    v.x += w.x;
+    v.y += w.y;
+    v.z += w.z;
+    v.w += w.w;
+  }
+  if (DW) {
+    float4* o = reinterpret_cast<float4*>(p.dW + (size_t)x * p.C + c);
+    if (p.beta) {
+      const float4 d = *o;
+      v.x += d.x;
+      v.y += d.y;
+      v.z += d.z;
+      v.w += d.w;
+    }
+    *o = v;
+  } else {
+    const int y = p.targets[x];
+    if (y >= 0 && y < p.V) {
+      const float sc = p.acc->scale;
+      const __nv_bfloat16* wr = p.Wt + (size_t)y * p.C + c;
+      v.x -= sc * __bfloat162float(wr[0]);
+      v.y -= sc * __bfloat162float(wr[1]);
+      v.z -= sc * __bfloat162float(wr[2]);
+      v.w -= sc * __bfloat162float(wr[3]);
+    }
+    __nv_bfloat16* o = p.dh + (size_t)x * p.C + c;
+    o[0] = __float2bfloat16_rn(v.x);
+    o[1] = __float2bfloat16_rn(v.y);
+    o[2] = __float2bfloat16_rn(v.z);
+    o[3] = __float2bfloat16_rn(v.w);
   }
 }
 
@@ -701,6 +838,20 @@ bool make_map3(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, ui
   cuuint32_t box[3] = {64, box_rows, box_chunks};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [cols/256][4][rows][64] view: box {64, box_rows, 2, cols/256} loads, for every 256-column
+// chunk, two 64-column atoms (this CTA's half of the chunk) of box_rows rows in one instruction.
+bool make_map4(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {64, rows, 4, cols / 256};
+  cuuint64_t strides[3] = {cols * 2, 128, 512};
+  cuuint32_t box[4] = {64, box_rows, 2, (cuuint32_t)(cols / 256)};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -740,6 +891,10 @@ bool tc_supported(int64_t C, int64_t V, int bf16) {
 }
 
 int64_t tc_parts(int64_t N) { return (N + 255) / 256; }
+
+int64_t tc_pairs() { return num_sms() / 2; }
+
+size_t tc_part_bytes(int64_t C) { return (size_t)2 * (size_t)tc_pairs() * G_XT * (size_t)C * sizeof(float); }
 
 
 cudaError_t tc_lse(const StepArgs& a, const Scratch& sc, Launch& L) {
@@ -787,7 +942,7 @@ cudaError_t tc_grad(const StepArgs& a, const Scratch& sc, Launch& L) {
   const int64_t nX = DW ? a.V : a.N, nY = DW ? a.N : a.V;
   CUtensorMap mx, mys, mya;
   if (!make_map3(&mx, X, (uint64_t)nX, (uint64_t)a.C, G_XT / 2, 2) ||
-      !make_map3(&mys, Y, (uint64_t)nY, (uint64_t)a.C, 128, 2) || !make_map3(&mya, Y, (uint64_t)nY, (uint64_t)a.C, 64, 2))
+      !make_map3(&mys, Y, (uint64_t)nY, (uint64_t)a.C, 128, 2) || !make_map4(&mya, Y, (uint64_t)nY, (uint64_t)a.C, 64))
     return cudaErrorInvalidValue;
   GradParams p;
   p.targets = a.targets;
@@ -798,15 +953,40 @@ cudaError_t tc_grad(const StepArgs& a, const Scratch& sc, Launch& L) {
   p.Wt = static_cast<const __nv_bfloat16*>(a.W);
   p.dW = a.dW;
   p.dh = static_cast<__nv_bfloat16*>(a.dh);
+  p.part = sc.tc_part;
   p.N = (int)a.N;
   p.V = (int)a.V;
   p.C = (int)a.C;
   p.beta = a.beta;
+  const int nblk = (int)((nY + G_YB - 1) / G_YB);
+  const int T = (int)((nX + G_XT - 1) / G_XT);
+  const long long U = (long long)T * nblk;
+  // every pair covers at least a sixth of a tile, so a split tile has a handful of partials
+  long long P = tc_pairs();
+  if (P > U * 6 / nblk) P = U * 6 / nblk;
+  if (P > U) P = U;  // every pair gets at least one unit
+  if (P < 1) P = 1;
+  const Sched sch{U, (int)P, nblk};
   const int smem = grad_smem_bytes((int)a.C);
   cudaFuncSetAttribute(tc_grad_kernel<DW>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  const unsigned pairs = (unsigned)((nX + G_XT - 1) / G_XT);
   L.begin(DW ? K_DW : K_DH);
-  tc_grad_kernel<DW><<<2 * pairs, G_THREADS, smem, L.st>>>(mx, mys, mya, p);
+  tc_grad_kernel<DW><<<(unsigned)(2 * P), G_THREADS, smem, L.st>>>(mx, mys, mya, p);
+  L.end();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  SplitTiles sp;
+  sp.n = 0;
+  for (int q = 1; q < sch.P; ++q) {
+    const long long u = sch.u0(q);
+    if (u % nblk == 0) continue;              // the boundary falls between tiles
+    const int t = (int)(u / nblk);
+    if (sp.n > 0 && sp.t[sp.n - 1] == t) continue;
+    if (sp.n == MAX_SPLIT_TILES) return cudaErrorInvalidValue;
+    sp.t[sp.n++] = t;
+  }
+  if (sp.n == 0) return cudaSuccess;
+  L.begin(K_FINISH);
+  tc_split_combine_kernel<DW><<<dim3((unsigned)sp.n, (unsigned)((G_XT * a.C / 4 + 255) / 256)), 256, 0, L.st>>>(p, sch, sp);
   L.end();
   return cudaGetLastError();
 }

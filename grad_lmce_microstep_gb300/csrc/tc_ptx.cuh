@@ -136,6 +136,15 @@ __device__ __forceinline__ void tma_load_3d_cg2(uint32_t dst, const void* map, u
       : "memory");
 }
 
+// 4D form of the pair load.
+__device__ __forceinline__ void tma_load_4d_cg2(uint32_t dst, const void* map, uint32_t bar_cluster, int x, int y, int z,
+                                                int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
 // ---- tcgen05 ----------------------------------------------------------------------------
 template <int CG>
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
