@@ -38,7 +38,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="lmce", choices=["lmce", "reference"])
     p.add_argument("--workload", default="gpt2_124m_head")
-    p.add_argument("--path", default="auto", choices=["auto", "simt", "tcgen05"])
+    p.add_argument("--path", default="auto", choices=["auto", "simt", "tcgen05", "tcgen05_two_pass"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample-rows", type=int, default=2048)
@@ -270,15 +270,16 @@ def run_lmce(args, rank, world, local_rank):
 
     pk, pk_kind = peaks()
     # algorithmic work: 6 C V flops per token for the whole path, 2 C V for each of the three
-    # contractions (logits, dW, dh); the recomputed logits of the gradient passes are not counted.
+    # contractions (logits, dW, dh); the recomputed logits of the gradient passes are not counted
+    # (the one-pass logsumexp + dh kernel does the logits and dh contractions: 4 C V).
     flop_tok = 6.0 * w.C * w.V
     kinds = {k: v for k, v in prof.items() if v[1] > 0}
     dom = max(kinds, key=lambda k: kinds[k][0])
     dom_ms, dom_n = kinds[dom]
     tok_per_launch = tokens_rank / w.G
-    alg_flop_launch = {"lse": 2.0, "dW": 2.0, "dh": 2.0, "finish": 0.0}[dom] * w.C * w.V * tok_per_launch
+    alg_flop_launch = {"lse": 2.0, "dW": 2.0, "dh": 2.0, "lse_dh": 4.0, "finish": 0.0}[dom] * w.C * w.V * tok_per_launch
     achieved = alg_flop_launch / (dom_ms / dom_n / 1e3) / 1e12
-    if L.path == "tcgen05":
+    if L.path.startswith("tcgen05"):
         peak = pk["bf16_tflops_sustained"] if "bf16_tflops_sustained" in pk else pk["bf16_tflops"]
         bound = "tensor"
     else:
@@ -308,7 +309,7 @@ def run_lmce(args, rank, world, local_rank):
                          "peak_tflops": pk.get("bf16_tflops_sustained") or pk["bf16_tflops"],
                          "peak": f"bf16 sustained, {pk_kind}"},
         "roofline": {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": ncu_traffic(dom) if L.path == "tcgen05" else None,
+                     "frac": achieved / peak, "traffic": ncu_traffic(dom) if L.path.startswith("tcgen05") else None,
                      "peak_source": ("bf16_tflops_sustained of " + pk_kind) if bound == "tensor"
                      else "fp32 FFMA: 152 SMs x 128 lanes x 2 flop x max SM clock"},
         "kernels_ms": {k: {"total_ms": v[0], "launches": v[1], "avg_ms": v[0] / v[1]} for k, v in kinds.items()},

@@ -25,7 +25,7 @@ __global__ void __launch_bounds__(FIN_T) finish_kernel(const double* __restrict_
                                                        const int* __restrict__ part_cnt,
                                                        const unsigned* __restrict__ part_err,
                                                        int64_t nparts, int norm, int G,
-                                                       long long global_valid, DevAcc* acc) {
+                                                       long long global_valid, DevAcc* acc, int mode) {
   __shared__ double sl[FIN_T];
   __shared__ long long sc[FIN_T];
   __shared__ unsigned se[FIN_T];
@@ -34,8 +34,8 @@ __global__ void __launch_bounds__(FIN_T) finish_kernel(const double* __restrict_
   long long c = 0;
   unsigned e = 0;
   for (int64_t i = t; i < nparts; i += FIN_T) {
-    l += part_loss[i];
-    c += part_cnt[i];
+    if (mode != FIN_COUNT) l += part_loss[i];
+    if (mode != FIN_LOSS) c += part_cnt[i];
     e |= part_err[i];
   }
   sl[t] = l;
@@ -51,27 +51,32 @@ __global__ void __launch_bounds__(FIN_T) finish_kernel(const double* __restrict_
     __syncthreads();
   }
   if (t == 0) {
-    double loss_k = sl[0];
-    long long cnt_k = sc[0];
-    double s;
-    if (norm == LMCE_NORM_GLOBAL) s = global_valid > 0 ? 1.0 / (double)global_valid : 0.0;
-    else s = cnt_k > 0 ? 1.0 / ((double)cnt_k * (double)G) : 0.0;
-    acc->scale = (float)s;
-    acc->loss_sum += loss_k;
-    acc->objective += s * loss_k;
-    acc->count += cnt_k;
+    const double loss_k = sl[0];
+    const long long cnt_k = sc[0];
     acc->err |= se[0];
-    if (!isfinite(loss_k)) acc->err |= ERR_BIT_NONFINITE;
-    acc->micro += 1;
+    if (mode != FIN_LOSS) {
+      double s;
+      if (norm == LMCE_NORM_GLOBAL) s = global_valid > 0 ? 1.0 / (double)global_valid : 0.0;
+      else s = cnt_k > 0 ? 1.0 / ((double)cnt_k * (double)G) : 0.0;
+      acc->scale = (float)s;
+      acc->scale64 = s;
+      acc->count += cnt_k;
+    }
+    if (mode != FIN_COUNT) {
+      acc->loss_sum += loss_k;
+      acc->objective += acc->scale64 * loss_k;
+      if (!isfinite(loss_k)) acc->err |= ERR_BIT_NONFINITE;
+      acc->micro += 1;
+    }
   }
 }
 
 }  // namespace
 
-cudaError_t launch_finish(const StepArgs& a, const Scratch& s, int64_t nparts, Launch& L) {
+cudaError_t launch_finish(const StepArgs& a, const Scratch& s, int64_t nparts, Launch& L, int mode) {
   L.begin(K_FINISH);
   finish_kernel<<<1, FIN_T, 0, L.st>>>(s.part_loss, s.part_cnt, s.part_err, nparts, a.norm, a.G,
-                                       (long long)a.global_valid, s.acc);
+                                       (long long)a.global_valid, s.acc, mode);
   L.end();
   return cudaGetLastError();
 }
@@ -84,7 +89,7 @@ struct lmce_handle {
   lmce_config cfg;
   float* dW;
   int device;
-  int path;            // resolved: LMCE_PATH_SIMT or LMCE_PATH_TCGEN05
+  int path;            // resolved: LMCE_PATH_SIMT, LMCE_PATH_TCGEN05 or LMCE_PATH_TCGEN05_TWO_PASS
   Scratch sc;
   DevAcc* host_acc;    // pinned
   bool first;          // next micro-step writes dW instead of adding
@@ -113,6 +118,8 @@ static void free_scratch(lmce_handle* h) {
   cudaFree(h->sc.tc_part_l);
   cudaFree(h->sc.tc_zt);
   cudaFree(h->sc.tc_part);
+  cudaFree(h->sc.tc_part_lm);
+  cudaFree(h->sc.tc_tile_flag);
   if (h->host_acc) cudaFreeHost(h->host_acc);
   memset(&h->sc, 0, sizeof(h->sc));
   h->host_acc = nullptr;
@@ -125,13 +132,13 @@ extern "C" int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out)
   if (cfg->C > (1 << 20) || cfg->V > (1LL << 31) || cfg->max_N > (1LL << 31)) return LMCE_ERR_ARG;
   if (cfg->dtype != LMCE_BF16 && cfg->dtype != LMCE_FP32) return LMCE_ERR_ARG;
   if (cfg->norm != LMCE_NORM_GLOBAL && cfg->norm != LMCE_NORM_MICRO_MEAN) return LMCE_ERR_ARG;
-  if (cfg->path < LMCE_PATH_AUTO || cfg->path > LMCE_PATH_TCGEN05 || cfg->reserved != 0) return LMCE_ERR_ARG;
+  if (cfg->path < LMCE_PATH_AUTO || cfg->path > LMCE_PATH_TCGEN05_TWO_PASS || cfg->reserved != 0) return LMCE_ERR_ARG;
   const bool tc_ok = tc_supported(cfg->C, cfg->V, cfg->dtype == LMCE_BF16);
   const bool simt_ok = cfg->C <= 2048;
   int path;
-  if (cfg->path == LMCE_PATH_TCGEN05) {
+  if (cfg->path == LMCE_PATH_TCGEN05 || cfg->path == LMCE_PATH_TCGEN05_TWO_PASS) {
     if (!tc_ok) return LMCE_ERR_ARG;
-    path = LMCE_PATH_TCGEN05;
+    path = cfg->path;
   } else if (cfg->path == LMCE_PATH_SIMT) {
     if (!simt_ok) return LMCE_ERR_ARG;
     path = LMCE_PATH_SIMT;
@@ -162,11 +169,15 @@ extern "C" int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out)
             cudaMalloc(&h->sc.acc, sizeof(DevAcc)) == cudaSuccess &&
             cudaMallocHost(&h->host_acc, sizeof(DevAcc)) == cudaSuccess &&
             cudaMemset(h->sc.acc, 0, sizeof(DevAcc)) == cudaSuccess;
-  if (ok && path == LMCE_PATH_TCGEN05) {
+  if (ok && path != LMCE_PATH_SIMT) {
     const size_t slices = sizeof(float) * (size_t)TC_MAX_SPLIT * (size_t)maxN;
+    const size_t tiles = (size_t)(maxN + TC_TILE_ROWS - 1) / TC_TILE_ROWS;
     ok = cudaMalloc(&h->sc.tc_part_m, slices) == cudaSuccess && cudaMalloc(&h->sc.tc_part_l, slices) == cudaSuccess &&
          cudaMalloc(&h->sc.tc_zt, sizeof(float) * maxN) == cudaSuccess &&
-         cudaMalloc(&h->sc.tc_part, tc_part_bytes(cfg->C)) == cudaSuccess;
+         cudaMalloc(&h->sc.tc_part, tc_part_bytes(cfg->C)) == cudaSuccess &&
+         cudaMalloc(&h->sc.tc_part_lm, tc_part_lm_bytes()) == cudaSuccess &&
+         cudaMalloc(&h->sc.tc_tile_flag, sizeof(unsigned) * tiles) == cudaSuccess &&
+         cudaMemset(h->sc.tc_tile_flag, 0, sizeof(unsigned) * tiles) == cudaSuccess;
   }
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
@@ -184,7 +195,7 @@ extern "C" int lmce_microstep(lmce_handle* h, const void* hidden, const void* W,
   const lmce_config& c = h->cfg;
   if (N < 0 || N > c.max_N) return LMCE_ERR_ARG;
   if (N > 0 && (!hidden || !W || !targets || !dh)) return LMCE_ERR_ARG;
-  if (h->path == LMCE_PATH_TCGEN05 && N > 0) {
+  if (h->path != LMCE_PATH_SIMT && N > 0) {
     if (((uintptr_t)hidden | (uintptr_t)W | (uintptr_t)dh | (uintptr_t)h->dW) & 15) return LMCE_ERR_ARG;
   }
   cudaStream_t st = (cudaStream_t)stream;
@@ -212,6 +223,7 @@ extern "C" int lmce_microstep(lmce_handle* h, const void* hidden, const void* W,
   a.global_valid = global_valid;
   a.beta = h->first ? 0 : 1;
   a.bf16 = c.dtype == LMCE_BF16;
+  a.tc_two_pass = h->path == LMCE_PATH_TCGEN05_TWO_PASS;
   if (N == 0) {
     // An empty micro-step still counts; the first one of a step leaves dW = 0.
     if (h->first && cudaMemsetAsync(h->dW, 0, sizeof(float) * (size_t)c.V * c.C, st) != cudaSuccess)
@@ -223,7 +235,7 @@ extern "C" int lmce_microstep(lmce_handle* h, const void* hidden, const void* W,
   Launch L;
   L.st = st;
   L.prof = &h->prof;
-  cudaError_t e = h->path == LMCE_PATH_TCGEN05 ? tc_microstep(a, h->sc, L) : simt_microstep(a, h->sc, L);
+  cudaError_t e = h->path != LMCE_PATH_SIMT ? tc_microstep(a, h->sc, L) : simt_microstep(a, h->sc, L);
   h->launches += L.n;
   if (e != cudaSuccess) return LMCE_ERR_CUDA;
   h->first = false;

@@ -10,7 +10,7 @@
 namespace lmce {
 
 // Kernel kinds for the timing records (same values as LMCE_KIND_* in lmce.h).
-enum Kind { K_LSE = 0, K_FINISH = 1, K_DW = 2, K_DH = 3, K_COUNT = 4 };
+enum Kind { K_LSE = 0, K_FINISH = 1, K_DW = 2, K_DH = 3, K_LSE_DH = 4, K_COUNT = 5 };
 
 // Optional CUDA-event records around every kernel launch.
 struct Prof {
@@ -65,6 +65,7 @@ struct DevAcc {
   unsigned int micro; // micro-steps that ran
   float scale;        // s of the micro-step being processed (read by the gradient kernels)
   float pad_;
+  double scale64;     // the same s in double precision (weights the objective)
 };
 
 constexpr unsigned ERR_BIT_BAD_TARGET = 1u;
@@ -87,6 +88,7 @@ struct StepArgs {
   int64_t global_valid;
   int32_t beta;           // 0: dW = grad, 1: dW += grad
   int32_t bf16;           // 1: dtype bf16, 0: fp32
+  int32_t tc_two_pass;    // tensor-core path: 1 = separate logsumexp pass, 0 = one-pass lse + dh
 };
 
 // Library-owned device scratch.
@@ -102,13 +104,19 @@ struct Scratch {
   float* tc_part_l;    // [TC_MAX_SPLIT][max_N] per-slice sum of 2^(x - max)
   float* tc_zt;        // [max_N] target logit
   float* tc_part;      // gradient passes: fp32 partial sums of split tiles, [2 * pairs][128][C]
+  float* tc_part_lm;   // logsumexp + dh pass: per-slot (base-2 max, sum) of split tiles, [2 * pairs][2][128]
+  unsigned* tc_tile_flag;  // logsumexp + dh pass: per 128-token tile, 1 = recompute exactly
 };
 
 constexpr int TC_MAX_SPLIT = 32;
 
 // Fixed-order reduction of the per-block partials of one micro-step into the step
 // accumulators; also computes this micro-step's gradient scale.  One launch.
-cudaError_t launch_finish(const StepArgs& a, const Scratch& s, int64_t nparts, Launch& L);
+//   FIN_ALL  : loss, count and error partials (scale from the count)
+//   FIN_COUNT: count and error partials only (sets the scale before any gradient kernel)
+//   FIN_LOSS : loss and error partials, with the scale FIN_COUNT set
+enum FinMode { FIN_ALL = 0, FIN_COUNT = 1, FIN_LOSS = 2 };
+cudaError_t launch_finish(const StepArgs& a, const Scratch& s, int64_t nparts, Launch& L, int mode = FIN_ALL);
 
 // SIMT path (fp32 FFMA).
 int64_t simt_parts(int64_t N);
@@ -116,12 +124,18 @@ size_t simt_grad_smem(int64_t C);
 cudaError_t simt_microstep(const StepArgs& a, const Scratch& s, Launch& L);
 // The two gradient passes alone (lse and the scale already on the device).
 cudaError_t simt_grads(const StepArgs& a, const Scratch& s, Launch& L);
+// Exact logsumexp and dh of the rows of the 128-token tiles whose flag is set (every other
+// block returns at once): the repair of the one-pass logsumexp + dh kernel.
+constexpr int TC_TILE_ROWS = 128;
+cudaError_t simt_repair_lse(const StepArgs& a, const Scratch& s, Launch& L);
+cudaError_t simt_repair_dh(const StepArgs& a, const Scratch& s, Launch& L);
 
 // Tensor-core path (tcgen05 + TMA).
 bool tc_supported(int64_t C, int64_t V, int bf16);
 int64_t tc_parts(int64_t N);
 int64_t tc_pairs();
 size_t tc_part_bytes(int64_t C);
+size_t tc_part_lm_bytes();
 cudaError_t tc_microstep(const StepArgs& a, const Scratch& s, Launch& L);
 
 }  // namespace lmce

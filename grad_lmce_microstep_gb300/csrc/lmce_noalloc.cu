@@ -111,6 +111,7 @@ extern "C" int lmce_microstep_noalloc(const lmce_config* cfg, const void* hidden
     a.global_valid = global_valid;
     a.beta = accumulate_dW ? 1 : 0;
     a.bf16 = cfg->dtype == LMCE_BF16;
+    a.tc_two_pass = 0;
     Launch L;
     L.st = s;
     L.prof = nullptr;

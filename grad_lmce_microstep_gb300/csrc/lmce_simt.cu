@@ -67,11 +67,15 @@ __device__ __forceinline__ void logit_tile(const T* __restrict__ X, int64_t own0
   }
 }
 
+// gate == nullptr: the lse pass of the SIMT path (lse, row loss, per-block partials).
+// gate != nullptr: repair mode, only the logsumexp of the rows of flagged 128-token tiles.
 template <typename T>
 __global__ void __launch_bounds__(NT) simt_lse_kernel(StepArgs a, float* __restrict__ lse_out,
                                                       double* __restrict__ part_loss,
                                                       int* __restrict__ part_cnt,
-                                                      unsigned* __restrict__ part_err) {
+                                                      unsigned* __restrict__ part_err,
+                                                      const unsigned* __restrict__ gate) {
+  if (gate && !gate[(int64_t)blockIdx.x * R / TC_TILE_ROWS]) return;  // block-uniform
   __shared__ float Xs[BK][R];
   __shared__ float Ys[BK][BT + 1];
   __shared__ float zt[R];
@@ -112,6 +116,10 @@ __global__ void __launch_bounds__(NT) simt_lse_kernel(StepArgs a, float* __restr
     m = mn;
   }
   __syncthreads();
+  if (gate) {
+    if (q == 0 && n < a.N) lse_out[n] = m + logf(l);
+    return;
+  }
   if (q == 0) {
     double loss = 0.0;
     int valid = 0;
@@ -148,9 +156,12 @@ __global__ void __launch_bounds__(NT) simt_lse_kernel(StepArgs a, float* __restr
 
 // DW = true : own R vocabulary rows, stream the tokens, acc = dW rows.
 // DW = false: own R token rows, stream the vocabulary, acc = dh rows.
+// gate != nullptr (dh pass only): repair mode, only blocks inside flagged 128-token tiles run.
 template <typename T, bool DW>
 __global__ void __launch_bounds__(NT) simt_grad_kernel(StepArgs a, const float* __restrict__ lse,
-                                                       const DevAcc* __restrict__ acc_dev) {
+                                                       const DevAcc* __restrict__ acc_dev,
+                                                       const unsigned* __restrict__ gate) {
+  if (!DW && gate && !gate[(int64_t)blockIdx.x * R / TC_TILE_ROWS]) return;  // block-uniform
   __shared__ float Xs[BK][R];
   __shared__ float Ys[BK][BT + 1];
   __shared__ float dzs[R][BT];
@@ -235,12 +246,12 @@ static cudaError_t simt_grads_t(const StepArgs& a, const Scratch& sc, Launch& L)
   cudaFuncSetAttribute(kdw, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   cudaFuncSetAttribute(kdh, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   L.begin(K_DW);
-  kdw<<<(unsigned)((a.V + R - 1) / R), NT, smem, L.st>>>(a, sc.lse, sc.acc);
+  kdw<<<(unsigned)((a.V + R - 1) / R), NT, smem, L.st>>>(a, sc.lse, sc.acc, nullptr);
   L.end();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   L.begin(K_DH);
-  kdh<<<(unsigned)simt_parts(a.N), NT, smem, L.st>>>(a, sc.lse, sc.acc);
+  kdh<<<(unsigned)simt_parts(a.N), NT, smem, L.st>>>(a, sc.lse, sc.acc, nullptr);
   L.end();
   return cudaGetLastError();
 }
@@ -249,7 +260,7 @@ template <typename T>
 static cudaError_t simt_run(const StepArgs& a, const Scratch& sc, Launch& L) {
   const int64_t nb = simt_parts(a.N);
   L.begin(K_LSE);
-  simt_lse_kernel<T><<<(unsigned)nb, NT, 0, L.st>>>(a, sc.lse, sc.part_loss, sc.part_cnt, sc.part_err);
+  simt_lse_kernel<T><<<(unsigned)nb, NT, 0, L.st>>>(a, sc.lse, sc.part_loss, sc.part_cnt, sc.part_err, nullptr);
   L.end();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -264,6 +275,27 @@ cudaError_t simt_microstep(const StepArgs& a, const Scratch& sc, Launch& L) {
 
 cudaError_t simt_grads(const StepArgs& a, const Scratch& sc, Launch& L) {
   return a.bf16 ? simt_grads_t<__nv_bfloat16>(a, sc, L) : simt_grads_t<float>(a, sc, L);
+}
+
+// Repair of the one-pass tensor-core logsumexp + dh kernel (bf16): the exact two passes,
+// restricted to flagged tiles.  Both launches cover every row block; blocks outside flagged
+// tiles return before touching memory, so the common case costs two near-empty launches.
+cudaError_t simt_repair_lse(const StepArgs& a, const Scratch& sc, Launch& L) {
+  L.begin(K_LSE);
+  simt_lse_kernel<__nv_bfloat16><<<(unsigned)simt_parts(a.N), NT, 0, L.st>>>(a, sc.lse, nullptr, nullptr, nullptr,
+                                                                              sc.tc_tile_flag);
+  L.end();
+  return cudaGetLastError();
+}
+
+cudaError_t simt_repair_dh(const StepArgs& a, const Scratch& sc, Launch& L) {
+  const size_t smem = simt_grad_smem(a.C);
+  auto kdh = simt_grad_kernel<__nv_bfloat16, false>;
+  cudaFuncSetAttribute(kdh, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  L.begin(K_DH);
+  kdh<<<(unsigned)simt_parts(a.N), NT, smem, L.st>>>(a, sc.lse, sc.acc, sc.tc_tile_flag);
+  L.end();
+  return cudaGetLastError();
 }
 
 }  // namespace lmce

@@ -308,43 +308,63 @@ __global__ void __launch_bounds__(256) tc_combine_kernel(const float* __restrict
 }
 
 // ---- pass 2: gradients ----------------------------------------------------------------
-// One kernel shape serves both contractions of the backward pass.  A CTA pair owns 128
-// "X" rows and streams the other operand "Y" in blocks of 256 rows:
-//   dW pass: X = W (vocabulary rows), Y = h (tokens);  acc^T[c][v] = sum_n h[n][c] dz[n][v]
-//   dh pass: X = h (tokens), Y = W (vocabulary rows);   acc^T[c][n] = sum_v W[v][c] dz[n][v]
+// One kernel shape serves the three passes that contract a recomputed logit tile.  A CTA
+// pair owns 128 "X" rows and streams the other operand "Y" in blocks of 256 rows:
+//   dW pass     : X = W (vocabulary rows), Y = h (tokens); acc^T[c][v] = sum_n h[n][c] dz[n][v]
+//   dh pass     : X = h (tokens), Y = W (vocabulary rows);  acc^T[c][n] = sum_v W[v][c] dz[n][v]
+//   lse+dh pass : as the dh pass, with the softmax normaliser found on the way (below)
 // with dz[n][v] = s (softmax(z_n)[v] - [v == y_n]) ("How I trained my own GPT-2 124M",
 // section 4, differentiated; s from the gradient-accumulation normalisation).
 // Per block: S^T = Y_blk . X^T (cta_group::2, M = 256 stream rows, N = 128, K = C) lands in
 // TMEM; eight epilogue warps (two per TMEM lane quarter, one per half of the 128 columns)
-// form s*softmax = 2^(z log2 e + log2 s - lse log2 e) with one FFMA and one ex2 per
-// element, round to bf16 and write it, already in the 128-byte-swizzled MN-major operand
-// layout, into the CTA that supplies that half of N (its own or the peer's, over DSMEM).
-// The one-hot part is applied once per row: the dW pass fixes the target's element of its
-// row (from the target logit pass 1 kept), the dh pass subtracts s*W[y_n] when it writes dh.
+// turn it into the bf16 operand of the second product and write it, already in the
+// 128-byte-swizzled MN-major layout, into the CTA that supplies that half of N (its own or
+// the peer's, over DSMEM).  dW and dh passes: s*softmax = 2^(z log2 e + log2 s - lse log2 e),
+// one FFMA and one ex2 per element; the one-hot part is applied once per row (dW: the
+// target's element of its row, from the target logit; dh: s*W[y_n] subtracted when dh is
+// written).
 // acc^T[C x 128] += Y_blk^T . dz (cta_group::2, M = 256 C rows per chunk, K = 256 stream
 // rows) accumulates in TMEM for the whole stream, one 64-row quarter of dz at a time as
 // soon as that quarter is written.  The S tile of block j+1 is computed while the epilogue
 // works on block j.  Every output element has one owner: deterministic.
+//
+// The lse+dh pass needs no logsumexp beforehand.  It is the online softmax of flash
+// attention with the stale-maximum rule of FlashAttention-4 taken to its end: each token
+// column's base-2 reference m_n is fixed once, as the exact maximum over the first block of
+// the pair's range (agreed between the two CTAs over DSMEM), and never moved.  The operand
+// is p = 2^(z log2 e - m_n) and the epilogue also sums p per column (a butterfly over the 32
+// rows of a warp, kept in two registers per lane), so at the end of the range
+//   acc^T[c][n] = sum_v W[v][c] p[n][v],   l_n = sum_v p[n][v],
+//   dh_n = s (acc^T[.][n] / l_n - W[y_n]),   lse_n = (m_n + log2 l_n) ln 2.
+// An element above m_n + 80 (p > 2^80, where fp32 sums could start to lose range) flags its
+// 128-token tile; the host then runs the exact two-pass repair on flagged tiles only.
 constexpr int G_XT = 128;                  // X rows per pair (64 per CTA)
 constexpr int G_YB = 256;                  // stream rows per block (128 per CTA)
 constexpr int G_ST = 3;                    // ring slots
 constexpr int G_SLOT = 49152;              // S stage: Y 128 rows x 128 C (32 KB) + X 64 x 128 (16 KB);
                                            // accumulation stage: Y 64 rows x 128 C for every chunk (<= 48 KB)
 constexpr int G_SLOT_X = 32768;            // offset of the X box inside an S-stage slot
-constexpr int G_DZ = G_YB * 128;           // one dz buffer: 256 K-rows x 64 bf16 = 32 KB (two of them)
+constexpr int G_DZ = G_YB * 128;           // one dz buffer: 256 K-rows x 64 bf16 = 32 KB
+constexpr int G_NDZ = 2;                   // dz buffers
 constexpr int G_EPI_WARPS = 8;
 constexpr int G_THREADS = 96 + 32 * G_EPI_WARPS;   // warps 0 and 10 TMA, 1 MMA, 2-9 epilogue
+constexpr float FL_LIMIT = 80.f;           // lse+dh pass: largest exponent of p kept
+
+enum GradMode { GM_DW = 0, GM_DH = 1, GM_FL = 2 };
 
 struct GradParams {
   const int32_t* targets;
-  const float* lse;
-  const float* zt;       // target logits (pass 1)
+  const float* lse;      // dW and dh passes: per-row logsumexp (natural log)
+  const float* zt;       // dW pass: target logits
   const DevAcc* acc;     // scale of this micro-step
   unsigned* err;
   float* dW;             // dW pass output (fp32 [V, C])
-  __nv_bfloat16* dh;     // dh pass output (bf16 [N, C])
-  const __nv_bfloat16* Wt;  // dh pass: W, for the one-hot term
+  __nv_bfloat16* dh;     // dh / lse+dh pass output (bf16 [N, C])
+  const __nv_bfloat16* Wt;  // W, for the one-hot term of dh
   float* part;           // [2 * pairs][128][C] fp32 partial sums of split tiles
+  float* part_lm;        // lse+dh pass: [2 * pairs][2][128] (m, l) of split tiles
+  float* lse_out;        // lse+dh pass: per-row logsumexp
+  unsigned* tile_flag;   // lse+dh pass: per 128-token tile, set when the tile needs the repair
   int N, V, C;
   int beta;              // dW pass: 0 writes, 1 adds
 };
@@ -353,7 +373,7 @@ struct GradParams {
 // of P takes units [U pi / P, U (pi + 1) / P).  Its range crosses X tiles in segments; a segment
 // that covers a whole tile writes the output directly, a segment that covers part of a tile
 // (at most the pair's first and last) writes fp32 partial sums to slot 2 pi (first segment) or
-// 2 pi + 1, and tc_split_combine_kernel adds the partials of each split tile in pair order.
+// 2 pi + 1, and the split-combine kernels add the partials of each split tile in pair order.
 struct Sched {
   long long U;  // tiles * blocks per tile
   int P;        // pairs
@@ -368,7 +388,7 @@ struct Sched {
 };
 
 __host__ __device__ constexpr int grad_smem_bytes(int C) {
-  return G_ST * G_SLOT + 2 * G_DZ + 1024 + 0 * C;
+  return G_ST * G_SLOT + G_NDZ * G_DZ + 1024 + 0 * C;
 }
 
 __device__ __forceinline__ void st_shared_b16(uint32_t addr, uint16_t v, bool remote) {
@@ -376,22 +396,61 @@ __device__ __forceinline__ void st_shared_b16(uint32_t addr, uint16_t v, bool re
   else asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
 
-template <bool DW>
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
+// One halving step of the column reduction below: lanes with bit O set keep the upper H of
+// their 2H values and receive the partner's upper H, the others the lower halves.
+template <bool MAX, int H, int O>
+__device__ __forceinline__ void col_step(float (&v)[64], bool hi) {
+#pragma unroll
+  for (int i = 0; i < H; ++i) {
+    const float keep = hi ? v[i + H] : v[i];
+    const float send = hi ? v[i] : v[i + H];
+    const float got = __shfl_xor_sync(0xffffffffu, send, O);
+    v[i] = MAX ? fmaxf(keep, got) : keep + got;
+  }
+}
+
+// Column reduction of a 32 x 64 register tile (row = lane): afterwards lane L holds the max
+// or sum over the 32 rows of columns 2L and 2L + 1 in v[0], v[1].  62 shuffles, fixed order.
+template <bool MAX>
+__device__ __forceinline__ void col_reduce64(float (&v)[64], int lane) {
+  col_step<MAX, 32, 16>(v, lane & 16);
+  col_step<MAX, 16, 8>(v, lane & 8);
+  col_step<MAX, 8, 4>(v, lane & 4);
+  col_step<MAX, 4, 2>(v, lane & 2);
+  col_step<MAX, 2, 1>(v, lane & 1);
+}
+
+template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     tc_grad_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmYs,
                    const __grid_constant__ CUtensorMap tmYa, GradParams p) {
+  constexpr bool DW = MODE == GM_DW;
+  constexpr bool FL = MODE == GM_FL;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int KC = p.C / 128;                 // S phase stages per block (128 C each)
   const int NCH = p.C / 256;                // 256-row C chunks of acc^T
   uint8_t* sY = smem;                       // ring of G_ST slots
-  uint8_t* sDZ = sY + G_ST * G_SLOT;        // [2][256 rows][128 B]
+  uint8_t* sDZ = sY + G_ST * G_SLOT;        // [G_NDZ][256 rows][128 B]
   __shared__ __align__(8) uint64_t full[G_ST], empty[G_ST];
-  __shared__ __align__(8) uint64_t s_full, s_empty, dz_full[2][4], dz_empty[2], acc_full, acc_empty, drain_bar;
+  __shared__ __align__(8) uint64_t s_full, s_empty, dz_full[G_NDZ][4], dz_empty[G_NDZ], acc_full, acc_empty, drain_bar;
+  __shared__ __align__(8) uint64_t mx_full, lx_full;   // lse+dh pass: the peer's column max / sum arrived
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int epi_abort;
-  __shared__ float col_c[G_XT];             // dh pass: per-column log2(s) - lse log2(e), or -inf
-  __shared__ int col_y[G_XT];               // dh pass: per-column target (or -1: no gradient)
+  __shared__ float col_c[G_XT];             // dh: log2(s) - lse log2(e) or -inf;  lse+dh: reference m_n (base 2)
+  __shared__ int col_y[G_XT];               // dh, lse+dh: per-column target (or -1: no gradient)
+  __shared__ float fl_q[4][G_XT];           // lse+dh: per-lane-quarter column max / sum
+  __shared__ float fl_loc[G_XT];            // lse+dh: this CTA's column max / sum
+  __shared__ float fl_pm[2][G_XT], fl_pl[2][G_XT];  // lse+dh: the peer's column max / sum (by segment parity)
+  __shared__ float fl_L[G_XT];              // lse+dh: l_n of the pair
+  __shared__ float fl_f[G_XT];              // lse+dh: s / l_n for a valid target, else 0
+  __shared__ float fl_s[G_XT];              // lse+dh: s for a valid target, else 0
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -413,13 +472,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     }
     mbar_init(smem_u32(&s_full), 1);
     mbar_init(smem_u32(&s_empty), 2);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < G_NDZ; ++b) {
       for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&dz_full[b][q]), 4);
       mbar_init(smem_u32(&dz_empty[b]), 1);
     }
     mbar_init(smem_u32(&acc_full), 1);
     mbar_init(smem_u32(&acc_empty), 2);
     mbar_init(smem_u32(&drain_bar), 1);
+    mbar_init(smem_u32(&mx_full), 1);
+    mbar_init(smem_u32(&lx_full), 1);
     epi_abort = 0;
     fence_mbar_init();
   }
@@ -521,7 +582,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           }
           if (j >= 1) {
             // accumulation of block j-1, one 64-row quarter of dz at a time
-            const int jb = j - 1, gb = g + jb, db = gb & 1;
+            const int jb = j - 1, gb = g + jb, db = gb % G_NDZ;
             if (jb == 0) {
               // the epilogue must have drained the previous segment's accumulator
               if (!mbar_wait_cluster(smem_u32(&acc_empty), (sg & 1) ^ 1, WAIT_NS)) {
@@ -533,7 +594,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             }
             const uint32_t dzb = smem_u32(sDZ) + db * G_DZ;
             for (int q = 0; q < 4 && ok; ++q) {
-              if (!mbar_wait_cluster(smem_u32(&dz_full[db][q]), (gb >> 1) & 1, WAIT_NS)) {
+              if (!mbar_wait_cluster(smem_u32(&dz_full[db][q]), (gb / G_NDZ) & 1, WAIT_NS)) {
                 record_timeout(p.err, 23);
                 ok = false;
                 break;
@@ -581,13 +642,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     const uint32_t leader_dz_full = mapa(smem_u32(&dz_full[0][0]), 0) + (uint32_t)(kb >> 6) * 8;
     const bool remote = hf != (int)rank;         // column half hf is supplied by CTA hf
     const uint32_t dz_dst = remote ? mapa(smem_u32(sDZ), (uint32_t)hf) : smem_u32(sDZ);
+    const uint32_t peer = rank ^ 1u;
     int g = 0, sg = 0;
     for (int t = t_first; t <= t_last; ++t, ++sg) {
       const int b0 = (int)(max(ub, (long long)t * nblk) - (long long)t * nblk);
       const int nb = (int)(min(ue, (long long)(t + 1) * nblk) - (long long)t * nblk) - b0;
       const int x0 = t * G_XT;
+      float lacc0 = 0.f, lacc1 = 0.f;             // lse+dh: column sums of p, columns hf*64 + 2 lane (+1)
       if (!DW) {
-        // per-column constants of this X tile (tokens): target and log2(s) - lse log2(e)
+        // per-column constants of this X tile (tokens): the target, and for the dh pass
+        // log2(s) - lse log2(e), for the lse+dh pass the scale of a valid target
         if (et < G_XT) {
           const int n = x0 + et;
           int y = -1;
@@ -596,11 +660,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             const int tg = p.targets[n];
             if (tg >= 0 && tg < p.V) {
               y = tg;
-              c = log2s - p.lse[n] * LOG2E;
+              if (!FL) c = log2s - p.lse[n] * LOG2E;
             }
           }
           col_y[et] = y;
-          col_c[et] = c;
+          if (FL) fl_s[et] = y >= 0 ? s : 0.f;
+          else col_c[et] = c;
         }
         asm volatile("bar.sync 1, 256;" ::: "memory");
       }
@@ -645,27 +710,76 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           if (rank == 0) mbar_arrive(smem_u32(&s_empty));
           else mbar_arrive_cluster(leader_s_empty);
         }
-        // s * softmax for my row and column half; rows past the stream end get 0 (dh pass:
-        // their W rows are zero-filled and contribute nothing)
         uint32_t packed[32];
+        if (FL) {
+          const bool row_ok = ys < p.V;             // rows past the vocabulary are zero-filled: no term
+          if (j == 0) {
+            // reference m_n: the exact column max of this first block over both CTAs' rows
+            float v[64];
 #pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          float c0, c1;
-          if (DW) {
-            c0 = crow;
-            c1 = crow;
-          } else {
-            c0 = col_c[hf * 64 + e];
-            c1 = col_c[hf * 64 + e + 1];
+            for (int e = 0; e < 64; ++e) v[e] = row_ok ? z[e] : -INFINITY;
+            col_reduce64<true>(v, lane);
+            fl_q[q][hf * 64 + 2 * lane] = v[0];
+            fl_q[q][hf * 64 + 2 * lane + 1] = v[1];
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            if (et < G_XT) {
+              const float m = fmaxf(fmaxf(fl_q[0][et], fl_q[1][et]), fmaxf(fl_q[2][et], fl_q[3][et]));
+              fl_loc[et] = m;
+              st_cluster_f32(mapa(smem_u32(&fl_pm[sg & 1][et]), peer), m);
+              fence_acq_rel_cluster();
+            }
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            if (et == 0) {
+              mbar_arrive_cluster(mapa(smem_u32(&mx_full), peer));
+              if (!mbar_wait_cluster(smem_u32(&mx_full), sg & 1, WAIT_NS)) {
+                record_timeout(p.err, 29);
+                epi_abort = 1;
+              }
+            }
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            if (epi_abort) break;
+            if (et < G_XT) col_c[et] = fmaxf(fl_loc[et], fl_pm[sg & 1][et]) * LOG2E;
+            asm volatile("bar.sync 1, 256;" ::: "memory");
           }
-          const float d0 = ex2_approx(fmaf(z[e], LOG2E, c0));
-          const float d1 = ex2_approx(fmaf(z[e + 1], LOG2E, c1));
-          __nv_bfloat162 pr = __floats2bfloat162_rn(d0, d1);
-          packed[e / 2] = *reinterpret_cast<uint32_t*>(&pr);
+          // p = 2^(z log2 e - m_n); rows past the vocabulary contribute nothing
+          float tmax = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            const float tt = fmaf(z[e], LOG2E, -col_c[hf * 64 + e]);
+            tmax = fmaxf(tmax, tt);
+            z[e] = row_ok ? ex2_approx(tt) : 0.f;
+          }
+          if (row_ok && tmax > FL_LIMIT) atomicOr(p.tile_flag + t, 1u);
+#pragma unroll
+          for (int e = 0; e < 64; e += 2) {
+            __nv_bfloat162 pr = __floats2bfloat162_rn(z[e], z[e + 1]);
+            packed[e / 2] = *reinterpret_cast<uint32_t*>(&pr);
+          }
+          col_reduce64<false>(z, lane);
+          lacc0 += z[0];
+          lacc1 += z[1];
+        } else {
+          // s * softmax for my row and column half; rows past the stream end get 0 (dh pass:
+          // their W rows are zero-filled and contribute nothing)
+#pragma unroll
+          for (int e = 0; e < 64; e += 2) {
+            float c0, c1;
+            if (DW) {
+              c0 = crow;
+              c1 = crow;
+            } else {
+              c0 = col_c[hf * 64 + e];
+              c1 = col_c[hf * 64 + e + 1];
+            }
+            const float d0 = ex2_approx(fmaf(z[e], LOG2E, c0));
+            const float d1 = ex2_approx(fmaf(z[e + 1], LOG2E, c1));
+            __nv_bfloat162 pr = __floats2bfloat162_rn(d0, d1);
+            packed[e / 2] = *reinterpret_cast<uint32_t*>(&pr);
+          }
         }
-        // dz buffer gb&1 is free once the accumulation two blocks back has completed
-        const int db = gb & 1;
-        if (!mbar_wait(smem_u32(&dz_empty[db]), ((gb >> 1) & 1) ^ 1, WAIT_NS)) {
+        // dz buffer db is free once the accumulation G_NDZ blocks back has completed
+        const int db = gb % G_NDZ;
+        if (!mbar_wait(smem_u32(&dz_empty[db]), ((gb / G_NDZ) & 1) ^ 1, WAIT_NS)) {
           record_timeout(p.err, 26);
           epi_abort = 1;
         }
@@ -702,7 +816,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       if (epi_abort) break;
       tc_fence_after();
       const bool whole = b0 == 0 && nb == nblk;
-      float* part = p.part + (size_t)(2 * pi + (sg == 0 ? 0 : 1)) * G_XT * p.C;
+      const int slot = 2 * pi + (sg == 0 ? 0 : 1);
+      if (FL) {
+        // l_n: this CTA's column sums (four lane quarters), then the peer's over DSMEM
+        fl_q[q][hf * 64 + 2 * lane] = lacc0;
+        fl_q[q][hf * 64 + 2 * lane + 1] = lacc1;
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (et < G_XT) {
+          const float l = (fl_q[0][et] + fl_q[1][et]) + (fl_q[2][et] + fl_q[3][et]);
+          fl_loc[et] = l;
+          st_cluster_f32(mapa(smem_u32(&fl_pl[sg & 1][et]), peer), l);
+          fence_acq_rel_cluster();
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (et == 0) {
+          mbar_arrive_cluster(mapa(smem_u32(&lx_full), peer));
+          if (!mbar_wait_cluster(smem_u32(&lx_full), sg & 1, WAIT_NS)) {
+            record_timeout(p.err, 30);
+            epi_abort = 1;
+          }
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (epi_abort) break;
+        if (et < G_XT) {
+          // both CTAs add the two halves in rank order: the same l_n in each
+          const float mine = fl_loc[et], other = fl_pl[sg & 1][et];
+          const float l = rank == 0 ? mine + other : other + mine;
+          fl_L[et] = l;
+          fl_f[et] = fl_s[et] != 0.f ? fl_s[et] / l : 0.f;
+          const int n = x0 + et;
+          if (rank == 0) {
+            if (whole) {
+              if (n < p.N) p.lse_out[n] = (col_c[et] + log2f(l)) * LN2;
+            } else {
+              p.part_lm[((size_t)slot * 2 + 0) * G_XT + et] = col_c[et];
+              p.part_lm[((size_t)slot * 2 + 1) * G_XT + et] = l;
+            }
+          }
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+      }
+      float* part = p.part + (size_t)slot * G_XT * p.C;
       for (int i = 0; i < NCH; ++i) {
         const int c = i * 256 + (int)rank * 128 + kl;   // my C row of the accumulator
 #pragma unroll 1
@@ -719,6 +873,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
               if (DW) {
                 float* o = p.dW + (size_t)x * p.C + c;
                 *o = p.beta ? (*o + v[e]) : v[e];
+              } else if (FL) {
+                const int y = col_y[xl];
+                float val = 0.f;
+                if (y >= 0) val = v[e] * fl_f[xl] - fl_s[xl] * __bfloat162float(p.Wt[(size_t)y * p.C + c]);
+                p.dh[(size_t)x * p.C + c] = __float2bfloat16_rn(val);
               } else {
                 float val = v[e];
                 const int y = col_y[xl];
@@ -755,36 +914,64 @@ struct SplitTiles {
   int t[MAX_SPLIT_TILES];
 };
 
+// The partial slots of split tile t, in pair order (slot 2q for the pair's first segment).
+__device__ __forceinline__ int split_slots(const Sched& sch, int t, int* slots) {
+  const long long tb = (long long)t * sch.nblk, te = tb + sch.nblk;
+  const int pa = sch.pair_of(tb), pz = sch.pair_of(te - 1);
+  int n = 0;
+  for (int q = pa; q <= pz && n < 16; ++q) slots[n++] = 2 * q + ((long long)t == sch.u0(q) / sch.nblk ? 0 : 1);
+  return n;
+}
+
 // Adds the partial sums of every split X tile in pair order and writes the output exactly as
 // the gradient kernel does for whole tiles.  grid: (split tiles, ceil(128 * C / 1024)); each
 // thread handles four consecutive C columns of one row.
-template <bool DW>
+template <int MODE>
 __global__ void __launch_bounds__(256) tc_split_combine_kernel(GradParams p, Sched sch, const __grid_constant__ SplitTiles sp) {
+  constexpr bool DW = MODE == GM_DW;
+  constexpr bool FL = MODE == GM_FL;
   __shared__ int slots[16];
   __shared__ int nslots;
+  __shared__ float wts[16][G_XT];   // lse+dh: 2^(m_k - M) per slot and row
+  __shared__ float fac[G_XT];       // lse+dh: s / l for a valid target, else 0
   const int t = sp.t[blockIdx.x];
-  if (threadIdx.x == 0) {
-    const long long tb = (long long)t * sch.nblk, te = tb + sch.nblk;
-    const int pa = sch.pair_of(tb), pz = sch.pair_of(te - 1);
-    int n = 0;
-    for (int q = pa; q <= pz && n < 16; ++q) slots[n++] = 2 * q + ((long long)t == sch.u0(q) / sch.nblk ? 0 : 1);
-    nslots = n;
-  }
+  if (threadIdx.x == 0) nslots = split_slots(sch, t, slots);
   __syncthreads();
+  const int nX = DW ? p.V : p.N;
+  if (FL && threadIdx.x < G_XT) {
+    // merge the slots' (m, l) of my row: M = max m_k, l = sum l_k 2^(m_k - M)
+    const int xl = threadIdx.x, x = t * G_XT + xl;
+    float M = -INFINITY;
+    for (int k = 0; k < nslots; ++k) M = fmaxf(M, p.part_lm[((size_t)slots[k] * 2 + 0) * G_XT + xl]);
+    float l = 0.f;
+    for (int k = 0; k < nslots; ++k) {
+      const float w = exp2f(p.part_lm[((size_t)slots[k] * 2 + 0) * G_XT + xl] - M);
+      wts[k][xl] = w;
+      l += p.part_lm[((size_t)slots[k] * 2 + 1) * G_XT + xl] * w;
+    }
+    float f = 0.f;
+    if (x < p.N) {
+      const int y = p.targets[x];
+      if (y >= 0 && y < p.V) f = p.acc->scale / l;
+      if (blockIdx.y == 0) p.lse_out[x] = (M + log2f(l)) * LN2;
+    }
+    fac[xl] = f;
+  }
+  if (FL) __syncthreads();
   const int idx4 = blockIdx.y * 256 + threadIdx.x;       // index of a group of 4 columns
   const int per_row = p.C / 4;
   if (idx4 >= G_XT * per_row) return;
   const int xl = idx4 / per_row, c = (idx4 % per_row) * 4;
   const int x = t * G_XT + xl;
-  const int nX = DW ? p.V : p.N;
   if (x >= nX) return;
   float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int k = 0; k < nslots; ++k) {
     const float4 w = *reinterpret_cast<const float4*>(p.part + ((size_t)slots[k] * G_XT + xl) * p.C + c);
-    v.x += w.x;
-    v.y += w.y;
-    v.z += w.z;
-    v.w += w.w;
+    const float a = FL ? wts[k][xl] : 1.f;
+    v.x += FL ? w.x * a : w.x;
+    v.y += FL ? w.y * a : w.y;
+    v.z += FL ? w.z * a : w.z;
+    v.w += FL ? w.w * a : w.w;
   }
   if (DW) {
     float4* o = reinterpret_cast<float4*>(p.dW + (size_t)x * p.C + c);
@@ -798,7 +985,20 @@ __global__ void __launch_bounds__(256) tc_split_combine_kernel(GradParams p, Sch
     *o = v;
   } else {
     const int y = p.targets[x];
-    if (y >= 0 && y < p.V) {
+    __nv_bfloat16* o = p.dh + (size_t)x * p.C + c;
+    if (FL) {
+      const float f = fac[xl];
+      if (f == 0.f) {
+        v = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        const float sc = p.acc->scale;
+        const __nv_bfloat16* wr = p.Wt + (size_t)y * p.C + c;
+        v.x = v.x * f - sc * __bfloat162float(wr[0]);
+        v.y = v.y * f - sc * __bfloat162float(wr[1]);
+        v.z = v.z * f - sc * __bfloat162float(wr[2]);
+        v.w = v.w * f - sc * __bfloat162float(wr[3]);
+      }
+    } else if (y >= 0 && y < p.V) {
       const float sc = p.acc->scale;
       const __nv_bfloat16* wr = p.Wt + (size_t)y * p.C + c;
       v.x -= sc * __bfloat162float(wr[0]);
@@ -806,11 +1006,110 @@ __global__ void __launch_bounds__(256) tc_split_combine_kernel(GradParams p, Sch
       v.z -= sc * __bfloat162float(wr[2]);
       v.w -= sc * __bfloat162float(wr[3]);
     }
-    __nv_bfloat16* o = p.dh + (size_t)x * p.C + c;
     o[0] = __float2bfloat16_rn(v.x);
     o[1] = __float2bfloat16_rn(v.y);
     o[2] = __float2bfloat16_rn(v.z);
     o[3] = __float2bfloat16_rn(v.w);
+  }
+}
+
+// ---- per-row pre / post passes of the lse+dh path -----------------------------------------
+constexpr int PRE_ROWS = 32;   // rows per block of the pre pass (8 warps x 4 rows)
+
+// Before the lse+dh pass: target validity, the target logit z_t = h_n . W[y_n] (fp32 sum of
+// the exact bf16 products; C % 256 == 0), per-block valid counts and error flags, and the
+// tile flags cleared.
+__global__ void __launch_bounds__(256) rows_pre_kernel(StepArgs a, float* __restrict__ zt, int* __restrict__ part_cnt,
+                                                       unsigned* __restrict__ part_err, unsigned* __restrict__ tile_flag,
+                                                       int ntiles) {
+  __shared__ int sc[8];
+  __shared__ unsigned se[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0 && (int)blockIdx.x < ntiles) tile_flag[blockIdx.x] = 0u;
+  const __nv_bfloat16* H = static_cast<const __nv_bfloat16*>(a.hidden);
+  const __nv_bfloat16* W = static_cast<const __nv_bfloat16*>(a.W);
+  int cnt = 0;
+  unsigned err = 0;
+  for (int r = 0; r < PRE_ROWS / 8; ++r) {
+    const int64_t n = (int64_t)blockIdx.x * PRE_ROWS + warp * (PRE_ROWS / 8) + r;
+    if (n >= a.N) break;
+    const int y = a.targets[n];
+    const bool valid = y >= 0 && (int64_t)y < a.V;
+    float acc = 0.f;
+    if (valid) {
+      const uint4* hr = reinterpret_cast<const uint4*>(H + n * a.C);
+      const uint4* wr = reinterpret_cast<const uint4*>(W + (int64_t)y * a.C);
+      for (int64_t i = lane; i < a.C / 8; i += 32) {
+        const uint4 hv = hr[i], wv = wr[i];
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&hv);
+        const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&wv);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 hf = __bfloat1622float2(h2[k]), wf = __bfloat1622float2(w2[k]);
+          acc = fmaf(hf.x, wf.x, acc);
+          acc = fmaf(hf.y, wf.y, acc);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    }
+    if (lane == 0) {
+      zt[n] = acc;
+      cnt += valid ? 1 : 0;
+      if (!valid && y != a.ignore_id) err |= ERR_BIT_BAD_TARGET;
+    }
+  }
+  if (lane == 0) {
+    sc[warp] = cnt;
+    se[warp] = err;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int c = 0;
+    unsigned e = 0;
+    for (int w = 0; w < 8; ++w) {
+      c += sc[w];
+      e |= se[w];
+    }
+    part_cnt[blockIdx.x] = c;
+    part_err[blockIdx.x] = e;
+  }
+}
+
+// After it: row loss lse - z_t and the per-block loss partials for the fixed-order sum.
+__global__ void __launch_bounds__(256) rows_post_kernel(StepArgs a, const float* __restrict__ lse,
+                                                        const float* __restrict__ zt, double* __restrict__ part_loss,
+                                                        unsigned* __restrict__ part_err) {
+  __shared__ double sl[256];
+  __shared__ unsigned se[256];
+  const int t = threadIdx.x;
+  const int64_t n = (int64_t)blockIdx.x * 256 + t;
+  double loss = 0.0;
+  unsigned err = 0;
+  if (n < a.N) {
+    const int y = a.targets[n];
+    if (y >= 0 && (int64_t)y < a.V) {
+      const float li = lse[n] - zt[n];
+      loss = (double)li;
+      if (!isfinite(li)) err |= ERR_BIT_NONFINITE;
+      if (a.row_loss) a.row_loss[n] = li;
+    } else if (a.row_loss) {
+      a.row_loss[n] = 0.f;
+    }
+  }
+  sl[t] = loss;
+  se[t] = err;
+  __syncthreads();
+  for (int o = 128; o > 0; o >>= 1) {
+    if (t < o) {
+      sl[t] += sl[t + o];
+      se[t] |= se[t + o];
+    }
+    __syncthreads();
+  }
+  if (t == 0) {
+    part_loss[blockIdx.x] = sl[0];
+    part_err[blockIdx.x] = se[0];
   }
 }
 
@@ -896,6 +1195,8 @@ int64_t tc_pairs() { return num_sms() / 2; }
 
 size_t tc_part_bytes(int64_t C) { return (size_t)2 * (size_t)tc_pairs() * G_XT * (size_t)C * sizeof(float); }
 
+size_t tc_part_lm_bytes() { return (size_t)2 * (size_t)tc_pairs() * 2 * G_XT * sizeof(float); }
+
 
 cudaError_t tc_lse(const StepArgs& a, const Scratch& sc, Launch& L) {
   CUtensorMap mh, mw;
@@ -935,8 +1236,9 @@ cudaError_t tc_lse(const StepArgs& a, const Scratch& sc, Launch& L) {
 
 bool tc_grad_supported(int64_t C) { return C % 256 == 0 && C >= 256 && C <= 768; }
 
-template <bool DW>
+template <int MODE>
 cudaError_t tc_grad(const StepArgs& a, const Scratch& sc, Launch& L) {
+  constexpr bool DW = MODE == GM_DW;
   const void* X = DW ? a.W : a.hidden;
   const void* Y = DW ? a.hidden : a.W;
   const int64_t nX = DW ? a.V : a.N, nY = DW ? a.N : a.V;
@@ -954,6 +1256,9 @@ cudaError_t tc_grad(const StepArgs& a, const Scratch& sc, Launch& L) {
   p.dW = a.dW;
   p.dh = static_cast<__nv_bfloat16*>(a.dh);
   p.part = sc.tc_part;
+  p.part_lm = sc.tc_part_lm;
+  p.lse_out = sc.lse;
+  p.tile_flag = sc.tc_tile_flag;
   p.N = (int)a.N;
   p.V = (int)a.V;
   p.C = (int)a.C;
@@ -968,9 +1273,9 @@ cudaError_t tc_grad(const StepArgs& a, const Scratch& sc, Launch& L) {
   if (P < 1) P = 1;
   const Sched sch{U, (int)P, nblk};
   const int smem = grad_smem_bytes((int)a.C);
-  cudaFuncSetAttribute(tc_grad_kernel<DW>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  L.begin(DW ? K_DW : K_DH);
-  tc_grad_kernel<DW><<<(unsigned)(2 * P), G_THREADS, smem, L.st>>>(mx, mys, mya, p);
+  cudaFuncSetAttribute(tc_grad_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  L.begin(MODE == GM_DW ? K_DW : MODE == GM_DH ? K_DH : K_LSE_DH);
+  tc_grad_kernel<MODE><<<(unsigned)(2 * P), G_THREADS, smem, L.st>>>(mx, mys, mya, p);
   L.end();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -986,18 +1291,43 @@ cudaError_t tc_grad(const StepArgs& a, const Scratch& sc, Launch& L) {
   }
   if (sp.n == 0) return cudaSuccess;
   L.begin(K_FINISH);
-  tc_split_combine_kernel<DW><<<dim3((unsigned)sp.n, (unsigned)((G_XT * a.C / 4 + 255) / 256)), 256, 0, L.st>>>(p, sch, sp);
+  tc_split_combine_kernel<MODE><<<dim3((unsigned)sp.n, (unsigned)((G_XT * a.C / 4 + 255) / 256)), 256, 0, L.st>>>(p, sch, sp);
   L.end();
   return cudaGetLastError();
 }
 
+// Default order: the per-row pre pass (target logits, valid count, hence the scale), the
+// one-pass logsumexp + dh, the exact repair of flagged tiles (two near-empty launches when
+// none is flagged), the row losses, then the dW pass.
+static cudaError_t tc_microstep_fused(const StepArgs& a, const Scratch& sc, Launch& L) {
+  const int64_t npre = (a.N + PRE_ROWS - 1) / PRE_ROWS;
+  const int ntiles = (int)((a.N + TC_TILE_ROWS - 1) / TC_TILE_ROWS);
+  L.begin(K_FINISH);
+  rows_pre_kernel<<<(unsigned)npre, 256, 0, L.st>>>(a, sc.tc_zt, sc.part_cnt, sc.part_err, sc.tc_tile_flag, ntiles);
+  L.end();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if ((e = launch_finish(a, sc, npre, L, FIN_COUNT)) != cudaSuccess) return e;
+  if ((e = tc_grad<GM_FL>(a, sc, L)) != cudaSuccess) return e;
+  if ((e = simt_repair_lse(a, sc, L)) != cudaSuccess) return e;
+  if ((e = simt_repair_dh(a, sc, L)) != cudaSuccess) return e;
+  const int64_t nparts = tc_parts(a.N);
+  L.begin(K_FINISH);
+  rows_post_kernel<<<(unsigned)nparts, 256, 0, L.st>>>(a, sc.lse, sc.tc_zt, sc.part_loss, sc.part_err);
+  L.end();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_finish(a, sc, nparts, L, FIN_LOSS)) != cudaSuccess) return e;
+  return tc_grad<GM_DW>(a, sc, L);
+}
+
 cudaError_t tc_microstep(const StepArgs& a, const Scratch& sc, Launch& L) {
+  if (tc_grad_supported(a.C) && !a.tc_two_pass) return tc_microstep_fused(a, sc, L);
   cudaError_t e = tc_lse(a, sc, L);
   if (e != cudaSuccess) return e;
   if (!tc_grad_supported(a.C)) return simt_grads(a, sc, L);
-  e = tc_grad<true>(a, sc, L);
+  e = tc_grad<GM_DW>(a, sc, L);
   if (e != cudaSuccess) return e;
-  return tc_grad<false>(a, sc, L);
+  return tc_grad<GM_DH>(a, sc, L);
 }
 
 }  // namespace lmce

@@ -26,7 +26,7 @@ ERR_STATE = 7
 
 DTYPES = {"bf16": 0, "fp32": 1}
 NORMS = {"global": 0, "micro_mean": 1}
-PATHS = {"auto": 0, "simt": 1, "tcgen05": 2}
+PATHS = {"auto": 0, "simt": 1, "tcgen05": 2, "tcgen05_two_pass": 3}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 TORCH_DTYPES = {"bf16": torch.bfloat16, "fp32": torch.float32}
 
@@ -36,7 +36,7 @@ EXPORTS = ("lmce_create", "lmce_microstep", "lmce_finalize", "lmce_destroy", "lm
 
 NOALLOC_MAX_N = 65536
 
-KINDS = {"lse": 0, "finish": 1, "dW": 2, "dh": 3}
+KINDS = {"lse": 0, "finish": 1, "dW": 2, "dh": 3, "lse_dh": 4}
 
 
 class Config(ctypes.Structure):

@@ -63,7 +63,12 @@ typedef enum {
 typedef enum {
   LMCE_PATH_AUTO = 0,       /* tensor-core path when the shape allows it, else SIMT      */
   LMCE_PATH_SIMT = 1,       /* fp32 FFMA kernels (any C <= 2048, any V, either dtype)    */
-  LMCE_PATH_TCGEN05 = 2     /* tcgen05/TMA kernels: bf16, C % 256 == 0, 256 <= C <= 1024 */
+  LMCE_PATH_TCGEN05 = 2,    /* tcgen05/TMA kernels: bf16, C % 256 == 0, 256 <= C <= 1024.
+                               For C <= 768: one pass for logsumexp and dh (online softmax,
+                               exact repair of rare out-of-range tiles), one pass for dW;
+                               for larger C: a logsumexp pass, then dW and dh             */
+  LMCE_PATH_TCGEN05_TWO_PASS = 3  /* tensor cores, shapes as above, always a separate
+                                     logsumexp pass before the dW and dh passes          */
 } lmce_path;
 
 typedef struct lmce_config {
@@ -137,18 +142,21 @@ LMCE_API const char* lmce_status_string(int status);
 /* lmce_launch_count -- kernels this handle has launched since create (host counter). */
 LMCE_API int64_t lmce_launch_count(const lmce_handle* h);
 
-/* lmce_selected_path -- LMCE_PATH_SIMT or LMCE_PATH_TCGEN05: the path micro-steps run. */
+/* lmce_selected_path -- LMCE_PATH_SIMT, LMCE_PATH_TCGEN05 or LMCE_PATH_TCGEN05_TWO_PASS:
+ * the path micro-steps run. */
 LMCE_API int lmce_selected_path(const lmce_handle* h);
 
 /* ---- kernel timing (benchmark instrumentation) --------------------------------------
  * When enabled, the library records a CUDA event pair around every kernel it launches
  * (on the stream the kernel runs on) so that per-kernel device time can be read back.
  * Kinds: */
-#define LMCE_KIND_LSE     0  /* logits tiles + online logsumexp + per-row loss           */
-#define LMCE_KIND_FINISH  1  /* fixed-order loss / count reduction, gradient scale        */
+#define LMCE_KIND_LSE     0  /* logits tiles + online logsumexp (+ per-row loss)         */
+#define LMCE_KIND_FINISH  1  /* per-row passes, split-tile combines, fixed-order loss /  */
+                             /* count reductions, gradient scale                        */
 #define LMCE_KIND_DW      2  /* recomputed logits -> dlogits -> dW accumulation           */
 #define LMCE_KIND_DH      3  /* recomputed logits -> dlogits -> dh                        */
-#define LMCE_KIND_COUNT   4
+#define LMCE_KIND_LSE_DH  4  /* logits tiles -> online softmax -> logsumexp and dh        */
+#define LMCE_KIND_COUNT   5
 
 /* lmce_profile -- enable (1: clears earlier records) or disable (0) the event records. */
 LMCE_API int lmce_profile(lmce_handle* h, int enable);

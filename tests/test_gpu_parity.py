@@ -13,14 +13,14 @@ from gpu_util import GRAD_REL, assert_parity, max_rel_err, run_lib, run_oracle, 
 
 pytestmark = pytest.mark.gpu
 
-PATHS_BF16 = ["simt", "tcgen05"]
+PATHS_BF16 = ["simt", "tcgen05", "tcgen05_two_pass"]
 
 
 def _need_path(path, C, V, dtype):
-    if path == "tcgen05":
+    if path.startswith("tcgen05"):
         W = torch.zeros(V, C, dtype=torch.float32, device="cuda")
         try:
-            M.Lmce(C, V, 1, W, dtype, path="tcgen05").close()
+            M.Lmce(C, V, 1, W, dtype, path=path).close()
         except M.LmceError as e:
             if e.status == M.ERR_ARG:
                 pytest.xfail("tensor-core path does not take this shape yet")
@@ -64,6 +64,23 @@ def test_logit_stress_small(path):
     ref = run_oracle(w)
     assert max(float(m.lse.max()) for m in ref.micro) > 40.0
     assert_parity(got, ref, "bf16")
+
+
+def test_lse_dh_repair_of_out_of_range_tiles():
+    # One vocabulary row aligned with one token's hidden state: that token's logit there is
+    # ~0.5 |h|^2 ~ 128 nats above its first-block maximum, beyond the one-pass kernel's range
+    # (2^80), so its 128-token tile is flagged and recomputed by the exact repair; without the
+    # repair that row's dh and loss would be inf / NaN.
+    w = I.custom([300, 173], 256, 1000, "bf16", seed=11)
+    h5 = w.micro[0][0][5].float()
+    w.W[700] = (0.5 * h5).to(w.W.dtype)
+    w.micro[1][1][17] = 700
+    ref = run_oracle(w)
+    assert ref.micro[0].lse[5] > 100.0
+    for path in ("tcgen05", "tcgen05_two_pass"):
+        got = run_lib(w, path=path)
+        assert got["status"] == M.OK
+        assert_parity(got, ref, "bf16")
 
 
 def test_wide_hidden_c1024():
