@@ -546,6 +546,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       // ---------------- MMA issuer (leader CTA; the peer issues nothing) ----------------
       const uint32_t idS = idesc_bf16(256, G_XT, 0, 0);
       const uint32_t idA = idesc_bf16(256, G_XT, 1, 1);
+      // descriptors of slot 0 / dz buffer 0; an operand elsewhere is the same descriptor plus
+      // its byte offset / 16 (start-address field, no carry: shared memory < 256 KB)
+      const uint64_t dYs = sdesc_sw128(smem_u32(sY), 16, 1024);             // S phase, K-major
+      const uint64_t dXs = sdesc_sw128(smem_u32(sY) + G_SLOT_X, 16, 1024);
+      const uint64_t dYa = sdesc_sw128(smem_u32(sY), 8192, 1024);           // accumulation, MN-major
+      const uint64_t dDZ = sdesc_sw128(smem_u32(sDZ), 32768, 1024);
       bool ok = true;
       int it = 0, g = 0, sg = 0;              // stage counter, global block counter, segment counter
       for (int t = t_first; t <= t_last && ok; ++t, ++sg) {
@@ -569,12 +575,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
                 break;
               }
               tc_fence_after();
-              const uint32_t a = smem_u32(sY) + st * G_SLOT;
-              const uint32_t b = a + G_SLOT_X;
+              const uint64_t a = dYs + (uint32_t)(st * (G_SLOT >> 4));
+              const uint64_t b = dXs + (uint32_t)(st * (G_SLOT >> 4));
+              // atom (64 columns: Y 16 KB, X 8 KB apart), then 16-column (32 B) steps
 #pragma unroll
               for (int k = 0; k < 8; ++k)
-                mma_ss<2>(tS, sdesc_sw128(a + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-                          sdesc_sw128(b + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), idS, (kc | k) != 0);
+                mma_ss<2>(tS, a + ((k >> 2) * 1024 + (k & 3) * 2), b + ((k >> 2) * 512 + (k & 3) * 2), idS,
+                          (kc | k) != 0);
               mma_commit_mc2(smem_u32(&empty[st]), 3);
             }
             if (!ok) break;
@@ -592,7 +599,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
               }
               tc_fence_after();
             }
-            const uint32_t dzb = smem_u32(sDZ) + db * G_DZ;
             for (int q = 0; q < 4 && ok; ++q) {
               if (!mbar_wait_cluster(smem_u32(&dz_full[db][q]), (gb / G_NDZ) & 1, WAIT_NS)) {
                 record_timeout(p.err, 23);
@@ -607,12 +613,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
               }
               ++it;
               tc_fence_after();
-              const uint32_t a = smem_u32(sY) + st * G_SLOT;
+              const uint64_t a = dYa + (uint32_t)(st * (G_SLOT >> 4));
+              const uint64_t b = dDZ + (uint32_t)((db * G_DZ + q * 8192) >> 4);
+              // chunk i: 16 KB apart; K steps of 16 rows: 2 KB apart in both operands
               for (int i = 0; i < NCH; ++i) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                  mma_ss<2>(tmem + i * 128, sdesc_sw128(a + i * 16384 + k * 2048, 8192, 1024),
-                            sdesc_sw128(dzb + q * 8192 + k * 2048, 32768, 1024), idA, (jb | q | k) != 0);
+                  mma_ss<2>(tmem + i * 128, a + (i * 1024 + k * 128), b + k * 128, idA, (jb | q | k) != 0);
               }
               mma_commit_mc2(smem_u32(&empty[st]), 3);
             }
@@ -624,6 +631,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         g += nb;
       }
       if (!ok) {
+        // give up: wait (bounded) for the MMAs already issued before TMEM is released
         mma_commit<2>(smem_u32(&drain_bar));
         mbar_wait(smem_u32(&drain_bar), 0, WAIT_NS);
       }
