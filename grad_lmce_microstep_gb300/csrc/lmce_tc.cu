@@ -340,17 +340,32 @@ __global__ void __launch_bounds__(256) tc_combine_kernel(const float* __restrict
 // 128-token tile; the host then runs the exact two-pass repair on flagged tiles only.
 constexpr int G_XT = 128;                  // X rows per pair (64 per CTA)
 constexpr int G_YB = 256;                  // stream rows per block (128 per CTA)
-constexpr int G_ST = 3;                    // ring slots
-constexpr int G_SLOT = 49152;              // S stage: Y 128 rows x 128 C (32 KB) + X 64 x 128 (16 KB);
-                                           // accumulation stage: Y 64 rows x 128 C for every chunk (<= 48 KB)
-constexpr int G_SLOT_X = 32768;            // offset of the X box inside an S-stage slot
 constexpr int G_DZ = G_YB * 128;           // one dz buffer: 256 K-rows x 64 bf16 = 32 KB
-constexpr int G_NDZ = 2;                   // dz buffers
 constexpr int G_EPI_WARPS = 8;
 constexpr int G_THREADS = 96 + 32 * G_EPI_WARPS;   // warps 0 and 10 TMA, 1 MMA, 2-9 epilogue
 constexpr float FL_LIMIT = 80.f;           // lse+dh pass: largest exponent of p kept
 
 enum GradMode { GM_DW = 0, GM_DH = 1, GM_FL = 2 };
+
+// Ring geometry per mode: NST slots of SLOT bytes.  An S stage carries SK 64-column atoms of
+// K = C (per CTA: 128 stream rows, then 64 X rows at SK * 16 KB); an accumulation stage
+// carries AQ 64-row quarters of the stream block for every 256-row C chunk (per chunk two
+// 64-column atoms, AQ * 16 KB); NDZ dz buffers.
+template <int MODE>
+struct Geo {
+  static constexpr int NST = 3, SLOT = 49152, SK = 2, AQ = 1, NDZ = 2;
+};
+// dW pass: two 96 KB slots (fewer, larger stages: 2.18 against 2.23 ms at the 124M head) and one
+// dz buffer; 225 KB of dynamic shared memory, which leaves room only for this mode's small
+// static arrays.
+template <>
+struct Geo<GM_DW> {
+  static constexpr int NST = 2, SLOT = 98304, SK = 4, AQ = 2, NDZ = 1;
+};
+template <int MODE>
+constexpr int geo_smem_bytes() {
+  return Geo<MODE>::NST * Geo<MODE>::SLOT + Geo<MODE>::NDZ * G_DZ + 1024;
+}
 
 struct GradParams {
   const int32_t* targets;
@@ -386,10 +401,6 @@ struct Sched {
     return p;
   }
 };
-
-__host__ __device__ constexpr int grad_smem_bytes(int C) {
-  return G_ST * G_SLOT + G_NDZ * G_DZ + 1024 + 0 * C;
-}
 
 __device__ __forceinline__ void st_shared_b16(uint32_t addr, uint16_t v, bool remote) {
   if (remote) asm volatile("st.shared::cluster.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
@@ -432,14 +443,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
                    const __grid_constant__ CUtensorMap tmYa, GradParams p) {
   constexpr bool DW = MODE == GM_DW;
   constexpr bool FL = MODE == GM_FL;
+  constexpr int NST = Geo<MODE>::NST, SLOT = Geo<MODE>::SLOT, SK = Geo<MODE>::SK, AQ = Geo<MODE>::AQ;
+  constexpr int NDZ = Geo<MODE>::NDZ;
+  static_assert(SK * 24576 <= SLOT && AQ * 16384 * 3 <= SLOT && 4 % AQ == 0, "stage does not fit its slot");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int KC = p.C / 128;                 // S phase stages per block (128 C each)
+  const int KC = p.C / (64 * SK);           // S phase stages per block
   const int NCH = p.C / 256;                // 256-row C chunks of acc^T
-  uint8_t* sY = smem;                       // ring of G_ST slots
-  uint8_t* sDZ = sY + G_ST * G_SLOT;        // [G_NDZ][256 rows][128 B]
-  __shared__ __align__(8) uint64_t full[G_ST], empty[G_ST];
-  __shared__ __align__(8) uint64_t s_full, s_empty, dz_full[G_NDZ][4], dz_empty[G_NDZ], acc_full, acc_empty, drain_bar;
+  uint8_t* sY = smem;                       // ring of NST slots
+  uint8_t* sDZ = sY + NST * SLOT;           // [NDZ][256 rows][128 B]
+  __shared__ __align__(8) uint64_t full[NST], empty[NST];
+  __shared__ __align__(8) uint64_t s_full, s_empty, dz_full[NDZ][4], dz_empty[NDZ], acc_full, acc_empty, drain_bar;
   __shared__ __align__(8) uint64_t mx_full, lx_full;   // lse+dh pass: the peer's column max / sum arrived
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int epi_abort;
@@ -466,13 +480,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
   const float log2s = log2f(s);             // -inf when s == 0: every dz is then 0
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < G_ST; ++i) {
+    for (int i = 0; i < NST; ++i) {
       mbar_init(smem_u32(&full[i]), 1);
       mbar_init(smem_u32(&empty[i]), 1);
     }
     mbar_init(smem_u32(&s_full), 1);
     mbar_init(smem_u32(&s_empty), 2);
-    for (int b = 0; b < G_NDZ; ++b) {
+    for (int b = 0; b < NDZ; ++b) {
       for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&dz_full[b][q]), 4);
       mbar_init(smem_u32(&dz_empty[b]), 1);
     }
@@ -512,29 +526,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       const int nb = (int)(min(ue, (long long)(t + 1) * nblk) - (long long)t * nblk) - b0;
       const int x0 = t * G_XT;
       for (int j = 0; j <= nb && ok; ++j) {
-        const int nst = (j < nb ? KC : 0) + (j >= 1 ? 4 : 0);
+        const int nst = (j < nb ? KC : 0) + (j >= 1 ? 4 / AQ : 0);
         for (int u = 0; u < nst; ++u, ++it) {
           if ((it & 1) != pw) continue;
-          const int st = it % G_ST;
+          const int st = it % NST;
           const bool sphase = j < nb && u < KC;
           bool w = true;
           if (lane == 0) {
-            w = mbar_wait(smem_u32(&empty[st]), ((it / G_ST) & 1) ^ 1, WAIT_NS);
+            w = mbar_wait(smem_u32(&empty[st]), ((it / NST) & 1) ^ 1, WAIT_NS);
             if (!w) record_timeout(p.err, 17);
-            else if (rank == 0) mbar_expect_tx(smem_u32(&full[st]), sphase ? 2 * (32768 + 16384) : 2 * 16384 * NCH);
+            else if (rank == 0) mbar_expect_tx(smem_u32(&full[st]), sphase ? 2 * SK * 24576 : 2 * AQ * 16384 * NCH);
           }
           if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
-          const uint32_t dst = smem_u32(sY) + st * G_SLOT;
+          const uint32_t dst = smem_u32(sY) + st * SLOT;
           const uint32_t bar = lead_full + st * 8;
           if (sphase) {
-            // S phase of block b0+j: my 128 stream rows and my 64 X rows, C columns [128u, 128u + 128)
-            if (lane == 0) tma_load_3d_cg2(dst, &tmYs, bar, 0, (b0 + j) * G_YB + (int)rank * 128, u * 2);
-            else if (lane == 1) tma_load_3d_cg2(dst + G_SLOT_X, &tmX, bar, 0, x0 + (int)rank * 64, u * 2);
+            // S phase of block b0+j: my 128 stream rows and my 64 X rows, SK atoms of K from 64 SK u
+            if (lane == 0) tma_load_3d_cg2(dst, &tmYs, bar, 0, (b0 + j) * G_YB + (int)rank * 128, u * SK);
+            else if (lane == 1) tma_load_3d_cg2(dst + SK * 16384, &tmX, bar, 0, x0 + (int)rank * 64, u * SK);
           } else if (lane == 0) {
-            // accumulation phase of block b0+j-1, quarter q (64 stream rows): my 128 C of every
-            // chunk, one 4D box [chunk][atom][64 rows][64]
+            // accumulation phase of block b0+j-1, quarters AQ q .. AQ q + AQ - 1 (64 AQ stream rows):
+            // my 128 C of every chunk, one 4D box [chunk][atom][64 AQ rows][64]
             const int q = u - (j < nb ? KC : 0);
-            const int row = (b0 + j - 1) * G_YB + q * 64;
+            const int row = (b0 + j - 1) * G_YB + q * 64 * AQ;
             tma_load_4d_cg2(dst, &tmYa, bar, 0, row, 2 * (int)rank, 0);
           }
           __syncwarp();
@@ -549,8 +563,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       // descriptors of slot 0 / dz buffer 0; an operand elsewhere is the same descriptor plus
       // its byte offset / 16 (start-address field, no carry: shared memory < 256 KB)
       const uint64_t dYs = sdesc_sw128(smem_u32(sY), 16, 1024);             // S phase, K-major
-      const uint64_t dXs = sdesc_sw128(smem_u32(sY) + G_SLOT_X, 16, 1024);
-      const uint64_t dYa = sdesc_sw128(smem_u32(sY), 8192, 1024);           // accumulation, MN-major
+      const uint64_t dXs = sdesc_sw128(smem_u32(sY) + SK * 16384, 16, 1024);
+      const uint64_t dYa = sdesc_sw128(smem_u32(sY), AQ * 8192, 1024);      // accumulation, MN-major
       const uint64_t dDZ = sdesc_sw128(smem_u32(sDZ), 32768, 1024);
       bool ok = true;
       int it = 0, g = 0, sg = 0;              // stage counter, global block counter, segment counter
@@ -568,18 +582,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             }
             tc_fence_after();
             for (int kc = 0; kc < KC; ++kc, ++it) {
-              const int st = it % G_ST;
-              if (!mbar_wait(smem_u32(&full[st]), (it / G_ST) & 1, WAIT_NS)) {
+              const int st = it % NST;
+              if (!mbar_wait(smem_u32(&full[st]), (it / NST) & 1, WAIT_NS)) {
                 record_timeout(p.err, 22);
                 ok = false;
                 break;
               }
               tc_fence_after();
-              const uint64_t a = dYs + (uint32_t)(st * (G_SLOT >> 4));
-              const uint64_t b = dXs + (uint32_t)(st * (G_SLOT >> 4));
+              const uint64_t a = dYs + (uint32_t)(st * (SLOT >> 4));
+              const uint64_t b = dXs + (uint32_t)(st * (SLOT >> 4));
               // atom (64 columns: Y 16 KB, X 8 KB apart), then 16-column (32 B) steps
 #pragma unroll
-              for (int k = 0; k < 8; ++k)
+              for (int k = 0; k < 4 * SK; ++k)
                 mma_ss<2>(tS, a + ((k >> 2) * 1024 + (k & 3) * 2), b + ((k >> 2) * 512 + (k & 3) * 2), idS,
                           (kc | k) != 0);
               mma_commit_mc2(smem_u32(&empty[st]), 3);
@@ -589,7 +603,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           }
           if (j >= 1) {
             // accumulation of block j-1, one 64-row quarter of dz at a time
-            const int jb = j - 1, gb = g + jb, db = gb % G_NDZ;
+            const int jb = j - 1, gb = g + jb, db = gb % NDZ;
             if (jb == 0) {
               // the epilogue must have drained the previous segment's accumulator
               if (!mbar_wait_cluster(smem_u32(&acc_empty), (sg & 1) ^ 1, WAIT_NS)) {
@@ -599,27 +613,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
               }
               tc_fence_after();
             }
-            for (int q = 0; q < 4 && ok; ++q) {
-              if (!mbar_wait_cluster(smem_u32(&dz_full[db][q]), (gb / G_NDZ) & 1, WAIT_NS)) {
-                record_timeout(p.err, 23);
-                ok = false;
-                break;
+            for (int q = 0; q < 4 / AQ && ok; ++q) {
+              for (int r = 0; r < AQ && ok; ++r) {
+                if (!mbar_wait_cluster(smem_u32(&dz_full[db][q * AQ + r]), (gb / NDZ) & 1, WAIT_NS)) {
+                  record_timeout(p.err, 23);
+                  ok = false;
+                }
               }
-              const int st = it % G_ST;
-              if (!mbar_wait(smem_u32(&full[st]), (it / G_ST) & 1, WAIT_NS)) {
+              if (!ok) break;
+              const int st = it % NST;
+              if (!mbar_wait(smem_u32(&full[st]), (it / NST) & 1, WAIT_NS)) {
                 record_timeout(p.err, 24);
                 ok = false;
                 break;
               }
               ++it;
               tc_fence_after();
-              const uint64_t a = dYa + (uint32_t)(st * (G_SLOT >> 4));
-              const uint64_t b = dDZ + (uint32_t)((db * G_DZ + q * 8192) >> 4);
-              // chunk i: 16 KB apart; K steps of 16 rows: 2 KB apart in both operands
+              const uint64_t a = dYa + (uint32_t)(st * (SLOT >> 4));
+              const uint64_t b = dDZ + (uint32_t)((db * G_DZ + q * AQ * 8192) >> 4);
+              // chunk i: AQ * 16 KB apart; K steps of 16 rows: 2 KB apart in both operands
               for (int i = 0; i < NCH; ++i) {
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                  mma_ss<2>(tmem + i * 128, a + (i * 1024 + k * 128), b + k * 128, idA, (jb | q | k) != 0);
+                for (int k = 0; k < 4 * AQ; ++k)
+                  mma_ss<2>(tmem + i * 128, a + (i * AQ * 1024 + k * 128), b + k * 128, idA, (jb | q | k) != 0);
               }
               mma_commit_mc2(smem_u32(&empty[st]), 3);
             }
@@ -785,9 +801,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             packed[e / 2] = *reinterpret_cast<uint32_t*>(&pr);
           }
         }
-        // dz buffer db is free once the accumulation G_NDZ blocks back has completed
-        const int db = gb % G_NDZ;
-        if (!mbar_wait(smem_u32(&dz_empty[db]), ((gb / G_NDZ) & 1) ^ 1, WAIT_NS)) {
+        // dz buffer db is free once the accumulation NDZ blocks back has completed
+        const int db = gb % NDZ;
+        if (!mbar_wait(smem_u32(&dz_empty[db]), ((gb / NDZ) & 1) ^ 1, WAIT_NS)) {
           record_timeout(p.err, 26);
           epi_abort = 1;
         }
@@ -1251,8 +1267,10 @@ cudaError_t tc_grad(const StepArgs& a, const Scratch& sc, Launch& L) {
   const void* Y = DW ? a.hidden : a.W;
   const int64_t nX = DW ? a.V : a.N, nY = DW ? a.N : a.V;
   CUtensorMap mx, mys, mya;
-  if (!make_map3(&mx, X, (uint64_t)nX, (uint64_t)a.C, G_XT / 2, 2) ||
-      !make_map3(&mys, Y, (uint64_t)nY, (uint64_t)a.C, 128, 2) || !make_map4(&mya, Y, (uint64_t)nY, (uint64_t)a.C, 64))
+  constexpr int SK = Geo<MODE>::SK, AQ = Geo<MODE>::AQ;
+  if (!make_map3(&mx, X, (uint64_t)nX, (uint64_t)a.C, G_XT / 2, SK) ||
+      !make_map3(&mys, Y, (uint64_t)nY, (uint64_t)a.C, 128, SK) ||
+      !make_map4(&mya, Y, (uint64_t)nY, (uint64_t)a.C, 64 * AQ))
     return cudaErrorInvalidValue;
   GradParams p;
   p.targets = a.targets;
@@ -1280,7 +1298,7 @@ cudaError_t tc_grad(const StepArgs& a, const Scratch& sc, Launch& L) {
   if (P > U) P = U;  // every pair gets at least one unit
   if (P < 1) P = 1;
   const Sched sch{U, (int)P, nblk};
-  const int smem = grad_smem_bytes((int)a.C);
+  const int smem = geo_smem_bytes<MODE>();
   cudaFuncSetAttribute(tc_grad_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   L.begin(MODE == GM_DW ? K_DW : MODE == GM_DH ? K_DH : K_LSE_DH);
   tc_grad_kernel<MODE><<<(unsigned)(2 * P), G_THREADS, smem, L.st>>>(mx, mys, mya, p);
