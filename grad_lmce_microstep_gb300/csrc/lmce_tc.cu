@@ -381,6 +381,7 @@ struct GradParams {
   float* lse_out;        // lse+dh pass: per-row logsumexp
   unsigned* tile_flag;   // lse+dh pass: per 128-token tile, set when the tile needs the repair
   int N, V, C;
+  int ch0, nch;          // 256-row C chunks [ch0, ch0 + nch) of acc^T handled by this launch (nch <= 3)
   int beta;              // dW pass: 0 writes, 1 adds
 };
 
@@ -449,7 +450,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int KC = p.C / (64 * SK);           // S phase stages per block
-  const int NCH = p.C / 256;                // 256-row C chunks of acc^T
+  const int NCH = p.nch;                    // 256-row C chunks of acc^T in TMEM (from chunk p.ch0 on)
   uint8_t* sY = smem;                       // ring of NST slots
   uint8_t* sDZ = sY + NST * SLOT;           // [NDZ][256 rows][128 B]
   __shared__ __align__(8) uint64_t full[NST], empty[NST];
@@ -549,7 +550,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             // my 128 C of every chunk, one 4D box [chunk][atom][64 AQ rows][64]
             const int q = u - (j < nb ? KC : 0);
             const int row = (b0 + j - 1) * G_YB + q * 64 * AQ;
-            tma_load_4d_cg2(dst, &tmYa, bar, 0, row, 2 * (int)rank, 0);
+            tma_load_4d_cg2(dst, &tmYa, bar, 0, row, 2 * (int)rank, p.ch0);
           }
           __syncwarp();
         }
@@ -882,7 +883,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       }
       float* part = p.part + (size_t)slot * G_XT * p.C;
       for (int i = 0; i < NCH; ++i) {
-        const int c = i * 256 + (int)rank * 128 + kl;   // my C row of the accumulator
+        const int c = (p.ch0 + i) * 256 + (int)rank * 128 + kl;   // my C row of the accumulator
 #pragma unroll 1
         for (int cc = 0; cc < 2; ++cc) {
           float v[32];
@@ -948,8 +949,8 @@ __device__ __forceinline__ int split_slots(const Sched& sch, int t, int* slots) 
 }
 
 // Adds the partial sums of every split X tile in pair order and writes the output exactly as
-// the gradient kernel does for whole tiles.  grid: (split tiles, ceil(128 * C / 1024)); each
-// thread handles four consecutive C columns of one row.
+// the gradient kernel does for whole tiles.  grid: (split tiles, ceil(128 * 256 nch / 1024));
+// each thread handles four consecutive C columns of one row of the launch's chunk range.
 template <int MODE>
 __global__ void __launch_bounds__(256) tc_split_combine_kernel(GradParams p, Sched sch, const __grid_constant__ SplitTiles sp) {
   constexpr bool DW = MODE == GM_DW;
@@ -983,9 +984,9 @@ __global__ void __launch_bounds__(256) tc_split_combine_kernel(GradParams p, Sch
   }
   if (FL) __syncthreads();
   const int idx4 = blockIdx.y * 256 + threadIdx.x;       // index of a group of 4 columns
-  const int per_row = p.C / 4;
+  const int per_row = p.nch * 64;                         // this launch's C chunks only
   if (idx4 >= G_XT * per_row) return;
-  const int xl = idx4 / per_row, c = (idx4 % per_row) * 4;
+  const int xl = idx4 / per_row, c = p.ch0 * 256 + (idx4 % per_row) * 4;
   const int x = t * G_XT + xl;
   if (x >= nX) return;
   float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1165,14 +1166,15 @@ bool make_map3(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [cols/256][4][rows][64] view: box {64, box_rows, 2, cols/256} loads, for every 256-column
-// chunk, two 64-column atoms (this CTA's half of the chunk) of box_rows rows in one instruction.
-bool make_map4(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// [cols/256][4][rows][64] view: box {64, box_rows, 2, box_chunks} loads, for box_chunks
+// consecutive 256-column chunks, two 64-column atoms (this CTA's half of the chunk) of box_rows
+// rows in one instruction.
+bool make_map4(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_chunks) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[4] = {64, rows, 4, cols / 256};
   cuuint64_t strides[3] = {cols * 2, 128, 512};
-  cuuint32_t box[4] = {64, box_rows, 2, (cuuint32_t)(cols / 256)};
+  cuuint32_t box[4] = {64, box_rows, 2, box_chunks};
   cuuint32_t es[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1258,10 +1260,23 @@ cudaError_t tc_lse(const StepArgs& a, const Scratch& sc, Launch& L) {
   return launch_finish(a, sc, nparts, L);
 }
 
-bool tc_grad_supported(int64_t C) { return C % 256 == 0 && C >= 256 && C <= 768; }
+bool tc_grad_supported(int64_t C) { return C % 256 == 0 && C >= 256 && C <= 1024; }
+
+// TMEM holds at most three 256-row C chunks of acc^T beside the logits tile; a wider C runs the
+// pass once per range of chunks (each run recomputes the logits).  Ranges as even as possible.
+constexpr int TC_MAX_CHUNKS = 3;
+int chunk_ranges(int64_t C, int* ch0, int* nch) {
+  const int n = (int)(C / 256);
+  const int runs = (n + TC_MAX_CHUNKS - 1) / TC_MAX_CHUNKS;
+  for (int r = 0; r < runs; ++r) {
+    ch0[r] = n * r / runs;
+    nch[r] = n * (r + 1) / runs - ch0[r];
+  }
+  return runs;
+}
 
 template <int MODE>
-cudaError_t tc_grad(const StepArgs& a, const Scratch& sc, Launch& L) {
+cudaError_t tc_grad_range(const StepArgs& a, const Scratch& sc, Launch& L, int ch0, int nch) {
   constexpr bool DW = MODE == GM_DW;
   const void* X = DW ? a.W : a.hidden;
   const void* Y = DW ? a.hidden : a.W;
@@ -1270,7 +1285,7 @@ cudaError_t tc_grad(const StepArgs& a, const Scratch& sc, Launch& L) {
   constexpr int SK = Geo<MODE>::SK, AQ = Geo<MODE>::AQ;
   if (!make_map3(&mx, X, (uint64_t)nX, (uint64_t)a.C, G_XT / 2, SK) ||
       !make_map3(&mys, Y, (uint64_t)nY, (uint64_t)a.C, 128, SK) ||
-      !make_map4(&mya, Y, (uint64_t)nY, (uint64_t)a.C, 64 * AQ))
+      !make_map4(&mya, Y, (uint64_t)nY, (uint64_t)a.C, 64 * AQ, (uint32_t)nch))
     return cudaErrorInvalidValue;
   GradParams p;
   p.targets = a.targets;
@@ -1288,6 +1303,8 @@ cudaError_t tc_grad(const StepArgs& a, const Scratch& sc, Launch& L) {
   p.N = (int)a.N;
   p.V = (int)a.V;
   p.C = (int)a.C;
+  p.ch0 = ch0;
+  p.nch = nch;
   p.beta = a.beta;
   const int nblk = (int)((nY + G_YB - 1) / G_YB);
   const int T = (int)((nX + G_XT - 1) / G_XT);
@@ -1317,9 +1334,20 @@ cudaError_t tc_grad(const StepArgs& a, const Scratch& sc, Launch& L) {
   }
   if (sp.n == 0) return cudaSuccess;
   L.begin(K_FINISH);
-  tc_split_combine_kernel<MODE><<<dim3((unsigned)sp.n, (unsigned)((G_XT * a.C / 4 + 255) / 256)), 256, 0, L.st>>>(p, sch, sp);
+  tc_split_combine_kernel<MODE><<<dim3((unsigned)sp.n, (unsigned)((G_XT * 64 * nch + 255) / 256)), 256, 0, L.st>>>(p, sch, sp);
   L.end();
   return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t tc_grad(const StepArgs& a, const Scratch& sc, Launch& L) {
+  int ch0[4], nch[4];
+  const int runs = chunk_ranges(a.C, ch0, nch);
+  for (int r = 0; r < runs; ++r) {
+    const cudaError_t e = tc_grad_range<MODE>(a, sc, L, ch0[r], nch[r]);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 // Default order: the per-row pre pass (target logits, valid count, hence the scale), the

@@ -63,10 +63,10 @@ typedef enum {
 typedef enum {
   LMCE_PATH_AUTO = 0,       /* tensor-core path when the shape allows it, else SIMT      */
   LMCE_PATH_SIMT = 1,       /* fp32 FFMA kernels (any C <= 2048, any V, either dtype)    */
-  LMCE_PATH_TCGEN05 = 2,    /* tcgen05/TMA kernels: bf16, C % 256 == 0, 256 <= C <= 1024.
-                               For C <= 768: one pass for logsumexp and dh (online softmax,
-                               exact repair of rare out-of-range tiles), one pass for dW;
-                               for larger C: a logsumexp pass, then dW and dh             */
+  LMCE_PATH_TCGEN05 = 2,    /* tcgen05/TMA kernels: bf16, C % 256 == 0, 256 <= C <= 1024:
+                               one pass for logsumexp and dh (online softmax, exact repair of
+                               rare out-of-range tiles), one pass for dW; C > 768 runs each
+                               pass once per range of at most 768 columns of the gradient */
   LMCE_PATH_TCGEN05_TWO_PASS = 3  /* tensor cores, shapes as above, always a separate
                                      logsumexp pass before the dW and dh passes          */
 } lmce_path;

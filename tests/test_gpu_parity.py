@@ -83,9 +83,19 @@ def test_lse_dh_repair_of_out_of_range_tiles():
         assert_parity(got, ref, "bf16")
 
 
-def test_wide_hidden_c1024():
-    # C = 1024: tensor-core logsumexp, SIMT gradients (the tensor-core gradient pass takes C <= 768)
+@pytest.mark.parametrize("path", ["tcgen05", "tcgen05_two_pass"])
+def test_wide_hidden_c1024(path):
+    # C = 1024: TMEM holds three 256-row chunks of the gradient beside the logits tile, so each
+    # tensor-core gradient pass runs twice, over C columns [0, 512) and [512, 1024)
     w = I.custom([300, 140], 1024, 900, "bf16", seed=9, ignore_frac=0.05)
+    got = run_lib(w, path=path)
+    assert got["status"] == M.OK
+    assert_parity(got, run_oracle(w), "bf16")
+
+
+def test_c512_one_range():
+    # C = 512: two chunks in one range; ragged token and vocabulary tails
+    w = I.custom([333, 129], 512, 1100, "bf16", seed=12, ignore_frac=0.1)
     got = run_lib(w, path="tcgen05")
     assert got["status"] == M.OK
     assert_parity(got, run_oracle(w), "bf16")
