@@ -131,15 +131,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(L_THREADS, 1)
   } else if (warp == 1) {
     if (rank == 1) {
       // the peer CTA issues nothing: its TMA loads complete on the leader's barriers
-    } else if (lane == 0) {
-      // ---------------- MMA issuer (leader CTA) ----------------
+    } else {
+      // ---------------- MMA issuer (leader CTA): the whole warp runs the loop, waits are
+      // polled by all lanes and decided together, elect.sync picks the issuing lane ----------------
       const uint32_t idesc = idesc_bf16(256, 256, 0, 0);
+      const uint64_t dA = sdesc_sw128(smem_u32(smem), 16, 1024), dB = sdesc_sw128(smem_u32(smem) + L_STAGE_A, 16, 1024);
       int it = 0;
       bool ok = true;
       for (int t = 0; t < ntiles && ok; ++t) {
         const int b = t & 1;
-        if (!mbar_wait_cluster(smem_u32(&acc_empty[b]), ((t >> 1) & 1) ^ 1, WAIT_NS)) {
-          record_timeout(p.err, 3);
+        const bool we = __all_sync(0xffffffffu, mbar_wait_cluster(smem_u32(&acc_empty[b]), ((t >> 1) & 1) ^ 1, WAIT_NS));
+        if (!we) {
+          if (lane == 0) record_timeout(p.err, 3);
           ok = false;
           break;
         }
@@ -148,25 +151,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(L_THREADS, 1)
         for (int kc = 0; kc < kchunks; ++kc, ++it) {
           const int s = it % L_ST;
           const uint32_t ph = (it / L_ST) & 1;
-          if (!mbar_wait(smem_u32(&full[s]), ph, WAIT_NS)) {
-            record_timeout(p.err, 4);
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[s]), ph, WAIT_NS))) {
+            if (lane == 0) record_timeout(p.err, 4);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a = smem_u32(smem + s * L_STAGE), bb = a + L_STAGE_A;
+          const uint64_t a = dA + (uint32_t)(s * (L_STAGE >> 4)), bb = dB + (uint32_t)(s * (L_STAGE >> 4));
 #pragma unroll
           for (int k = 0; k < L_BK / 16; ++k) {
-            const uint32_t off = (k >> 2) * (L_BM * 128) + (k & 3) * 32;  // atom (64 columns), then 16-column step
-            mma_ss<2>(d, sdesc_sw128(a + off, 16, 1024), sdesc_sw128(bb + off, 16, 1024), idesc, (kc | k) != 0);
+            // atom (64 columns, 128 rows x 128 B apart), then 16-column (32 B) steps
+            const uint32_t off = ((k >> 2) * (L_BM * 128) + (k & 3) * 32) >> 4;
+            mma_ss2_elect(d, a + off, bb + off, idesc, (kc | k) != 0);
           }
-          mma_commit_mc2(smem_u32(&empty[s]), 3);
+          mma_commit_mc2_elect(smem_u32(&empty[s]), 3);
         }
-        if (ok) mma_commit_mc2(smem_u32(&acc_full[b]), 3);
+        if (ok) mma_commit_mc2_elect(smem_u32(&acc_full[b]), 3);
       }
       if (!ok) {
         // give up: wait (bounded) for the MMAs already issued before TMEM is released
-        mma_commit<2>(smem_u32(&drain_bar));
+        mma_commit2_elect(smem_u32(&drain_bar));
         mbar_wait(smem_u32(&drain_bar), 0, WAIT_NS);
       }
     }
@@ -557,8 +561,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    if (rank == 0 && lane == 0) {
+    if (rank == 0) {
       // ---------------- MMA issuer (leader CTA; the peer issues nothing) ----------------
+      // The whole warp runs the loop (warp-uniform descriptors); every wait is polled by all
+      // lanes and decided together; elect.sync picks the one lane that issues MMAs and commits.
+      auto wait_w = [&](uint32_t bar, uint32_t parity, bool cluster, unsigned where) -> bool {
+        const bool w = cluster ? mbar_wait_cluster(bar, parity, WAIT_NS) : mbar_wait(bar, parity, WAIT_NS);
+        const bool all = __all_sync(0xffffffffu, w);
+        if (!all && lane == 0) record_timeout(p.err, where);
+        return all;
+      };
       const uint32_t idS = idesc_bf16(256, G_XT, 0, 0);
       const uint32_t idA = idesc_bf16(256, G_XT, 1, 1);
       // descriptors of slot 0 / dz buffer 0; an operand elsewhere is the same descriptor plus
@@ -576,16 +588,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           if (j < nb) {
             // S^T of block j (the epilogue must have read the previous block's)
             const int gb = g + j;
-            if (!mbar_wait_cluster(smem_u32(&s_empty), (gb & 1) ^ 1, WAIT_NS)) {
-              record_timeout(p.err, 21);
+            if (!wait_w(smem_u32(&s_empty), (gb & 1) ^ 1, true, 21)) {
               ok = false;
               break;
             }
             tc_fence_after();
             for (int kc = 0; kc < KC; ++kc, ++it) {
               const int st = it % NST;
-              if (!mbar_wait(smem_u32(&full[st]), (it / NST) & 1, WAIT_NS)) {
-                record_timeout(p.err, 22);
+              if (!wait_w(smem_u32(&full[st]), (it / NST) & 1, false, 22)) {
                 ok = false;
                 break;
               }
@@ -595,20 +605,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
               // atom (64 columns: Y 16 KB, X 8 KB apart), then 16-column (32 B) steps
 #pragma unroll
               for (int k = 0; k < 4 * SK; ++k)
-                mma_ss<2>(tS, a + ((k >> 2) * 1024 + (k & 3) * 2), b + ((k >> 2) * 512 + (k & 3) * 2), idS,
-                          (kc | k) != 0);
-              mma_commit_mc2(smem_u32(&empty[st]), 3);
+                mma_ss2_elect(tS, a + ((k >> 2) * 1024 + (k & 3) * 2), b + ((k >> 2) * 512 + (k & 3) * 2), idS,
+                              (kc | k) != 0);
+              mma_commit_mc2_elect(smem_u32(&empty[st]), 3);
             }
             if (!ok) break;
-            mma_commit_mc2(smem_u32(&s_full), 3);
+            mma_commit_mc2_elect(smem_u32(&s_full), 3);
           }
           if (j >= 1) {
             // accumulation of block j-1, one 64-row quarter of dz at a time
             const int jb = j - 1, gb = g + jb, db = gb % NDZ;
             if (jb == 0) {
               // the epilogue must have drained the previous segment's accumulator
-              if (!mbar_wait_cluster(smem_u32(&acc_empty), (sg & 1) ^ 1, WAIT_NS)) {
-                record_timeout(p.err, 28);
+              if (!wait_w(smem_u32(&acc_empty), (sg & 1) ^ 1, true, 28)) {
                 ok = false;
                 break;
               }
@@ -616,15 +625,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             }
             for (int q = 0; q < 4 / AQ && ok; ++q) {
               for (int r = 0; r < AQ && ok; ++r) {
-                if (!mbar_wait_cluster(smem_u32(&dz_full[db][q * AQ + r]), (gb / NDZ) & 1, WAIT_NS)) {
-                  record_timeout(p.err, 23);
-                  ok = false;
-                }
+                if (!wait_w(smem_u32(&dz_full[db][q * AQ + r]), (gb / NDZ) & 1, true, 23)) ok = false;
               }
               if (!ok) break;
               const int st = it % NST;
-              if (!mbar_wait(smem_u32(&full[st]), (it / NST) & 1, WAIT_NS)) {
-                record_timeout(p.err, 24);
+              if (!wait_w(smem_u32(&full[st]), (it / NST) & 1, false, 24)) {
                 ok = false;
                 break;
               }
@@ -636,20 +641,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
               for (int i = 0; i < NCH; ++i) {
 #pragma unroll
                 for (int k = 0; k < 4 * AQ; ++k)
-                  mma_ss<2>(tmem + i * 128, a + (i * AQ * 1024 + k * 128), b + k * 128, idA, (jb | q | k) != 0);
+                  mma_ss2_elect(tmem + i * 128, a + (i * AQ * 1024 + k * 128), b + k * 128, idA, (jb | q | k) != 0);
               }
-              mma_commit_mc2(smem_u32(&empty[st]), 3);
+              mma_commit_mc2_elect(smem_u32(&empty[st]), 3);
             }
             if (!ok) break;
-            mma_commit_mc2(smem_u32(&dz_empty[db]), 3);
-            if (jb == nb - 1) mma_commit_mc2(smem_u32(&acc_full), 3);
+            mma_commit_mc2_elect(smem_u32(&dz_empty[db]), 3);
+            if (jb == nb - 1) mma_commit_mc2_elect(smem_u32(&acc_full), 3);
           }
         }
         g += nb;
       }
       if (!ok) {
         // give up: wait (bounded) for the MMAs already issued before TMEM is released
-        mma_commit<2>(smem_u32(&drain_bar));
+        mma_commit2_elect(smem_u32(&drain_bar));
         mbar_wait(smem_u32(&drain_bar), 0, WAIT_NS);
       }
     }

@@ -189,6 +189,19 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
         : "memory");
 }
 
+// The same for a whole warp that runs the issue loop together: elect.sync picks one lane inside
+// the instruction sequence, so the loop stays warp-uniform and its descriptors stay in uniform
+// registers (a loop run by lane 0 alone issues an MMA every ~50 ns at N = 128, this one at the
+// pipe's ~33 ns).  Every lane of the warp must execute it with the same operands.
+__device__ __forceinline__ void mma_ss2_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` (this CTA) when every earlier tcgen05 op of this thread completed.
 template <int CG>
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -196,6 +209,21 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
   else
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// Warp-uniform forms of the commits, issued by the lane elect.sync picks (the same lane that
+// issued the MMAs of a warp-uniform loop).
+__device__ __forceinline__ void mma_commit2_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_mc2_elect(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(bar),
+      "h"(mask)
+      : "memory");
 }
 // Same, arriving on the barrier at the same offset in every CTA of `mask`.
 __device__ __forceinline__ void mma_commit_mc2(uint32_t bar, uint16_t mask) {
