@@ -359,13 +359,6 @@ template <int MODE>
 struct Geo {
   static constexpr int NST = 3, SLOT = 49152, SK = 2, AQ = 1, NDZ = 2;
 };
-// dW pass: two 96 KB slots (fewer, larger stages: 2.18 against 2.23 ms at the 124M head) and one
-// dz buffer; 225 KB of dynamic shared memory, which leaves room only for this mode's small
-// static arrays.
-template <>
-struct Geo<GM_DW> {
-  static constexpr int NST = 2, SLOT = 98304, SK = 4, AQ = 2, NDZ = 1;
-};
 template <int MODE>
 constexpr int geo_smem_bytes() {
   return Geo<MODE>::NST * Geo<MODE>::SLOT + Geo<MODE>::NDZ * G_DZ + 1024;
