@@ -411,30 +411,6 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
 
 __device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 
-// One halving step of the column reduction below: lanes with bit O set keep the upper H of
-// their 2H values and receive the partner's upper H, the others the lower halves.
-template <bool MAX, int H, int O>
-__device__ __forceinline__ void col_step(float (&v)[64], bool hi) {
-#pragma unroll
-  for (int i = 0; i < H; ++i) {
-    const float keep = hi ? v[i + H] : v[i];
-    const float send = hi ? v[i] : v[i + H];
-    const float got = __shfl_xor_sync(0xffffffffu, send, O);
-    v[i] = MAX ? fmaxf(keep, got) : keep + got;
-  }
-}
-
-// Column reduction of a 32 x 64 register tile (row = lane): afterwards lane L holds the max
-// or sum over the 32 rows of columns 2L and 2L + 1 in v[0], v[1].  62 shuffles, fixed order.
-template <bool MAX>
-__device__ __forceinline__ void col_reduce64(float (&v)[64], int lane) {
-  col_step<MAX, 32, 16>(v, lane & 16);
-  col_step<MAX, 16, 8>(v, lane & 8);
-  col_step<MAX, 8, 4>(v, lane & 4);
-  col_step<MAX, 4, 2>(v, lane & 2);
-  col_step<MAX, 2, 1>(v, lane & 1);
-}
-
 template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     tc_grad_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmYs,
@@ -449,20 +425,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
   const int KC = p.C / (64 * SK);           // S phase stages per block
   const int NCH = p.nch;                    // 256-row C chunks of acc^T in TMEM (from chunk p.ch0 on)
   uint8_t* sY = smem;                       // ring of NST slots
-  uint8_t* sDZ = sY + NST * SLOT;           // [NDZ][256 rows][128 B]
+  uint8_t* sDZ = sY + NST * SLOT;           // [NDZ][4 K atoms][64 X rows][128 B], K-major
   __shared__ __align__(8) uint64_t full[NST], empty[NST];
   __shared__ __align__(8) uint64_t s_full, s_empty, dz_full[NDZ][4], dz_empty[NDZ], acc_full, acc_empty, drain_bar;
-  __shared__ __align__(8) uint64_t mx_full, lx_full;   // lse+dh pass: the peer's column max / sum arrived
+  __shared__ __align__(8) uint64_t lx_full;   // lse+dh pass: the peer's s / l_x arrived
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int epi_abort;
-  __shared__ float col_c[G_XT];             // dh: log2(s) - lse log2(e) or -inf;  lse+dh: reference m_n (base 2)
-  __shared__ int col_y[G_XT];               // dh, lse+dh: per-column target (or -1: no gradient)
-  __shared__ float fl_q[4][G_XT];           // lse+dh: per-lane-quarter column max / sum
-  __shared__ float fl_loc[G_XT];            // lse+dh: this CTA's column max / sum
-  __shared__ float fl_pm[2][G_XT], fl_pl[2][G_XT];  // lse+dh: the peer's column max / sum (by segment parity)
-  __shared__ float fl_L[G_XT];              // lse+dh: l_n of the pair
-  __shared__ float fl_f[G_XT];              // lse+dh: s / l_n for a valid target, else 0
-  __shared__ float fl_s[G_XT];              // lse+dh: s for a valid target, else 0
+  __shared__ __align__(16) float col_c[G_YB];  // dW: per stream token log2(s) - lse log2(e), or -inf (read as float4)
+  __shared__ int hit_cnt[2];                // dW: one-hot hits of the block (by block parity)
+  __shared__ uint16_t hit[2][G_YB];         // dW: (token in block) << 8 | X row in tile
+  __shared__ float fl_red[4][64];           // lse+dh: row max / sum over each 64-column quarter
+  __shared__ float fl_f[G_XT];              // lse+dh: s / l_x for a valid target, else 0 (both CTAs' rows)
+  __shared__ int col_y[G_XT];               // dh, lse+dh: target of each X row (token) of the tile, or -1
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -491,8 +465,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     mbar_init(smem_u32(&acc_full), 1);
     mbar_init(smem_u32(&acc_empty), 2);
     mbar_init(smem_u32(&drain_bar), 1);
-    mbar_init(smem_u32(&mx_full), 1);
     mbar_init(smem_u32(&lx_full), 1);
+    hit_cnt[0] = 0;
+    hit_cnt[1] = 0;
     epi_abort = 0;
     fence_mbar_init();
   }
@@ -504,7 +479,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  const uint32_t tS = tmem + NCH * 128;     // S^T columns after the accumulator chunks
+  const uint32_t tS = tmem + NCH * 128;     // S tile columns after the accumulator chunks
 
   if (warp == 0 || warp == 10) {
     // ---------------- TMA producers: two warps take alternate stages; in each, lane 0 waits
@@ -564,14 +539,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         if (!all && lane == 0) record_timeout(p.err, where);
         return all;
       };
-      const uint32_t idS = idesc_bf16(256, G_XT, 0, 0);
-      const uint32_t idA = idesc_bf16(256, G_XT, 1, 1);
+      // S = X . Y_blk^T: M = 128 X rows (64 per CTA), N = 256 stream rows (128 per CTA), K-major
+      const uint32_t idS = idesc_bf16(128, G_YB, 0, 0);
+      // acc^T += Y_blk^T . dz: M = 256 C rows per chunk (MN-major), N = 128 X rows (K-major dz)
+      const uint32_t idA = idesc_bf16(256, G_XT, 1, 0);
       // descriptors of slot 0 / dz buffer 0; an operand elsewhere is the same descriptor plus
       // its byte offset / 16 (start-address field, no carry: shared memory < 256 KB)
       const uint64_t dYs = sdesc_sw128(smem_u32(sY), 16, 1024);             // S phase, K-major
       const uint64_t dXs = sdesc_sw128(smem_u32(sY) + SK * 16384, 16, 1024);
       const uint64_t dYa = sdesc_sw128(smem_u32(sY), AQ * 8192, 1024);      // accumulation, MN-major
-      const uint64_t dDZ = sdesc_sw128(smem_u32(sDZ), 32768, 1024);
+      const uint64_t dDZ = sdesc_sw128(smem_u32(sDZ), 16, 1024);            // dz, K-major
       bool ok = true;
       int it = 0, g = 0, sg = 0;              // stage counter, global block counter, segment counter
       for (int t = t_first; t <= t_last && ok; ++t, ++sg) {
@@ -579,7 +556,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         const int nb = (int)(min(ue, (long long)(t + 1) * nblk) - (long long)t * nblk) - b0;
         for (int j = 0; j <= nb && ok; ++j) {
           if (j < nb) {
-            // S^T of block j (the epilogue must have read the previous block's)
+            // S of block j (the epilogue must have read the previous block's)
             const int gb = g + j;
             if (!wait_w(smem_u32(&s_empty), (gb & 1) ^ 1, true, 21)) {
               ok = false;
@@ -593,12 +570,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
                 break;
               }
               tc_fence_after();
-              const uint64_t a = dYs + (uint32_t)(st * (SLOT >> 4));
-              const uint64_t b = dXs + (uint32_t)(st * (SLOT >> 4));
-              // atom (64 columns: Y 16 KB, X 8 KB apart), then 16-column (32 B) steps
+              const uint64_t a = dXs + (uint32_t)(st * (SLOT >> 4));
+              const uint64_t b = dYs + (uint32_t)(st * (SLOT >> 4));
+              // atom (64 columns: X 8 KB, Y 16 KB apart), then 16-column (32 B) steps
 #pragma unroll
               for (int k = 0; k < 4 * SK; ++k)
-                mma_ss2_elect(tS, a + ((k >> 2) * 1024 + (k & 3) * 2), b + ((k >> 2) * 512 + (k & 3) * 2), idS,
+                mma_ss2_elect(tS, a + ((k >> 2) * 512 + (k & 3) * 2), b + ((k >> 2) * 1024 + (k & 3) * 2), idS,
                               (kc | k) != 0);
               mma_commit_mc2_elect(smem_u32(&empty[st]), 3);
             }
@@ -606,7 +583,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             mma_commit_mc2_elect(smem_u32(&s_full), 3);
           }
           if (j >= 1) {
-            // accumulation of block j-1, one 64-row quarter of dz at a time
+            // accumulation of block j-1, AQ 64-row quarters of dz at a time
             const int jb = j - 1, gb = g + jb, db = gb % NDZ;
             if (jb == 0) {
               // the epilogue must have drained the previous segment's accumulator
@@ -630,11 +607,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
               tc_fence_after();
               const uint64_t a = dYa + (uint32_t)(st * (SLOT >> 4));
               const uint64_t b = dDZ + (uint32_t)((db * G_DZ + q * AQ * 8192) >> 4);
-              // chunk i: AQ * 16 KB apart; K steps of 16 rows: 2 KB apart in both operands
+              // chunk i: AQ * 16 KB apart; K steps of 16 rows: A 2 KB apart, dz 32 B within its
+              // 64-row K atom (atoms 8 KB apart)
               for (int i = 0; i < NCH; ++i) {
 #pragma unroll
                 for (int k = 0; k < 4 * AQ; ++k)
-                  mma_ss2_elect(tmem + i * 128, a + (i * AQ * 1024 + k * 128), b + k * 128, idA, (jb | q | k) != 0);
+                  mma_ss2_elect(tmem + i * 128, a + (i * AQ * 1024 + k * 128), b + ((k >> 2) * 512 + (k & 3) * 2), idA,
+                                (jb | q | k) != 0);
               }
               mma_commit_mc2_elect(smem_u32(&empty[st]), 3);
             }
@@ -653,60 +632,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     }
   } else if (warp <= 9) {
     // ---------------- epilogue: warps 2..9 ----------------
-    // warp -> (TMEM lane quarter q = warp % 4, column half hf); thread = one stream row
-    const int q = warp & 3;
+    // The S tile holds this CTA's 64 X rows x the block's 256 stream rows: TMEM lanes 0-63 the
+    // stream columns 0-127, lanes 64-127 the columns 128-255 (128 TMEM columns).  Warp -> TMEM
+    // lane quarter qd = warp % 4 and column half hf; thread = one X row and 64 stream columns,
+    // i.e. one 64-column K atom of the dz operand, which it writes as one swizzled 128-byte row.
+    const int qd = warp & 3;
     const int hf = (warp - 2) >> 2;
     const int et = (warp - 2) * 32 + lane;        // 0..255 within the epilogue warps
-    const int kl = q * 32 + lane;                 // TMEM lane = my stream row in this CTA
-    const int kb = (int)rank * 128 + kl;          // row within the 256-row block
-    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const int xr = 32 * (qd & 1) + lane;          // my X row in this CTA (0..63)
+    const int xl = (int)rank * 64 + xr;           // my X row in the pair's 128-row tile
+    const int ks = (qd >> 1) * 2 + hf;            // my 64-column quarter of the stream block
+    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const uint32_t leader_s_empty = mapa(smem_u32(&s_empty), 0);
     const uint32_t leader_acc_empty = mapa(smem_u32(&acc_empty), 0);
-    const uint32_t leader_dz_full = mapa(smem_u32(&dz_full[0][0]), 0) + (uint32_t)(kb >> 6) * 8;
-    const bool remote = hf != (int)rank;         // column half hf is supplied by CTA hf
-    const uint32_t dz_dst = remote ? mapa(smem_u32(sDZ), (uint32_t)hf) : smem_u32(sDZ);
+    // dz quarter ks of buffer b: leader's dz_full[b][ks] (4 arrivals: two warps per CTA)
+    const uint32_t dzf = mapa(smem_u32(&dz_full[0][ks]), 0);
+    const uint32_t dz_row = smem_u32(sDZ) + ks * 8192;   // + buffer * G_DZ, row xr
     const uint32_t peer = rank ^ 1u;
     int g = 0, sg = 0;
     for (int t = t_first; t <= t_last; ++t, ++sg) {
       const int b0 = (int)(max(ub, (long long)t * nblk) - (long long)t * nblk);
       const int nb = (int)(min(ue, (long long)(t + 1) * nblk) - (long long)t * nblk) - b0;
       const int x0 = t * G_XT;
-      float lacc0 = 0.f, lacc1 = 0.f;             // lse+dh: column sums of p, columns hf*64 + 2 lane (+1)
+      const int xg = x0 + xl;                     // my X row
+      // dh / lse+dh: my token's target and (dh) log2(s) - lse log2(e); the targets of all 128
+      // rows of the tile for the flush
+      float crow = -INFINITY;
+      int yrow = -1;
       if (!DW) {
-        // per-column constants of this X tile (tokens): the target, and for the dh pass
-        // log2(s) - lse log2(e), for the lse+dh pass the scale of a valid target
+        if (xg < p.N) {
+          const int tg = p.targets[xg];
+          if (tg >= 0 && tg < p.V) {
+            yrow = tg;
+            if (!FL) crow = log2s - p.lse[xg] * LOG2E;
+          }
+        }
         if (et < G_XT) {
           const int n = x0 + et;
           int y = -1;
-          float c = -INFINITY;
+          if (n < p.N) {
+            const int tg = p.targets[n];
+            if (tg >= 0 && tg < p.V) y = tg;
+          }
+          col_y[et] = y;
+        }
+      }
+      float m2 = 0.f, lacc = 0.f;                 // lse+dh: my row's reference (base 2) and sum of p
+      for (int j = 0; j < nb; ++j) {
+        const int gb = g + j;
+        const int ys0 = (b0 + j) * G_YB;          // first stream row of the block
+        // dW: stream token et's constant and one-hot hit, loaded while S is computed
+        float cc = -INFINITY;
+        int hr = -1;
+        if (DW) {
+          const int n = ys0 + et;
           if (n < p.N) {
             const int tg = p.targets[n];
             if (tg >= 0 && tg < p.V) {
-              y = tg;
-              if (!FL) c = log2s - p.lse[n] * LOG2E;
-            }
-          }
-          col_y[et] = y;
-          if (FL) fl_s[et] = y >= 0 ? s : 0.f;
-          else col_c[et] = c;
-        }
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-      }
-      for (int j = 0; j < nb; ++j) {
-        const int gb = g + j;
-        const int ys = (b0 + j) * G_YB + kb;        // my stream row
-        // dW pass: my token's target, logsumexp and target logit, loaded while S is computed
-        float crow = -INFINITY;                     // log2(s) - lse log2(e), -inf: no gradient
-        int xt = -1;                                // my target's column in this X tile
-        float fix = 0.f;                            // dz of that element: s (p_t - 1)
-        if (DW && ys < p.N) {
-          const int tg = p.targets[ys];
-          if (tg >= 0 && tg < p.V) {
-            const float l2 = p.lse[ys] * LOG2E;
-            crow = log2s - l2;
-            if (tg >= x0 && tg < x0 + G_XT) {
-              xt = tg - x0;
-              fix = s * (ex2_approx(fmaf(p.zt[ys], LOG2E, -l2)) - 1.f);
+              cc = log2s - p.lse[n] * LOG2E;
+              if (tg >= x0 && tg < x0 + G_XT) hr = tg - x0;
             }
           }
         }
@@ -728,77 +712,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           for (int e = 0; e < 32; ++e) z[32 + e] = v[e];
         }
         tc_fence_before();
+        if (DW) {
+          // this block's per-token constants and hits (last block's readers are past the barrier above)
+          col_c[et] = cc;
+          if (et == 0) hit_cnt[(gb + 1) & 1] = 0;
+          if (hr >= 0) hit[gb & 1][atomicAdd(&hit_cnt[gb & 1], 1)] = (uint16_t)((et << 8) | hr);
+        }
         asm volatile("bar.sync 1, 256;" ::: "memory");
         if (warp == 2 && lane == 0) {
           if (rank == 0) mbar_arrive(smem_u32(&s_empty));
           else mbar_arrive_cluster(leader_s_empty);
         }
-        uint32_t packed[32];
         if (FL) {
-          const bool row_ok = ys < p.V;             // rows past the vocabulary are zero-filled: no term
+          // columns past the vocabulary (last block only) carry no term
+          const int nvalid = min(64, p.V - (ys0 + ks * 64));
           if (j == 0) {
-            // reference m_n: the exact column max of this first block over both CTAs' rows
-            float v[64];
+            // reference m: the exact maximum of my row over this first block (four quarters)
+            float mx = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < 64; ++e) v[e] = row_ok ? z[e] : -INFINITY;
-            col_reduce64<true>(v, lane);
-            fl_q[q][hf * 64 + 2 * lane] = v[0];
-            fl_q[q][hf * 64 + 2 * lane + 1] = v[1];
+            for (int e = 0; e < 64; ++e)
+              if (e < nvalid) mx = fmaxf(mx, z[e]);
+            fl_red[ks][xr] = mx;
             asm volatile("bar.sync 1, 256;" ::: "memory");
-            if (et < G_XT) {
-              const float m = fmaxf(fmaxf(fl_q[0][et], fl_q[1][et]), fmaxf(fl_q[2][et], fl_q[3][et]));
-              fl_loc[et] = m;
-              st_cluster_f32(mapa(smem_u32(&fl_pm[sg & 1][et]), peer), m);
-              fence_acq_rel_cluster();
-            }
-            asm volatile("bar.sync 1, 256;" ::: "memory");
-            if (et == 0) {
-              mbar_arrive_cluster(mapa(smem_u32(&mx_full), peer));
-              if (!mbar_wait_cluster(smem_u32(&mx_full), sg & 1, WAIT_NS)) {
-                record_timeout(p.err, 29);
-                epi_abort = 1;
-              }
-            }
-            asm volatile("bar.sync 1, 256;" ::: "memory");
-            if (epi_abort) break;
-            if (et < G_XT) col_c[et] = fmaxf(fl_loc[et], fl_pm[sg & 1][et]) * LOG2E;
-            asm volatile("bar.sync 1, 256;" ::: "memory");
+            m2 = fmaxf(fmaxf(fl_red[0][xr], fl_red[1][xr]), fmaxf(fl_red[2][xr], fl_red[3][xr])) * LOG2E;
           }
-          // p = 2^(z log2 e - m_n); rows past the vocabulary contribute nothing
-          float tmax = -INFINITY;
+          // p = 2^(z log2 e - m); its row sum in four partial accumulators (fixed order)
+          float tmax = -INFINITY, ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
 #pragma unroll
           for (int e = 0; e < 64; ++e) {
-            const float tt = fmaf(z[e], LOG2E, -col_c[hf * 64 + e]);
-            tmax = fmaxf(tmax, tt);
-            z[e] = row_ok ? ex2_approx(tt) : 0.f;
+            const float tt = fmaf(z[e], LOG2E, -m2);
+            const float pv = e < nvalid ? ex2_approx(tt) : 0.f;
+            if (e < nvalid) tmax = fmaxf(tmax, tt);
+            z[e] = pv;
+            if ((e & 3) == 0) ps0 += pv;
+            else if ((e & 3) == 1) ps1 += pv;
+            else if ((e & 3) == 2) ps2 += pv;
+            else ps3 += pv;
           }
-          if (row_ok && tmax > FL_LIMIT) atomicOr(p.tile_flag + t, 1u);
+          lacc += (ps0 + ps1) + (ps2 + ps3);
+          if (tmax > FL_LIMIT) atomicOr(p.tile_flag + t, 1u);
+        } else if (DW) {
+          // my columns whose token targets my row: dz there is s (p - 1)
+          uint64_t fix = 0;
+          const int nh = hit_cnt[gb & 1];
+          for (int i = 0; i < nh; ++i) {
+            const int hv = hit[gb & 1][i];
+            if ((hv & 255) == xl && (hv >> 14) == ks) fix |= 1ull << ((hv >> 8) & 63);
+          }
+          // s * softmax per token column (its constant from the table), minus s at the hits
 #pragma unroll
-          for (int e = 0; e < 64; e += 2) {
-            __nv_bfloat162 pr = __floats2bfloat162_rn(z[e], z[e + 1]);
-            packed[e / 2] = *reinterpret_cast<uint32_t*>(&pr);
+          for (int e = 0; e < 64; e += 4) {
+            const float4 c4 = *reinterpret_cast<const float4*>(&col_c[ks * 64 + e]);
+            z[e] = ex2_approx(fmaf(z[e], LOG2E, c4.x)) - ((fix >> e) & 1 ? s : 0.f);
+            z[e + 1] = ex2_approx(fmaf(z[e + 1], LOG2E, c4.y)) - ((fix >> (e + 1)) & 1 ? s : 0.f);
+            z[e + 2] = ex2_approx(fmaf(z[e + 2], LOG2E, c4.z)) - ((fix >> (e + 2)) & 1 ? s : 0.f);
+            z[e + 3] = ex2_approx(fmaf(z[e + 3], LOG2E, c4.w)) - ((fix >> (e + 3)) & 1 ? s : 0.f);
           }
-          col_reduce64<false>(z, lane);
-          lacc0 += z[0];
-          lacc1 += z[1];
         } else {
-          // s * softmax for my row and column half; rows past the stream end get 0 (dh pass:
-          // their W rows are zero-filled and contribute nothing)
+          // s * softmax of my row (its constant); stream rows past the vocabulary have zero W
 #pragma unroll
-          for (int e = 0; e < 64; e += 2) {
-            float c0, c1;
-            if (DW) {
-              c0 = crow;
-              c1 = crow;
-            } else {
-              c0 = col_c[hf * 64 + e];
-              c1 = col_c[hf * 64 + e + 1];
-            }
-            const float d0 = ex2_approx(fmaf(z[e], LOG2E, c0));
-            const float d1 = ex2_approx(fmaf(z[e + 1], LOG2E, c1));
-            __nv_bfloat162 pr = __floats2bfloat162_rn(d0, d1);
-            packed[e / 2] = *reinterpret_cast<uint32_t*>(&pr);
-          }
+          for (int e = 0; e < 64; ++e) z[e] = ex2_approx(fmaf(z[e], LOG2E, crow));
+        }
+        uint32_t packed[32];
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {
+          __nv_bfloat162 pr = __floats2bfloat162_rn(z[e], z[e + 1]);
+          packed[e / 2] = *reinterpret_cast<uint32_t*>(&pr);
         }
         // dz buffer db is free once the accumulation NDZ blocks back has completed
         const int db = gb % NDZ;
@@ -806,28 +785,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           record_timeout(p.err, 26);
           epi_abort = 1;
         }
+        // my row of K atom ks, K-major, 128-byte swizzle: all in this CTA's shared memory
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const uint32_t addr = dz_dst + db * G_DZ + sw128_offset(kb, c * 16);
+          const uint32_t addr = dz_row + db * G_DZ + sw128_offset(xr, c * 16);
           const uint32_t* w = packed + c * 4;
-          if (remote)
-            asm volatile("st.shared::cluster.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
-                         "r"(w[2]), "r"(w[3])
-                         : "memory");
-          else
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-                         "r"(w[3])
-                         : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                       : "memory");
         }
-        if (DW && xt >= hf * 64 && xt < hf * 64 + 64) {
-          __nv_bfloat16 fb = __float2bfloat16_rn(fix);
-          st_shared_b16(dz_dst + db * G_DZ + sw128_offset(kb, (xt - hf * 64) * 2), *reinterpret_cast<uint16_t*>(&fb),
-                        remote);
-        }
-        if (remote) fence_proxy_async();
-        else fence_proxy_async_smem();
+        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(leader_dz_full + db * 32);
+        if (lane == 0) {
+          if (rank == 0) mbar_arrive(smem_u32(&dz_full[db][ks]));
+          else mbar_arrive_cluster(dzf + db * 32);
+        }
       }
       // accumulator -> output (whole tile) or partial slot (part of a tile); an abort is
       // acted on only right after a barrier, so every epilogue thread takes the same branch
@@ -841,14 +812,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       const bool whole = b0 == 0 && nb == nblk;
       const int slot = 2 * pi + (sg == 0 ? 0 : 1);
       if (FL) {
-        // l_n: this CTA's column sums (four lane quarters), then the peer's over DSMEM
-        fl_q[q][hf * 64 + 2 * lane] = lacc0;
-        fl_q[q][hf * 64 + 2 * lane + 1] = lacc1;
+        // l_x of my rows (four quarters, fixed order); s / l_x for both CTAs' rows via DSMEM
+        fl_red[ks][xr] = lacc;
         asm volatile("bar.sync 1, 256;" ::: "memory");
-        if (et < G_XT) {
-          const float l = (fl_q[0][et] + fl_q[1][et]) + (fl_q[2][et] + fl_q[3][et]);
-          fl_loc[et] = l;
-          st_cluster_f32(mapa(smem_u32(&fl_pl[sg & 1][et]), peer), l);
+        if (ks == 0) {
+          const float l = (fl_red[0][xr] + fl_red[1][xr]) + (fl_red[2][xr] + fl_red[3][xr]);
+          const float f = yrow >= 0 ? s / l : 0.f;
+          fl_f[xl] = f;
+          st_cluster_f32(mapa(smem_u32(&fl_f[xl]), peer), f);
+          if (whole) {
+            if (xg < p.N) p.lse_out[xg] = (m2 + log2f(l)) * LN2;
+          } else {
+            p.part_lm[((size_t)slot * 2 + 0) * G_XT + xl] = m2;
+            p.part_lm[((size_t)slot * 2 + 1) * G_XT + xl] = l;
+          }
           fence_acq_rel_cluster();
         }
         asm volatile("bar.sync 1, 256;" ::: "memory");
@@ -861,25 +838,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         }
         asm volatile("bar.sync 1, 256;" ::: "memory");
         if (epi_abort) break;
-        if (et < G_XT) {
-          // both CTAs add the two halves in rank order: the same l_n in each
-          const float mine = fl_loc[et], other = fl_pl[sg & 1][et];
-          const float l = rank == 0 ? mine + other : other + mine;
-          fl_L[et] = l;
-          fl_f[et] = fl_s[et] != 0.f ? fl_s[et] / l : 0.f;
-          const int n = x0 + et;
-          if (rank == 0) {
-            if (whole) {
-              if (n < p.N) p.lse_out[n] = (col_c[et] + log2f(l)) * LN2;
-            } else {
-              p.part_lm[((size_t)slot * 2 + 0) * G_XT + et] = col_c[et];
-              p.part_lm[((size_t)slot * 2 + 1) * G_XT + et] = l;
-            }
-          }
-        }
-        asm volatile("bar.sync 1, 256;" ::: "memory");
       }
+      // acc^T in TMEM: lane = C row, column = X row of the tile; thread: lane quarter qd, columns hf*64..
       float* part = p.part + (size_t)slot * G_XT * p.C;
+      const int kl = qd * 32 + lane;
       for (int i = 0; i < NCH; ++i) {
         const int c = (p.ch0 + i) * 256 + (int)rank * 128 + kl;   // my C row of the accumulator
 #pragma unroll 1
@@ -888,23 +850,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           tmem_ld32(tmem + i * 128 + lane_off + hf * 64 + cc * 32, v);
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const int xl = hf * 64 + cc * 32 + e;
-            const int x = x0 + xl;
+            const int xc = hf * 64 + cc * 32 + e;
+            const int x = x0 + xc;
             if (!whole) {
-              part[(size_t)xl * p.C + c] = v[e];
+              part[(size_t)xc * p.C + c] = v[e];
             } else if (x < nX) {
               if (DW) {
                 float* o = p.dW + (size_t)x * p.C + c;
                 *o = p.beta ? (*o + v[e]) : v[e];
-              } else if (FL) {
-                const int y = col_y[xl];
-                float val = 0.f;
-                if (y >= 0) val = v[e] * fl_f[xl] - fl_s[xl] * __bfloat162float(p.Wt[(size_t)y * p.C + c]);
-                p.dh[(size_t)x * p.C + c] = __float2bfloat16_rn(val);
               } else {
-                float val = v[e];
-                const int y = col_y[xl];
-                if (y >= 0) val -= s * __bfloat162float(p.Wt[(size_t)y * p.C + c]);
+                const int y = col_y[xc];
+                float val = 0.f;
+                if (y >= 0) val = (FL ? v[e] * fl_f[xc] : v[e]) - s * __bfloat162float(p.Wt[(size_t)y * p.C + c]);
                 p.dh[(size_t)x * p.C + c] = __float2bfloat16_rn(val);
               }
             }
