@@ -427,7 +427,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
   uint8_t* sY = smem;                       // ring of NST slots
   uint8_t* sDZ = sY + NST * SLOT;           // [NDZ][4 K atoms][64 X rows][128 B], K-major
   __shared__ __align__(8) uint64_t full[NST], empty[NST];
-  __shared__ __align__(8) uint64_t s_full, s_empty, dz_full[NDZ][4], dz_empty[NDZ], acc_full, acc_empty, drain_bar;
+  __shared__ __align__(8) uint64_t s_full, s_empty, dz_full[NDZ], dz_empty[NDZ], acc_full, acc_empty, drain_bar;
   __shared__ __align__(8) uint64_t lx_full;   // lse+dh pass: the peer's s / l_x arrived
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int epi_abort;
@@ -459,7 +459,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     mbar_init(smem_u32(&s_full), 1);
     mbar_init(smem_u32(&s_empty), 2);
     for (int b = 0; b < NDZ; ++b) {
-      for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&dz_full[b][q]), 4);
+      mbar_init(smem_u32(&dz_full[b]), 16);    // every epilogue warp of both CTAs, once per block
       mbar_init(smem_u32(&dz_empty[b]), 1);
     }
     mbar_init(smem_u32(&acc_full), 1);
@@ -594,10 +594,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
               tc_fence_after();
             }
             for (int q = 0; q < 4 / AQ && ok; ++q) {
-              for (int r = 0; r < AQ && ok; ++r) {
-                if (!wait_w(smem_u32(&dz_full[db][q * AQ + r]), (gb / NDZ) & 1, true, 23)) ok = false;
+              // the whole dz tile of the block (one wait per block: the epilogue is far ahead)
+              if (q == 0 && !wait_w(smem_u32(&dz_full[db]), (gb / NDZ) & 1, true, 23)) {
+                ok = false;
+                break;
               }
-              if (!ok) break;
               const int st = it % NST;
               if (!wait_w(smem_u32(&full[st]), (it / NST) & 1, false, 24)) {
                 ok = false;
@@ -645,8 +646,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const uint32_t leader_s_empty = mapa(smem_u32(&s_empty), 0);
     const uint32_t leader_acc_empty = mapa(smem_u32(&acc_empty), 0);
-    // dz quarter ks of buffer b: leader's dz_full[b][ks] (4 arrivals: two warps per CTA)
-    const uint32_t dzf = mapa(smem_u32(&dz_full[0][ks]), 0);
+    // dz buffer b: leader's dz_full[b] (16 arrivals: every epilogue warp of both CTAs)
+    const uint32_t dzf = mapa(smem_u32(&dz_full[0]), 0);
     const uint32_t dz_row = smem_u32(sDZ) + ks * 8192;   // + buffer * G_DZ, row xr
     const uint32_t peer = rank ^ 1u;
     int g = 0, sg = 0;
@@ -796,8 +797,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          if (rank == 0) mbar_arrive(smem_u32(&dz_full[db][ks]));
-          else mbar_arrive_cluster(dzf + db * 32);
+          if (rank == 0) mbar_arrive(smem_u32(&dz_full[db]));
+          else mbar_arrive_cluster(dzf + db * 8);
         }
       }
       // accumulator -> output (whole tile) or partial slot (part of a tile); an abort is
