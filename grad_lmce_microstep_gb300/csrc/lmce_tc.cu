@@ -355,13 +355,16 @@ enum GradMode { GM_DW = 0, GM_DH = 1, GM_FL = 2 };
 // K = C (per CTA: 128 stream rows, then 64 X rows at SK * 16 KB); an accumulation stage
 // carries AQ 64-row quarters of the stream block for every 256-row C chunk (per chunk two
 // 64-column atoms, AQ * 16 KB); NDZ dz buffers.
+// Four 48 KB slots and one dz buffer (4 x 48 + 32 KB dynamic + 3 KB static = the 227 KB a CTA may
+// have): with the epilogue finishing a block's dz well before the pipe needs it, a deeper ring
+// pays more than a second dz buffer.
 template <int MODE>
 struct Geo {
-  static constexpr int NST = 3, SLOT = 49152, SK = 2, AQ = 1, NDZ = 2;
+  static constexpr int NST = 4, SLOT = 49152, SK = 2, AQ = 1, NDZ = 1;
 };
 template <int MODE>
 constexpr int geo_smem_bytes() {
-  return Geo<MODE>::NST * Geo<MODE>::SLOT + Geo<MODE>::NDZ * G_DZ + 1024;
+  return Geo<MODE>::NST * Geo<MODE>::SLOT + Geo<MODE>::NDZ * G_DZ;   // the buffer is declared 1024-aligned
 }
 
 struct GradParams {
@@ -420,8 +423,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
   constexpr int NST = Geo<MODE>::NST, SLOT = Geo<MODE>::SLOT, SK = Geo<MODE>::SK, AQ = Geo<MODE>::AQ;
   constexpr int NDZ = Geo<MODE>::NDZ;
   static_assert(SK * 24576 <= SLOT && AQ * 16384 * 3 <= SLOT && 4 % AQ == 0, "stage does not fit its slot");
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 128-byte-swizzled operands need 1024-byte alignment; the launch reserves no slack for
+  // realigning, so a misaligned buffer is reported (both CTAs of the pair see the same layout
+  // and leave together) instead of being used
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) record_timeout(p.err, 31);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   const int KC = p.C / (64 * SK);           // S phase stages per block
   const int NCH = p.nch;                    // 256-row C chunks of acc^T in TMEM (from chunk p.ch0 on)
   uint8_t* sY = smem;                       // ring of NST slots
