@@ -857,22 +857,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         const int c = (p.ch0 + i) * 256 + (int)rank * 128 + kl;   // my C row of the accumulator
 #pragma unroll 1
         for (int cc = 0; cc < 2; ++cc) {
+          const int xb = hf * 64 + cc * 32;       // first tile column of this round
+          // the round's global operands (dW to add to, W[y] of the one-hot term) are all loaded
+          // before its first store: the compiler may not move a load above a store that could
+          // alias it, and one DRAM round trip per element would dominate the flush
+          float o[32];
+          if (whole) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              o[e] = 0.f;
+              if (DW) {
+                if (p.beta && x0 + xb + e < nX) o[e] = p.dW[(size_t)(x0 + xb + e) * p.C + c];
+              } else {
+                const int y = col_y[xb + e];
+                if (y >= 0) o[e] = __bfloat162float(p.Wt[(size_t)y * p.C + c]);
+              }
+            }
+          }
           float v[32];
-          tmem_ld32(tmem + i * 128 + lane_off + hf * 64 + cc * 32, v);
+          tmem_ld32(tmem + i * 128 + lane_off + xb, v);
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const int xc = hf * 64 + cc * 32 + e;
+            const int xc = xb + e;
             const int x = x0 + xc;
             if (!whole) {
               part[(size_t)xc * p.C + c] = v[e];
             } else if (x < nX) {
               if (DW) {
-                float* o = p.dW + (size_t)x * p.C + c;
-                *o = p.beta ? (*o + v[e]) : v[e];
+                p.dW[(size_t)x * p.C + c] = p.beta ? (o[e] + v[e]) : v[e];
               } else {
-                const int y = col_y[xc];
                 float val = 0.f;
-                if (y >= 0) val = (FL ? v[e] * fl_f[xc] : v[e]) - s * __bfloat162float(p.Wt[(size_t)y * p.C + c]);
+                if (col_y[xc] >= 0) val = (FL ? v[e] * fl_f[xc] : v[e]) - s * o[e];
                 p.dh[(size_t)x * p.C + c] = __float2bfloat16_rn(val);
               }
             }
