@@ -417,7 +417,8 @@ __device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.ac
 template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     tc_grad_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmYs,
-                   const __grid_constant__ CUtensorMap tmYa, GradParams p) {
+                   const __grid_constant__ CUtensorMap tmYa, const __grid_constant__ CUtensorMap tmO,
+                   const __grid_constant__ CUtensorMap tmP, GradParams p) {
   constexpr bool DW = MODE == GM_DW;
   constexpr bool FL = MODE == GM_FL;
   constexpr int NST = Geo<MODE>::NST, SLOT = Geo<MODE>::SLOT, SK = Geo<MODE>::SK, AQ = Geo<MODE>::AQ;
@@ -660,7 +661,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     const uint32_t dzf = mapa(smem_u32(&dz_full[0]), 0);
     const uint32_t dz_row = smem_u32(sDZ) + ks * 8192;   // + buffer * G_DZ, row xr
     const uint32_t peer = rank ^ 1u;
+    if (et == 0) {
+      tma_prefetch_desc(&tmO);
+      tma_prefetch_desc(&tmP);
+    }
     int g = 0, sg = 0;
+    // dh passes, whole tiles: the one-hot rows W[y] of a 256-column chunk, 16 B per thread and row
+    // (16 threads per 256-byte row, rows wr + 16 j), loaded one chunk ahead of their use
+    const int wr = et >> 4, ws = et & 15;
+    uint4 wv[8];
+    auto wload = [&](int i) {
+      const int c0 = (p.ch0 + i) * 256 + (int)rank * 128;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int y = col_y[wr + 16 * j];   // rows without a target read row 0 and ignore it
+        wv[j] = __ldg(reinterpret_cast<const uint4*>(p.Wt + (size_t)(y >= 0 ? y : 0) * p.C + c0) + ws);
+      }
+    };
     for (int t = t_first; t <= t_last; ++t, ++sg) {
       const int b0 = (int)(max(ub, (long long)t * nblk) - (long long)t * nblk);
       const int nb = (int)(min(ue, (long long)(t + 1) * nblk) - (long long)t * nblk) - b0;
@@ -813,6 +830,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       }
       // accumulator -> output (whole tile) or partial slot (part of a tile); an abort is
       // acted on only right after a barrier, so every epilogue thread takes the same branch
+      const bool whole = b0 == 0 && nb == nblk;
+      if (!DW && whole) wload(0);   // in flight while the last accumulation completes
       if (!mbar_wait(smem_u32(&acc_full), sg & 1, WAIT_NS)) {
         record_timeout(p.err, 27);
         epi_abort = 1;
@@ -820,7 +839,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       asm volatile("bar.sync 1, 256;" ::: "memory");
       if (epi_abort) break;
       tc_fence_after();
-      const bool whole = b0 == 0 && nb == nblk;
       const int slot = 2 * pi + (sg == 0 ? 0 : 1);
       if (FL) {
         // l_x of my rows (four quarters, fixed order); s / l_x for both CTAs' rows via DSMEM
@@ -850,50 +868,92 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         asm volatile("bar.sync 1, 256;" ::: "memory");
         if (epi_abort) break;
       }
-      // acc^T in TMEM: lane = C row, column = X row of the tile; thread: lane quarter qd, columns hf*64..
-      float* part = p.part + (size_t)slot * G_XT * p.C;
+      // acc^T in TMEM: lane = C row, column = X row of the tile; thread: lane quarter qd (C rows
+      // qd*32 + lane of this CTA's 128 per chunk), columns from hf*64.  The dW pass and whole dh
+      // tiles leave through the dz buffer (idle: the segment's accumulation has completed) by
+      // TMA, so the flush is not limited by the rate at which one SM retires scattered stores:
+      //  - dW pass: 16-column rounds through two 16 KB halves, each round two boxes of 16 X rows
+      //    x 128 C (accumulating into dW: reduce-add at L2; else stores; partial tiles: stores);
+      //  - bf16 dh of a whole tile: one 256-column chunk at a time; the rows W[y] of its one-hot
+      //    term are first stored into the buffer (row x at 256 B x) and dh overwrites them.
       const int kl = qd * 32 + lane;
-      for (int i = 0; i < NCH; ++i) {
-        const int c = (p.ch0 + i) * 256 + (int)rank * 128 + kl;   // my C row of the accumulator
+      const uint32_t stg = smem_u32(sDZ);
+      if (!DW && whole) {
+        __nv_bfloat16* sw = reinterpret_cast<__nv_bfloat16*>(sDZ);
+        for (int i = 0; i < NCH; ++i) {
+          const int c0 = (p.ch0 + i) * 256 + (int)rank * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(sDZ + (wr + 16 * j) * 256 + ws * 16) = wv[j];
+          asm volatile("bar.sync 1, 256;" ::: "memory");
+          if (i + 1 < NCH) wload(i + 1);
 #pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
-          const int xb = hf * 64 + cc * 32;       // first tile column of this round
-          // the round's global operands (dW to add to, W[y] of the one-hot term) are all loaded
-          // before its first store: the compiler may not move a load above a store that could
-          // alias it, and one DRAM round trip per element would dominate the flush
-          float o[32];
-          if (whole) {
+          for (int cc = 0; cc < 2; ++cc) {
+            float v[32];
+            tmem_ld32(tmem + i * 128 + lane_off + hf * 64 + cc * 32, v);
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              o[e] = 0.f;
-              if (DW) {
-                if (p.beta && x0 + xb + e < nX) o[e] = p.dW[(size_t)(x0 + xb + e) * p.C + c];
-              } else {
-                const int y = col_y[xb + e];
-                if (y >= 0) o[e] = __bfloat162float(p.Wt[(size_t)y * p.C + c]);
-              }
+              const int xc = hf * 64 + cc * 32 + e;
+              __nv_bfloat16* q = sw + xc * 128 + kl;
+              float val = 0.f;
+              if (col_y[xc] >= 0) val = (FL ? v[e] * fl_f[xc] : v[e]) - s * __bfloat162float(*q);
+              *q = __float2bfloat16_rn(val);
             }
           }
-          float v[32];
-          tmem_ld32(tmem + i * 128 + lane_off + xb, v);
+          fence_proxy_async_smem();
+          asm volatile("bar.sync 1, 256;" ::: "memory");
+          if (et == 0) {
+            tma_store_2d(&tmO, stg, c0, x0);   // rows past N are clipped
+            bulk_commit();
+            bulk_wait_read0();                 // the next chunk's rows go to the same buffer
+          }
+          asm volatile("bar.sync 1, 256;" ::: "memory");
+        }
+      } else if (!DW) {
+        // partial tile of a dh pass: fp32 partial sums with plain stores (measured faster here
+        // than the staged path, whose TMA traffic competes with this pass's operand stream)
+        float* part = p.part + (size_t)slot * G_XT * p.C;
+        for (int i = 0; i < NCH; ++i) {
+          const int c = (p.ch0 + i) * 256 + (int)rank * 128 + kl;
+#pragma unroll 1
+          for (int cc = 0; cc < 2; ++cc) {
+            float v[32];
+            tmem_ld32(tmem + i * 128 + lane_off + hf * 64 + cc * 32, v);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int xc = xb + e;
-            const int x = x0 + xc;
-            if (!whole) {
-              part[(size_t)xc * p.C + c] = v[e];
-            } else if (x < nX) {
-              if (DW) {
-                p.dW[(size_t)x * p.C + c] = p.beta ? (o[e] + v[e]) : v[e];
-              } else {
-                float val = 0.f;
-                if (col_y[xc] >= 0) val = (FL ? v[e] * fl_f[xc] : v[e]) - s * o[e];
-                p.dh[(size_t)x * p.C + c] = __float2bfloat16_rn(val);
+            for (int e = 0; e < 32; ++e) part[(size_t)(hf * 64 + cc * 32 + e) * p.C + c] = v[e];
+          }
+        }
+      } else {
+        float* sf = reinterpret_cast<float*>(sDZ);
+        int r = 0;
+        for (int i = 0; i < NCH; ++i) {
+          const int c0 = (p.ch0 + i) * 256 + (int)rank * 128;
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc, ++r) {
+            float v[16];
+            tmem_ld16(tmem + i * 128 + lane_off + hf * 64 + cc * 16, v);
+            float* buf = sf + (r & 1) * 4096;           // rows hf*16 + e, 128 floats each
+#pragma unroll
+            for (int e = 0; e < 16; ++e) buf[(hf * 16 + e) * 128 + kl] = v[e];
+            fence_proxy_async_smem();
+            if (et == 0) bulk_wait_read0();             // last round's boxes have read the other half
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            if (et == 0) {
+              const uint32_t src = stg + (uint32_t)(r & 1) * 16384;
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int xr0 = h * 64 + cc * 16;
+                // a whole tile's box may reach past the last row (clipped), never start there
+                if (!whole) tma_store_2d(&tmP, src + h * 8192, c0, slot * G_XT + xr0);
+                else if (x0 + xr0 >= nX) continue;
+                else if (p.beta) tma_reduce_add_2d(&tmO, src + h * 8192, c0, x0 + xr0);
+                else tma_store_2d(&tmO, src + h * 8192, c0, x0 + xr0);
               }
+              bulk_commit();
             }
           }
         }
       }
+      if (et == 0) bulk_wait_read0();   // the buffer holds the next block's dz
       tc_fence_before();
       asm volatile("bar.sync 1, 256;" ::: "memory");
       if (warp == 2 && lane == 0) {
@@ -902,6 +962,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       }
       g += nb;
     }
+    if (et == 0) bulk_wait0();   // every flush's global writes are performed before the CTA exits
   }
 
   tc_fence_before();
@@ -1162,6 +1223,21 @@ bool make_map4(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row-major [rows][cols] fp32 or bf16 matrix, box {128 columns, box_rows rows}, no swizzle: the
+// gradient kernels' flush writes its staged tiles through these (stores and reduce-adds).
+bool make_map_rows(CUtensorMap* m, void* ptr, uint64_t rows, uint64_t cols, bool f32, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const uint64_t es = f32 ? 4 : 2;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * es};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t el[2] = {1, 1};
+  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, el,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int num_sms() {
   static int n = 0;
   if (!n) {
@@ -1262,11 +1338,15 @@ cudaError_t tc_grad_range(const StepArgs& a, const Scratch& sc, Launch& L, int c
   const void* X = DW ? a.W : a.hidden;
   const void* Y = DW ? a.hidden : a.W;
   const int64_t nX = DW ? a.V : a.N, nY = DW ? a.N : a.V;
-  CUtensorMap mx, mys, mya;
+  CUtensorMap mx, mys, mya, mo, mp;
   constexpr int SK = Geo<MODE>::SK, AQ = Geo<MODE>::AQ;
+  // flush targets: dW (fp32, 16-row boxes) or dh (bf16, whole 128-row tiles); the fp32 partial slots
+  const bool mo_ok = DW ? make_map_rows(&mo, a.dW, (uint64_t)a.V, (uint64_t)a.C, true, 16)
+                        : make_map_rows(&mo, a.dh, (uint64_t)a.N, (uint64_t)a.C, false, G_XT);
   if (!make_map3(&mx, X, (uint64_t)nX, (uint64_t)a.C, G_XT / 2, SK) ||
       !make_map3(&mys, Y, (uint64_t)nY, (uint64_t)a.C, 128, SK) ||
-      !make_map4(&mya, Y, (uint64_t)nY, (uint64_t)a.C, 64 * AQ, (uint32_t)nch))
+      !make_map4(&mya, Y, (uint64_t)nY, (uint64_t)a.C, 64 * AQ, (uint32_t)nch) || !mo_ok ||
+      !make_map_rows(&mp, sc.tc_part, (uint64_t)(2 * tc_pairs() * G_XT), (uint64_t)a.C, true, 16))
     return cudaErrorInvalidValue;
   GradParams p;
   p.targets = a.targets;
@@ -1299,7 +1379,7 @@ cudaError_t tc_grad_range(const StepArgs& a, const Scratch& sc, Launch& L, int c
   const int smem = geo_smem_bytes<MODE>();
   cudaFuncSetAttribute(tc_grad_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   L.begin(MODE == GM_DW ? K_DW : MODE == GM_DH ? K_DH : K_LSE_DH);
-  tc_grad_kernel<MODE><<<(unsigned)(2 * P), G_THREADS, smem, L.st>>>(mx, mys, mya, p);
+  tc_grad_kernel<MODE><<<(unsigned)(2 * P), G_THREADS, smem, L.st>>>(mx, mys, mya, mo, mp, p);
   L.end();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
