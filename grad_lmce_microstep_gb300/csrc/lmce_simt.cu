@@ -174,7 +174,9 @@ __global__ void __launch_bounds__(NT) simt_grad_kernel(StepArgs a, const float* 
   const int64_t nstr = DW ? a.N : a.V;
   const int tid = threadIdx.x, r = tid >> 4, q = tid & 15;
   const int64_t own0 = (int64_t)blockIdx.x * R;
-  const float s = acc_dev->scale;
+  // global normalisation: the caller's 1 / global_valid (the value the finish pass stores, and
+  // available before it); micro-step mean: the scale the count pass set
+  const float s = a.norm == 0 ? (float)(1.0 / (double)a.global_valid) : acc_dev->scale;
   for (int64_t i = tid; i < (int64_t)R * a.C; i += NT) accs[i] = 0.f;
   // per-owned-row constants for the dh pass
   int yown = a.ignore_id;

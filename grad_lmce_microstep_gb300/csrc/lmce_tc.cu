@@ -370,8 +370,9 @@ constexpr int geo_smem_bytes() {
 struct GradParams {
   const int32_t* targets;
   const float* lse;      // dW and dh passes: per-row logsumexp (natural log)
-  const float* zt;       // dW pass: target logits
-  const DevAcc* acc;     // scale of this micro-step
+  float* zt_out;         // lse+dh pass: target logit of each row (from the logits tile)
+  const DevAcc* acc;     // scale of this micro-step (when scale_fixed < 0)
+  float scale_fixed;     // >= 0: the scale, fixed by the caller's global valid count
   unsigned* err;
   float* dW;             // dW pass output (fp32 [V, C])
   __nv_bfloat16* dh;     // dh / lse+dh pass output (bf16 [N, C])
@@ -384,6 +385,10 @@ struct GradParams {
   int ch0, nch;          // 256-row C chunks [ch0, ch0 + nch) of acc^T handled by this launch (nch <= 3)
   int beta;              // dW pass: 0 writes, 1 adds
 };
+
+__device__ __forceinline__ float grad_scale(const GradParams& p) {
+  return p.scale_fixed >= 0.f ? p.scale_fixed : p.acc->scale;
+}
 
 // Balanced persistent schedule.  Work units are (X tile t, stream block j), t-major; pair pi
 // of P takes units [U pi / P, U (pi + 1) / P).  Its range crosses X tiles in segments; a segment
@@ -459,7 +464,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
   const int pi = blockIdx.x >> 1;
   const long long ub = sch.u0(pi), ue = sch.u0(pi + 1);
   const int t_first = (int)(ub / nblk), t_last = (int)((ue - 1) / nblk);
-  const float s = p.acc->scale;
+  const float s = grad_scale(p);
   const float log2s = log2f(s);             // -inf when s == 0: every dz is then 0
 
   if (threadIdx.x == 0) {
@@ -764,6 +769,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             asm volatile("bar.sync 1, 256;" ::: "memory");
             m2 = fmaxf(fmaxf(fl_red[0][xr], fl_red[1][xr]), fmaxf(fl_red[2][xr], fl_red[3][xr])) * LOG2E;
           }
+          // my row's target logit, when its column falls in my quarter of this block
+          const int tq = yrow - (ys0 + ks * 64);
+          if (tq >= 0 && tq < 64) {
+            float zv = 0.f;
+#pragma unroll
+            for (int e = 0; e < 64; ++e) zv = (tq == e) ? z[e] : zv;
+            p.zt_out[xg] = zv;
+          }
           // p = 2^(z log2 e - m); its row sum in four partial accumulators (fixed order)
           float tmax = -INFINITY, ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
 #pragma unroll
@@ -1001,6 +1014,7 @@ __global__ void __launch_bounds__(256) tc_split_combine_kernel(GradParams p, Sch
   __shared__ int nslots;
   __shared__ float wts[16][G_XT];   // lse+dh: 2^(m_k - M) per slot and row
   __shared__ float fac[G_XT];       // lse+dh: s / l for a valid target, else 0
+  __shared__ int rowy[G_XT];        // dh passes: each row's target, or -1
   const int t = sp.t[blockIdx.x];
   if (threadIdx.x == 0) nslots = split_slots(sch, t, slots);
   __syncthreads();
@@ -1019,12 +1033,21 @@ __global__ void __launch_bounds__(256) tc_split_combine_kernel(GradParams p, Sch
     float f = 0.f;
     if (x < p.N) {
       const int y = p.targets[x];
-      if (y >= 0 && y < p.V) f = p.acc->scale / l;
+      if (y >= 0 && y < p.V) f = grad_scale(p) / l;
       if (blockIdx.y == 0) p.lse_out[x] = (M + log2f(l)) * LN2;
     }
     fac[xl] = f;
   }
-  if (FL) __syncthreads();
+  if (!DW && threadIdx.x < G_XT) {
+    const int x = t * G_XT + threadIdx.x;
+    int y = -1;
+    if (x < p.N) {
+      const int tg = p.targets[x];
+      if (tg >= 0 && tg < p.V) y = tg;
+    }
+    rowy[threadIdx.x] = y;
+  }
+  if (!DW) __syncthreads();
   const int idx4 = blockIdx.y * 256 + threadIdx.x;       // index of a group of 4 columns
   const int per_row = p.nch * 64;                         // this launch's C chunks only
   if (idx4 >= G_XT * per_row) return;
@@ -1051,131 +1074,104 @@ __global__ void __launch_bounds__(256) tc_split_combine_kernel(GradParams p, Sch
     }
     *o = v;
   } else {
-    const int y = p.targets[x];
-    __nv_bfloat16* o = p.dh + (size_t)x * p.C + c;
-    if (FL) {
-      const float f = fac[xl];
-      if (f == 0.f) {
-        v = make_float4(0.f, 0.f, 0.f, 0.f);
-      } else {
-        const float sc = p.acc->scale;
-        const __nv_bfloat16* wr = p.Wt + (size_t)y * p.C + c;
-        v.x = v.x * f - sc * __bfloat162float(wr[0]);
-        v.y = v.y * f - sc * __bfloat162float(wr[1]);
-        v.z = v.z * f - sc * __bfloat162float(wr[2]);
-        v.w = v.w * f - sc * __bfloat162float(wr[3]);
-      }
-    } else if (y >= 0 && y < p.V) {
-      const float sc = p.acc->scale;
-      const __nv_bfloat16* wr = p.Wt + (size_t)y * p.C + c;
-      v.x -= sc * __bfloat162float(wr[0]);
-      v.y -= sc * __bfloat162float(wr[1]);
-      v.z -= sc * __bfloat162float(wr[2]);
-      v.w -= sc * __bfloat162float(wr[3]);
+    // dh: the row's one-hot term with one 8-byte load of W[y], one 8-byte store of dh
+    const int y = rowy[xl];
+    const float f = FL ? fac[xl] : 1.f;
+    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (y >= 0) {
+      const float sc = grad_scale(p);
+      const uint2 wv = *reinterpret_cast<const uint2*>(p.Wt + (size_t)y * p.C + c);
+      const float2 w01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv.x));
+      const float2 w23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv.y));
+      r.x = (FL ? v.x * f : v.x) - sc * w01.x;
+      r.y = (FL ? v.y * f : v.y) - sc * w01.y;
+      r.z = (FL ? v.z * f : v.z) - sc * w23.x;
+      r.w = (FL ? v.w * f : v.w) - sc * w23.y;
     }
-    o[0] = __float2bfloat16_rn(v.x);
-    o[1] = __float2bfloat16_rn(v.y);
-    o[2] = __float2bfloat16_rn(v.z);
-    o[3] = __float2bfloat16_rn(v.w);
+    __nv_bfloat162 o01 = __floats2bfloat162_rn(r.x, r.y), o23 = __floats2bfloat162_rn(r.z, r.w);
+    uint2 ov;
+    ov.x = *reinterpret_cast<uint32_t*>(&o01);
+    ov.y = *reinterpret_cast<uint32_t*>(&o23);
+    *reinterpret_cast<uint2*>(p.dh + (size_t)x * p.C + c) = ov;
   }
 }
 
 // ---- per-row pre / post passes of the lse+dh path -----------------------------------------
-constexpr int PRE_ROWS = 32;   // rows per block of the pre pass (8 warps x 4 rows)
 
-// Before the lse+dh pass: target validity, the target logit z_t = h_n . W[y_n] (fp32 sum of
-// the exact bf16 products; C % 256 == 0), per-block valid counts and error flags, and the
-// tile flags cleared.
-__global__ void __launch_bounds__(256) rows_pre_kernel(StepArgs a, float* __restrict__ zt, int* __restrict__ part_cnt,
-                                                       unsigned* __restrict__ part_err, unsigned* __restrict__ tile_flag,
-                                                       int ntiles) {
-  __shared__ int sc[8];
-  __shared__ unsigned se[8];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0 && (int)blockIdx.x < ntiles) tile_flag[blockIdx.x] = 0u;
-  const __nv_bfloat16* H = static_cast<const __nv_bfloat16*>(a.hidden);
-  const __nv_bfloat16* W = static_cast<const __nv_bfloat16*>(a.W);
-  int cnt = 0;
-  unsigned err = 0;
-  for (int r = 0; r < PRE_ROWS / 8; ++r) {
-    const int64_t n = (int64_t)blockIdx.x * PRE_ROWS + warp * (PRE_ROWS / 8) + r;
-    if (n >= a.N) break;
-    const int y = a.targets[n];
-    const bool valid = y >= 0 && (int64_t)y < a.V;
-    float acc = 0.f;
-    if (valid) {
-      const uint4* hr = reinterpret_cast<const uint4*>(H + n * a.C);
-      const uint4* wr = reinterpret_cast<const uint4*>(W + (int64_t)y * a.C);
-      for (int64_t i = lane; i < a.C / 8; i += 32) {
-        const uint4 hv = hr[i], wv = wr[i];
-        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&hv);
-        const __nv_bfloat162* w2 = reinterpret_cast<const __nv_bfloat162*>(&wv);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 hf = __bfloat1622float2(h2[k]), wf = __bfloat1622float2(w2[k]);
-          acc = fmaf(hf.x, wf.x, acc);
-          acc = fmaf(hf.y, wf.y, acc);
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    }
-    if (lane == 0) {
-      zt[n] = acc;
-      cnt += valid ? 1 : 0;
-      if (!valid && y != a.ignore_id) err |= ERR_BIT_BAD_TARGET;
-    }
-  }
-  if (lane == 0) {
-    sc[warp] = cnt;
-    se[warp] = err;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int c = 0;
-    unsigned e = 0;
-    for (int w = 0; w < 8; ++w) {
-      c += sc[w];
-      e |= se[w];
-    }
-    part_cnt[blockIdx.x] = c;
-    part_err[blockIdx.x] = e;
-  }
-}
-
-// After it: row loss lse - z_t and the per-block loss partials for the fixed-order sum.
-__global__ void __launch_bounds__(256) rows_post_kernel(StepArgs a, const float* __restrict__ lse,
-                                                        const float* __restrict__ zt, double* __restrict__ part_loss,
-                                                        unsigned* __restrict__ part_err) {
-  __shared__ double sl[256];
+// Before the lse+dh pass when the scale depends on this micro-step's valid count
+// (normalisation by the micro-step mean): per-block valid counts and target errors.
+__global__ void __launch_bounds__(256) rows_pre_kernel(StepArgs a, int* __restrict__ part_cnt, unsigned* __restrict__ part_err) {
+  __shared__ int sc[256];
   __shared__ unsigned se[256];
   const int t = threadIdx.x;
   const int64_t n = (int64_t)blockIdx.x * 256 + t;
+  int cnt = 0;
+  unsigned err = 0;
+  if (n < a.N) {
+    const int y = a.targets[n];
+    if (y >= 0 && (int64_t)y < a.V) cnt = 1;
+    else if (y != a.ignore_id) err = ERR_BIT_BAD_TARGET;
+  }
+  sc[t] = cnt;
+  se[t] = err;
+  __syncthreads();
+  for (int o = 128; o > 0; o >>= 1) {
+    if (t < o) {
+      sc[t] += sc[t + o];
+      se[t] |= se[t + o];
+    }
+    __syncthreads();
+  }
+  if (t == 0) {
+    part_cnt[blockIdx.x] = sc[0];
+    part_err[blockIdx.x] = se[0];
+  }
+}
+
+// After the lse+dh pass and its repairs: row loss lse - z_t, per-block loss partials for the
+// fixed-order sum, valid counts and target / non-finite errors; the repair flags of this
+// block's two 128-token tiles are cleared for the next micro-step.
+__global__ void __launch_bounds__(256) rows_post_kernel(StepArgs a, const float* __restrict__ lse,
+                                                        const float* __restrict__ zt, double* __restrict__ part_loss,
+                                                        int* __restrict__ part_cnt, unsigned* __restrict__ part_err,
+                                                        unsigned* __restrict__ tile_flag, int ntiles) {
+  __shared__ double sl[256];
+  __shared__ int sc[256];
+  __shared__ unsigned se[256];
+  const int t = threadIdx.x;
+  const int64_t n = (int64_t)blockIdx.x * 256 + t;
+  if (t < 2 && (int)blockIdx.x * 2 + t < ntiles) tile_flag[blockIdx.x * 2 + t] = 0u;
   double loss = 0.0;
+  int cnt = 0;
   unsigned err = 0;
   if (n < a.N) {
     const int y = a.targets[n];
     if (y >= 0 && (int64_t)y < a.V) {
       const float li = lse[n] - zt[n];
       loss = (double)li;
+      cnt = 1;
       if (!isfinite(li)) err |= ERR_BIT_NONFINITE;
       if (a.row_loss) a.row_loss[n] = li;
-    } else if (a.row_loss) {
-      a.row_loss[n] = 0.f;
+    } else {
+      if (y != a.ignore_id) err |= ERR_BIT_BAD_TARGET;
+      if (a.row_loss) a.row_loss[n] = 0.f;
     }
   }
   sl[t] = loss;
+  sc[t] = cnt;
   se[t] = err;
   __syncthreads();
   for (int o = 128; o > 0; o >>= 1) {
     if (t < o) {
       sl[t] += sl[t + o];
+      sc[t] += sc[t + o];
       se[t] |= se[t + o];
     }
     __syncthreads();
   }
   if (t == 0) {
     part_loss[blockIdx.x] = sl[0];
+    part_cnt[blockIdx.x] = sc[0];
     part_err[blockIdx.x] = se[0];
   }
 }
@@ -1351,8 +1347,9 @@ cudaError_t tc_grad_range(const StepArgs& a, const Scratch& sc, Launch& L, int c
   GradParams p;
   p.targets = a.targets;
   p.lse = sc.lse;
-  p.zt = sc.tc_zt;
+  p.zt_out = sc.tc_zt;
   p.acc = sc.acc;
+  p.scale_fixed = a.norm == 0 ? (float)(1.0 / (double)a.global_valid) : -1.f;   // 0: global normalisation
   p.err = &sc.acc->err;
   p.Wt = static_cast<const __nv_bfloat16*>(a.W);
   p.dW = a.dW;
@@ -1411,27 +1408,31 @@ cudaError_t tc_grad(const StepArgs& a, const Scratch& sc, Launch& L) {
   return cudaSuccess;
 }
 
-// Default order: the per-row pre pass (target logits, valid count, hence the scale), the
-// one-pass logsumexp + dh, the exact repair of flagged tiles (two near-empty launches when
-// none is flagged), the row losses, then the dW pass.
+// Default order.  With global normalisation the scale is the caller's 1 / global_valid and the
+// one-pass logsumexp + dh runs first; with the micro-step mean, a count pass and its finish set
+// the scale before it.  Then: the exact repair of flagged tiles (two near-empty launches when
+// none is flagged), the row losses and counts, their fixed-order reduction, the dW pass.
 static cudaError_t tc_microstep_fused(const StepArgs& a, const Scratch& sc, Launch& L) {
-  const int64_t npre = (a.N + PRE_ROWS - 1) / PRE_ROWS;
+  const int64_t nparts = tc_parts(a.N);   // 256 rows per partial
   const int ntiles = (int)((a.N + TC_TILE_ROWS - 1) / TC_TILE_ROWS);
-  L.begin(K_FINISH);
-  rows_pre_kernel<<<(unsigned)npre, 256, 0, L.st>>>(a, sc.tc_zt, sc.part_cnt, sc.part_err, sc.tc_tile_flag, ntiles);
-  L.end();
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if ((e = launch_finish(a, sc, npre, L, FIN_COUNT)) != cudaSuccess) return e;
+  const bool global = a.norm == 0;
+  cudaError_t e;
+  if (!global) {
+    L.begin(K_FINISH);
+    rows_pre_kernel<<<(unsigned)nparts, 256, 0, L.st>>>(a, sc.part_cnt, sc.part_err);
+    L.end();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_finish(a, sc, nparts, L, FIN_COUNT)) != cudaSuccess) return e;
+  }
   if ((e = tc_grad<GM_FL>(a, sc, L)) != cudaSuccess) return e;
   if ((e = simt_repair_lse(a, sc, L)) != cudaSuccess) return e;
   if ((e = simt_repair_dh(a, sc, L)) != cudaSuccess) return e;
-  const int64_t nparts = tc_parts(a.N);
   L.begin(K_FINISH);
-  rows_post_kernel<<<(unsigned)nparts, 256, 0, L.st>>>(a, sc.lse, sc.tc_zt, sc.part_loss, sc.part_err);
+  rows_post_kernel<<<(unsigned)nparts, 256, 0, L.st>>>(a, sc.lse, sc.tc_zt, sc.part_loss, sc.part_cnt, sc.part_err,
+                                                       sc.tc_tile_flag, ntiles);
   L.end();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = launch_finish(a, sc, nparts, L, FIN_LOSS)) != cudaSuccess) return e;
+  if ((e = launch_finish(a, sc, nparts, L, global ? FIN_ALL : FIN_LOSS)) != cudaSuccess) return e;
   return tc_grad<GM_DW>(a, sc, L);
 }
 
