@@ -17,6 +17,7 @@ namespace lmce {
 namespace {
 
 constexpr int R = 16;    // rows owned by one block
+static_assert(TC_TILE_ROWS % R == 0, "a repair block walks whole R-row groups of its tile");
 constexpr int BT = 64;   // streamed rows per tile
 constexpr int BK = 32;   // reduction chunk
 constexpr int NT = 256;  // threads per block
@@ -67,15 +68,11 @@ __device__ __forceinline__ void logit_tile(const T* __restrict__ X, int64_t own0
   }
 }
 
-// gate == nullptr: the lse pass of the SIMT path (lse, row loss, per-block partials).
-// gate != nullptr: repair mode, only the logsumexp of the rows of flagged 128-token tiles.
+// Rows grp*R .. grp*R + R - 1.  repair == false: the lse pass of the SIMT path (lse, row loss,
+// the group's partials at index grp); repair == true: only the logsumexp.
 template <typename T>
-__global__ void __launch_bounds__(NT) simt_lse_kernel(StepArgs a, float* __restrict__ lse_out,
-                                                      double* __restrict__ part_loss,
-                                                      int* __restrict__ part_cnt,
-                                                      unsigned* __restrict__ part_err,
-                                                      const unsigned* __restrict__ gate) {
-  if (gate && !gate[(int64_t)blockIdx.x * R / TC_TILE_ROWS]) return;  // block-uniform
+__device__ void simt_lse_rows(const StepArgs& a, float* __restrict__ lse_out, double* __restrict__ part_loss,
+                              int* __restrict__ part_cnt, unsigned* __restrict__ part_err, int64_t grp, bool repair) {
   __shared__ float Xs[BK][R];
   __shared__ float Ys[BK][BT + 1];
   __shared__ float zt[R];
@@ -85,7 +82,7 @@ __global__ void __launch_bounds__(NT) simt_lse_kernel(StepArgs a, float* __restr
   const T* H = static_cast<const T*>(a.hidden);
   const T* W = static_cast<const T*>(a.W);
   const int tid = threadIdx.x, r = tid >> 4, q = tid & 15;
-  const int64_t n0 = (int64_t)blockIdx.x * R, n = n0 + r;
+  const int64_t n0 = grp * R, n = n0 + r;
   const int y = (n < a.N) ? a.targets[n] : a.ignore_id;
   if (q == 0) zt[r] = 0.f;
   float m = -INFINITY, l = 0.f;
@@ -116,7 +113,7 @@ __global__ void __launch_bounds__(NT) simt_lse_kernel(StepArgs a, float* __restr
     m = mn;
   }
   __syncthreads();
-  if (gate) {
+  if (repair) {
     if (q == 0 && n < a.N) lse_out[n] = m + logf(l);
     return;
   }
@@ -148,20 +145,40 @@ __global__ void __launch_bounds__(NT) simt_lse_kernel(StepArgs a, float* __restr
     int c = 0;
     unsigned e = 0;
     for (int i = 0; i < R; ++i) { t += rl[i]; c += rv[i]; e |= re[i]; }
-    part_loss[blockIdx.x] = t;
-    part_cnt[blockIdx.x] = c;
-    part_err[blockIdx.x] = e;
+    part_loss[grp] = t;
+    part_cnt[grp] = c;
+    part_err[grp] = e;
   }
 }
 
+// gate == nullptr: the lse pass of the SIMT path, one block per R rows.
+// gate != nullptr: repair mode, one block per 128-token tile: the logsumexp of the rows of a
+// flagged tile (its R-row groups in turn); other blocks return at once.
+template <typename T>
+__global__ void __launch_bounds__(NT) simt_lse_kernel(StepArgs a, float* __restrict__ lse_out,
+                                                      double* __restrict__ part_loss,
+                                                      int* __restrict__ part_cnt,
+                                                      unsigned* __restrict__ part_err,
+                                                      const unsigned* __restrict__ gate) {
+  if (!gate) {
+    simt_lse_rows<T>(a, lse_out, part_loss, part_cnt, part_err, blockIdx.x, false);
+    return;
+  }
+  if (!gate[blockIdx.x]) return;  // block-uniform
+  for (int g = 0; g < TC_TILE_ROWS / R; ++g) {
+    const int64_t grp = (int64_t)blockIdx.x * (TC_TILE_ROWS / R) + g;
+    if (grp * R >= a.N) break;
+    simt_lse_rows<T>(a, lse_out, part_loss, part_cnt, part_err, grp, true);
+    __syncthreads();
+  }
+}
+
+// Owned rows grp*R .. grp*R + R - 1.
 // DW = true : own R vocabulary rows, stream the tokens, acc = dW rows.
 // DW = false: own R token rows, stream the vocabulary, acc = dh rows.
-// gate != nullptr (dh pass only): repair mode, only blocks inside flagged 128-token tiles run.
 template <typename T, bool DW>
-__global__ void __launch_bounds__(NT) simt_grad_kernel(StepArgs a, const float* __restrict__ lse,
-                                                       const DevAcc* __restrict__ acc_dev,
-                                                       const unsigned* __restrict__ gate) {
-  if (!DW && gate && !gate[(int64_t)blockIdx.x * R / TC_TILE_ROWS]) return;  // block-uniform
+__device__ void simt_grad_rows(const StepArgs& a, const float* __restrict__ lse, const DevAcc* __restrict__ acc_dev,
+                               int64_t grp) {
   __shared__ float Xs[BK][R];
   __shared__ float Ys[BK][BT + 1];
   __shared__ float dzs[R][BT];
@@ -173,7 +190,7 @@ __global__ void __launch_bounds__(NT) simt_grad_kernel(StepArgs a, const float* 
   const int64_t nown = DW ? a.V : a.N;
   const int64_t nstr = DW ? a.N : a.V;
   const int tid = threadIdx.x, r = tid >> 4, q = tid & 15;
-  const int64_t own0 = (int64_t)blockIdx.x * R;
+  const int64_t own0 = grp * R;
   // global normalisation: the caller's 1 / global_valid (the value the finish pass stores, and
   // available before it); micro-step mean: the scale the count pass set
   const float s = a.norm == 0 ? (float)(1.0 / (double)a.global_valid) : acc_dev->scale;
@@ -233,6 +250,26 @@ __global__ void __launch_bounds__(NT) simt_grad_kernel(StepArgs a, const float* 
   }
 }
 
+// gate == nullptr: one block per R owned rows.
+// gate != nullptr (dh pass only): repair mode, one block per 128-token tile: the dh rows of a
+// flagged tile (its R-row groups in turn); other blocks return at once.
+template <typename T, bool DW>
+__global__ void __launch_bounds__(NT) simt_grad_kernel(StepArgs a, const float* __restrict__ lse,
+                                                       const DevAcc* __restrict__ acc_dev,
+                                                       const unsigned* __restrict__ gate) {
+  if (DW || !gate) {
+    simt_grad_rows<T, DW>(a, lse, acc_dev, blockIdx.x);
+    return;
+  }
+  if (!gate[blockIdx.x]) return;  // block-uniform
+  for (int g = 0; g < TC_TILE_ROWS / R; ++g) {
+    const int64_t grp = (int64_t)blockIdx.x * (TC_TILE_ROWS / R) + g;
+    if (grp * R >= a.N) break;
+    __syncthreads();   // the previous group's reads of the shared accumulators are done
+    simt_grad_rows<T, DW>(a, lse, acc_dev, grp);
+  }
+}
+
 }  // namespace
 
 int64_t simt_parts(int64_t N) { return (N + R - 1) / R; }
@@ -284,8 +321,8 @@ cudaError_t simt_grads(const StepArgs& a, const Scratch& sc, Launch& L) {
 // tiles return before touching memory, so the common case costs two near-empty launches.
 cudaError_t simt_repair_lse(const StepArgs& a, const Scratch& sc, Launch& L) {
   L.begin(K_LSE);
-  simt_lse_kernel<__nv_bfloat16><<<(unsigned)simt_parts(a.N), NT, 0, L.st>>>(a, sc.lse, nullptr, nullptr, nullptr,
-                                                                              sc.tc_tile_flag);
+  const unsigned ntiles = (unsigned)((a.N + TC_TILE_ROWS - 1) / TC_TILE_ROWS);
+  simt_lse_kernel<__nv_bfloat16><<<ntiles, NT, 0, L.st>>>(a, sc.lse, nullptr, nullptr, nullptr, sc.tc_tile_flag);
   L.end();
   return cudaGetLastError();
 }
@@ -295,7 +332,8 @@ cudaError_t simt_repair_dh(const StepArgs& a, const Scratch& sc, Launch& L) {
   auto kdh = simt_grad_kernel<__nv_bfloat16, false>;
   cudaFuncSetAttribute(kdh, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   L.begin(K_DH);
-  kdh<<<(unsigned)simt_parts(a.N), NT, smem, L.st>>>(a, sc.lse, sc.acc, sc.tc_tile_flag);
+  const unsigned ntiles = (unsigned)((a.N + TC_TILE_ROWS - 1) / TC_TILE_ROWS);
+  kdh<<<ntiles, NT, smem, L.st>>>(a, sc.lse, sc.acc, sc.tc_tile_flag);
   L.end();
   return cudaGetLastError();
 }
