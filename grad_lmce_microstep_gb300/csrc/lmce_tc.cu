@@ -408,11 +408,6 @@ struct Sched {
   }
 };
 
-__device__ __forceinline__ void st_shared_b16(uint32_t addr, uint16_t v, bool remote) {
-  if (remote) asm volatile("st.shared::cluster.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-  else asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-}
-
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
@@ -1004,8 +999,10 @@ __device__ __forceinline__ int split_slots(const Sched& sch, int t, int* slots) 
 }
 
 // Adds the partial sums of every split X tile in pair order and writes the output exactly as
-// the gradient kernel does for whole tiles.  grid: (split tiles, ceil(128 * 256 nch / 1024));
-// each thread handles four consecutive C columns of one row of the launch's chunk range.
+// the gradient kernel does for whole tiles.  grid: (split tiles, COMB_BLOCKS); a block covers a
+// COMB_BLOCKS-th of the tile's (row, four-column group) pairs, COMB_U groups per thread at a time
+// with every load of a batch issued before its stores.
+constexpr int COMB_BLOCKS = 8, COMB_U = 4;
 template <int MODE>
 __global__ void __launch_bounds__(256) tc_split_combine_kernel(GradParams p, Sched sch, const __grid_constant__ SplitTiles sp) {
   constexpr bool DW = MODE == GM_DW;
@@ -1019,80 +1016,104 @@ __global__ void __launch_bounds__(256) tc_split_combine_kernel(GradParams p, Sch
   if (threadIdx.x == 0) nslots = split_slots(sch, t, slots);
   __syncthreads();
   const int nX = DW ? p.V : p.N;
-  if (FL && threadIdx.x < G_XT) {
-    // merge the slots' (m, l) of my row: M = max m_k, l = sum l_k 2^(m_k - M)
-    const int xl = threadIdx.x, x = t * G_XT + xl;
-    float M = -INFINITY;
-    for (int k = 0; k < nslots; ++k) M = fmaxf(M, p.part_lm[((size_t)slots[k] * 2 + 0) * G_XT + xl]);
-    float l = 0.f;
-    for (int k = 0; k < nslots; ++k) {
-      const float w = exp2f(p.part_lm[((size_t)slots[k] * 2 + 0) * G_XT + xl] - M);
-      wts[k][xl] = w;
-      l += p.part_lm[((size_t)slots[k] * 2 + 1) * G_XT + xl] * w;
-    }
-    float f = 0.f;
-    if (x < p.N) {
-      const int y = p.targets[x];
-      if (y >= 0 && y < p.V) f = grad_scale(p) / l;
-      if (blockIdx.y == 0) p.lse_out[x] = (M + log2f(l)) * LN2;
-    }
-    fac[xl] = f;
-  }
+  const float s = grad_scale(p);
   if (!DW && threadIdx.x < G_XT) {
-    const int x = t * G_XT + threadIdx.x;
+    const int xl = threadIdx.x, x = t * G_XT + xl;
     int y = -1;
     if (x < p.N) {
       const int tg = p.targets[x];
       if (tg >= 0 && tg < p.V) y = tg;
     }
-    rowy[threadIdx.x] = y;
+    rowy[xl] = y;
+    if (FL) {
+      // merge the slots' (m, l) of my row: M = max m_k, l = sum l_k 2^(m_k - M)
+      float M = -INFINITY;
+      for (int k = 0; k < nslots; ++k) M = fmaxf(M, p.part_lm[((size_t)slots[k] * 2 + 0) * G_XT + xl]);
+      float l = 0.f;
+      for (int k = 0; k < nslots; ++k) {
+        const float w = exp2f(p.part_lm[((size_t)slots[k] * 2 + 0) * G_XT + xl] - M);
+        wts[k][xl] = w;
+        l += p.part_lm[((size_t)slots[k] * 2 + 1) * G_XT + xl] * w;
+      }
+      fac[xl] = y >= 0 ? s / l : 0.f;
+      if (blockIdx.y == 0 && x < p.N) p.lse_out[x] = (M + log2f(l)) * LN2;
+    }
   }
   if (!DW) __syncthreads();
-  const int idx4 = blockIdx.y * 256 + threadIdx.x;       // index of a group of 4 columns
-  const int per_row = p.nch * 64;                         // this launch's C chunks only
-  if (idx4 >= G_XT * per_row) return;
-  const int xl = idx4 / per_row, c = p.ch0 * 256 + (idx4 % per_row) * 4;
-  const int x = t * G_XT + xl;
-  if (x >= nX) return;
-  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k = 0; k < nslots; ++k) {
-    const float4 w = *reinterpret_cast<const float4*>(p.part + ((size_t)slots[k] * G_XT + xl) * p.C + c);
-    const float a = FL ? wts[k][xl] : 1.f;
-    v.x += FL ? w.x * a : w.x;
-    v.y += FL ? w.y * a : w.y;
-    v.z += FL ? w.z * a : w.z;
-    v.w += FL ? w.w * a : w.w;
-  }
-  if (DW) {
-    float4* o = reinterpret_cast<float4*>(p.dW + (size_t)x * p.C + c);
-    if (p.beta) {
-      const float4 d = *o;
-      v.x += d.x;
-      v.y += d.y;
-      v.z += d.z;
-      v.w += d.w;
+  const int per_row = p.nch * 64;                         // four-column groups per row (this launch's chunks)
+  const int total = G_XT * per_row;
+  const int ns = nslots;
+  for (int base = (blockIdx.y * 256 + threadIdx.x) * COMB_U; base < total; base += COMB_BLOCKS * 256 * COMB_U) {
+    int xl[COMB_U], c[COMB_U];
+    bool ok[COMB_U];
+    float4 v[COMB_U];
+#pragma unroll
+    for (int u = 0; u < COMB_U; ++u) {
+      const int idx = base + u;                           // consecutive groups: one row, adjacent columns
+      xl[u] = idx / per_row;
+      c[u] = p.ch0 * 256 + (idx % per_row) * 4;
+      ok[u] = idx < total && t * G_XT + xl[u] < nX;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    *o = v;
-  } else {
-    // dh: the row's one-hot term with one 8-byte load of W[y], one 8-byte store of dh
-    const int y = rowy[xl];
-    const float f = FL ? fac[xl] : 1.f;
-    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (y >= 0) {
-      const float sc = grad_scale(p);
-      const uint2 wv = *reinterpret_cast<const uint2*>(p.Wt + (size_t)y * p.C + c);
-      const float2 w01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv.x));
-      const float2 w23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv.y));
-      r.x = (FL ? v.x * f : v.x) - sc * w01.x;
-      r.y = (FL ? v.y * f : v.y) - sc * w01.y;
-      r.z = (FL ? v.z * f : v.z) - sc * w23.x;
-      r.w = (FL ? v.w * f : v.w) - sc * w23.y;
+    for (int k = 0; k < ns; ++k) {
+#pragma unroll
+      for (int u = 0; u < COMB_U; ++u) {
+        if (!ok[u]) continue;
+        const float4 w = *reinterpret_cast<const float4*>(p.part + ((size_t)slots[k] * G_XT + xl[u]) * p.C + c[u]);
+        const float a = FL ? wts[k][xl[u]] : 1.f;
+        v[u].x += FL ? w.x * a : w.x;
+        v[u].y += FL ? w.y * a : w.y;
+        v[u].z += FL ? w.z * a : w.z;
+        v[u].w += FL ? w.w * a : w.w;
+      }
     }
-    __nv_bfloat162 o01 = __floats2bfloat162_rn(r.x, r.y), o23 = __floats2bfloat162_rn(r.z, r.w);
-    uint2 ov;
-    ov.x = *reinterpret_cast<uint32_t*>(&o01);
-    ov.y = *reinterpret_cast<uint32_t*>(&o23);
-    *reinterpret_cast<uint2*>(p.dh + (size_t)x * p.C + c) = ov;
+    if (DW) {
+      float4 d[COMB_U];
+#pragma unroll
+      for (int u = 0; u < COMB_U; ++u) {
+        d[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (ok[u] && p.beta) d[u] = *reinterpret_cast<const float4*>(p.dW + (size_t)(t * G_XT + xl[u]) * p.C + c[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < COMB_U; ++u) {
+        if (!ok[u]) continue;
+        float4 r = v[u];
+        if (p.beta) {
+          r.x += d[u].x;
+          r.y += d[u].y;
+          r.z += d[u].z;
+          r.w += d[u].w;
+        }
+        *reinterpret_cast<float4*>(p.dW + (size_t)(t * G_XT + xl[u]) * p.C + c[u]) = r;
+      }
+    } else {
+      // dh: the row's one-hot term with one 8-byte load of W[y], one 8-byte store of dh
+      uint2 wv[COMB_U];
+#pragma unroll
+      for (int u = 0; u < COMB_U; ++u) {
+        wv[u] = make_uint2(0u, 0u);
+        if (ok[u] && rowy[xl[u]] >= 0) wv[u] = *reinterpret_cast<const uint2*>(p.Wt + (size_t)rowy[xl[u]] * p.C + c[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < COMB_U; ++u) {
+        if (!ok[u]) continue;
+        const float f = FL ? fac[xl[u]] : 1.f;
+        float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (rowy[xl[u]] >= 0) {
+          const float2 w01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[u].x));
+          const float2 w23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[u].y));
+          r.x = (FL ? v[u].x * f : v[u].x) - s * w01.x;
+          r.y = (FL ? v[u].y * f : v[u].y) - s * w01.y;
+          r.z = (FL ? v[u].z * f : v[u].z) - s * w23.x;
+          r.w = (FL ? v[u].w * f : v[u].w) - s * w23.y;
+        }
+        __nv_bfloat162 o01 = __floats2bfloat162_rn(r.x, r.y), o23 = __floats2bfloat162_rn(r.z, r.w);
+        uint2 ov;
+        ov.x = *reinterpret_cast<uint32_t*>(&o01);
+        ov.y = *reinterpret_cast<uint32_t*>(&o23);
+        *reinterpret_cast<uint2*>(p.dh + (size_t)(t * G_XT + xl[u]) * p.C + c[u]) = ov;
+      }
+    }
   }
 }
 
@@ -1392,7 +1413,7 @@ cudaError_t tc_grad_range(const StepArgs& a, const Scratch& sc, Launch& L, int c
   }
   if (sp.n == 0) return cudaSuccess;
   L.begin(K_FINISH);
-  tc_split_combine_kernel<MODE><<<dim3((unsigned)sp.n, (unsigned)((G_XT * 64 * nch + 255) / 256)), 256, 0, L.st>>>(p, sch, sp);
+  tc_split_combine_kernel<MODE><<<dim3((unsigned)sp.n, (unsigned)COMB_BLOCKS), 256, 0, L.st>>>(p, sch, sp);
   L.end();
   return cudaGetLastError();
 }
