@@ -26,7 +26,7 @@ What it computes, in the order the pages give it:
   pad target is ignored by the loss.  Its id is -100 here (the default of the
   PyTorch cross-entropy function the multi-GPU page cites).
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 padded vocabulary columns take part in the softmax; a target outside [0, V)
 that is not the ignore id is treated as ignored and flagged; dh is the
 gradient of the scaled objective for this micro-step only (overwritten each
