@@ -71,6 +71,82 @@ __global__ void __launch_bounds__(FIN_T) finish_kernel(const double* __restrict_
   }
 }
 
+// Sum of squares of n floats to float64 accuracy without float64 arithmetic per element (a
+// GB300 runs float64 at a small fraction of its float32 rate): each square is split exactly
+// into x*x + fma(x, x, -x*x), and a thread accumulates its terms as a double-single pair (S, E)
+// with Knuth's TwoSum, in round-to-nearest intrinsics the compiler may not contract.  Block b
+// takes the fixed range [b*per, (b+1)*per) in 16-byte steps, each thread a fixed strided subset
+// in order; the threads' S + E are added in float64 in a fixed-shape tree, and one block adds
+// the blocks' partials in block order.  The same order on every call.
+struct DSum {
+  float S = 0.f, E = 0.f;
+  __device__ __forceinline__ void add_sq(float x) {
+    const float p = __fmul_rn(x, x);
+    const float e = __fmaf_rn(x, x, -p);             // x*x - p, exactly
+    const float t = __fadd_rn(S, p);
+    const float z = __fsub_rn(t, S);
+    const float err = __fadd_rn(__fsub_rn(S, __fsub_rn(t, z)), __fsub_rn(p, z));   // (S + p) - t, exactly
+    E = __fadd_rn(E, __fadd_rn(err, e));
+    S = t;
+  }
+};
+constexpr int SQ_T = 256, SQ_BLOCKS = 608;   // 4 blocks per SM of a 152-SM GB300
+__global__ void __launch_bounds__(SQ_T) sumsq_part_kernel(const float* __restrict__ x, int64_t n, int64_t per,
+                                                         double* __restrict__ part) {
+  __shared__ double sh[SQ_T];
+  const int64_t b0 = (int64_t)blockIdx.x * per, b1 = b0 + per < n ? b0 + per : n;
+  DSum d;
+  if ((((uintptr_t)x) & 15) == 0 && (b0 & 3) == 0) {
+    const int64_t v0 = b0 / 4, v1 = b1 / 4;   // whole float4 groups of the range
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    // eight loads in flight per thread, then their terms in the same order as a plain strided loop
+    int64_t i = v0 + threadIdx.x;
+    for (; i + 7 * SQ_T < v1; i += 8 * SQ_T) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = x4[i + u * SQ_T];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        d.add_sq(v[u].x);
+        d.add_sq(v[u].y);
+        d.add_sq(v[u].z);
+        d.add_sq(v[u].w);
+      }
+    }
+    for (; i < v1; i += SQ_T) {
+      const float4 v = x4[i];
+      d.add_sq(v.x);
+      d.add_sq(v.y);
+      d.add_sq(v.z);
+      d.add_sq(v.w);
+    }
+    for (int64_t i = v1 * 4 + threadIdx.x; i < b1; i += SQ_T) d.add_sq(x[i]);
+  } else {
+    for (int64_t i = b0 + threadIdx.x; i < b1; i += SQ_T) d.add_sq(x[i]);
+  }
+  sh[threadIdx.x] = (double)d.S + (double)d.E;
+  __syncthreads();
+  for (int o = SQ_T / 2; o > 0; o >>= 1) {
+    if (threadIdx.x < o) sh[threadIdx.x] += sh[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) part[blockIdx.x] = sh[0];
+}
+
+__global__ void __launch_bounds__(SQ_T) sumsq_final_kernel(const double* __restrict__ part, int nparts,
+                                                          double* __restrict__ out) {
+  __shared__ double sh[SQ_T];
+  double acc = 0.0;
+  for (int i = threadIdx.x; i < nparts; i += SQ_T) acc += part[i];
+  sh[threadIdx.x] = acc;
+  __syncthreads();
+  for (int o = SQ_T / 2; o > 0; o >>= 1) {
+    if (threadIdx.x < o) sh[threadIdx.x] += sh[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *out = sh[0];
+}
+
 }  // namespace
 
 cudaError_t launch_finish(const StepArgs& a, const Scratch& s, int64_t nparts, Launch& L, int mode) {
@@ -92,7 +168,8 @@ struct lmce_handle {
   int path;            // resolved: LMCE_PATH_SIMT, LMCE_PATH_TCGEN05 or LMCE_PATH_TCGEN05_TWO_PASS
   Scratch sc;
   DevAcc* host_acc;    // pinned
-  bool first;          // next micro-step writes dW instead of adding
+  bool first;          // next micro-step writes dW instead of adding (unless LMCE_ACCUMULATE_FROM_START)
+  double* sumsq_part;  // lmce_dw_sumsq: per-block float64 partials, then the result
   int attempted;       // micro-steps accepted since create/finalize
   int64_t launches;
   Prof prof;
@@ -120,6 +197,8 @@ static void free_scratch(lmce_handle* h) {
   cudaFree(h->sc.tc_part);
   cudaFree(h->sc.tc_part_lm);
   cudaFree(h->sc.tc_tile_flag);
+  cudaFree(h->sumsq_part);
+  h->sumsq_part = nullptr;
   if (h->host_acc) cudaFreeHost(h->host_acc);
   memset(&h->sc, 0, sizeof(h->sc));
   h->host_acc = nullptr;
@@ -132,7 +211,8 @@ extern "C" int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out)
   if (cfg->C > (1 << 20) || cfg->V > (1LL << 31) || cfg->max_N > (1LL << 31)) return LMCE_ERR_ARG;
   if (cfg->dtype != LMCE_BF16 && cfg->dtype != LMCE_FP32) return LMCE_ERR_ARG;
   if (cfg->norm != LMCE_NORM_GLOBAL && cfg->norm != LMCE_NORM_MICRO_MEAN) return LMCE_ERR_ARG;
-  if (cfg->path < LMCE_PATH_AUTO || cfg->path > LMCE_PATH_TCGEN05_TWO_PASS || cfg->reserved != 0) return LMCE_ERR_ARG;
+  if (cfg->path < LMCE_PATH_AUTO || cfg->path > LMCE_PATH_TCGEN05_TWO_PASS) return LMCE_ERR_ARG;
+  if (cfg->flags & ~LMCE_ACCUMULATE_FROM_START) return LMCE_ERR_ARG;
   const bool tc_ok = tc_supported(cfg->C, cfg->V, cfg->dtype == LMCE_BF16);
   const bool simt_ok = cfg->C <= 2048;
   int path;
@@ -179,6 +259,7 @@ extern "C" int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out)
          cudaMalloc(&h->sc.tc_tile_flag, sizeof(unsigned) * tiles) == cudaSuccess &&
          cudaMemset(h->sc.tc_tile_flag, 0, sizeof(unsigned) * tiles) == cudaSuccess;
   }
+  ok = ok && cudaMalloc(&h->sumsq_part, sizeof(double) * (SQ_BLOCKS + 1)) == cudaSuccess;
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
     free_scratch(h);
@@ -221,12 +302,15 @@ extern "C" int lmce_microstep(lmce_handle* h, const void* hidden, const void* W,
   a.norm = c.norm;
   a.G = c.grad_accum_steps;
   a.global_valid = global_valid;
-  a.beta = h->first ? 0 : 1;
+  // the first micro-step of a step writes dW, unless the caller has already put part of the
+  // step's gradient there
+  const bool write_dW = h->first && !(c.flags & LMCE_ACCUMULATE_FROM_START);
+  a.beta = write_dW ? 0 : 1;
   a.bf16 = c.dtype == LMCE_BF16;
   a.tc_two_pass = h->path == LMCE_PATH_TCGEN05_TWO_PASS;
   if (N == 0) {
     // An empty micro-step still counts; the first one of a step leaves dW = 0.
-    if (h->first && cudaMemsetAsync(h->dW, 0, sizeof(float) * (size_t)c.V * c.C, st) != cudaSuccess)
+    if (write_dW && cudaMemsetAsync(h->dW, 0, sizeof(float) * (size_t)c.V * c.C, st) != cudaSuccess)
       return LMCE_ERR_CUDA;
     h->first = false;
     h->attempted += 1;
@@ -262,6 +346,30 @@ extern "C" int lmce_finalize(lmce_handle* h, double* loss_sum, int64_t* valid_co
   if (r.err & ERR_BIT_BAD_TARGET) return LMCE_ERR_BAD_TARGET;
   if ((r.err & ERR_BIT_NONFINITE) || !isfinite(r.loss_sum)) return LMCE_ERR_NONFINITE;
   if (r.count == 0) return LMCE_ERR_NO_VALID;
+  return LMCE_OK;
+}
+
+extern "C" int lmce_dw_sumsq(lmce_handle* h, double* sumsq, void* stream) {
+  if (!h || !sumsq) return LMCE_ERR_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t n = h->cfg.V * h->cfg.C;
+  const int64_t per = ((n + SQ_BLOCKS - 1) / SQ_BLOCKS + 3) / 4 * 4;   // a multiple of 4 elements
+  Launch L;
+  L.st = st;
+  L.prof = &h->prof;
+  L.begin(K_FINISH);
+  sumsq_part_kernel<<<SQ_BLOCKS, SQ_T, 0, st>>>(h->dW, n, per, h->sumsq_part);
+  L.end();
+  L.begin(K_FINISH);
+  sumsq_final_kernel<<<1, SQ_T, 0, st>>>(h->sumsq_part, SQ_BLOCKS, h->sumsq_part + SQ_BLOCKS);
+  L.end();
+  h->launches += L.n;
+  if (cudaGetLastError() != cudaSuccess) return LMCE_ERR_CUDA;
+  double r = 0.0;
+  if (cudaMemcpyAsync(&r, h->sumsq_part + SQ_BLOCKS, sizeof(double), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return LMCE_ERR_CUDA;
+  *sumsq = r;
   return LMCE_OK;
 }
 

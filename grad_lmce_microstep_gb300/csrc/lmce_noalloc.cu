@@ -67,7 +67,7 @@ extern "C" int lmce_microstep_noalloc(const lmce_config* cfg, const void* hidden
   if (cfg->C <= 0 || cfg->C > 2048 || cfg->V <= 0 || cfg->V > (1LL << 31)) return LMCE_ERR_ARG;
   if (cfg->dtype != LMCE_BF16 && cfg->dtype != LMCE_FP32) return LMCE_ERR_ARG;
   if (cfg->norm != LMCE_NORM_GLOBAL && cfg->norm != LMCE_NORM_MICRO_MEAN) return LMCE_ERR_ARG;
-  if (cfg->grad_accum_steps < 1 || cfg->reserved != 0) return LMCE_ERR_ARG;
+  if (cfg->grad_accum_steps < 1 || cfg->flags != 0) return LMCE_ERR_ARG;
   if (cfg->path != LMCE_PATH_AUTO && cfg->path != LMCE_PATH_SIMT) return LMCE_ERR_ARG;
   if (N < 0 || N > NA_MAX_N || simt_parts(N) > NA_PARTS) return LMCE_ERR_ARG;
   if (N > 0 && (!hidden || !W || !targets || !dh)) return LMCE_ERR_ARG;

@@ -32,7 +32,7 @@ TORCH_DTYPES = {"bf16": torch.bfloat16, "fp32": torch.float32}
 
 EXPORTS = ("lmce_create", "lmce_microstep", "lmce_finalize", "lmce_destroy", "lmce_status_string",
            "lmce_launch_count", "lmce_selected_path", "lmce_profile", "lmce_profile_read",
-           "lmce_microstep_noalloc")
+           "lmce_microstep_noalloc", "lmce_dw_sumsq")
 
 NOALLOC_MAX_N = 65536
 
@@ -43,7 +43,9 @@ class Config(ctypes.Structure):
     _fields_ = [("C", ctypes.c_int64), ("V", ctypes.c_int64), ("max_N", ctypes.c_int64),
                 ("dtype", ctypes.c_int32), ("ignore_id", ctypes.c_int32), ("norm", ctypes.c_int32),
                 ("grad_accum_steps", ctypes.c_int32), ("path", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("flags", ctypes.c_int32)]
+
+ACCUMULATE_FROM_START = 1   # Config.flags: the first micro-step adds to dW instead of writing it
 
 
 class LmceError(RuntimeError):
@@ -71,6 +73,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.lmce_finalize.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64),
                                 ctypes.POINTER(ctypes.c_double), vp]
     L.lmce_finalize.restype = i32
+    L.lmce_dw_sumsq.argtypes = [vp, ctypes.POINTER(ctypes.c_double), vp]
+    L.lmce_dw_sumsq.restype = i32
     L.lmce_destroy.argtypes = [vp]
     L.lmce_destroy.restype = i32
     L.lmce_status_string.argtypes = [i32]
@@ -124,14 +128,14 @@ class Lmce:
 
     def __init__(self, C: int, V: int, max_N: int, dW: torch.Tensor, dtype: str = "bf16",
                  ignore_id: int = -100, norm: str = "global", grad_accum_steps: int = 1,
-                 path: str = "auto"):
+                 path: str = "auto", accumulate_from_start: bool = False):
         _check_dev(dW, "dW", torch.float32, (V, C))
         self.lib = load()
         self.C, self.V, self.max_N = int(C), int(V), int(max_N)
         self.dtype = dtype
         self.dW = dW
         cfg = Config(self.C, self.V, self.max_N, DTYPES[dtype], int(ignore_id), NORMS[norm],
-                     int(grad_accum_steps), PATHS[path], 0)
+                     int(grad_accum_steps), PATHS[path], ACCUMULATE_FROM_START if accumulate_from_start else 0)
         h = ctypes.c_void_p()
         st = self.lib.lmce_create(ctypes.byref(cfg), _ptr(dW), ctypes.byref(h))
         if st != OK:
@@ -176,6 +180,14 @@ class Lmce:
                 raise LmceError(st, "lmce_finalize")
             return ls.value, cnt.value, mean.value
         return ls.value, cnt.value, mean.value, st
+
+    def dw_sumsq(self, stream=None) -> float:
+        """Sum of dW**2 over all elements, float64, fixed reduction order (waits for the stream)."""
+        out = ctypes.c_double()
+        st = self.lib.lmce_dw_sumsq(self.handle, ctypes.byref(out), _stream(stream))
+        if st != OK:
+            raise LmceError(st, "lmce_dw_sumsq")
+        return out.value
 
     def profile(self, enable: bool):
         """Record CUDA events around every kernel launch (enable=True clears old records)."""

@@ -25,7 +25,8 @@
  *   - Every call returns an int status (LMCE_OK or an LMCE_ERR_* code) and never
  *     throws; no device code traps or asserts.
  *   - Calls on one handle must be issued from one host thread and enqueue on one
- *     stream (or on streams the caller orders).  Only lmce_finalize blocks the host.
+ *     stream (or on streams the caller orders).  Only lmce_finalize and lmce_dw_sumsq
+ *     block the host.
  */
 #ifndef LMCE_H_
 #define LMCE_H_
@@ -80,8 +81,13 @@ typedef struct lmce_config {
   int32_t norm;             /* lmce_norm                                                     */
   int32_t grad_accum_steps; /* G >= 1; used by LMCE_NORM_MICRO_MEAN                          */
   int32_t path;             /* lmce_path                                                     */
-  int32_t reserved;         /* must be 0                                                     */
+  int32_t flags;            /* 0 or LMCE_ACCUMULATE_FROM_START                               */
 } lmce_config;
+
+/* cfg.flags: the first micro-step after create or finalize ADDS its gradient to dW instead of
+ * writing it, for a caller that has already written part of the step's gradient into the same
+ * buffer (the embedding backward of the tied wte / lm_head matrix). */
+#define LMCE_ACCUMULATE_FROM_START 1
 
 typedef struct lmce_handle lmce_handle;
 
@@ -91,9 +97,11 @@ typedef struct lmce_handle lmce_handle;
  * error word: about 12 * max_N + 64 KB of device memory) and return a handle in *out.
  *   dW : device, fp32 [V, C], owned by the caller and kept by the handle until
  *        lmce_destroy.  The first lmce_microstep after create or finalize WRITES it
- *        (dW = this micro-step's gradient); later ones ADD to it.
+ *        (dW = this micro-step's gradient) unless cfg.flags has LMCE_ACCUMULATE_FROM_START;
+ *        later ones ADD to it.
  * Errors: LMCE_ERR_ARG (null cfg/dW/out, C or V <= 0, max_N < 0, unknown dtype/norm/path,
- *         G < 1, a forced path the shape does not allow), LMCE_ERR_ARCH, LMCE_ERR_CUDA.
+ *         G < 1, unknown flags, a forced path the shape does not allow), LMCE_ERR_ARCH,
+ *         LMCE_ERR_CUDA.
  */
 LMCE_API int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out);
 
@@ -132,6 +140,17 @@ LMCE_API int lmce_microstep(lmce_handle* h, const void* hidden, const void* W, c
  */
 LMCE_API int lmce_finalize(lmce_handle* h, double* loss_sum, int64_t* valid_count, double* loss_mean,
                   void* stream);
+
+/*
+ * lmce_dw_sumsq -- the sum over every element of dW of dW^2 to float64 accuracy, reduced in a
+ * fixed order (bitwise reproducible): the squared global norm a gradient clip
+ * (clip_grad_norm_ over the tied matrix) needs.  Enqueued on `stream` after the work already
+ * there, then waited for.  Reads dW as it stands (any number of micro-steps; normally after the
+ * last one of a step and before the optimizer).
+ *   sumsq : host -- the result
+ * Errors: LMCE_ERR_ARG (null h or sumsq), LMCE_ERR_CUDA.
+ */
+LMCE_API int lmce_dw_sumsq(lmce_handle* h, double* sumsq, void* stream);
 
 /* lmce_destroy -- free the library scratch (not dW) and the handle.  NULL is allowed. */
 LMCE_API int lmce_destroy(lmce_handle* h);
@@ -179,7 +198,8 @@ LMCE_API int lmce_profile_read(lmce_handle* h, int kind, double* total_ms, int64
  * routine.  Its scratch (per-row logsumexp, per-block partials, accumulators) is a fixed
  * array of about 360 KB compiled into the library, which every GPU that loads the library
  * holds until the process exits.
- *   cfg             : as for lmce_create; max_N is ignored, path must be AUTO or SIMT,
+ *   cfg             : as for lmce_create; max_N is ignored, flags must be 0 (accumulate_dW
+ *                     says whether dW is written or added to), path must be AUTO or SIMT,
  *                     C <= 2048
  *   hidden, W, targets, N, global_valid, dh, row_loss : as for lmce_microstep
  *   dW              : device, fp32 [V, C]; written (accumulate_dW == 0) or added to (!= 0)

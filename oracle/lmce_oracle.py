@@ -244,6 +244,15 @@ def dW_rows(micro_batches, W, lses, scales, vs, ignore_id: int = IGNORE_ID) -> n
     return out
 
 
+def dw_sumsq(dW) -> float:
+    """Sum over every element of dW of dW**2, in float64: the squared global norm that a
+    gradient clip divides by ("Reproduce GPT-2 124M", training configuration: the global-norm
+    clip grad_norm_clip = 1.0, applied with torch.nn.utils.clip_grad_norm_ after the
+    accumulation and before the optimizer)."""
+    x = f64(dW).ravel()
+    return float(np.dot(x, x))
+
+
 # ---------------------------------------------------------------------------
 # Closed forms used as pins
 # ---------------------------------------------------------------------------

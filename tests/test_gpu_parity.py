@@ -129,6 +129,68 @@ def test_empty_first_micro_step_writes_zero():
     assert max_rel_err(dW.double().cpu().numpy(), ref.dW) <= GRAD_REL["bf16"]
 
 
+
+def _valid_count(w):
+    return sum(int(((y >= 0) & (y < w.V)).sum()) for _, y in w.micro)
+
+
+@pytest.mark.parametrize("path", PATHS_BF16)
+def test_accumulate_from_start(path):
+    # dW already holds part of the step's gradient (the tied matrix's embedding backward): with
+    # LMCE_ACCUMULATE_FROM_START the first micro-step adds to it, and an empty first micro-step
+    # leaves it as it is
+    w = I.custom([0, 300, 173], 256, 1000, "bf16", seed=13, ignore_frac=0.1)
+    _need_path(path, w.C, w.V, w.dtype)
+    W, mbs = to_dev(w)
+    D = torch.randn(w.V, w.C, generator=torch.Generator().manual_seed(7)).mul_(1e-3)
+    dW = D.cuda()
+    L = M.Lmce(w.C, w.V, 300, dW, "bf16", grad_accum_steps=len(mbs), path=path, accumulate_from_start=True)
+    gv = _valid_count(w)
+    for h, y in mbs:
+        L.microstep(h, W, y, gv, torch.empty_like(h))
+    ls, cnt, mean = L.finalize()
+    L.close()
+    ref = run_oracle(w)
+    assert cnt == ref.count
+    got = dW.double().cpu().numpy() - D.double().numpy()
+    assert max_rel_err(got, ref.dW) <= GRAD_REL["bf16"]
+
+
+@pytest.mark.parametrize("path", PATHS_BF16)
+def test_dw_sumsq(path):
+    # the squared global norm of dW for a gradient clip: float64, fixed reduction order
+    w = I.custom([300, 173], 256, 1000, "bf16", seed=14, ignore_frac=0.1)
+    _need_path(path, w.C, w.V, w.dtype)
+    W, mbs = to_dev(w)
+    dW = torch.empty(w.V, w.C, device="cuda")
+    L = M.Lmce(w.C, w.V, 300, dW, "bf16", grad_accum_steps=len(mbs), path=path)
+    gv = _valid_count(w)
+    for h, y in mbs:
+        L.microstep(h, W, y, gv, torch.empty_like(h))
+    L.finalize()
+    a = L.dw_sumsq()
+    b = L.dw_sumsq()
+    L.close()
+    assert a == b
+    mine = O.dw_sumsq(dW.cpu().numpy())          # the same float32 values, another summation order
+    assert abs(a - mine) <= 1e-11 * mine
+    want = O.dw_sumsq(run_oracle(w).dW)          # the oracle's gradient: within the gradient tolerance
+    assert abs(a - want) <= 2 * GRAD_REL["bf16"] * want
+
+
+def test_dw_sumsq_odd_size_and_zero():
+    # V * C not a multiple of four, and all-zero dW (an empty step): exact
+    w = I.custom([0], 64, 301, "fp32", seed=15)
+    W, mbs = to_dev(w)
+    dW = torch.full((w.V, w.C), 5.0, device="cuda")
+    L = M.Lmce(w.C, w.V, 1, dW, "fp32")
+    assert L.dw_sumsq() == 25.0 * w.V * w.C
+    L.microstep(mbs[0][0], W, mbs[0][1], 1, torch.empty(0, w.C, device="cuda"))
+    L.finalize(check=False)
+    assert L.dw_sumsq() == 0.0
+    L.close()
+
+
 def test_no_valid_target():
     w = I.custom([64], 64, 100, "bf16", seed=6, ignore_frac=1.0)
     W, mbs = to_dev(w)

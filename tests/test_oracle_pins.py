@@ -317,3 +317,14 @@ def test_sampled_helpers_agree():
     lse, rl, dh = O.row_outputs(h[[2, 3]], W, y[[2, 3]], scales[1])
     assert np.abs(dh - r.micro[1].dh[[2, 3]]).max() < 1e-15
     assert np.abs(rl - r.micro[1].row_loss[[2, 3]]).max() < 1e-15
+
+
+def test_dw_sumsq_worked_examples():
+    # 3-4-5 and 1-2-2 triangles, and the invariants a plain sum of squares must keep
+    assert O.dw_sumsq(np.array([[3.0, 4.0]])) == 25.0
+    assert O.dw_sumsq(np.array([[1.0], [2.0], [2.0]])) == 9.0
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((7, 5))
+    assert abs(O.dw_sumsq(3.0 * x) - 9.0 * O.dw_sumsq(x)) <= 1e-12 * O.dw_sumsq(x) * 9.0
+    assert abs(O.dw_sumsq(x) - (O.dw_sumsq(x[:3]) + O.dw_sumsq(x[3:]))) <= 1e-12 * O.dw_sumsq(x)
+    assert O.dw_sumsq(np.zeros((4, 4))) == 0.0
