@@ -147,6 +147,73 @@ __global__ void __launch_bounds__(SQ_T) sumsq_final_kernel(const double* __restr
   if (threadIdx.x == 0) *out = sh[0];
 }
 
+// One AdamW step over the tied matrix, each element read and written once (30 bytes: dW, p, m, v
+// in; p, m, v and the bf16 copy of p out).  Decoupled weight decay and bias-corrected moments as
+// torch.optim.AdamW, with the betas, eps and decay of "How I trained my own GPT-2 124M",
+// section 6 "Implementing the Optimizer"; the update is one pass over the whole state, the fused
+// form of "Making LLM training fast", section "The optimizer step".
+struct AdamCoef {
+  float clip, b1, omb1, b2, omb2, decay, step_size, sqrt_bc2, eps;
+};
+__device__ __forceinline__ void adamw_elem(float g, float& p, float& m, float& v, const AdamCoef& k) {
+  g = k.clip * g;
+  m = k.b1 * m + k.omb1 * g;
+  v = k.b2 * v + k.omb2 * (g * g);
+  const float den = sqrtf(v) / k.sqrt_bc2 + k.eps;
+  p = p * k.decay - k.step_size * (m / den);
+}
+constexpr int AW_T = 256, AW_BLOCKS = 1216;   // 8 blocks per SM of a 152-SM GB300
+__global__ void __launch_bounds__(AW_T) adamw_kernel(const float* __restrict__ g, float* __restrict__ p,
+                                                    float* __restrict__ m, float* __restrict__ v,
+                                                    __nv_bfloat16* __restrict__ w, int64_t n, int vec,
+                                                    AdamCoef k) {
+  const int64_t stride = (int64_t)gridDim.x * AW_T;
+  int64_t i0 = (int64_t)blockIdx.x * AW_T + threadIdx.x;
+  if (vec) {
+    const int64_t n4 = n / 4;
+    const float4* g4 = reinterpret_cast<const float4*>(g);
+    float4* p4 = reinterpret_cast<float4*>(p);
+    float4* m4 = reinterpret_cast<float4*>(m);
+    float4* v4 = reinterpret_cast<float4*>(v);
+    for (int64_t i = i0; i < n4; i += stride) {
+      const float4 gg = __ldcs(g4 + i);
+      float4 pp = __ldcs(p4 + i), mm = __ldcs(m4 + i), vv = __ldcs(v4 + i);
+      adamw_elem(gg.x, pp.x, mm.x, vv.x, k);
+      adamw_elem(gg.y, pp.y, mm.y, vv.y, k);
+      adamw_elem(gg.z, pp.z, mm.z, vv.z, k);
+      adamw_elem(gg.w, pp.w, mm.w, vv.w, k);
+      __stcs(p4 + i, pp);
+      __stcs(m4 + i, mm);
+      __stcs(v4 + i, vv);
+      if (w) {   // the next forward reads W: a plain store leaves it in L2
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(pp.x, pp.y), hi = __floats2bfloat162_rn(pp.z, pp.w);
+        uint2 u;
+        u.x = *reinterpret_cast<const unsigned*>(&lo);
+        u.y = *reinterpret_cast<const unsigned*>(&hi);
+        reinterpret_cast<uint2*>(w)[i] = u;
+      }
+    }
+    i0 += n4 * 4;   // the ragged tail, fewer than 4 elements
+    for (int64_t i = i0; i < n; i += stride) {
+      float pp = p[i], mm = m[i], vv = v[i];
+      adamw_elem(g[i], pp, mm, vv, k);
+      p[i] = pp;
+      m[i] = mm;
+      v[i] = vv;
+      if (w) w[i] = __float2bfloat16_rn(pp);
+    }
+    return;
+  }
+  for (int64_t i = i0; i < n; i += stride) {
+    float pp = p[i], mm = m[i], vv = v[i];
+    adamw_elem(g[i], pp, mm, vv, k);
+    p[i] = pp;
+    m[i] = mm;
+    v[i] = vv;
+    if (w) w[i] = __float2bfloat16_rn(pp);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_finish(const StepArgs& a, const Scratch& s, int64_t nparts, Launch& L, int mode) {
@@ -371,6 +438,37 @@ extern "C" int lmce_dw_sumsq(lmce_handle* h, double* sumsq, void* stream) {
     return LMCE_ERR_CUDA;
   *sumsq = r;
   return LMCE_OK;
+}
+
+extern "C" int lmce_adamw(lmce_handle* h, float* p, float* m, float* v, void* W_out, int64_t step, float lr,
+                          float beta1, float beta2, float eps, float weight_decay, float clip, void* stream) {
+  if (!h || !p || !m || !v || step < 1) return LMCE_ERR_ARG;
+  if (!(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f) || !(eps >= 0.f)) return LMCE_ERR_ARG;
+  if (!isfinite(lr) || !isfinite(weight_decay) || !isfinite(clip)) return LMCE_ERR_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t n = h->cfg.V * h->cfg.C;
+  // bias corrections in float64 on the host, then the per-element constants in float32
+  const double bc1 = 1.0 - pow((double)beta1, (double)step), bc2 = 1.0 - pow((double)beta2, (double)step);
+  AdamCoef k;
+  k.clip = clip;
+  k.b1 = beta1;
+  k.omb1 = (float)(1.0 - (double)beta1);
+  k.b2 = beta2;
+  k.omb2 = (float)(1.0 - (double)beta2);
+  k.decay = (float)(1.0 - (double)lr * (double)weight_decay);
+  k.step_size = (float)((double)lr / bc1);
+  k.sqrt_bc2 = (float)sqrt(bc2);
+  k.eps = eps;
+  const uintptr_t al = (uintptr_t)h->dW | (uintptr_t)p | (uintptr_t)m | (uintptr_t)v | (uintptr_t)W_out;
+  const int vec = (al & 15) == 0;
+  Launch L;
+  L.st = st;
+  L.prof = &h->prof;
+  L.begin(K_FINISH);
+  adamw_kernel<<<AW_BLOCKS, AW_T, 0, st>>>(h->dW, p, m, v, (__nv_bfloat16*)W_out, n, vec, k);
+  L.end();
+  h->launches += L.n;
+  return cudaGetLastError() == cudaSuccess ? LMCE_OK : LMCE_ERR_CUDA;
 }
 
 extern "C" int lmce_destroy(lmce_handle* h) {

@@ -8,6 +8,7 @@ missing this module raises; there is no CPU fallback.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 
 import torch
@@ -32,7 +33,7 @@ TORCH_DTYPES = {"bf16": torch.bfloat16, "fp32": torch.float32}
 
 EXPORTS = ("lmce_create", "lmce_microstep", "lmce_finalize", "lmce_destroy", "lmce_status_string",
            "lmce_launch_count", "lmce_selected_path", "lmce_profile", "lmce_profile_read",
-           "lmce_microstep_noalloc", "lmce_dw_sumsq")
+           "lmce_microstep_noalloc", "lmce_dw_sumsq", "lmce_adamw")
 
 NOALLOC_MAX_N = 65536
 
@@ -75,6 +76,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.lmce_finalize.restype = i32
     L.lmce_dw_sumsq.argtypes = [vp, ctypes.POINTER(ctypes.c_double), vp]
     L.lmce_dw_sumsq.restype = i32
+    f32 = ctypes.c_float
+    L.lmce_adamw.argtypes = [vp, vp, vp, vp, vp, i64, f32, f32, f32, f32, f32, f32, vp]
+    L.lmce_adamw.restype = i32
     L.lmce_destroy.argtypes = [vp]
     L.lmce_destroy.restype = i32
     L.lmce_status_string.argtypes = [i32]
@@ -91,6 +95,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.lmce_microstep_noalloc.restype = i32
     _lib = L
     return L
+
+
+def clip_coef(sumsq: float, max_norm: float = 1.0) -> float:
+    """Global-norm clip coefficient for lmce_adamw's `clip`: max_norm / (sqrt(sumsq) + 1e-6), at most 1.
+
+    sumsq is the sum of squares over every gradient of the model (lmce_dw_sumsq gives the tied
+    matrix's share), as torch.nn.utils.clip_grad_norm_ computes it.
+    """
+    return min(1.0, float(max_norm) / (math.sqrt(float(sumsq)) + 1e-6))
 
 
 def status_string(status: int) -> str:
@@ -188,6 +201,24 @@ class Lmce:
         if st != OK:
             raise LmceError(st, "lmce_dw_sumsq")
         return out.value
+
+    def adamw(self, p, m, v, step: int, lr: float, W_out=None, betas=(0.9, 0.95), eps: float = 1e-8,
+              weight_decay: float = 0.1, clip: float = 1.0, stream=None):
+        """One AdamW step on the master weights p with this handle's dW (enqueued, no wait).
+
+        p, m, v: CUDA fp32 [V, C], updated in place (m = v = 0 before step 1); W_out: CUDA bf16
+        [V, C] or None, receives p rounded to bf16; clip: the global-norm clip coefficient.
+        """
+        shape = (self.V, self.C)
+        for t, name in ((p, "p"), (m, "m"), (v, "v")):
+            _check_dev(t, name, torch.float32, shape)
+        if W_out is not None:
+            _check_dev(W_out, "W_out", torch.bfloat16, shape)
+        st = self.lib.lmce_adamw(self.handle, _ptr(p), _ptr(m), _ptr(v), _ptr(W_out), int(step), float(lr),
+                                 float(betas[0]), float(betas[1]), float(eps), float(weight_decay),
+                                 float(clip), _stream(stream))
+        if st != OK:
+            raise LmceError(st, "lmce_adamw")
 
     def profile(self, enable: bool):
         """Record CUDA events around every kernel launch (enable=True clears old records)."""

@@ -152,6 +152,32 @@ LMCE_API int lmce_finalize(lmce_handle* h, double* loss_sum, int64_t* valid_coun
  */
 LMCE_API int lmce_dw_sumsq(lmce_handle* h, double* sumsq, void* stream);
 
+/*
+ * lmce_adamw -- one AdamW step on the tied matrix, after lmce_finalize, in one pass over the
+ * elements (decoupled weight decay and Adam's bias correction, as torch.optim.AdamW):
+ *   g = clip * dW
+ *   m = beta1 * m + (1 - beta1) * g           v = beta2 * v + (1 - beta2) * g^2
+ *   p = p * (1 - lr * weight_decay) - (lr / (1 - beta1^step)) * m / (sqrt(v) / sqrt(1 - beta2^step) + eps)
+ *   W_out = p rounded to nearest-even bf16
+ * in float32 (the bias corrections in float64 on the host).
+ *   h            : the handle whose dW holds the step's gradient (read only)
+ *   p, m, v      : device, fp32 [V, C]: master weights and the two moment estimates, updated in
+ *                  place (m and v zero before the first step); caller-owned
+ *   W_out        : device, bf16 [V, C] (the W the next forward reads), or NULL; caller-owned.
+ *                  Any alignment; when dW, p, m, v and W_out are all 16-byte aligned the kernel
+ *                  moves 16-byte vectors
+ *   step         : t >= 1, the step being taken
+ *   clip         : the global-norm clip coefficient, min(1, max_norm / (norm + 1e-6)) (1 for none)
+ *   lr, beta1, beta2, eps, weight_decay : as torch.optim.AdamW; "How I trained my own GPT-2 124M",
+ *                  section 6 "Implementing the Optimizer", uses 0.9, 0.95, 1e-8 and 0.1, with
+ *                  decay on every tensor of two or more dimensions (W is one)
+ * Enqueued on `stream`; does not block.  Counted under LMCE profile kind 1 (the finish kind).
+ * Errors: LMCE_ERR_ARG (null h/p/m/v, step < 1, a beta outside [0, 1), eps < 0 or NaN, a
+ *         non-finite lr, weight_decay or clip), LMCE_ERR_CUDA.
+ */
+LMCE_API int lmce_adamw(lmce_handle* h, float* p, float* m, float* v, void* W_out, int64_t step, float lr,
+                        float beta1, float beta2, float eps, float weight_decay, float clip, void* stream);
+
 /* lmce_destroy -- free the library scratch (not dW) and the handle.  NULL is allowed. */
 LMCE_API int lmce_destroy(lmce_handle* h);
 

@@ -22,6 +22,9 @@ What it computes, in the order the pages give it:
   normalisation here is therefore the global token-weighted mean (scale
   s = 1 / global valid count); the pages' own loss/G rule is kept as
   ``norm="micro_mean"`` (s_k = 1 / (valid_k * G)).
+* "How I trained my own GPT-2 124M", section 6, and "Reproduce GPT-2 124M", training
+  configuration: after the accumulation the gradient is clipped to a global norm of
+  1.0 and AdamW updates the weights (``dw_sumsq``, ``clip_coef``, ``adamw_step``).
 * zerotofrontier "GPT", section "Document boundaries, packing and masking": a
   pad target is ignored by the loss.  Its id is -100 here (the default of the
   PyTorch cross-entropy function the multi-GPU page cites).
@@ -251,6 +254,37 @@ def dw_sumsq(dW) -> float:
     accumulation and before the optimizer)."""
     x = f64(dW).ravel()
     return float(np.dot(x, x))
+
+
+def clip_coef(sumsq: float, max_norm: float = 1.0) -> float:
+    """The factor a global-norm clip multiplies every gradient by: max_norm / (norm + 1e-6),
+    never above 1, with norm = sqrt(sum of squares over all gradients) (same training
+    configuration; the 1e-6 guard is torch.nn.utils.clip_grad_norm_'s)."""
+    return min(1.0, max_norm / (math.sqrt(sumsq) + 1e-6))
+
+
+def adamw_step(p, m, v, g, step: int, lr: float, betas=(0.9, 0.95), eps: float = 1e-8,
+               weight_decay: float = 0.1, clip: float = 1.0):
+    """One AdamW update in float64, returning new (p, m, v).
+
+    "How I trained my own GPT-2 124M", section 6 (Implementing the Optimizer): Adam with a
+    decoupled weight decay that pulls every weight of a tensor with two or more dimensions
+    toward zero, built as torch.optim.AdamW with betas (0.9, 0.95), eps 1e-8 and decay 0.1
+    (training loop: learning rate 6e-4).  The update is that optimizer's: the decay
+    multiplies the weight by 1 - lr * weight_decay, the moments are exponential averages of
+    the gradient and of its square, each divided by 1 - beta^step to remove the bias of
+    their zero start, and the step is lr * mhat / (sqrt(vhat) + eps).  The gradient is
+    first multiplied by the clip coefficient.
+    """
+    b1, b2 = betas
+    g = clip * f64(g)
+    p, m, v = f64(p), f64(m), f64(v)
+    m = b1 * m + (1.0 - b1) * g
+    v = b2 * v + (1.0 - b2) * g * g
+    mhat = m / (1.0 - b1 ** step)
+    vhat = v / (1.0 - b2 ** step)
+    p = p * (1.0 - lr * weight_decay) - lr * mhat / (np.sqrt(vhat) + eps)
+    return p, m, v
 
 
 # ---------------------------------------------------------------------------

@@ -59,6 +59,14 @@ def test_argument_errors_before_any_device_call(lib):
     assert lib.lmce_microstep(None, None, None, None, 0, 0, None, None, None) == M.ERR_ARG
     assert lib.lmce_finalize(None, None, None, None, None) == M.ERR_ARG
     assert lib.lmce_dw_sumsq(None, None, None) == M.ERR_ARG
+    assert lib.lmce_adamw(None, None, None, None, None, 1, 1e-3, 0.9, 0.95, 1e-8, 0.1, 1.0, None) == M.ERR_ARG
     assert lib.lmce_destroy(None) == M.OK
     assert lib.lmce_profile(None, 1) == M.ERR_ARG
     assert lib.lmce_launch_count(None) == 0
+
+
+def test_clip_coef_host_helper():
+    # the binding's clip coefficient is the oracle's global-norm clip rule
+    from oracle import lmce_oracle as O
+    for sumsq, mx in ((4.0, 1.0), (0.25, 1.0), (0.0, 1.0), (1e6, 0.5), (1.0, 1.0)):
+        assert M.clip_coef(sumsq, mx) == O.clip_coef(sumsq, mx)

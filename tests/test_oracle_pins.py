@@ -328,3 +328,69 @@ def test_dw_sumsq_worked_examples():
     assert abs(O.dw_sumsq(3.0 * x) - 9.0 * O.dw_sumsq(x)) <= 1e-12 * O.dw_sumsq(x) * 9.0
     assert abs(O.dw_sumsq(x) - (O.dw_sumsq(x[:3]) + O.dw_sumsq(x[3:]))) <= 1e-12 * O.dw_sumsq(x)
     assert O.dw_sumsq(np.zeros((4, 4))) == 0.0
+
+
+def test_clip_coef_worked_examples_and_torch():
+    # norm 2 > 1: scaled down to norm 1 (up to the 1e-6 guard); norm 0.5 < 1: untouched
+    assert O.clip_coef(4.0, 1.0) == 1.0 / (2.0 + 1e-6)
+    assert O.clip_coef(0.25, 1.0) == 1.0
+    assert O.clip_coef(0.0, 1.0) == 1.0
+    # torch's global-norm clip over two tensors scales each by the same coefficient
+    rng = np.random.default_rng(11)
+    a, b = rng.standard_normal((6, 4)), rng.standard_normal(9)
+    ta, tb = torch.zeros(6, 4, dtype=torch.float64), torch.zeros(9, dtype=torch.float64)
+    ta.grad, tb.grad = torch.tensor(a), torch.tensor(b)
+    torch.nn.utils.clip_grad_norm_([ta, tb], 1.0, foreach=False)
+    c = O.clip_coef(O.dw_sumsq(a) + O.dw_sumsq(b), 1.0)
+    assert c < 1.0
+    np.testing.assert_allclose(ta.grad.numpy(), c * a, rtol=1e-14, atol=0)
+    np.testing.assert_allclose(tb.grad.numpy(), c * b, rtol=1e-14, atol=0)
+
+
+def test_adamw_first_step_closed_form():
+    # m = v = 0, t = 1: mhat = g and vhat = g^2, so the step is lr * g / (|g| + eps), plus the decay
+    rng = np.random.default_rng(12)
+    p = rng.standard_normal(50)
+    g = rng.standard_normal(50)
+    g[:3] = (0.0, 1e-9, -1e-9)
+    lr, wd, eps = 6e-4, 0.1, 1e-8
+    p1, m1, v1 = O.adamw_step(p, np.zeros(50), np.zeros(50), g, 1, lr, (0.9, 0.95), eps, wd)
+    np.testing.assert_allclose(p1, p * (1 - lr * wd) - lr * g / (np.abs(g) + eps), rtol=1e-13, atol=1e-18)
+    np.testing.assert_allclose(m1, 0.1 * g, rtol=1e-14)
+    np.testing.assert_allclose(v1, 0.05 * g * g, rtol=1e-14)
+    assert p1[0] == p[0] * (1 - lr * wd)   # a zero gradient leaves only the decay
+
+
+def test_adamw_constant_gradient_geometric_series():
+    # a constant gradient keeps mhat = g and vhat = g^2 at every step (the bias correction is
+    # exact), so T steps sum a geometric series: p_T = p0 d^T - u (1 - d^T) / (1 - d)
+    rng = np.random.default_rng(13)
+    p0 = rng.standard_normal(20)
+    g = rng.standard_normal(20) * 1e-2
+    lr, wd, eps, T = 1e-3, 0.1, 1e-8, 25
+    p, m, v = p0.copy(), np.zeros(20), np.zeros(20)
+    for t in range(1, T + 1):
+        p, m, v = O.adamw_step(p, m, v, g, t, lr, (0.9, 0.95), eps, wd)
+    d = 1 - lr * wd
+    u = lr * g / (np.abs(g) + eps)
+    np.testing.assert_allclose(p, p0 * d ** T - u * (1 - d ** T) / (1 - d), rtol=1e-11, atol=1e-15)
+
+
+@pytest.mark.parametrize("clip", [1.0, 0.37])
+def test_adamw_matches_torch_optim(clip):
+    # torch.optim.AdamW in float64 over several steps of varying gradients
+    rng = np.random.default_rng(14)
+    shape = (7, 9)
+    p0 = rng.standard_normal(shape)
+    w = torch.nn.Parameter(torch.tensor(p0))
+    opt = torch.optim.AdamW([w], lr=6e-4, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1, foreach=False)
+    p, m, v = p0.copy(), np.zeros(shape), np.zeros(shape)
+    for t in range(1, 6):
+        g = rng.standard_normal(shape) * (0.1 * t)
+        w.grad = torch.tensor(clip * g)
+        opt.step()
+        p, m, v = O.adamw_step(p, m, v, g, t, 6e-4, (0.9, 0.95), 1e-8, 0.1, clip)
+    st = opt.state[w]
+    np.testing.assert_allclose(p, w.detach().numpy(), rtol=1e-13, atol=1e-16)
+    np.testing.assert_allclose(m, st["exp_avg"].numpy(), rtol=1e-13, atol=1e-18)
+    np.testing.assert_allclose(v, st["exp_avg_sq"].numpy(), rtol=1e-13, atol=1e-20)
