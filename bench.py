@@ -40,6 +40,8 @@ def parse():
     p.add_argument("--workload", default="gpt2_124m_head")
     p.add_argument("--path", default="auto", choices=["auto", "simt", "tcgen05", "tcgen05_two_pass"])
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--compact", action="store_true",
+                   help="micro-steps over the valid rows only (lmce_microstep_compact)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample-rows", type=int, default=2048)
     return p.parse_args()
@@ -190,14 +192,22 @@ def run_lmce(args, rank, world, local_rank):
     dhs = [torch.empty_like(h) for h, _ in mbs]
     dW = torch.empty(w.V, w.C, dtype=torch.float32, device=dev)
     max_N = max(int(y.numel()) for _, y in mbs)
-    L = M.Lmce(w.C, w.V, max_N, dW, w.dtype, norm="global", grad_accum_steps=w.G, path=args.path)
+    L = M.Lmce(w.C, w.V, max_N, dW, w.dtype, norm="global", grad_accum_steps=w.G, path=args.path,
+               compact=args.compact)
+    nvs = w.valid_counts()
     gv = dp.global_valid_count(sum(w.valid_counts()), device=dev if world > 1 else None)
     stream = torch.cuda.current_stream(dev)
     tokens_rank = w.tokens
 
-    def step():
-        for (h, y), dh in zip(mbs, dhs):
+    def micro(h, y, n_valid, dh):
+        if args.compact:
+            L.microstep_compact(h, W, y, n_valid, gv, dh, stream=stream)
+        else:
             L.microstep(h, W, y, gv, dh, stream=stream)
+
+    def step():
+        for (h, y), dh, nv in zip(mbs, dhs, nvs):
+            micro(h, y, nv, dh)
         res = L.finalize(stream=stream)
         if world > 1:
             dp.reduce_step(dW, res[0], res[1])
@@ -261,7 +271,7 @@ def run_lmce(args, rank, world, local_rank):
         def step_e2e(b):
             for k, dh in enumerate(dhs):
                 stream.wait_event(ready[b][k])
-                L.microstep(h_dev[b][k], W, y_dev[b][k], gv, dh, stream=stream)
+                micro(h_dev[b][k], y_dev[b][k], nvs[k], dh)
                 used[b][k].record(stream)
                 if k == 0:
                     issue_copies(1 - b)   # the next step's inputs stream in meanwhile
@@ -345,7 +355,10 @@ def run_lmce(args, rank, world, local_rank):
     dom = max(kinds, key=lambda k: kinds[k][0])
     dom_ms, dom_n = kinds[dom]
     tok_per_launch = tokens_rank / w.G
-    alg_flop_launch = {"lse": 2.0, "dW": 2.0, "dh": 2.0, "lse_dh": 4.0, "finish": 0.0}[dom] * w.C * w.V * tok_per_launch
+    valid_rank = sum(nvs)
+    # rows one heavy launch processes: every row, or the valid rows alone when compacted
+    rows_per_launch = valid_rank / w.G if args.compact else tok_per_launch
+    alg_flop_launch = {"lse": 2.0, "dW": 2.0, "dh": 2.0, "lse_dh": 4.0, "finish": 0.0}[dom] * w.C * w.V * rows_per_launch
     achieved = alg_flop_launch / (dom_ms / dom_n / 1e3) / 1e12
     if L.path.startswith("tcgen05"):
         peak = pk["bf16_tflops_sustained"] if "bf16_tflops_sustained" in pk else pk["bf16_tflops"]
@@ -354,7 +367,9 @@ def run_lmce(args, rank, world, local_rank):
         clk = (clocks or {}).get("sm_max_mhz") or pk.get("sm_max_mhz", 2070.0)
         peak = N_SM * FP32_LANES_PER_SM * 2 * clk * 1e6 / 1e12
         bound = "alu"
-    total_frac = value / world * flop_tok / 1e12 / (pk.get("bf16_tflops_sustained") or pk["bf16_tflops"])
+    # useful work: 6 C V flop per VALID token (an ignored row's gradient is zero)
+    valid_per_s = value * valid_rank / tokens_rank
+    total_frac = valid_per_s / world * flop_tok / 1e12 / (pk.get("bf16_tflops_sustained") or pk["bf16_tflops"])
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         rate, secs = oracle_sample_rate(w, args.cpu_sample_rows)
@@ -367,13 +382,15 @@ def run_lmce(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "fp32",
         "data": "synthetic",
         "config": {"workload": args.workload, "tokens_per_step": tokens_rank * world, "micro_steps": w.G,
-                   "micro_batch_tokens": int(tok_per_launch), "C": w.C, "V": w.V, "path": L.path,
+                   "micro_batch_tokens": int(tok_per_launch), "valid_tokens": [int(n) for n in nvs],
+                   "C": w.C, "V": w.V, "path": L.path, "compact": bool(args.compact),
                    "parallelism": f"dp{world}",
                    "l2": "no flush: inputs larger than L2 (per step %d distinct h buffers of %.0f MB, "
                          "W %.0f MB, fp32 dW %.0f MB)" % (w.G, mbs[0][0].numel() * 2 / 1e6,
                                                          W.numel() * W.element_size() / 1e6,
                                                          dW.numel() * 4 / 1e6)},
-        "frac_of_peak": {"value": total_frac, "flop_per_token": flop_tok,
+        "valid_tokens_per_s": valid_per_s,
+        "frac_of_peak": {"value": total_frac, "flop_per_token": flop_tok, "tokens": "valid",
                          "peak_tflops": pk.get("bf16_tflops_sustained") or pk["bf16_tflops"],
                          "peak": f"bf16 sustained, {pk_kind}"},
         "roofline": {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

@@ -237,6 +237,7 @@ struct lmce_handle {
   DevAcc* host_acc;    // pinned
   bool first;          // next micro-step writes dW instead of adding (unless LMCE_ACCUMULATE_FROM_START)
   double* sumsq_part;  // lmce_dw_sumsq: per-block float64 partials, then the result
+  CompactScratch cs;   // lmce_microstep_compact (LMCE_COMPACT_VALID_ROWS), else all null
   int attempted;       // micro-steps accepted since create/finalize
   int64_t launches;
   Prof prof;
@@ -266,6 +267,17 @@ static void free_scratch(lmce_handle* h) {
   cudaFree(h->sc.tc_tile_flag);
   cudaFree(h->sumsq_part);
   h->sumsq_part = nullptr;
+  cudaFree(h->cs.h_c);
+  cudaFree(h->cs.dh_c);
+  cudaFree(h->cs.y_c);
+  cudaFree(h->cs.rl_c);
+  cudaFree(h->cs.pos);
+  cudaFree(h->cs.blk_cnt);
+  cudaFree(h->cs.blk_err);
+  cudaFree(h->cs.blk_off);
+  cudaFree(h->cs.total);
+  cudaFreeHost(h->cs.host_total);
+  h->cs = CompactScratch{};
   if (h->host_acc) cudaFreeHost(h->host_acc);
   memset(&h->sc, 0, sizeof(h->sc));
   h->host_acc = nullptr;
@@ -279,7 +291,7 @@ extern "C" int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out)
   if (cfg->dtype != LMCE_BF16 && cfg->dtype != LMCE_FP32) return LMCE_ERR_ARG;
   if (cfg->norm != LMCE_NORM_GLOBAL && cfg->norm != LMCE_NORM_MICRO_MEAN) return LMCE_ERR_ARG;
   if (cfg->path < LMCE_PATH_AUTO || cfg->path > LMCE_PATH_TCGEN05_TWO_PASS) return LMCE_ERR_ARG;
-  if (cfg->flags & ~LMCE_ACCUMULATE_FROM_START) return LMCE_ERR_ARG;
+  if (cfg->flags & ~(LMCE_ACCUMULATE_FROM_START | LMCE_COMPACT_VALID_ROWS)) return LMCE_ERR_ARG;
   const bool tc_ok = tc_supported(cfg->C, cfg->V, cfg->dtype == LMCE_BF16);
   const bool simt_ok = cfg->C <= 2048;
   int path;
@@ -327,6 +339,22 @@ extern "C" int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out)
          cudaMemset(h->sc.tc_tile_flag, 0, sizeof(unsigned) * tiles) == cudaSuccess;
   }
   ok = ok && cudaMalloc(&h->sumsq_part, sizeof(double) * (SQ_BLOCKS + 1)) == cudaSuccess;
+  if (ok && (cfg->flags & LMCE_COMPACT_VALID_ROWS)) {
+    const size_t rows = (size_t)maxN * (size_t)cfg->C * (cfg->dtype == LMCE_BF16 ? 2 : 4);
+    const size_t nb = (size_t)compact_blocks(maxN);
+    CompactScratch& q = h->cs;
+    ok = cudaMalloc(&q.h_c, rows) == cudaSuccess && cudaMalloc(&q.dh_c, rows) == cudaSuccess &&
+         cudaMalloc(&q.y_c, sizeof(int32_t) * maxN) == cudaSuccess &&
+         cudaMalloc(&q.rl_c, sizeof(float) * maxN) == cudaSuccess &&
+         cudaMalloc(&q.pos, sizeof(int32_t) * maxN) == cudaSuccess &&
+         cudaMalloc(&q.blk_cnt, sizeof(int) * nb) == cudaSuccess &&
+         cudaMalloc(&q.blk_err, sizeof(unsigned) * nb) == cudaSuccess &&
+         cudaMalloc(&q.blk_off, sizeof(int64_t) * nb) == cudaSuccess &&
+         cudaMalloc(&q.total, sizeof(int64_t)) == cudaSuccess &&
+         cudaMallocHost(&q.host_total, sizeof(int64_t)) == cudaSuccess &&
+         // defined contents for rows a wrong n_valid would read: zero rows, targets -1
+         cudaMemset(q.h_c, 0, rows) == cudaSuccess && cudaMemset(q.y_c, 0xff, sizeof(int32_t) * maxN) == cudaSuccess;
+  }
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
     free_scratch(h);
@@ -337,16 +365,12 @@ extern "C" int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out)
   return LMCE_OK;
 }
 
-extern "C" int lmce_microstep(lmce_handle* h, const void* hidden, const void* W, const int32_t* targets,
-                              int64_t N, int64_t global_valid, void* dh, float* row_loss, void* stream) {
-  if (!h) return LMCE_ERR_ARG;
+namespace {
+
+// The micro-step after argument checks: hidden, dh (and the TMA-read W, dW) already validated.
+int run_microstep(lmce_handle* h, const void* hidden, const void* W, const int32_t* targets, int64_t N,
+                  int64_t global_valid, void* dh, float* row_loss, cudaStream_t st) {
   const lmce_config& c = h->cfg;
-  if (N < 0 || N > c.max_N) return LMCE_ERR_ARG;
-  if (N > 0 && (!hidden || !W || !targets || !dh)) return LMCE_ERR_ARG;
-  if (h->path != LMCE_PATH_SIMT && N > 0) {
-    if (((uintptr_t)hidden | (uintptr_t)W | (uintptr_t)dh | (uintptr_t)h->dW) & 15) return LMCE_ERR_ARG;
-  }
-  cudaStream_t st = (cudaStream_t)stream;
   const size_t esz = c.dtype == LMCE_BF16 ? 2 : 4;
   if (c.norm == LMCE_NORM_GLOBAL && global_valid <= 0) {
     if (N > 0 && cudaMemsetAsync(dh, 0, (size_t)N * c.C * esz, st) != cudaSuccess) return LMCE_ERR_CUDA;
@@ -394,6 +418,65 @@ extern "C" int lmce_microstep(lmce_handle* h, const void* hidden, const void* W,
   return LMCE_OK;
 }
 
+}  // namespace
+
+extern "C" int lmce_microstep(lmce_handle* h, const void* hidden, const void* W, const int32_t* targets,
+                              int64_t N, int64_t global_valid, void* dh, float* row_loss, void* stream) {
+  if (!h) return LMCE_ERR_ARG;
+  if (N < 0 || N > h->cfg.max_N) return LMCE_ERR_ARG;
+  if (N > 0 && (!hidden || !W || !targets || !dh)) return LMCE_ERR_ARG;
+  if (h->path != LMCE_PATH_SIMT && N > 0) {
+    if (((uintptr_t)hidden | (uintptr_t)W | (uintptr_t)dh | (uintptr_t)h->dW) & 15) return LMCE_ERR_ARG;
+  }
+  return run_microstep(h, hidden, W, targets, N, global_valid, dh, row_loss, (cudaStream_t)stream);
+}
+
+extern "C" int lmce_microstep_compact(lmce_handle* h, const void* hidden, const void* W, const int32_t* targets,
+                                      int64_t N, int64_t n_valid, int64_t global_valid, void* dh, float* row_loss,
+                                      void* stream) {
+  if (!h || !h->cs.h_c) return LMCE_ERR_ARG;
+  const lmce_config& c = h->cfg;
+  if (N < 0 || N > c.max_N || n_valid < -1 || n_valid > N) return LMCE_ERR_ARG;
+  if (N > 0 && (!hidden || !W || !targets || !dh)) return LMCE_ERR_ARG;
+  const size_t esz = c.dtype == LMCE_BF16 ? 2 : 4;
+  if (N > 0 && (((uintptr_t)hidden | (uintptr_t)dh) & (esz - 1))) return LMCE_ERR_ARG;
+  if (h->path != LMCE_PATH_SIMT && N > 0 && (((uintptr_t)W | (uintptr_t)h->dW) & 15)) return LMCE_ERR_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (c.norm == LMCE_NORM_GLOBAL && global_valid <= 0)   // refused before any launch, as lmce_microstep
+    return run_microstep(h, hidden, W, targets, N, global_valid, dh, row_loss, st);
+  StepArgs a{};
+  a.hidden = hidden;
+  a.targets = targets;
+  a.dh = dh;
+  a.row_loss = row_loss;
+  a.N = N;
+  a.C = c.C;
+  a.V = c.V;
+  a.ignore_id = c.ignore_id;
+  a.bf16 = c.dtype == LMCE_BF16;
+  Launch L;
+  L.st = st;
+  L.prof = &h->prof;
+  cudaError_t e = compact_rows(a, h->cs, h->sc.acc, n_valid, L);
+  h->launches += L.n;
+  if (e != cudaSuccess) return LMCE_ERR_CUDA;
+  if (n_valid < 0) {
+    if (cudaMemcpyAsync(h->cs.host_total, h->cs.total, sizeof(int64_t), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return LMCE_ERR_CUDA;
+    n_valid = *h->cs.host_total;
+  }
+  const int s = run_microstep(h, h->cs.h_c, W, h->cs.y_c, n_valid, global_valid, h->cs.dh_c,
+                              row_loss ? h->cs.rl_c : nullptr, st);
+  if (s != LMCE_OK) return s;
+  Launch L2;
+  L2.st = st;
+  L2.prof = &h->prof;
+  e = compact_scatter(a, h->cs, n_valid, L2);
+  h->launches += L2.n;
+  return e == cudaSuccess ? LMCE_OK : LMCE_ERR_CUDA;
+}
+
 extern "C" int lmce_finalize(lmce_handle* h, double* loss_sum, int64_t* valid_count, double* loss_mean,
                              void* stream) {
   if (!h) return LMCE_ERR_ARG;
@@ -410,6 +493,7 @@ extern "C" int lmce_finalize(lmce_handle* h, double* loss_sum, int64_t* valid_co
   h->attempted = 0;
   if (cudaMemsetAsync(h->sc.acc, 0, sizeof(DevAcc), st) != cudaSuccess) return LMCE_ERR_CUDA;
   if (r.err & ERR_BIT_TIMEOUT) return LMCE_ERR_CUDA;  // a bounded device wait ran out
+  if (r.err & ERR_BIT_COUNT) return LMCE_ERR_ARG;     // a compacted micro-step's n_valid was wrong
   if (r.err & ERR_BIT_BAD_TARGET) return LMCE_ERR_BAD_TARGET;
   if ((r.err & ERR_BIT_NONFINITE) || !isfinite(r.loss_sum)) return LMCE_ERR_NONFINITE;
   if (r.count == 0) return LMCE_ERR_NO_VALID;

@@ -72,6 +72,7 @@ constexpr unsigned ERR_BIT_BAD_TARGET = 1u;
 constexpr unsigned ERR_BIT_NONFINITE = 2u;
 // A bounded device wait ran out (tensor-core path); bits 8..15 say which wait.
 constexpr unsigned ERR_BIT_TIMEOUT = 4u;
+constexpr unsigned ERR_BIT_COUNT = 8u;      // a compacted micro-step's valid count was not the caller's
 
 // Arguments of one micro-step as the kernels see them.
 struct StepArgs {
@@ -109,6 +110,28 @@ struct Scratch {
 };
 
 constexpr int TC_MAX_SPLIT = 32;
+
+// Scratch of the valid-row compaction (allocated when the handle is created with
+// LMCE_COMPACT_VALID_ROWS): the compacted rows, their targets, dh and row losses, each row's
+// position, and the per-block counts and offsets.
+struct CompactScratch {
+  void* h_c;           // [max_N, C] dtype
+  void* dh_c;          // [max_N, C] dtype
+  int32_t* y_c;        // [max_N]
+  float* rl_c;         // [max_N]
+  int32_t* pos;        // [max_N] position of row n among the valid rows, -1 if ignored
+  int* blk_cnt;        // [compact_blocks(max_N)]
+  unsigned* blk_err;   // [compact_blocks(max_N)]
+  int64_t* blk_off;    // [compact_blocks(max_N)]
+  int64_t* total;      // [1] valid rows found
+  int64_t* host_total; // pinned [1]
+};
+int64_t compact_blocks(int64_t N);
+// count + scan + gather of a.hidden / a.targets (a.N rows) into the compact buffers; the
+// valid total is checked against n_valid (>= 0) and bad targets are flagged in acc->err
+cudaError_t compact_rows(const StepArgs& a, const CompactScratch& cs, DevAcc* acc, int64_t n_valid, Launch& L);
+// dh / row_loss of a.N rows from the first n_valid compact rows, zero for the ignored rows
+cudaError_t compact_scatter(const StepArgs& a, const CompactScratch& cs, int64_t n_valid, Launch& L);
 
 // Fixed-order reduction of the per-block partials of one micro-step into the step
 // accumulators; also computes this micro-step's gradient scale.  One launch.

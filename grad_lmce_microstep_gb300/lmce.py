@@ -33,7 +33,7 @@ TORCH_DTYPES = {"bf16": torch.bfloat16, "fp32": torch.float32}
 
 EXPORTS = ("lmce_create", "lmce_microstep", "lmce_finalize", "lmce_destroy", "lmce_status_string",
            "lmce_launch_count", "lmce_selected_path", "lmce_profile", "lmce_profile_read",
-           "lmce_microstep_noalloc", "lmce_dw_sumsq", "lmce_adamw")
+           "lmce_microstep_noalloc", "lmce_dw_sumsq", "lmce_adamw", "lmce_microstep_compact")
 
 NOALLOC_MAX_N = 65536
 
@@ -47,6 +47,7 @@ class Config(ctypes.Structure):
                 ("flags", ctypes.c_int32)]
 
 ACCUMULATE_FROM_START = 1   # Config.flags: the first micro-step adds to dW instead of writing it
+COMPACT_VALID_ROWS = 2      # Config.flags: scratch for microstep_compact
 
 
 class LmceError(RuntimeError):
@@ -71,6 +72,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.lmce_create.restype = i32
     L.lmce_microstep.argtypes = [vp, vp, vp, vp, i64, i64, vp, vp, vp]
     L.lmce_microstep.restype = i32
+    L.lmce_microstep_compact.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, vp]
+    L.lmce_microstep_compact.restype = i32
     L.lmce_finalize.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64),
                                 ctypes.POINTER(ctypes.c_double), vp]
     L.lmce_finalize.restype = i32
@@ -141,14 +144,15 @@ class Lmce:
 
     def __init__(self, C: int, V: int, max_N: int, dW: torch.Tensor, dtype: str = "bf16",
                  ignore_id: int = -100, norm: str = "global", grad_accum_steps: int = 1,
-                 path: str = "auto", accumulate_from_start: bool = False):
+                 path: str = "auto", accumulate_from_start: bool = False, compact: bool = False):
         _check_dev(dW, "dW", torch.float32, (V, C))
         self.lib = load()
         self.C, self.V, self.max_N = int(C), int(V), int(max_N)
         self.dtype = dtype
         self.dW = dW
         cfg = Config(self.C, self.V, self.max_N, DTYPES[dtype], int(ignore_id), NORMS[norm],
-                     int(grad_accum_steps), PATHS[path], ACCUMULATE_FROM_START if accumulate_from_start else 0)
+                     int(grad_accum_steps), PATHS[path],
+                     (ACCUMULATE_FROM_START if accumulate_from_start else 0) | (COMPACT_VALID_ROWS if compact else 0))
         h = ctypes.c_void_p()
         st = self.lib.lmce_create(ctypes.byref(cfg), _ptr(dW), ctypes.byref(h))
         if st != OK:
@@ -179,6 +183,28 @@ class Lmce:
                                      int(global_valid), _ptr(dh), _ptr(row_loss), _stream(stream))
         if check and st != OK:
             raise LmceError(st, "lmce_microstep")
+        return st
+
+    def microstep_compact(self, hidden, W, targets, n_valid: int = -1, global_valid: int = 0, dh=None,
+                          row_loss=None, stream=None, check: bool = True) -> int:
+        """A micro-step over the rows with a target in [0, V) only (handle made with compact=True).
+
+        n_valid: this micro-step's valid targets, or -1 to let the library count them (blocking).
+        dh and row_loss get zeros on the ignored rows.
+        """
+        N = int(targets.numel())
+        tdt = TORCH_DTYPES[self.dtype]
+        if N > 0:
+            _check_dev(hidden, "hidden", tdt, (N, self.C))
+            _check_dev(W, "W", tdt, (self.V, self.C))
+            _check_dev(targets, "targets", torch.int32, (N,))
+            _check_dev(dh, "dh", tdt, (N, self.C))
+            if row_loss is not None:
+                _check_dev(row_loss, "row_loss", torch.float32, (N,))
+        st = self.lib.lmce_microstep_compact(self.handle, _ptr(hidden), _ptr(W), _ptr(targets), N, int(n_valid),
+                                             int(global_valid), _ptr(dh), _ptr(row_loss), _stream(stream))
+        if check and st != OK:
+            raise LmceError(st, "lmce_microstep_compact")
         return st
 
     def finalize(self, stream=None, check: bool = True):
@@ -257,8 +283,10 @@ class Lmce:
 
 
 def run_step(W, micro_batches, dtype: str, norm: str = "global", path: str = "auto", ignore_id: int = -100,
-             row_loss: bool = False, dW=None, global_valid=None):
+             row_loss: bool = False, dW=None, global_valid=None, compact: bool = False):
     """Convenience: one optimizer step over CUDA micro-batches [(h, y)].
+
+    compact=True runs every micro-step over its valid rows only (lmce_microstep_compact).
 
     Returns (dW, [dh_k], [row_loss_k or None], (loss_sum, count, loss_mean, status)).
     """
@@ -268,13 +296,17 @@ def run_step(W, micro_batches, dtype: str, norm: str = "global", path: str = "au
         dW = torch.empty(V, C, dtype=torch.float32, device=W.device)
     if global_valid is None:
         global_valid = sum(int(((y >= 0) & (y < V)).sum()) for _, y in micro_batches)
-    L = Lmce(C, V, max_N, dW, dtype, ignore_id, norm, len(micro_batches), path)
+    L = Lmce(C, V, max_N, dW, dtype, ignore_id, norm, len(micro_batches), path, compact=compact)
     try:
         dhs, rls = [], []
         for h, y in micro_batches:
             dh = torch.empty_like(h)
             rl = torch.empty(y.numel(), dtype=torch.float32, device=W.device) if row_loss else None
-            L.microstep(h, W, y, global_valid, dh, rl, check=False)
+            if compact:
+                n_valid = int(((y >= 0) & (y < V)).sum())
+                L.microstep_compact(h, W, y, n_valid, global_valid, dh, rl, check=False)
+            else:
+                L.microstep(h, W, y, global_valid, dh, rl, check=False)
             dhs.append(dh)
             rls.append(rl)
         res = L.finalize(check=False)

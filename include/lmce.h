@@ -81,13 +81,16 @@ typedef struct lmce_config {
   int32_t norm;             /* lmce_norm                                                     */
   int32_t grad_accum_steps; /* G >= 1; used by LMCE_NORM_MICRO_MEAN                          */
   int32_t path;             /* lmce_path                                                     */
-  int32_t flags;            /* 0 or LMCE_ACCUMULATE_FROM_START                               */
+  int32_t flags;            /* 0, or LMCE_ACCUMULATE_FROM_START | LMCE_COMPACT_VALID_ROWS    */
 } lmce_config;
 
 /* cfg.flags: the first micro-step after create or finalize ADDS its gradient to dW instead of
  * writing it, for a caller that has already written part of the step's gradient into the same
  * buffer (the embedding backward of the tied wte / lm_head matrix). */
 #define LMCE_ACCUMULATE_FROM_START 1
+/* cfg.flags: also allocate the scratch of lmce_microstep_compact (two [max_N, C] row buffers of
+ * the input dtype and 16 bytes per row). */
+#define LMCE_COMPACT_VALID_ROWS 2
 
 typedef struct lmce_handle lmce_handle;
 
@@ -127,6 +130,26 @@ LMCE_API int lmce_microstep(lmce_handle* h, const void* hidden, const void* W, c
                    int64_t N, int64_t global_valid, void* dh, float* row_loss, void* stream);
 
 /*
+ * lmce_microstep_compact -- lmce_microstep over the valid rows only.  A row whose target is
+ * ignored (masked pad spans: zerotofrontier "GPT", section "Document boundaries, packing and
+ * masking") adds nothing to the loss, dh or dW, so the library gathers the rows with a target in
+ * [0, V), in their input order, runs both passes over those n_valid rows and scatters dh (and
+ * row_loss) back, with zeros on the ignored rows.  The results equal lmce_microstep's up to the
+ * summation order of dW (the valid rows sit in other tiles).
+ *   n_valid : the valid targets of this micro-step (the caller counts them as it counts
+ *             global_valid), 0 <= n_valid <= N; or -1: the library counts them and waits for the
+ *             count on `stream` (this call then blocks).  A count that differs from the targets
+ *             makes lmce_finalize return LMCE_ERR_ARG, with dh and dW of the step unusable.
+ *   other arguments as lmce_microstep.  The handle must have been created with
+ *   LMCE_COMPACT_VALID_ROWS.
+ * Errors: LMCE_ERR_ARG (as lmce_microstep, n_valid < -1 or > N, no compaction scratch),
+ *         LMCE_ERR_NO_VALID (as lmce_microstep), LMCE_ERR_CUDA.
+ */
+LMCE_API int lmce_microstep_compact(lmce_handle* h, const void* hidden, const void* W, const int32_t* targets,
+                                    int64_t N, int64_t n_valid, int64_t global_valid, void* dh, float* row_loss,
+                                    void* stream);
+
+/*
  * lmce_finalize -- synchronise `stream`, read the step's results and reset the handle
  * for the next optimizer step (the next micro-step writes dW again).
  *   loss_sum    : host, may be NULL -- sum of the valid rows' losses over the step
@@ -134,7 +157,8 @@ LMCE_API int lmce_microstep(lmce_handle* h, const void* hidden, const void* W, c
  *   loss_mean   : host, may be NULL -- sum_k s_k * loss_sum_k, the objective whose gradient
  *                 dW holds: the token mean for GLOBAL norm on one rank, the pages'
  *                 sum_k mean_k / G for MICRO_MEAN; NaN when no target was valid
- * Errors: LMCE_ERR_STATE (no micro-step since create/finalize), LMCE_ERR_BAD_TARGET,
+ * Errors: LMCE_ERR_STATE (no micro-step since create/finalize), LMCE_ERR_ARG (a compacted
+ *         micro-step's n_valid was not its targets' count), LMCE_ERR_BAD_TARGET,
  *         LMCE_ERR_NONFINITE, LMCE_ERR_NO_VALID, LMCE_ERR_CUDA.  Results are written
  *         whenever the device values could be read, errors included.
  */

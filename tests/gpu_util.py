@@ -19,10 +19,10 @@ def to_dev(w, device="cuda"):
     return W, mbs
 
 
-def run_lib(w, path="auto", norm="global", row_loss=True, global_valid=None):
+def run_lib(w, path="auto", norm="global", row_loss=True, global_valid=None, compact=False):
     W, mbs = to_dev(w)
     dW, dhs, rls, res = M.run_step(W, mbs, w.dtype, norm=norm, path=path, row_loss=row_loss,
-                                   global_valid=global_valid)
+                                   global_valid=global_valid, compact=compact)
     torch.cuda.synchronize()
     return {
         "dW": dW.double().cpu().numpy(),

@@ -1,0 +1,123 @@
+"""Valid-row compaction (lmce_microstep_compact) vs the float64 oracle and vs the plain micro-step.
+
+Masked spans as the pages' packing section makes them: the tail of every sequence is the ignore
+id, in micro-steps with different valid fractions, plus scattered ignored and bad targets."""
+
+import numpy as np
+import pytest
+import torch
+
+from grad_lmce_microstep_gb300 import inputs as I
+from grad_lmce_microstep_gb300 import lmce as M
+
+from gpu_util import GRAD_REL, assert_parity, max_rel_err, run_lib, run_oracle, to_dev
+
+pytestmark = pytest.mark.gpu
+
+PATHS_BF16 = ["simt", "tcgen05", "tcgen05_two_pass"]
+
+
+def _masked(seed, C=256, V=1000, T=128):
+    # four micro-steps of 3 sequences of T tokens (ragged 384-row micro-steps) whose tails of
+    # 0, T/4, T/2 and 3T/4 tokens are ignored, plus 5 % scattered ignored targets
+    w = I.custom([3 * T] * 4, C, V, "bf16", seed=seed, ignore_frac=0.05)
+    for k, tail in enumerate((0, T // 4, T // 2, 3 * T // 4)):
+        y = w.micro[k][1].view(3, T)
+        if tail:
+            y[:, T - tail:] = I.IGNORE_ID
+    return w
+
+
+def _need_path(path, C, V):
+    if path.startswith("tcgen05"):
+        W = torch.zeros(V, C, dtype=torch.float32, device="cuda")
+        try:
+            M.Lmce(C, V, 1, W, "bf16", path=path).close()
+        except M.LmceError as e:
+            if e.status == M.ERR_ARG:
+                pytest.xfail("tensor-core path does not take this shape yet")
+            raise
+
+
+@pytest.mark.parametrize("path", PATHS_BF16)
+@pytest.mark.parametrize("norm", ["global", "micro_mean"])
+def test_compact_matches_oracle(path, norm):
+    w = _masked(31)
+    _need_path(path, w.C, w.V)
+    got = run_lib(w, path=path, norm=norm, compact=True)
+    assert got["status"] == M.OK
+    ref = run_oracle(w, norm=norm)
+    assert_parity(got, ref, "bf16")
+    plain = run_lib(w, path=path, norm=norm)
+    assert max_rel_err(got["dW"], plain["dW"]) <= GRAD_REL["bf16"]
+    for k, (_, y) in enumerate(w.micro):
+        ign = ~((y >= 0) & (y < w.V)).numpy()
+        assert np.all(got["dh"][k][ign] == 0.0) and np.all(got["row_loss"][k][ign] == 0.0)
+        assert max_rel_err(got["dh"][k], plain["dh"][k]) <= GRAD_REL["bf16"]
+
+
+def test_compact_fp32_odd_C_and_library_count():
+    # fp32 on the SIMT path with a row size of 67 floats (4-byte row moves); n_valid = -1 lets
+    # the library count; the result equals the one with the caller's counts bit for bit
+    w = I.custom([200, 131], 67, 301, "fp32", seed=32, ignore_frac=0.3)
+    W, mbs = to_dev(w)
+    gv = sum(w.valid_counts())
+    outs = []
+    for counts in (w.valid_counts(), [-1] * len(mbs)):
+        dW = torch.empty(w.V, w.C, device="cuda")
+        L = M.Lmce(w.C, w.V, 200, dW, "fp32", grad_accum_steps=2, compact=True)
+        dhs = []
+        for (h, y), n in zip(mbs, counts):
+            dh = torch.full_like(h, 9.0)
+            L.microstep_compact(h, W, y, n, gv, dh)
+            dhs.append(dh)
+        res = L.finalize()
+        L.close()
+        outs.append((dW, dhs, res))
+    assert torch.equal(outs[0][0], outs[1][0]) and outs[0][2] == outs[1][2]
+    for a, b in zip(outs[0][1], outs[1][1]):
+        assert torch.equal(a, b)
+    got = {"dW": outs[0][0].double().cpu().numpy(), "dh": [d.double().cpu().numpy() for d in outs[0][1]],
+           "row_loss": [None, None], "loss_sum": outs[0][2][0], "count": outs[0][2][1], "loss_mean": outs[0][2][2]}
+    assert_parity(got, run_oracle(w), "fp32")
+
+
+def test_compact_all_ignored_micro_step_and_bad_targets():
+    # a micro-step with no valid target writes zero dh; bad targets are still reported
+    w = I.custom([256, 256], 256, 1000, "bf16", seed=33)
+    w.micro[0][1][:] = I.IGNORE_ID
+    w.micro[1][1][7] = 1000 + 4
+    got = run_lib(w, compact=True)
+    assert got["status"] == M.ERR_BAD_TARGET
+    assert np.all(got["dh"][0] == 0.0)
+    ref = run_oracle(w)
+    assert got["count"] == ref.count
+    assert max_rel_err(got["dW"], ref.dW) <= GRAD_REL["bf16"]
+    assert max_rel_err(got["dh"][1], ref.micro[1].dh) <= GRAD_REL["bf16"]
+
+
+@pytest.mark.parametrize("delta", [-5, 3])
+def test_compact_wrong_count_is_reported(delta):
+    w = I.custom([300], 256, 1000, "bf16", seed=34, ignore_frac=0.2)
+    W, mbs = to_dev(w)
+    (h, y), = mbs
+    n = w.valid_counts()[0]
+    dW = torch.empty(w.V, w.C, device="cuda")
+    L = M.Lmce(w.C, w.V, 300, dW, "bf16", compact=True)
+    L.microstep_compact(h, W, y, n + delta, n, torch.empty_like(h))
+    assert L.finalize(check=False)[3] == M.ERR_ARG
+    L.close()
+
+
+def test_compact_needs_its_scratch_and_checks_counts():
+    w = I.custom([64], 256, 1000, "bf16", seed=35)
+    W, mbs = to_dev(w)
+    (h, y), = mbs
+    dW = torch.empty(w.V, w.C, device="cuda")
+    L = M.Lmce(w.C, w.V, 64, dW, "bf16")
+    assert L.microstep_compact(h, W, y, 64, 64, torch.empty_like(h), check=False) == M.ERR_ARG
+    L.close()
+    L = M.Lmce(w.C, w.V, 64, dW, "bf16", compact=True)
+    for bad in (-2, 65):
+        assert L.microstep_compact(h, W, y, bad, 64, torch.empty_like(h), check=False) == M.ERR_ARG
+    L.close()
