@@ -14,7 +14,7 @@
 namespace lmce {
 namespace {
 
-constexpr int CP_ROWS = 128;   // rows per block of count and gather: one per thread
+constexpr int CP_ROWS = 32;    // rows per block of count, gather and scatter
 constexpr int SCAN_T = 1024;
 
 __device__ __forceinline__ bool valid_target(int y, int64_t V) { return y >= 0 && (int64_t)y < V; }
@@ -91,84 +91,95 @@ __global__ void __launch_bounds__(SCAN_T) compact_scan_kernel(const int* __restr
   }
 }
 
-template <typename U>
-__device__ __forceinline__ void copy_row(const char* __restrict__ src, char* __restrict__ dst, int64_t row_bytes,
-                                         int lane) {
-  const U* s = reinterpret_cast<const U*>(src);
-  U* d = reinterpret_cast<U*>(dst);
-  const int64_t n = row_bytes / (int64_t)sizeof(U);
-  for (int64_t k = lane; k < n; k += 32) d[k] = s[k];
-}
+// Row moves are flat over words (U = 16, 4 or 2 bytes, the widest that divides the row size and
+// both base addresses): a block moves the CP_ROWS rows of one count block, consecutive threads
+// taking consecutive words of a row so every warp access is coalesced, each thread with CP_U
+// loads in flight before its stores.  Word indices within a block fit 32 bits (CP_ROWS x the
+// words of a row <= 32 x 2^21).
+constexpr int CP_U = 4;
+constexpr int MV_T = 256;
 
 template <typename U>
-__device__ __forceinline__ void zero_row(char* __restrict__ dst, int64_t row_bytes, int lane) {
-  U* d = reinterpret_cast<U*>(dst);
-  const int64_t n = row_bytes / (int64_t)sizeof(U);
-  const U z = U();
-  for (int64_t k = lane; k < n; k += 32) d[k] = z;
-}
-
-// vec: 16 = rows move in 16-byte words, 4 = 4-byte words, 2 = 2-byte words (the host picks the
-// widest that divides the row size and both base addresses).
-__device__ __forceinline__ void copy_row_w(const char* src, char* dst, int64_t row_bytes, int vec, int lane) {
-  if (vec == 16) copy_row<uint4>(src, dst, row_bytes, lane);
-  else if (vec == 4) copy_row<unsigned>(src, dst, row_bytes, lane);
-  else copy_row<unsigned short>(src, dst, row_bytes, lane);
-}
-__device__ __forceinline__ void zero_row_w(char* dst, int64_t row_bytes, int vec, int lane) {
-  if (vec == 16) zero_row<uint4>(dst, row_bytes, lane);
-  else if (vec == 4) zero_row<unsigned>(dst, row_bytes, lane);
-  else zero_row<unsigned short>(dst, row_bytes, lane);
-}
-
-__global__ void __launch_bounds__(CP_ROWS) compact_gather_kernel(const char* __restrict__ hidden,
-                                                                const int32_t* __restrict__ y, int64_t N,
-                                                                int64_t V, int64_t row_bytes, int vec,
-                                                                const int64_t* __restrict__ blk_off,
-                                                                char* __restrict__ h_c, int32_t* __restrict__ y_c,
-                                                                int32_t* __restrict__ pos) {
-  __shared__ int wcnt[CP_ROWS / 32];
+__global__ void __launch_bounds__(MV_T) compact_gather_kernel(const U* __restrict__ hidden,
+                                                             const int32_t* __restrict__ y, int64_t N, int64_t V,
+                                                             unsigned w, const int64_t* __restrict__ blk_off,
+                                                             U* __restrict__ h_c, int32_t* __restrict__ y_c,
+                                                             int32_t* __restrict__ pos) {
   __shared__ int64_t rowpos[CP_ROWS];
-  const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
-  const int64_t n = (int64_t)blockIdx.x * CP_ROWS + t;
-  const int yt = n < N ? y[n] : -1;
-  const bool v = n < N && valid_target(yt, V);
-  const unsigned bal = __ballot_sync(0xffffffffu, v);
-  if (lane == 0) wcnt[wid] = __popc(bal);
-  __syncthreads();
-  int before = 0;
-  for (int w = 0; w < wid; ++w) before += wcnt[w];
-  const int64_t p = v ? blk_off[blockIdx.x] + before + __popc(bal & ((1u << lane) - 1u)) : -1;
-  if (n < N) {
-    pos[n] = (int32_t)p;
-    if (v) y_c[p] = yt;
-  }
-  rowpos[t] = p;
-  __syncthreads();
-  // each warp copies the valid rows among its block's rows r = wid, wid + 4, ...
+  const int t = threadIdx.x;
   const int64_t r0 = (int64_t)blockIdx.x * CP_ROWS;
-  for (int r = wid; r < CP_ROWS; r += CP_ROWS / 32) {
-    const int64_t q = rowpos[r];
-    if (q < 0) continue;
-    copy_row_w(hidden + (r0 + r) * row_bytes, h_c + q * row_bytes, row_bytes, vec, lane);
+  if (t < 32) {   // warp 0: one row per lane
+    const int64_t n = r0 + t;
+    const int yt = n < N ? y[n] : -1;
+    const bool v = n < N && valid_target(yt, V);
+    const unsigned bal = __ballot_sync(0xffffffffu, v);
+    const int64_t p = v ? blk_off[blockIdx.x] + __popc(bal & ((1u << t) - 1u)) : -1;
+    if (n < N) {
+      pos[n] = (int32_t)p;
+      if (v) y_c[p] = yt;
+    }
+    rowpos[t] = p;
+  }
+  __syncthreads();
+  const unsigned total = CP_ROWS * w;
+  for (unsigned c0 = t; c0 < total; c0 += MV_T * CP_U) {
+    U v[CP_U];
+    int64_t d[CP_U];
+#pragma unroll
+    for (int u = 0; u < CP_U; ++u) {
+      const unsigned c = c0 + u * MV_T;
+      d[u] = -1;
+      if (c < total) {
+        const unsigned r = c / w, col = c - r * w;
+        const int64_t q = rowpos[r];
+        if (q >= 0) {
+          v[u] = hidden[(r0 + r) * w + col];
+          d[u] = q * w + col;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < CP_U; ++u)
+      if (d[u] >= 0) h_c[d[u]] = v[u];
   }
 }
 
-// One warp per row; rows at or past n_valid (a count mismatch, already flagged) are zeroed.
-constexpr int SC_T = 256;
-__global__ void __launch_bounds__(SC_T) compact_scatter_kernel(const int32_t* __restrict__ pos, int64_t N,
-                                                              int64_t n_valid, int64_t row_bytes, int vec,
-                                                              const char* __restrict__ dh_c, char* __restrict__ dh,
-                                                              const float* __restrict__ rl_c,
+// dh[n] = dh_c[pos[n]] for the CP_ROWS rows of a block; rows without a position, or at or past
+// n_valid (a count mismatch, already flagged), are zeroed.
+template <typename U>
+__global__ void __launch_bounds__(MV_T) compact_scatter_kernel(const int32_t* __restrict__ pos, int64_t N,
+                                                              int64_t n_valid, unsigned w, const U* __restrict__ dh_c,
+                                                              U* __restrict__ dh, const float* __restrict__ rl_c,
                                                               float* __restrict__ row_loss) {
-  const int lane = threadIdx.x & 31;
-  const int64_t warps = (int64_t)gridDim.x * (SC_T / 32);
-  for (int64_t n = (int64_t)blockIdx.x * (SC_T / 32) + (threadIdx.x >> 5); n < N; n += warps) {
-    const int64_t q = pos[n];
+  __shared__ int64_t rowpos[CP_ROWS];
+  const int t = threadIdx.x;
+  const int64_t r0 = (int64_t)blockIdx.x * CP_ROWS;
+  const int rows = (int)(N - r0 < CP_ROWS ? N - r0 : CP_ROWS);
+  if (t < rows) {
+    const int64_t q = pos[r0 + t];
     const bool ok = q >= 0 && q < n_valid;
-    if (ok) copy_row_w(dh_c + q * row_bytes, dh + n * row_bytes, row_bytes, vec, lane);
-    else zero_row_w(dh + n * row_bytes, row_bytes, vec, lane);
-    if (row_loss && lane == 0) row_loss[n] = ok ? rl_c[q] : 0.f;
+    rowpos[t] = ok ? q : -1;
+    if (row_loss) row_loss[r0 + t] = ok ? rl_c[q] : 0.f;
+  }
+  __syncthreads();
+  const unsigned total = (unsigned)rows * w;
+  for (unsigned c0 = t; c0 < total; c0 += MV_T * CP_U) {
+    U v[CP_U];
+#pragma unroll
+    for (int u = 0; u < CP_U; ++u) {
+      const unsigned c = c0 + u * MV_T;
+      v[u] = U();
+      if (c < total) {
+        const unsigned r = c / w, col = c - r * w;
+        const int64_t q = rowpos[r];
+        if (q >= 0) v[u] = dh_c[q * w + col];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < CP_U; ++u) {
+      const unsigned c = c0 + u * MV_T;
+      if (c < total) dh[r0 * w + c] = v[u];
+    }
   }
 }
 
@@ -177,6 +188,19 @@ int pick_vec(int64_t row_bytes, const void* a, const void* b) {
   if (row_bytes % 16 == 0 && (al & 15) == 0) return 16;
   if (row_bytes % 4 == 0 && (al & 3) == 0) return 4;
   return 2;
+}
+
+template <typename U>
+void launch_gather(const StepArgs& a, const CompactScratch& cs, int64_t nblk, int64_t rb, cudaStream_t st) {
+  compact_gather_kernel<U><<<(unsigned)nblk, MV_T, 0, st>>>((const U*)a.hidden, a.targets, a.N, a.V,
+                                                            (unsigned)(rb / (int64_t)sizeof(U)), cs.blk_off,
+                                                            (U*)cs.h_c, cs.y_c, cs.pos);
+}
+
+template <typename U>
+void launch_scatter(const StepArgs& a, const CompactScratch& cs, int64_t n_valid, int64_t rb, cudaStream_t st) {
+  compact_scatter_kernel<U><<<(unsigned)compact_blocks(a.N), MV_T, 0, st>>>(
+      cs.pos, a.N, n_valid, (unsigned)(rb / (int64_t)sizeof(U)), (const U*)cs.dh_c, (U*)a.dh, cs.rl_c, a.row_loss);
 }
 
 }  // namespace
@@ -199,10 +223,11 @@ cudaError_t compact_rows(const StepArgs& a, const CompactScratch& cs, DevAcc* ac
   if (e != cudaSuccess || nblk == 0) return e;
   const int64_t esz = a.bf16 ? 2 : 4;
   const int64_t rb = a.C * esz;
+  const int vec = pick_vec(rb, a.hidden, cs.h_c);
   L.begin(K_FINISH);
-  compact_gather_kernel<<<(unsigned)nblk, CP_ROWS, 0, L.st>>>(
-      (const char*)a.hidden, a.targets, a.N, a.V, rb, pick_vec(rb, a.hidden, cs.h_c), cs.blk_off, (char*)cs.h_c,
-      cs.y_c, cs.pos);
+  if (vec == 16) launch_gather<uint4>(a, cs, nblk, rb, L.st);
+  else if (vec == 4) launch_gather<unsigned>(a, cs, nblk, rb, L.st);
+  else launch_gather<unsigned short>(a, cs, nblk, rb, L.st);
   L.end();
   return cudaGetLastError();
 }
@@ -211,11 +236,11 @@ cudaError_t compact_scatter(const StepArgs& a, const CompactScratch& cs, int64_t
   if (a.N == 0) return cudaSuccess;
   const int64_t esz = a.bf16 ? 2 : 4;
   const int64_t rb = a.C * esz;
-  int64_t blocks = (a.N + SC_T / 32 - 1) / (SC_T / 32);
-  if (blocks > 152 * 8) blocks = 152 * 8;
+  const int vec = pick_vec(rb, a.dh, cs.dh_c);
   L.begin(K_FINISH);
-  compact_scatter_kernel<<<(unsigned)blocks, SC_T, 0, L.st>>>(cs.pos, a.N, n_valid, rb, pick_vec(rb, a.dh, cs.dh_c),
-                                                             (const char*)cs.dh_c, (char*)a.dh, cs.rl_c, a.row_loss);
+  if (vec == 16) launch_scatter<uint4>(a, cs, n_valid, rb, L.st);
+  else if (vec == 4) launch_scatter<unsigned>(a, cs, n_valid, rb, L.st);
+  else launch_scatter<unsigned short>(a, cs, n_valid, rb, L.st);
   L.end();
   return cudaGetLastError();
 }
