@@ -25,6 +25,9 @@ What it computes, in the order the pages give it:
 * "How I trained my own GPT-2 124M", section 6, and "Reproduce GPT-2 124M", training
   configuration: after the accumulation the gradient is clipped to a global norm of
   1.0 and AdamW updates the weights (``dw_sumsq``, ``clip_coef``, ``adamw_step``).
+* "How I trained my own GPT-2 124M", section 2.8, and "Reproduce GPT-2 124M", model
+  definition: the final LayerNorm (or RMSNorm) that produces h, forward and backward
+  (``final_norm``, ``final_norm_backward``, ``step_ln``).
 * zerotofrontier "GPT", section "Document boundaries, packing and masking": a
   pad target is ignored by the loss.  Its id is -100 here (the default of the
   PyTorch cross-entropy function the multi-GPU page cites).
@@ -203,6 +206,86 @@ def step(micro_batches, W, norm: str = "global", G: int | None = None, global_va
         if want_dW:
             dW += r.dW
     return StepResult(loss_sum, sum(counts), sum(r.bad for r in res), objective, dW, res)
+
+
+# ---------------------------------------------------------------------------
+# The final normalisation in front of the head (ln_f)
+# ---------------------------------------------------------------------------
+
+def final_norm(x, gamma, beta=None, kind: str = "layernorm", eps: float = 1e-5):
+    """h = ln_f(x) in float64, with the per-row mean (0 for RMSNorm) and 1/std.
+
+    "How I trained my own GPT-2 124M", section 2.8: after the last block GPT-2 applies one
+    LayerNorm, ln_f, whose output feeds the tied head; LayerNorm centres each row, divides by
+    the square root of its (biased) variance plus eps, then scales by gamma and shifts by
+    beta.  "Reproduce GPT-2 124M" (model definition) uses an RMSNorm there instead: no
+    centring, the root mean square in place of the standard deviation, no shift.
+    """
+    x, g = f64(x), f64(gamma)
+    if kind == "layernorm":
+        mu = x.mean(axis=1)
+        var = ((x - mu[:, None]) ** 2).mean(axis=1)
+        rstd = 1.0 / np.sqrt(var + eps)
+        h = (x - mu[:, None]) * rstd[:, None] * g
+        if beta is not None:
+            h = h + f64(beta)
+    elif kind == "rmsnorm":
+        mu = np.zeros(x.shape[0])
+        rstd = 1.0 / np.sqrt((x * x).mean(axis=1) + eps)
+        h = x * rstd[:, None] * g
+    else:
+        raise ValueError(kind)
+    return h, mu, rstd
+
+
+def final_norm_backward(dh, x, gamma, kind: str = "layernorm", eps: float = 1e-5):
+    """(dx, dgamma, dbeta) of h = ln_f(x) for an upstream gradient dh, in float64.
+
+    With xhat the normalised row and g = dh * gamma: dgamma = sum over rows of dh * xhat,
+    dbeta = sum over rows of dh, and per row dx = rstd * (g - mean(g) - xhat * mean(g * xhat))
+    for LayerNorm (the mean(g) term drops for RMSNorm, which does not centre).
+    """
+    dh, x, gm = f64(dh), f64(x), f64(gamma)
+    _, mu, rstd = final_norm(x, np.ones_like(gm), None, kind, eps)
+    xhat = (x - mu[:, None]) * rstd[:, None]
+    g = dh * gm
+    proj = (g * xhat).mean(axis=1, keepdims=True)
+    if kind == "layernorm":
+        dx = rstd[:, None] * (g - g.mean(axis=1, keepdims=True) - xhat * proj)
+    else:
+        dx = rstd[:, None] * (g - xhat * proj)
+    return dx, (dh * xhat).sum(axis=0), dh.sum(axis=0)
+
+
+@dataclass
+class LnStepResult:
+    head: StepResult           # the head's step on the normalised rows
+    dx: list                   # per micro-step, float64 [N_k, C]
+    dgamma: np.ndarray         # summed over micro-steps
+    dbeta: np.ndarray
+
+
+def step_ln(micro_batches, gamma, beta, W, kind: str = "layernorm", eps: float = 1e-5,
+            h_round=None, **step_kw) -> LnStepResult:
+    """A whole step with ln_f in front: micro_batches holds (x_k, y_k); h_k = ln_f(x_k),
+    optionally rounded by ``h_round`` (the head's input dtype), goes through ``step``, and
+    each micro-step's dh goes back through the normalisation."""
+    hs, xs = [], []
+    for x, y in micro_batches:
+        h, _, _ = final_norm(x, gamma, beta, kind, eps)
+        if h_round is not None:
+            h = h_round(h)
+        hs.append((h, y))
+        xs.append(f64(x))
+    head = step(hs, W, **step_kw)
+    C = f64(gamma).shape[0]
+    dgamma, dbeta, dxs = np.zeros(C), np.zeros(C), []
+    for x, m in zip(xs, head.micro):
+        dx, dg, db = final_norm_backward(m.dh, x, gamma, kind, eps)
+        dxs.append(dx)
+        dgamma += dg
+        dbeta += db
+    return LnStepResult(head, dxs, dgamma, dbeta)
 
 
 # ---------------------------------------------------------------------------

@@ -394,3 +394,86 @@ def test_adamw_matches_torch_optim(clip):
     np.testing.assert_allclose(p, w.detach().numpy(), rtol=1e-13, atol=1e-16)
     np.testing.assert_allclose(m, st["exp_avg"].numpy(), rtol=1e-13, atol=1e-18)
     np.testing.assert_allclose(v, st["exp_avg_sq"].numpy(), rtol=1e-13, atol=1e-20)
+
+
+@pytest.mark.parametrize("kind", ["layernorm", "rmsnorm"])
+def test_final_norm_matches_torch_autograd(kind):
+    # PyTorch's float64 layer_norm / rms_norm and their autograd: h, dx, dgamma and dbeta
+    rng = np.random.default_rng(21)
+    N, C = 13, 24
+    x = rng.standard_normal((N, C)) * 3 + 1.5
+    gamma = 1 + 0.1 * rng.standard_normal(C)
+    beta = 0.1 * rng.standard_normal(C) if kind == "layernorm" else None
+    dh = rng.standard_normal((N, C))
+    eps = 1e-5
+    tx = torch.tensor(x, requires_grad=True)
+    tg = torch.tensor(gamma, requires_grad=True)
+    if kind == "layernorm":
+        tb = torch.tensor(beta, requires_grad=True)
+        th = torch.nn.functional.layer_norm(tx, (C,), tg, tb, eps)
+    else:
+        th = torch.nn.functional.rms_norm(tx, (C,), tg, eps)
+    th.backward(torch.tensor(dh))
+    h, _, _ = O.final_norm(x, gamma, beta, kind, eps)
+    np.testing.assert_allclose(h, th.detach().numpy(), rtol=1e-12, atol=1e-12)
+    dx, dg, db = O.final_norm_backward(dh, x, gamma, kind, eps)
+    np.testing.assert_allclose(dx, tx.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dg, tg.grad.numpy(), rtol=1e-10, atol=1e-12)
+    if kind == "layernorm":
+        np.testing.assert_allclose(db, tb.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_final_norm_invariants():
+    rng = np.random.default_rng(22)
+    x = rng.standard_normal((9, 16)) * 2 - 0.7
+    one, zero = np.ones(16), np.zeros(16)
+    # LayerNorm with unit scale and no shift: every row has mean 0 and mean square var / (var + eps)
+    eps = 1e-3
+    h, mu, rstd = O.final_norm(x, one, zero, "layernorm", eps)
+    var = x.var(axis=1)
+    np.testing.assert_allclose(h.mean(axis=1), 0.0, atol=1e-14)
+    np.testing.assert_allclose((h * h).mean(axis=1), var / (var + eps), rtol=1e-13)
+    # with eps = 0: LayerNorm ignores a shift and a positive scale of the row, RMSNorm a scale
+    a, b = 3.5, -2.25
+    np.testing.assert_allclose(O.final_norm(a * x + b, one, None, "layernorm", 0.0)[0],
+                               O.final_norm(x, one, None, "layernorm", 0.0)[0], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(O.final_norm(a * x, one, None, "rmsnorm", 0.0)[0],
+                               O.final_norm(x, one, None, "rmsnorm", 0.0)[0], rtol=1e-12, atol=1e-13)
+    # LayerNorm's input gradient has zero row sums (the output does not move with a row shift)
+    dh = rng.standard_normal(x.shape)
+    dx, _, _ = O.final_norm_backward(dh, x, 1 + 0.2 * rng.standard_normal(16), "layernorm", 1e-5)
+    np.testing.assert_allclose(dx.sum(axis=1), 0.0, atol=1e-12)
+
+
+@pytest.mark.parametrize("kind", ["layernorm", "rmsnorm"])
+def test_step_ln_finite_differences(kind):
+    # the whole objective as a function of x, gamma and beta, through ln_f and the head
+    C, V = 8, 11
+    W, mbs = _problem([5, 7], C, V, ignore=[(1, 2)], seed=23)
+    rng = np.random.default_rng(23)
+    xs = [(h * 1.7 + 0.4, y) for h, y in mbs]
+    gamma = 1 + 0.2 * rng.standard_normal(C)
+    beta = 0.2 * rng.standard_normal(C) if kind == "layernorm" else None
+    r = O.step_ln(xs, gamma, beta, W, kind, 1e-5)
+
+    def J(xs_, g_, b_):
+        return O.step_ln(xs_, g_, b_, W, kind, 1e-5).head.objective
+
+    e = 1e-6
+    num_g = np.array([(J(xs, gamma + e * np.eye(C)[c], beta) - J(xs, gamma - e * np.eye(C)[c], beta)) / (2 * e)
+                      for c in range(C)])
+    assert np.abs(num_g - r.dgamma).max() <= 1e-6 * max(1.0, np.abs(r.dgamma).max())
+    if beta is not None:
+        num_b = np.array([(J(xs, gamma, beta + e * np.eye(C)[c]) - J(xs, gamma, beta - e * np.eye(C)[c])) / (2 * e)
+                          for c in range(C)])
+        assert np.abs(num_b - r.dbeta).max() <= 1e-6 * max(1.0, np.abs(r.dbeta).max())
+    for k, (x, y) in enumerate(xs):
+        num = np.zeros_like(x)
+        for n in range(x.shape[0]):
+            for c in range(C):
+                xp = x.copy(); xp[n, c] += e
+                xm = x.copy(); xm[n, c] -= e
+                mp = list(xs); mp[k] = (xp, y)
+                mm = list(xs); mm[k] = (xm, y)
+                num[n, c] = (J(mp, gamma, beta) - J(mm, gamma, beta)) / (2 * e)
+        assert np.abs(num - r.dx[k]).max() <= 1e-6 * max(1.0, np.abs(r.dx[k]).max())
