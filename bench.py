@@ -40,6 +40,8 @@ def parse():
     p.add_argument("--workload", default="gpt2_124m_head")
     p.add_argument("--path", default="auto", choices=["auto", "simt", "tcgen05", "tcgen05_two_pass"])
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--final-norm", default=None, choices=["layernorm", "rmsnorm"],
+                   help="ln_f in front of the head (lmce_microstep_ln); inputs become the rows x before it")
     p.add_argument("--compact", action="store_true",
                    help="micro-steps over the valid rows only (lmce_microstep_compact)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -187,20 +189,33 @@ def run_lmce(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     w = I.make(args.workload, seed=rank)
+    if args.final_norm:   # the residual stream in front of ln_f: shifted, scaled rows
+        w.micro = [((h.float() * 1.7 + 0.4).to(h.dtype), y) for h, y in w.micro]
     W = w.W.to(dev)
     mbs = [(h.to(dev), y.to(dev)) for h, y in w.micro]
     dhs = [torch.empty_like(h) for h, _ in mbs]
     dW = torch.empty(w.V, w.C, dtype=torch.float32, device=dev)
     max_N = max(int(y.numel()) for _, y in mbs)
+    if args.compact and args.final_norm:
+        raise SystemExit("--compact and --final-norm are separate entry points")
     L = M.Lmce(w.C, w.V, max_N, dW, w.dtype, norm="global", grad_accum_steps=w.G, path=args.path,
-               compact=args.compact)
+               compact=args.compact, final_norm=bool(args.final_norm))
+    if args.final_norm:
+        gen = torch.Generator().manual_seed(rank)
+        ln_gamma = (1 + 0.1 * torch.randn(w.C, generator=gen)).to(dev)
+        ln_beta = (0.1 * torch.randn(w.C, generator=gen)).to(dev) if args.final_norm == "layernorm" else None
+        ln_dgamma = torch.empty(w.C, device=dev)
+        ln_dbeta = torch.empty(w.C, device=dev) if ln_beta is not None else None
     nvs = w.valid_counts()
     gv = dp.global_valid_count(sum(w.valid_counts()), device=dev if world > 1 else None)
     stream = torch.cuda.current_stream(dev)
     tokens_rank = w.tokens
 
     def micro(h, y, n_valid, dh):
-        if args.compact:
+        if args.final_norm:   # h is x and dh is dx here
+            L.microstep_ln(h, ln_gamma, ln_beta, W, y, gv, dh, ln_dgamma, ln_dbeta, args.final_norm, 1e-5,
+                           stream=stream)
+        elif args.compact:
             L.microstep_compact(h, W, y, n_valid, gv, dh, stream=stream)
         else:
             L.microstep(h, W, y, gv, dh, stream=stream)
@@ -344,6 +359,21 @@ def run_lmce(args, rank, world, local_rank):
                 "peak_gbs": pk["hbm_gbs"], "frac": sq_gbs / pk["hbm_gbs"] if sq_gbs else None,
                 "bound": "hbm", "value": sq_value}
     aw_gbs = aw_bytes / (aw_ms * 1e-3) / 1e9 if aw_ms > 0 else None
+    final_norm = None
+    if args.final_norm and "ln" in prof and prof["ln"][1] > 0:
+        # per micro-step: forward reads x and writes h, backward reads dh and x and writes dx (5
+        # row tensors), plus the dgamma / dbeta partials (fp32, one row per backward block) written
+        # and read once
+        esz = 2 if w.dtype == "bf16" else 4
+        nmicro = args.steps * w.G
+        ln_ms = prof["ln"][0] / nmicro
+        rows = tokens_rank // w.G
+        rpb = -(-rows // 304)   # the backward's row range per block: at most 304 blocks
+        ln_bytes = 5 * rows * w.C * esz + 2 * 2 * 4 * w.C * (-(-rows // rpb))
+        ln_gbs = ln_bytes / (ln_ms * 1e-3) / 1e9
+        final_norm = {"kind": args.final_norm, "ms_per_micro_step": ln_ms, "launches_per_micro_step":
+                      prof["ln"][1] / nmicro, "bytes_per_micro_step": int(ln_bytes), "achieved_gbs": ln_gbs,
+                      "peak_gbs": pk["hbm_gbs"], "frac": ln_gbs / pk["hbm_gbs"], "bound": "hbm"}
     adamw = {"ms": aw_ms, "launches": aw_n, "bytes": int(aw_bytes), "achieved_gbs": aw_gbs,
              "peak_gbs": pk["hbm_gbs"], "frac": aw_gbs / pk["hbm_gbs"] if aw_gbs else None, "bound": "hbm",
              "hyper": {"lr": 6e-4, "betas": [0.9, 0.95], "eps": 1e-8, "weight_decay": 0.1, "clip": clip}}
@@ -358,7 +388,7 @@ def run_lmce(args, rank, world, local_rank):
     valid_rank = sum(nvs)
     # rows one heavy launch processes: every row, or the valid rows alone when compacted
     rows_per_launch = valid_rank / w.G if args.compact else tok_per_launch
-    alg_flop_launch = {"lse": 2.0, "dW": 2.0, "dh": 2.0, "lse_dh": 4.0, "finish": 0.0}[dom] * w.C * w.V * rows_per_launch
+    alg_flop_launch = {"lse": 2.0, "dW": 2.0, "dh": 2.0, "lse_dh": 4.0}.get(dom, 0.0) * w.C * w.V * rows_per_launch
     achieved = alg_flop_launch / (dom_ms / dom_n / 1e3) / 1e12
     if L.path.startswith("tcgen05"):
         peak = pk["bf16_tflops_sustained"] if "bf16_tflops_sustained" in pk else pk["bf16_tflops"]
@@ -384,6 +414,7 @@ def run_lmce(args, rank, world, local_rank):
         "config": {"workload": args.workload, "tokens_per_step": tokens_rank * world, "micro_steps": w.G,
                    "micro_batch_tokens": int(tok_per_launch), "valid_tokens": [int(n) for n in nvs],
                    "C": w.C, "V": w.V, "path": L.path, "compact": bool(args.compact),
+                   "final_norm": args.final_norm,
                    "parallelism": f"dp{world}",
                    "l2": "no flush: inputs larger than L2 (per step %d distinct h buffers of %.0f MB, "
                          "W %.0f MB, fp32 dW %.0f MB)" % (w.G, mbs[0][0].numel() * 2 / 1e6,
@@ -403,6 +434,7 @@ def run_lmce(args, rank, world, local_rank):
         "gpu_launches": int(launches),
         "dw_sumsq": dw_sumsq,
         "adamw": adamw,
+        "final_norm": final_norm,
         "clocks": clocks,
         "check": {"loss_mean": res[2], "valid": res[1]},
     }

@@ -238,6 +238,13 @@ struct lmce_handle {
   bool first;          // next micro-step writes dW instead of adding (unless LMCE_ACCUMULATE_FROM_START)
   double* sumsq_part;  // lmce_dw_sumsq: per-block float64 partials, then the result
   CompactScratch cs;   // lmce_microstep_compact (LMCE_COMPACT_VALID_ROWS), else all null
+  struct {             // lmce_microstep_ln (LMCE_FINAL_NORM), else all null
+    void* h;           // [max_N, C] dtype: ln_f(x), the head's input
+    void* dh;          // [max_N, C] dtype: the head's dh
+    float* mean;       // [max_N]
+    float* rstd;       // [max_N]
+    float* part;       // [2][ln_part_rows()][C]
+  } ln;
   int attempted;       // micro-steps accepted since create/finalize
   int64_t launches;
   Prof prof;
@@ -278,6 +285,12 @@ static void free_scratch(lmce_handle* h) {
   cudaFree(h->cs.total);
   cudaFreeHost(h->cs.host_total);
   h->cs = CompactScratch{};
+  cudaFree(h->ln.h);
+  cudaFree(h->ln.dh);
+  cudaFree(h->ln.mean);
+  cudaFree(h->ln.rstd);
+  cudaFree(h->ln.part);
+  h->ln = {};
   if (h->host_acc) cudaFreeHost(h->host_acc);
   memset(&h->sc, 0, sizeof(h->sc));
   h->host_acc = nullptr;
@@ -291,7 +304,7 @@ extern "C" int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out)
   if (cfg->dtype != LMCE_BF16 && cfg->dtype != LMCE_FP32) return LMCE_ERR_ARG;
   if (cfg->norm != LMCE_NORM_GLOBAL && cfg->norm != LMCE_NORM_MICRO_MEAN) return LMCE_ERR_ARG;
   if (cfg->path < LMCE_PATH_AUTO || cfg->path > LMCE_PATH_TCGEN05_TWO_PASS) return LMCE_ERR_ARG;
-  if (cfg->flags & ~(LMCE_ACCUMULATE_FROM_START | LMCE_COMPACT_VALID_ROWS)) return LMCE_ERR_ARG;
+  if (cfg->flags & ~(LMCE_ACCUMULATE_FROM_START | LMCE_COMPACT_VALID_ROWS | LMCE_FINAL_NORM)) return LMCE_ERR_ARG;
   const bool tc_ok = tc_supported(cfg->C, cfg->V, cfg->dtype == LMCE_BF16);
   const bool simt_ok = cfg->C <= 2048;
   int path;
@@ -354,6 +367,13 @@ extern "C" int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out)
          cudaMallocHost(&q.host_total, sizeof(int64_t)) == cudaSuccess &&
          // defined contents for rows a wrong n_valid would read: zero rows, targets -1
          cudaMemset(q.h_c, 0, rows) == cudaSuccess && cudaMemset(q.y_c, 0xff, sizeof(int32_t) * maxN) == cudaSuccess;
+  }
+  if (ok && (cfg->flags & LMCE_FINAL_NORM)) {
+    const size_t rows = (size_t)maxN * (size_t)cfg->C * (cfg->dtype == LMCE_BF16 ? 2 : 4);
+    ok = cudaMalloc(&h->ln.h, rows) == cudaSuccess && cudaMalloc(&h->ln.dh, rows) == cudaSuccess &&
+         cudaMalloc(&h->ln.mean, sizeof(float) * maxN) == cudaSuccess &&
+         cudaMalloc(&h->ln.rstd, sizeof(float) * maxN) == cudaSuccess &&
+         cudaMalloc(&h->ln.part, sizeof(float) * 2 * (size_t)ln_part_rows() * (size_t)cfg->C) == cudaSuccess;
   }
   ok = ok && cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
@@ -473,6 +493,71 @@ extern "C" int lmce_microstep_compact(lmce_handle* h, const void* hidden, const 
   L2.st = st;
   L2.prof = &h->prof;
   e = compact_scatter(a, h->cs, n_valid, L2);
+  h->launches += L2.n;
+  return e == cudaSuccess ? LMCE_OK : LMCE_ERR_CUDA;
+}
+
+extern "C" int lmce_microstep_ln(lmce_handle* h, const void* x, const float* gamma, const float* beta,
+                                 int32_t ln_kind, float eps, const void* W, const int32_t* targets, int64_t N,
+                                 int64_t global_valid, void* dx, float* dgamma, float* dbeta, float* row_loss,
+                                 void* stream) {
+  if (!h || !h->ln.h) return LMCE_ERR_ARG;
+  const lmce_config& c = h->cfg;
+  if (N < 0 || N > c.max_N) return LMCE_ERR_ARG;
+  if (ln_kind != LMCE_LN_LAYERNORM && ln_kind != LMCE_LN_RMSNORM) return LMCE_ERR_ARG;
+  if (!(eps >= 0.f) || !gamma || !dgamma || (ln_kind == LMCE_LN_RMSNORM && (beta || dbeta))) return LMCE_ERR_ARG;
+  if (!beta && dbeta) return LMCE_ERR_ARG;
+  if (N > 0 && (!x || !W || !targets || !dx)) return LMCE_ERR_ARG;
+  const size_t esz = c.dtype == LMCE_BF16 ? 2 : 4;
+  if (N > 0 && (((uintptr_t)x | (uintptr_t)dx) & (esz - 1))) return LMCE_ERR_ARG;
+  if (h->path != LMCE_PATH_SIMT && N > 0 && (((uintptr_t)W | (uintptr_t)h->dW) & 15)) return LMCE_ERR_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (c.norm == LMCE_NORM_GLOBAL && global_valid <= 0) {   // refused: dx zeroed, parameters untouched
+    if (N > 0 && cudaMemsetAsync(dx, 0, (size_t)N * c.C * esz, st) != cudaSuccess) return LMCE_ERR_CUDA;
+    if (N > 0 && row_loss && cudaMemsetAsync(row_loss, 0, (size_t)N * sizeof(float), st) != cudaSuccess)
+      return LMCE_ERR_CUDA;
+    h->attempted += 1;
+    return LMCE_ERR_NO_VALID;
+  }
+  // the parameter gradients follow dW: written by the first micro-step of a step, then added
+  const bool write = h->first && !(c.flags & LMCE_ACCUMULATE_FROM_START);
+  LnArgs a{};
+  a.x = x;
+  a.gamma = gamma;
+  a.beta = beta;
+  a.h = h->ln.h;
+  a.dh = h->ln.dh;
+  a.dx = dx;
+  a.mean = h->ln.mean;
+  a.rstd = h->ln.rstd;
+  a.part_g = h->ln.part;
+  a.part_b = h->ln.part + (size_t)ln_part_rows() * (size_t)c.C;
+  a.dgamma = dgamma;
+  a.dbeta = dbeta;
+  a.N = N;
+  a.C = c.C;
+  a.rms = ln_kind == LMCE_LN_RMSNORM;
+  a.eps = eps;
+  a.bf16 = c.dtype == LMCE_BF16;
+  a.accumulate = write ? 0 : 1;
+  Launch L;
+  L.st = st;
+  L.prof = &h->prof;
+  cudaError_t e = ln_forward(a, L);
+  h->launches += L.n;
+  if (e != cudaSuccess) return LMCE_ERR_CUDA;
+  const int s = run_microstep(h, h->ln.h, W, targets, N, global_valid, h->ln.dh, row_loss, st);
+  if (s != LMCE_OK) return s;
+  if (N == 0) {   // an empty micro-step: the first one of a step leaves the parameter gradients 0
+    if (write && (cudaMemsetAsync(dgamma, 0, sizeof(float) * c.C, st) != cudaSuccess ||
+                  (dbeta && cudaMemsetAsync(dbeta, 0, sizeof(float) * c.C, st) != cudaSuccess)))
+      return LMCE_ERR_CUDA;
+    return LMCE_OK;
+  }
+  Launch L2;
+  L2.st = st;
+  L2.prof = &h->prof;
+  e = ln_backward(a, L2);
   h->launches += L2.n;
   return e == cudaSuccess ? LMCE_OK : LMCE_ERR_CUDA;
 }

@@ -211,12 +211,12 @@ cudaError_t compact_rows(const StepArgs& a, const CompactScratch& cs, DevAcc* ac
                          Launch& L) {
   const int64_t nblk = compact_blocks(a.N);
   if (nblk > 0) {
-    L.begin(K_FINISH);
+    L.begin(K_COMPACT);
     compact_count_kernel<<<(unsigned)nblk, CP_ROWS, 0, L.st>>>(a.targets, a.N, a.V, a.ignore_id, cs.blk_cnt,
                                                                cs.blk_err);
     L.end();
   }
-  L.begin(K_FINISH);
+  L.begin(K_COMPACT);
   compact_scan_kernel<<<1, SCAN_T, 0, L.st>>>(cs.blk_cnt, cs.blk_err, nblk, cs.blk_off, cs.total, n_valid, acc);
   L.end();
   cudaError_t e = cudaGetLastError();
@@ -224,7 +224,7 @@ cudaError_t compact_rows(const StepArgs& a, const CompactScratch& cs, DevAcc* ac
   const int64_t esz = a.bf16 ? 2 : 4;
   const int64_t rb = a.C * esz;
   const int vec = pick_vec(rb, a.hidden, cs.h_c);
-  L.begin(K_FINISH);
+  L.begin(K_COMPACT);
   if (vec == 16) launch_gather<uint4>(a, cs, nblk, rb, L.st);
   else if (vec == 4) launch_gather<unsigned>(a, cs, nblk, rb, L.st);
   else launch_gather<unsigned short>(a, cs, nblk, rb, L.st);
@@ -237,7 +237,7 @@ cudaError_t compact_scatter(const StepArgs& a, const CompactScratch& cs, int64_t
   const int64_t esz = a.bf16 ? 2 : 4;
   const int64_t rb = a.C * esz;
   const int vec = pick_vec(rb, a.dh, cs.dh_c);
-  L.begin(K_FINISH);
+  L.begin(K_COMPACT);
   if (vec == 16) launch_scatter<uint4>(a, cs, n_valid, rb, L.st);
   else if (vec == 4) launch_scatter<unsigned>(a, cs, n_valid, rb, L.st);
   else launch_scatter<unsigned short>(a, cs, n_valid, rb, L.st);

@@ -10,7 +10,7 @@
 namespace lmce {
 
 // Kernel kinds for the timing records (same values as LMCE_KIND_* in lmce.h).
-enum Kind { K_LSE = 0, K_FINISH = 1, K_DW = 2, K_DH = 3, K_LSE_DH = 4, K_COUNT = 5 };
+enum Kind { K_LSE = 0, K_FINISH = 1, K_DW = 2, K_DH = 3, K_LSE_DH = 4, K_LN = 5, K_COMPACT = 6, K_COUNT = 7 };
 
 // Optional CUDA-event records around every kernel launch.
 struct Prof {
@@ -132,6 +132,33 @@ int64_t compact_blocks(int64_t N);
 cudaError_t compact_rows(const StepArgs& a, const CompactScratch& cs, DevAcc* acc, int64_t n_valid, Launch& L);
 // dh / row_loss of a.N rows from the first n_valid compact rows, zero for the ignored rows
 cudaError_t compact_scatter(const StepArgs& a, const CompactScratch& cs, int64_t n_valid, Launch& L);
+
+// ln_f in front of the head (lmce_microstep_ln): forward x -> h with per-row mean / rstd, and
+// backward dh -> dx with the dgamma / dbeta partials of ln_blocks(N) row blocks reduced in order.
+struct LnArgs {
+  const void* x;        // [N, C] dtype
+  const float* gamma;   // [C]
+  const float* beta;    // [C] or nullptr
+  void* h;              // [N, C] dtype (forward output)
+  const void* dh;       // [N, C] dtype (backward input)
+  void* dx;             // [N, C] dtype
+  float* mean;          // [N]
+  float* rstd;          // [N]
+  float* part_g;        // [ln_part_rows(), C], the first ln_blocks(N) rows used
+  float* part_b;        // [ln_part_rows(), C]
+  float* dgamma;        // [C]
+  float* dbeta;         // [C] or nullptr
+  int64_t N, C;
+  int32_t rms;          // 1: RMSNorm, 0: LayerNorm
+  float eps;
+  int32_t bf16;
+  int32_t accumulate;   // 1: dgamma / dbeta +=, 0: =
+};
+int64_t ln_blocks(int64_t N);           // backward blocks (parameter-gradient partials) for N rows
+int64_t ln_rows_per_block(int64_t N);
+int64_t ln_part_rows();                 // the most ln_blocks(N) can be, for any N
+cudaError_t ln_forward(const LnArgs& a, Launch& L);
+cudaError_t ln_backward(const LnArgs& a, Launch& L);
 
 // Fixed-order reduction of the per-block partials of one micro-step into the step
 // accumulators; also computes this micro-step's gradient scale.  One launch.

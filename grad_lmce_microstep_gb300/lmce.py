@@ -33,11 +33,12 @@ TORCH_DTYPES = {"bf16": torch.bfloat16, "fp32": torch.float32}
 
 EXPORTS = ("lmce_create", "lmce_microstep", "lmce_finalize", "lmce_destroy", "lmce_status_string",
            "lmce_launch_count", "lmce_selected_path", "lmce_profile", "lmce_profile_read",
-           "lmce_microstep_noalloc", "lmce_dw_sumsq", "lmce_adamw", "lmce_microstep_compact")
+           "lmce_microstep_noalloc", "lmce_dw_sumsq", "lmce_adamw", "lmce_microstep_compact",
+           "lmce_microstep_ln")
 
 NOALLOC_MAX_N = 65536
 
-KINDS = {"lse": 0, "finish": 1, "dW": 2, "dh": 3, "lse_dh": 4}
+KINDS = {"lse": 0, "finish": 1, "dW": 2, "dh": 3, "lse_dh": 4, "ln": 5, "compact": 6}
 
 
 class Config(ctypes.Structure):
@@ -48,6 +49,8 @@ class Config(ctypes.Structure):
 
 ACCUMULATE_FROM_START = 1   # Config.flags: the first micro-step adds to dW instead of writing it
 COMPACT_VALID_ROWS = 2      # Config.flags: scratch for microstep_compact
+FINAL_NORM = 4              # Config.flags: scratch for microstep_ln
+LN_KINDS = {"layernorm": 0, "rmsnorm": 1}
 
 
 class LmceError(RuntimeError):
@@ -74,6 +77,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.lmce_microstep.restype = i32
     L.lmce_microstep_compact.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, vp]
     L.lmce_microstep_compact.restype = i32
+    L.lmce_microstep_ln.argtypes = [vp, vp, vp, vp, i32, ctypes.c_float, vp, vp, i64, i64, vp, vp, vp, vp, vp]
+    L.lmce_microstep_ln.restype = i32
     L.lmce_finalize.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64),
                                 ctypes.POINTER(ctypes.c_double), vp]
     L.lmce_finalize.restype = i32
@@ -144,7 +149,8 @@ class Lmce:
 
     def __init__(self, C: int, V: int, max_N: int, dW: torch.Tensor, dtype: str = "bf16",
                  ignore_id: int = -100, norm: str = "global", grad_accum_steps: int = 1,
-                 path: str = "auto", accumulate_from_start: bool = False, compact: bool = False):
+                 path: str = "auto", accumulate_from_start: bool = False, compact: bool = False,
+                 final_norm: bool = False):
         _check_dev(dW, "dW", torch.float32, (V, C))
         self.lib = load()
         self.C, self.V, self.max_N = int(C), int(V), int(max_N)
@@ -152,7 +158,8 @@ class Lmce:
         self.dW = dW
         cfg = Config(self.C, self.V, self.max_N, DTYPES[dtype], int(ignore_id), NORMS[norm],
                      int(grad_accum_steps), PATHS[path],
-                     (ACCUMULATE_FROM_START if accumulate_from_start else 0) | (COMPACT_VALID_ROWS if compact else 0))
+                     (ACCUMULATE_FROM_START if accumulate_from_start else 0) | (COMPACT_VALID_ROWS if compact else 0)
+                     | (FINAL_NORM if final_norm else 0))
         h = ctypes.c_void_p()
         st = self.lib.lmce_create(ctypes.byref(cfg), _ptr(dW), ctypes.byref(h))
         if st != OK:
@@ -205,6 +212,32 @@ class Lmce:
                                              int(global_valid), _ptr(dh), _ptr(row_loss), _stream(stream))
         if check and st != OK:
             raise LmceError(st, "lmce_microstep_compact")
+        return st
+
+    def microstep_ln(self, x, gamma, beta, W, targets, global_valid: int = 0, dx=None, dgamma=None, dbeta=None,
+                     kind: str = "layernorm", eps: float = 1e-5, row_loss=None, stream=None, check: bool = True) -> int:
+        """A micro-step with ln_f in front (handle made with final_norm=True): h = ln_f(x) feeds the
+        head, dx is written, dgamma / dbeta (fp32 [C]) are written or accumulated like dW."""
+        N = int(targets.numel())
+        tdt = TORCH_DTYPES[self.dtype]
+        _check_dev(gamma, "gamma", torch.float32, (self.C,))
+        _check_dev(dgamma, "dgamma", torch.float32, (self.C,))
+        if beta is not None:
+            _check_dev(beta, "beta", torch.float32, (self.C,))
+        if dbeta is not None:
+            _check_dev(dbeta, "dbeta", torch.float32, (self.C,))
+        if N > 0:
+            _check_dev(x, "x", tdt, (N, self.C))
+            _check_dev(W, "W", tdt, (self.V, self.C))
+            _check_dev(targets, "targets", torch.int32, (N,))
+            _check_dev(dx, "dx", tdt, (N, self.C))
+            if row_loss is not None:
+                _check_dev(row_loss, "row_loss", torch.float32, (N,))
+        st = self.lib.lmce_microstep_ln(self.handle, _ptr(x), _ptr(gamma), _ptr(beta), LN_KINDS[kind], float(eps),
+                                        _ptr(W), _ptr(targets), N, int(global_valid), _ptr(dx), _ptr(dgamma),
+                                        _ptr(dbeta), _ptr(row_loss), _stream(stream))
+        if check and st != OK:
+            raise LmceError(st, "lmce_microstep_ln")
         return st
 
     def finalize(self, stream=None, check: bool = True):

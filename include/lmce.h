@@ -81,7 +81,7 @@ typedef struct lmce_config {
   int32_t norm;             /* lmce_norm                                                     */
   int32_t grad_accum_steps; /* G >= 1; used by LMCE_NORM_MICRO_MEAN                          */
   int32_t path;             /* lmce_path                                                     */
-  int32_t flags;            /* 0, or LMCE_ACCUMULATE_FROM_START | LMCE_COMPACT_VALID_ROWS    */
+  int32_t flags;            /* 0 or an OR of the LMCE_ACCUMULATE_FROM_START, ... bits below  */
 } lmce_config;
 
 /* cfg.flags: the first micro-step after create or finalize ADDS its gradient to dW instead of
@@ -91,6 +91,13 @@ typedef struct lmce_config {
 /* cfg.flags: also allocate the scratch of lmce_microstep_compact (two [max_N, C] row buffers of
  * the input dtype and 16 bytes per row). */
 #define LMCE_COMPACT_VALID_ROWS 2
+/* cfg.flags: also allocate the scratch of lmce_microstep_ln (two [max_N, C] row buffers of the
+ * input dtype, 8 bytes per row, and 8 * C bytes per 32 rows of parameter-gradient partials). */
+#define LMCE_FINAL_NORM 4
+
+/* lmce_microstep_ln: the kind of ln_f */
+#define LMCE_LN_LAYERNORM 0
+#define LMCE_LN_RMSNORM   1
 
 typedef struct lmce_handle lmce_handle;
 
@@ -148,6 +155,32 @@ LMCE_API int lmce_microstep(lmce_handle* h, const void* hidden, const void* W, c
 LMCE_API int lmce_microstep_compact(lmce_handle* h, const void* hidden, const void* W, const int32_t* targets,
                                     int64_t N, int64_t n_valid, int64_t global_valid, void* dh, float* row_loss,
                                     void* stream);
+
+/*
+ * lmce_microstep_ln -- lmce_microstep with the final normalisation ln_f in front ("How I trained
+ * my own GPT-2 124M", section 2.8: LayerNorm; "Reproduce GPT-2 124M", model definition: RMSNorm):
+ *   h  = ln_f(x) = (x - mean) * rstd * gamma + beta, per row, rstd = 1 / sqrt(var + eps) with the
+ *        biased variance (RMSNorm: mean = 0, var = mean of x^2, no beta), computed in fp32 and
+ *        rounded to the input dtype (nearest-even) for the head
+ *   dx = the gradient through ln_f of the head's dh (bf16-rounded for bf16 handles):
+ *        rstd * (g - mean_c(g) - xhat * mean_c(g * xhat)), g = dh * gamma, xhat = (x - mean) * rstd
+ *        (RMSNorm: no mean_c(g) term)
+ *   dgamma = sum over rows of dh * xhat, dbeta = sum over rows of dh, fp32, summed in a fixed order;
+ *        written by the first micro-step of a step and added by later ones, exactly as dW.
+ *   x       : device, dtype [N, C] -- the last block's output, row-major
+ *   gamma   : device, fp32 [C];  beta : device, fp32 [C] or NULL (RMSNorm: must be NULL)
+ *   ln_kind : LMCE_LN_LAYERNORM or LMCE_LN_RMSNORM;  eps >= 0 (torch's LayerNorm default: 1e-5)
+ *   dx      : device, dtype [N, C], written
+ *   dgamma  : device, fp32 [C];  dbeta : device, fp32 [C] or NULL (NULL when beta is NULL)
+ *   W, targets, N, global_valid, row_loss, stream: as lmce_microstep.  The handle must have been
+ *   created with LMCE_FINAL_NORM; h and dh live in its scratch.
+ * Errors: LMCE_ERR_ARG (as lmce_microstep, a null gamma/dgamma, an unknown ln_kind, beta with
+ *         RMSNorm, eps < 0, no ln_f scratch), LMCE_ERR_NO_VALID (GLOBAL norm with
+ *         global_valid <= 0: dx is zeroed, dgamma, dbeta and dW untouched), LMCE_ERR_CUDA.
+ */
+LMCE_API int lmce_microstep_ln(lmce_handle* h, const void* x, const float* gamma, const float* beta, int32_t ln_kind,
+                               float eps, const void* W, const int32_t* targets, int64_t N, int64_t global_valid,
+                               void* dx, float* dgamma, float* dbeta, float* row_loss, void* stream);
 
 /*
  * lmce_finalize -- synchronise `stream`, read the step's results and reset the handle
@@ -225,7 +258,9 @@ LMCE_API int lmce_selected_path(const lmce_handle* h);
 #define LMCE_KIND_DW      2  /* recomputed logits -> dlogits -> dW accumulation           */
 #define LMCE_KIND_DH      3  /* recomputed logits -> dlogits -> dh                        */
 #define LMCE_KIND_LSE_DH  4  /* logits tiles -> online softmax -> logsumexp and dh        */
-#define LMCE_KIND_COUNT   5
+#define LMCE_KIND_LN      5  /* ln_f forward, backward and parameter-gradient reduction */
+#define LMCE_KIND_COMPACT 6  /* valid-row count, scan, gather and scatter               */
+#define LMCE_KIND_COUNT   7
 
 /* lmce_profile -- enable (1: clears earlier records) or disable (0) the event records. */
 LMCE_API int lmce_profile(lmce_handle* h, int enable);

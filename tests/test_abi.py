@@ -51,7 +51,7 @@ def test_argument_errors_before_any_device_call(lib):
     assert lib.lmce_create(ctypes.byref(cfg), None, ctypes.byref(h)) == M.ERR_ARG
     assert lib.lmce_create(None, ctypes.c_void_p(16), ctypes.byref(h)) == M.ERR_ARG
     for bad in (dict(C=0), dict(V=-1), dict(max_N=-5), dict(dtype=7), dict(norm=3), dict(path=9),
-                dict(grad_accum_steps=0), dict(flags=4), dict(C=4096, path=1)):
+                dict(grad_accum_steps=0), dict(flags=8), dict(C=4096, path=1)):
         c = M.Config(768, 50304, 1024, 0, -100, 0, 1, 0, 0)
         for k, v in bad.items():
             setattr(c, k, v)
@@ -60,6 +60,7 @@ def test_argument_errors_before_any_device_call(lib):
     assert lib.lmce_finalize(None, None, None, None, None) == M.ERR_ARG
     assert lib.lmce_dw_sumsq(None, None, None) == M.ERR_ARG
     assert lib.lmce_microstep_compact(None, None, None, None, 0, 0, 1, None, None, None) == M.ERR_ARG
+    assert lib.lmce_microstep_ln(None, None, None, None, 0, 1e-5, None, None, 0, 1, None, None, None, None, None) == M.ERR_ARG
     assert lib.lmce_adamw(None, None, None, None, None, 1, 1e-3, 0.9, 0.95, 1e-8, 0.1, 1.0, None) == M.ERR_ARG
     assert lib.lmce_destroy(None) == M.OK
     assert lib.lmce_profile(None, 1) == M.ERR_ARG
