@@ -225,7 +225,7 @@ def run_lmce(args, rank, world, local_rank):
             micro(h, y, nv, dh)
         res = L.finalize(stream=stream)
         if world > 1:
-            dp.reduce_step(dW, res[0], res[1])
+            dp.reduce_step(dW, res[0], res[1], extra=(ln_dgamma, ln_dbeta) if args.final_norm else ())
         return res
 
     def barrier():
@@ -290,7 +290,10 @@ def run_lmce(args, rank, world, local_rank):
                 used[b][k].record(stream)
                 if k == 0:
                     issue_copies(1 - b)   # the next step's inputs stream in meanwhile
-            return L.finalize(stream=stream)
+            res = L.finalize(stream=stream)
+            if world > 1:   # the same exchange as the device-timed step
+                dp.reduce_step(dW, res[0], res[1], extra=(ln_dgamma, ln_dbeta) if args.final_norm else ())
+            return res
 
         issue_copies(0)
         for i in range(max(1, args.warmup)):

@@ -7,8 +7,9 @@ on the host side of the library:
 1. before the first micro-step, a SUM all-reduce of the valid-target count, so
    that every rank scales its gradients by 1 / (valid targets over all ranks and
    micro-steps) -- the global token-weighted mean;
-2. after the last micro-step, a SUM all-reduce of the fp32 dW buffer and of
-   (loss_sum, valid_count).
+2. after the last micro-step, a SUM all-reduce of the fp32 dW buffer (and of any
+   other parameter gradient the step accumulated, such as ln_f's dgamma and dbeta)
+   and of (loss_sum, valid_count).
 
 The pages average gradients across ranks (DDP's AVG) after each rank divided its
 micro-batch means by grad_accum_steps ("Multi-GPU calculation of gradients for
@@ -37,11 +38,14 @@ def global_valid_count(local_valid: int, group=None, device=None) -> int:
     return int(t.item())
 
 
-def reduce_step(dW: torch.Tensor, loss_sum: float, valid_count: int, group=None):
-    """SUM-reduce dW in place and return the summed (loss_sum, valid_count)."""
+def reduce_step(dW: torch.Tensor, loss_sum: float, valid_count: int, group=None, extra=()):
+    """SUM-reduce dW (and every tensor in ``extra``) in place; return the summed (loss_sum, valid_count)."""
     if not _active(group):
         return float(loss_sum), int(valid_count)
     dist.all_reduce(dW, op=dist.ReduceOp.SUM, group=group)
+    for t in extra:
+        if t is not None:
+            dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
     scal = torch.tensor([float(loss_sum), float(valid_count)], dtype=torch.float64, device=dW.device)
     dist.all_reduce(scal, op=dist.ReduceOp.SUM, group=group)
     return float(scal[0].item()), int(round(scal[1].item()))

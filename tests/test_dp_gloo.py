@@ -45,6 +45,11 @@ def _problem(seed=21):
     return W, mbs
 
 
+def _ln_params(C, seed=22):
+    rng = np.random.default_rng(seed)
+    return 1 + 0.1 * rng.normal(size=C), 0.1 * rng.normal(size=C)
+
+
 def _worker(rank, world, port, out):
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
@@ -66,6 +71,12 @@ def _worker(rank, world, port, out):
         res["loss_sum"] = ls
         res["count"] = cnt
         res["objective"] = float(dp.reduce_step(torch.zeros(1, dtype=torch.float64), r.objective, 0)[0])
+        # ln_f in front: the rows' x shard like h; dgamma and dbeta are reduced beside dW
+        gamma, beta = _ln_params(W.shape[1])
+        rl = O.step_ln([(h * 1.3 + 0.2, y) for h, y in local], gamma, beta, W, "layernorm", 1e-5, global_valid=gv)
+        dW2, dg, db = torch.tensor(rl.head.dW), torch.tensor(rl.dgamma), torch.tensor(rl.dbeta)
+        dp.reduce_step(dW2, rl.head.loss_sum, rl.head.count, extra=(dg, db))
+        res["ln"] = (dW2.numpy(), dg.numpy(), db.numpy())
         # the two-GPU worked example: per-rank micro-mean objectives, averaged
         g = json.load(open(os.path.join(GOLDEN, "p5_worked_examples.json")))["two_gpu"]
         W2 = np.array([[1.0], [0.0]])
@@ -103,6 +114,11 @@ def test_two_rank_sum_reduction_matches_single_process():
         assert res["count"] == whole.count
         assert res["objective"] == pytest.approx(whole.objective, rel=1e-13)
         assert res["p5_avg"] == pytest.approx(g["ddp_average"], rel=1e-12)
+        gamma, beta = _ln_params(W.shape[1])
+        wl = O.step_ln([(h * 1.3 + 0.2, y) for h, y in mbs], gamma, beta, W, "layernorm", 1e-5)
+        dW2, dg, db = res["ln"]
+        assert np.abs(dW2 - wl.head.dW).max() < 1e-14
+        assert np.abs(dg - wl.dgamma).max() < 1e-13 and np.abs(db - wl.dbeta).max() < 1e-13
 
 
 def test_shard_rows_covers_everything():
