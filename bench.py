@@ -196,8 +196,6 @@ def run_lmce(args, rank, world, local_rank):
     dhs = [torch.empty_like(h) for h, _ in mbs]
     dW = torch.empty(w.V, w.C, dtype=torch.float32, device=dev)
     max_N = max(int(y.numel()) for _, y in mbs)
-    if args.compact and args.final_norm:
-        raise SystemExit("--compact and --final-norm are separate entry points")
     L = M.Lmce(w.C, w.V, max_N, dW, w.dtype, norm="global", grad_accum_steps=w.G, path=args.path,
                compact=args.compact, final_norm=bool(args.final_norm))
     if args.final_norm:
@@ -214,7 +212,7 @@ def run_lmce(args, rank, world, local_rank):
     def micro(h, y, n_valid, dh):
         if args.final_norm:   # h is x and dh is dx here
             L.microstep_ln(h, ln_gamma, ln_beta, W, y, gv, dh, ln_dgamma, ln_dbeta, args.final_norm, 1e-5,
-                           stream=stream)
+                           stream=stream, n_valid=n_valid if args.compact else None)
         elif args.compact:
             L.microstep_compact(h, W, y, n_valid, gv, dh, stream=stream)
         else:
@@ -370,7 +368,7 @@ def run_lmce(args, rank, world, local_rank):
         esz = 2 if w.dtype == "bf16" else 4
         nmicro = args.steps * w.G
         ln_ms = prof["ln"][0] / nmicro
-        rows = tokens_rank // w.G
+        rows = (sum(nvs) if args.compact else tokens_rank) // w.G   # rows one ln_f launch covers (mean)
         rpb = -(-rows // 304)   # the backward's row range per block: at most 304 blocks
         ln_bytes = 5 * rows * w.C * esz + 2 * 2 * 4 * w.C * (-(-rows // rpb))
         ln_gbs = ln_bytes / (ln_ms * 1e-3) / 1e9

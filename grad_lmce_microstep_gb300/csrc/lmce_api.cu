@@ -497,10 +497,12 @@ extern "C" int lmce_microstep_compact(lmce_handle* h, const void* hidden, const 
   return e == cudaSuccess ? LMCE_OK : LMCE_ERR_CUDA;
 }
 
-extern "C" int lmce_microstep_ln(lmce_handle* h, const void* x, const float* gamma, const float* beta,
-                                 int32_t ln_kind, float eps, const void* W, const int32_t* targets, int64_t N,
-                                 int64_t global_valid, void* dx, float* dgamma, float* dbeta, float* row_loss,
-                                 void* stream) {
+namespace {
+
+// Argument checks shared by the two ln_f entry points (N rows of x / dx in the input dtype).
+int check_ln_args(const lmce_handle* h, const void* x, const float* gamma, const float* beta, int32_t ln_kind,
+                  float eps, const void* W, const int32_t* targets, int64_t N, void* dx, float* dgamma,
+                  float* dbeta) {
   if (!h || !h->ln.h) return LMCE_ERR_ARG;
   const lmce_config& c = h->cfg;
   if (N < 0 || N > c.max_N) return LMCE_ERR_ARG;
@@ -511,14 +513,25 @@ extern "C" int lmce_microstep_ln(lmce_handle* h, const void* x, const float* gam
   const size_t esz = c.dtype == LMCE_BF16 ? 2 : 4;
   if (N > 0 && (((uintptr_t)x | (uintptr_t)dx) & (esz - 1))) return LMCE_ERR_ARG;
   if (h->path != LMCE_PATH_SIMT && N > 0 && (((uintptr_t)W | (uintptr_t)h->dW) & 15)) return LMCE_ERR_ARG;
-  cudaStream_t st = (cudaStream_t)stream;
-  if (c.norm == LMCE_NORM_GLOBAL && global_valid <= 0) {   // refused: dx zeroed, parameters untouched
-    if (N > 0 && cudaMemsetAsync(dx, 0, (size_t)N * c.C * esz, st) != cudaSuccess) return LMCE_ERR_CUDA;
-    if (N > 0 && row_loss && cudaMemsetAsync(row_loss, 0, (size_t)N * sizeof(float), st) != cudaSuccess)
-      return LMCE_ERR_CUDA;
-    h->attempted += 1;
-    return LMCE_ERR_NO_VALID;
-  }
+  return LMCE_OK;
+}
+
+// GLOBAL normalisation without a valid target: refused before any launch, dx (and row_loss)
+// zeroed, the parameter gradients untouched.
+int refuse_no_valid(lmce_handle* h, int64_t N, void* dx, float* row_loss, cudaStream_t st) {
+  const size_t esz = h->cfg.dtype == LMCE_BF16 ? 2 : 4;
+  if (N > 0 && cudaMemsetAsync(dx, 0, (size_t)N * h->cfg.C * esz, st) != cudaSuccess) return LMCE_ERR_CUDA;
+  if (N > 0 && row_loss && cudaMemsetAsync(row_loss, 0, (size_t)N * sizeof(float), st) != cudaSuccess)
+    return LMCE_ERR_CUDA;
+  h->attempted += 1;
+  return LMCE_ERR_NO_VALID;
+}
+
+// ln_f forward, the micro-step on its output, ln_f backward: N rows of x (already checked).
+int run_ln_step(lmce_handle* h, const void* x, const float* gamma, const float* beta, int32_t ln_kind, float eps,
+                const void* W, const int32_t* targets, int64_t N, int64_t global_valid, void* dx, float* dgamma,
+                float* dbeta, float* row_loss, cudaStream_t st) {
+  const lmce_config& c = h->cfg;
   // the parameter gradients follow dW: written by the first micro-step of a step, then added
   const bool write = h->first && !(c.flags & LMCE_ACCUMULATE_FROM_START);
   LnArgs a{};
@@ -558,6 +571,63 @@ extern "C" int lmce_microstep_ln(lmce_handle* h, const void* x, const float* gam
   L2.st = st;
   L2.prof = &h->prof;
   e = ln_backward(a, L2);
+  h->launches += L2.n;
+  return e == cudaSuccess ? LMCE_OK : LMCE_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" int lmce_microstep_ln(lmce_handle* h, const void* x, const float* gamma, const float* beta,
+                                 int32_t ln_kind, float eps, const void* W, const int32_t* targets, int64_t N,
+                                 int64_t global_valid, void* dx, float* dgamma, float* dbeta, float* row_loss,
+                                 void* stream) {
+  const int ck = check_ln_args(h, x, gamma, beta, ln_kind, eps, W, targets, N, dx, dgamma, dbeta);
+  if (ck != LMCE_OK) return ck;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (h->cfg.norm == LMCE_NORM_GLOBAL && global_valid <= 0) return refuse_no_valid(h, N, dx, row_loss, st);
+  return run_ln_step(h, x, gamma, beta, ln_kind, eps, W, targets, N, global_valid, dx, dgamma, dbeta, row_loss, st);
+}
+
+extern "C" int lmce_microstep_ln_compact(lmce_handle* h, const void* x, const float* gamma, const float* beta,
+                                         int32_t ln_kind, float eps, const void* W, const int32_t* targets,
+                                         int64_t N, int64_t n_valid, int64_t global_valid, void* dx,
+                                         float* dgamma, float* dbeta, float* row_loss, void* stream) {
+  const int ck = check_ln_args(h, x, gamma, beta, ln_kind, eps, W, targets, N, dx, dgamma, dbeta);
+  if (ck != LMCE_OK) return ck;
+  if (!h->cs.h_c || n_valid < -1 || n_valid > N) return LMCE_ERR_ARG;
+  const lmce_config& c = h->cfg;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (c.norm == LMCE_NORM_GLOBAL && global_valid <= 0) return refuse_no_valid(h, N, dx, row_loss, st);
+  // gather the valid rows of x (and their targets), run ln_f and the head on them, scatter dx
+  StepArgs a{};
+  a.hidden = x;
+  a.targets = targets;
+  a.dh = dx;
+  a.row_loss = row_loss;
+  a.N = N;
+  a.C = c.C;
+  a.V = c.V;
+  a.ignore_id = c.ignore_id;
+  a.bf16 = c.dtype == LMCE_BF16;
+  Launch L;
+  L.st = st;
+  L.prof = &h->prof;
+  cudaError_t e = compact_rows(a, h->cs, h->sc.acc, n_valid, L);
+  h->launches += L.n;
+  if (e != cudaSuccess) return LMCE_ERR_CUDA;
+  if (n_valid < 0) {
+    if (cudaMemcpyAsync(h->cs.host_total, h->cs.total, sizeof(int64_t), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return LMCE_ERR_CUDA;
+    n_valid = *h->cs.host_total;
+  }
+  const int s = run_ln_step(h, h->cs.h_c, gamma, beta, ln_kind, eps, W, h->cs.y_c, n_valid, global_valid,
+                            h->cs.dh_c, dgamma, dbeta, row_loss ? h->cs.rl_c : nullptr, st);
+  if (s != LMCE_OK) return s;
+  Launch L2;
+  L2.st = st;
+  L2.prof = &h->prof;
+  e = compact_scatter(a, h->cs, n_valid, L2);
   h->launches += L2.n;
   return e == cudaSuccess ? LMCE_OK : LMCE_ERR_CUDA;
 }

@@ -34,7 +34,7 @@ TORCH_DTYPES = {"bf16": torch.bfloat16, "fp32": torch.float32}
 EXPORTS = ("lmce_create", "lmce_microstep", "lmce_finalize", "lmce_destroy", "lmce_status_string",
            "lmce_launch_count", "lmce_selected_path", "lmce_profile", "lmce_profile_read",
            "lmce_microstep_noalloc", "lmce_dw_sumsq", "lmce_adamw", "lmce_microstep_compact",
-           "lmce_microstep_ln")
+           "lmce_microstep_ln", "lmce_microstep_ln_compact")
 
 NOALLOC_MAX_N = 65536
 
@@ -79,6 +79,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.lmce_microstep_compact.restype = i32
     L.lmce_microstep_ln.argtypes = [vp, vp, vp, vp, i32, ctypes.c_float, vp, vp, i64, i64, vp, vp, vp, vp, vp]
     L.lmce_microstep_ln.restype = i32
+    L.lmce_microstep_ln_compact.argtypes = [vp, vp, vp, vp, i32, ctypes.c_float, vp, vp, i64, i64, i64, vp, vp, vp,
+                                            vp, vp]
+    L.lmce_microstep_ln_compact.restype = i32
     L.lmce_finalize.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64),
                                 ctypes.POINTER(ctypes.c_double), vp]
     L.lmce_finalize.restype = i32
@@ -215,9 +218,14 @@ class Lmce:
         return st
 
     def microstep_ln(self, x, gamma, beta, W, targets, global_valid: int = 0, dx=None, dgamma=None, dbeta=None,
-                     kind: str = "layernorm", eps: float = 1e-5, row_loss=None, stream=None, check: bool = True) -> int:
+                     kind: str = "layernorm", eps: float = 1e-5, row_loss=None, stream=None, check: bool = True,
+                     n_valid=None) -> int:
         """A micro-step with ln_f in front (handle made with final_norm=True): h = ln_f(x) feeds the
-        head, dx is written, dgamma / dbeta (fp32 [C]) are written or accumulated like dW."""
+        head, dx is written, dgamma / dbeta (fp32 [C]) are written or accumulated like dW.
+
+        n_valid (an int, -1 = counted by the library): run over the valid rows only
+        (lmce_microstep_ln_compact; the handle also needs compact=True).
+        """
         N = int(targets.numel())
         tdt = TORCH_DTYPES[self.dtype]
         _check_dev(gamma, "gamma", torch.float32, (self.C,))
@@ -233,11 +241,19 @@ class Lmce:
             _check_dev(dx, "dx", tdt, (N, self.C))
             if row_loss is not None:
                 _check_dev(row_loss, "row_loss", torch.float32, (N,))
-        st = self.lib.lmce_microstep_ln(self.handle, _ptr(x), _ptr(gamma), _ptr(beta), LN_KINDS[kind], float(eps),
-                                        _ptr(W), _ptr(targets), N, int(global_valid), _ptr(dx), _ptr(dgamma),
-                                        _ptr(dbeta), _ptr(row_loss), _stream(stream))
+        if n_valid is None:
+            st = self.lib.lmce_microstep_ln(self.handle, _ptr(x), _ptr(gamma), _ptr(beta), LN_KINDS[kind],
+                                            float(eps), _ptr(W), _ptr(targets), N, int(global_valid), _ptr(dx),
+                                            _ptr(dgamma), _ptr(dbeta), _ptr(row_loss), _stream(stream))
+            what = "lmce_microstep_ln"
+        else:
+            st = self.lib.lmce_microstep_ln_compact(self.handle, _ptr(x), _ptr(gamma), _ptr(beta), LN_KINDS[kind],
+                                                    float(eps), _ptr(W), _ptr(targets), N, int(n_valid),
+                                                    int(global_valid), _ptr(dx), _ptr(dgamma), _ptr(dbeta),
+                                                    _ptr(row_loss), _stream(stream))
+            what = "lmce_microstep_ln_compact"
         if check and st != OK:
-            raise LmceError(st, "lmce_microstep_ln")
+            raise LmceError(st, what)
         return st
 
     def finalize(self, stream=None, check: bool = True):

@@ -183,6 +183,23 @@ LMCE_API int lmce_microstep_ln(lmce_handle* h, const void* x, const float* gamma
                                void* dx, float* dgamma, float* dbeta, float* row_loss, void* stream);
 
 /*
+ * lmce_microstep_ln_compact -- lmce_microstep_ln over the valid rows only: the rows of x whose
+ * target is in [0, V) are gathered in input order (as lmce_microstep_compact gathers h), ln_f, the
+ * head and ln_f's backward run on those n_valid rows, and dx (and row_loss) are scattered back with
+ * zeros on the ignored rows.  An ignored row's dh is zero, so its dx and its share of dgamma and
+ * dbeta are zero too: the results equal lmce_microstep_ln's up to summation order.
+ *   n_valid : as lmce_microstep_compact (-1: counted on the device, blocking).
+ *   other arguments as lmce_microstep_ln.  The handle must have been created with both
+ *   LMCE_FINAL_NORM and LMCE_COMPACT_VALID_ROWS.
+ * Errors: as lmce_microstep_ln, and LMCE_ERR_ARG for n_valid < -1 or > N or a handle without
+ *         the compaction scratch; a wrong n_valid is reported by lmce_finalize as LMCE_ERR_ARG.
+ */
+LMCE_API int lmce_microstep_ln_compact(lmce_handle* h, const void* x, const float* gamma, const float* beta,
+                                       int32_t ln_kind, float eps, const void* W, const int32_t* targets, int64_t N,
+                                       int64_t n_valid, int64_t global_valid, void* dx, float* dgamma, float* dbeta,
+                                       float* row_loss, void* stream);
+
+/*
  * lmce_finalize -- synchronise `stream`, read the step's results and reset the handle
  * for the next optimizer step (the next micro-step writes dW again).
  *   loss_sum    : host, may be NULL -- sum of the valid rows' losses over the step

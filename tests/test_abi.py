@@ -61,6 +61,7 @@ def test_argument_errors_before_any_device_call(lib):
     assert lib.lmce_dw_sumsq(None, None, None) == M.ERR_ARG
     assert lib.lmce_microstep_compact(None, None, None, None, 0, 0, 1, None, None, None) == M.ERR_ARG
     assert lib.lmce_microstep_ln(None, None, None, None, 0, 1e-5, None, None, 0, 1, None, None, None, None, None) == M.ERR_ARG
+    assert lib.lmce_microstep_ln_compact(None, None, None, None, 0, 1e-5, None, None, 0, 0, 1, None, None, None, None, None) == M.ERR_ARG
     assert lib.lmce_adamw(None, None, None, None, None, 1, 1e-3, 0.9, 0.95, 1e-8, 0.1, 1.0, None) == M.ERR_ARG
     assert lib.lmce_destroy(None) == M.OK
     assert lib.lmce_profile(None, 1) == M.ERR_ARG

@@ -33,7 +33,7 @@ def _xs(w):
     return [((h.float() * 1.7 + 0.4).to(TDT[w.dtype]), y) for h, y in w.micro]
 
 
-def _run(w, xs, gamma, beta, kind, eps, path="auto", steps=1):
+def _run(w, xs, gamma, beta, kind, eps, path="auto", steps=1, compact=False):
     C, V = w.C, w.V
     W = w.W.cuda()
     dW = torch.empty(V, C, device="cuda")
@@ -41,7 +41,7 @@ def _run(w, xs, gamma, beta, kind, eps, path="auto", steps=1):
     dbeta = torch.full((C,), 7.0, device="cuda") if beta is not None else None
     g, b = gamma.cuda(), (beta.cuda() if beta is not None else None)
     max_N = max(int(y.numel()) for _, y in xs)
-    L = M.Lmce(C, V, max_N, dW, w.dtype, grad_accum_steps=len(xs), path=path, final_norm=True)
+    L = M.Lmce(C, V, max_N, dW, w.dtype, grad_accum_steps=len(xs), path=path, final_norm=True, compact=compact)
     gv = sum(w.valid_counts())
     for _ in range(steps):   # a later step writes the parameter gradients afresh, as dW
         dxs, rls = [], []
@@ -49,7 +49,8 @@ def _run(w, xs, gamma, beta, kind, eps, path="auto", steps=1):
             xd, yd = x.cuda(), y.cuda()
             dx = torch.full_like(xd, 5.0)
             rl = torch.empty(yd.numel(), device="cuda")
-            L.microstep_ln(xd, g, b, W, yd, gv, dx, dgamma, dbeta, kind, eps, rl)
+            nv = int(((y >= 0) & (y < V)).sum()) if compact else None
+            L.microstep_ln(xd, g, b, W, yd, gv, dx, dgamma, dbeta, kind, eps, rl, n_valid=nv)
             dxs.append(dx)
             rls.append(rl)
         res = L.finalize()
@@ -109,6 +110,25 @@ def test_ln_widths(C, dtype):
     xs = _xs(w)
     gamma, beta = _params(C, "layernorm", 43)
     _check(w, xs, gamma, beta, "layernorm", 1e-5, _run(w, xs, gamma, beta, "layernorm", 1e-5))
+
+
+@pytest.mark.parametrize("path", ["simt", "tcgen05"])
+@pytest.mark.parametrize("kind", ["layernorm", "rmsnorm"])
+def test_ln_compact_masked_tails(path, kind):
+    # ln_f over the valid rows only: masked sequence tails and scattered ignored targets; dx of an
+    # ignored row is exactly zero, everything else matches the oracle's step_ln over all rows
+    T = 128
+    w = I.custom([3 * T] * 3, 256, 1000, "bf16", seed=45, ignore_frac=0.05)
+    for k, tail in enumerate((0, T // 2, 3 * T // 4)):
+        if tail:
+            w.micro[k][1].view(3, T)[:, T - tail:] = I.IGNORE_ID
+    xs = _xs(w)
+    gamma, beta = _params(w.C, kind, 45)
+    got = _run(w, xs, gamma, beta, kind, 1e-5, path=path, steps=2, compact=True)
+    _check(w, xs, gamma, beta, kind, 1e-5, got)
+    for (_, y), dx in zip(xs, got[1]):
+        ign = ~((y >= 0) & (y < w.V))
+        assert float(dx.cpu()[ign].abs().max()) == 0.0
 
 
 def test_ln_argument_errors_and_no_valid():
