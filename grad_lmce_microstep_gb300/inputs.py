@@ -23,7 +23,7 @@ IGNORE_ID = -100
 GPT2_REAL_VOCAB = 50257
 GPT2_PADDED_VOCAB = 50304
 
-_KIND = {"W": 1, "h": 101, "y": 201, "mask": 301, "stress": 401}
+_KIND = {"W": 1, "h": 101, "y": 201, "mask": 301, "stress": 401, "doclen": 501}
 
 
 def _gen(seed: int, kind: str, k: int = 0) -> torch.Generator:
@@ -117,6 +117,28 @@ def masked_unequal(seed: int = 0, B: int = 16, T: int = 1024) -> Workload:
     return w
 
 
+def padded_docs(seed: int = 0, B: int = 8, T: int = 2048, G: int = 4, mean_len: int = 600,
+                sd_len: int = 150) -> Workload:
+    """One document per row, the rest of the row padded (pad targets = -100): zerotofrontier
+    "GPT", section "Document boundaries, packing and masking", where ~600-token documents in
+    T = 2048 windows waste about 70 % of every batch.  Document lengths are seeded draws from a
+    normal(mean_len, sd_len) clipped to [16, T]; C = 768, V = 50304, bf16, G micro-steps of B rows."""
+    w = gpt2_head(seed, G=G, B=B, T=T, name="padded_docs")
+    lens = []
+    micro = []
+    for k, (h, y) in enumerate(w.micro):
+        L = torch.randn(B, generator=_gen(seed, "doclen", k)) * sd_len + mean_len
+        L = L.round().clamp(16, T).to(torch.int64)
+        y = y.clone().view(B, T)
+        pos = torch.arange(T).view(1, T)
+        y[pos >= L.view(B, 1)] = IGNORE_ID
+        micro.append((h, y.view(-1)))
+        lens.append([int(v) for v in L])
+    w.micro = micro
+    w.meta["doc_lengths"] = lens
+    return w
+
+
 def logit_stress(seed: int = 0, B: int = 8, T: int = 2048, G: int = 2, C: int = 1024,
                  scale_frac: float = 0.01, scale: float = 40.0, argmax_frac: float = 0.02) -> Workload:
     """C=1024: 1 % of h rows multiplied by 40 (in fp32, before the bf16 rounding) and 2 % of
@@ -155,6 +177,7 @@ WORKLOADS = {
     "gpt2_124m_full_batch": gpt2_full_batch,
     "masked_unequal": masked_unequal,
     "logit_stress": logit_stress,
+    "padded_docs": padded_docs,
 }
 
 

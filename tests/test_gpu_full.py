@@ -25,11 +25,11 @@ ROWS_PER_MICRO = 48
 DW_ROWS = 24
 
 
-def _run(w, W=None):
+def _run(w, W=None, compact=False):
     """Whole optimizer step on the GPU, keeping outputs on the device."""
     Wd = (w.W if W is None else W).cuda()
     mbs = [(h.cuda(), y.cuda()) for h, y in w.micro]
-    dW, dhs, rls, res = M.run_step(Wd, mbs, w.dtype, row_loss=True)
+    dW, dhs, rls, res = M.run_step(Wd, mbs, w.dtype, row_loss=True, compact=compact)
     torch.cuda.synchronize()
     return dW, dhs, rls, res
 
@@ -73,11 +73,14 @@ def _oracle_totals(w):
     return lses, loss
 
 
-@pytest.mark.parametrize("name", ["gpt2_124m_head", "masked_unequal"])
-def test_full_size_head(name):
+@pytest.mark.parametrize("name,compact", [("gpt2_124m_head", False), ("masked_unequal", False),
+                                          ("masked_unequal", True), ("padded_docs", True)])
+def test_full_size_head(name, compact):
+    # compact: the valid-row path (lmce_microstep_compact) in the launch configuration that
+    # bench.py --compact times
     w = I.make(name)
     rng = np.random.default_rng(7)
-    dW, dhs, rls, (ls, cnt, mean, st) = _run(w)
+    dW, dhs, rls, (ls, cnt, mean, st) = _run(w, compact=compact)
     assert st == M.OK
     counts = w.valid_counts()
     assert cnt == sum(counts)
@@ -87,6 +90,8 @@ def test_full_size_head(name):
     assert abs(mean - loss / sum(counts)) <= LOSS_REL * abs(loss / sum(counts))
     # rows from each micro-step, incl. the masked tail of the masked workload
     extra = (lambda k: [16383, 1023, 1024 * 16 - 1]) if name == "masked_unequal" else (lambda k: [0])
+    if name == "padded_docs":   # the last token of a document and the first pad after it
+        extra = lambda k: [r * 2048 + L + d for r, L in enumerate(w.meta["doc_lengths"][k][:3]) for d in (-1, 0)]
     _check_rows(w, dhs, rls, scales, rng, extra)
     # dW rows: random ones, the padded vocabulary tail and frequent targets
     ys = np.concatenate([O.i64(y) for _, y in w.micro])

@@ -42,3 +42,19 @@ def test_logit_stress_structure():
     assert int((norms > 20 * norms.median()).sum()) == w.meta["scaled_rows"] == 3
     assert w.meta["argmax_targets"] == 5
     assert int(y.min()) >= 0 and int(y.max()) < I.GPT2_PADDED_VOCAB
+
+
+def test_padded_docs_structure():
+    # one document per row, then pad: every row's valid targets are a prefix of its T positions,
+    # of the drawn length; about 70 % of the batch is padding, as the packing section says
+    w = I.make("padded_docs")
+    T = 2048
+    assert w.C == 768 and w.V == 50304 and len(w.micro) == 4
+    for (h, y), lens in zip(w.micro, w.meta["doc_lengths"]):
+        assert h.shape == (8 * T, 768)
+        rows = y.view(8, T)
+        for r, L in enumerate(lens):
+            assert 16 <= L <= T
+            assert bool((rows[r, :L] >= 0).all()) and bool((rows[r, L:] == I.IGNORE_ID).all())
+    frac = sum(w.valid_counts()) / w.tokens
+    assert 0.2 < frac < 0.35
