@@ -228,6 +228,8 @@ class Lmce:
         """
         N = int(targets.numel())
         tdt = TORCH_DTYPES[self.dtype]
+        if gamma is None or dgamma is None:
+            raise ValueError("gamma and dgamma are required")
         _check_dev(gamma, "gamma", torch.float32, (self.C,))
         _check_dev(dgamma, "dgamma", torch.float32, (self.C,))
         if beta is not None:

@@ -25,8 +25,14 @@
  *   - Every call returns an int status (LMCE_OK or an LMCE_ERR_* code) and never
  *     throws; no device code traps or asserts.
  *   - Calls on one handle must be issued from one host thread and enqueue on one
- *     stream (or on streams the caller orders).  Only lmce_finalize and lmce_dw_sumsq
- *     block the host.
+ *     stream (or on streams the caller orders).  Only lmce_finalize, lmce_dw_sumsq and
+ *     the compacting micro-steps given n_valid = -1 block the host.
+ *
+ * Beyond the head, on the same pages' training step: lmce_microstep_compact skips rows
+ * whose target is ignored, lmce_microstep_ln puts the final LayerNorm / RMSNorm (ln_f) in
+ * front of the head, lmce_dw_sumsq gives dW's share of the global clip norm and lmce_adamw
+ * applies the optimizer to W ("How I trained my own GPT-2 124M", sections 2.8 and 6;
+ * "Reproduce GPT-2 124M", training configuration).
  */
 #ifndef LMCE_H_
 #define LMCE_H_
