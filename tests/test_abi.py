@@ -73,3 +73,21 @@ def test_clip_coef_host_helper():
     from oracle import lmce_oracle as O
     for sumsq, mx in ((4.0, 1.0), (0.25, 1.0), (0.0, 1.0), (1e6, 0.5), (1.0, 1.0)):
         assert M.clip_coef(sumsq, mx) == O.clip_coef(sumsq, mx)
+
+
+def test_header_compiles_as_c_and_links(lib, tmp_path):
+    # a C99 program with warnings as errors, linked against the in-tree library, run on the CPU
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    here = os.path.dirname(os.path.abspath(__file__))
+    libdir = os.path.dirname(M.LIB_PATH)
+    exe = str(tmp_path / "c_abi_check")
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.dirname(HEADER),
+                    os.path.join(here, "c_abi_check.c"), "-o", exe, "-L" + libdir, "-llmce",
+                    "-Wl,-rpath," + libdir], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.strip() == "ok"
