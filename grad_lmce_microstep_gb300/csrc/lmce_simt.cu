@@ -152,8 +152,9 @@ __device__ void simt_lse_rows(const StepArgs& a, float* __restrict__ lse_out, do
 }
 
 // gate == nullptr: the lse pass of the SIMT path, one block per R rows.
-// gate != nullptr: repair mode, one block per 128-token tile: the logsumexp of the rows of a
-// flagged tile (its R-row groups in turn); other blocks return at once.
+// gate != nullptr: repair mode, grid (128-token tiles, R-row groups of a tile): a block of a
+// flagged tile takes the logsumexp of its R rows, so a tile's groups run on separate SMs; the
+// blocks of other tiles return at once.
 template <typename T>
 __global__ void __launch_bounds__(NT) simt_lse_kernel(StepArgs a, float* __restrict__ lse_out,
                                                       double* __restrict__ part_loss,
@@ -165,12 +166,9 @@ __global__ void __launch_bounds__(NT) simt_lse_kernel(StepArgs a, float* __restr
     return;
   }
   if (!gate[blockIdx.x]) return;  // block-uniform
-  for (int g = 0; g < TC_TILE_ROWS / R; ++g) {
-    const int64_t grp = (int64_t)blockIdx.x * (TC_TILE_ROWS / R) + g;
-    if (grp * R >= a.N) break;
-    simt_lse_rows<T>(a, lse_out, part_loss, part_cnt, part_err, grp, true);
-    __syncthreads();
-  }
+  const int64_t grp = (int64_t)blockIdx.x * (TC_TILE_ROWS / R) + blockIdx.y;
+  if (grp * R >= a.N) return;
+  simt_lse_rows<T>(a, lse_out, part_loss, part_cnt, part_err, grp, true);
 }
 
 // Owned rows grp*R .. grp*R + R - 1.
@@ -251,8 +249,9 @@ __device__ void simt_grad_rows(const StepArgs& a, const float* __restrict__ lse,
 }
 
 // gate == nullptr: one block per R owned rows.
-// gate != nullptr (dh pass only): repair mode, one block per 128-token tile: the dh rows of a
-// flagged tile (its R-row groups in turn); other blocks return at once.
+// gate != nullptr (dh pass only): repair mode, grid (128-token tiles, R-row groups of a tile): a
+// block of a flagged tile writes the dh rows of its R rows; the blocks of other tiles return at
+// once.
 template <typename T, bool DW>
 __global__ void __launch_bounds__(NT) simt_grad_kernel(StepArgs a, const float* __restrict__ lse,
                                                        const DevAcc* __restrict__ acc_dev,
@@ -262,12 +261,9 @@ __global__ void __launch_bounds__(NT) simt_grad_kernel(StepArgs a, const float* 
     return;
   }
   if (!gate[blockIdx.x]) return;  // block-uniform
-  for (int g = 0; g < TC_TILE_ROWS / R; ++g) {
-    const int64_t grp = (int64_t)blockIdx.x * (TC_TILE_ROWS / R) + g;
-    if (grp * R >= a.N) break;
-    __syncthreads();   // the previous group's reads of the shared accumulators are done
-    simt_grad_rows<T, DW>(a, lse, acc_dev, grp);
-  }
+  const int64_t grp = (int64_t)blockIdx.x * (TC_TILE_ROWS / R) + blockIdx.y;
+  if (grp * R >= a.N) return;
+  simt_grad_rows<T, DW>(a, lse, acc_dev, grp);
 }
 
 }  // namespace
@@ -322,7 +318,8 @@ cudaError_t simt_grads(const StepArgs& a, const Scratch& sc, Launch& L) {
 cudaError_t simt_repair_lse(const StepArgs& a, const Scratch& sc, Launch& L) {
   L.begin(K_LSE);
   const unsigned ntiles = (unsigned)((a.N + TC_TILE_ROWS - 1) / TC_TILE_ROWS);
-  simt_lse_kernel<__nv_bfloat16><<<ntiles, NT, 0, L.st>>>(a, sc.lse, nullptr, nullptr, nullptr, sc.tc_tile_flag);
+  const dim3 grid(ntiles, TC_TILE_ROWS / R);
+  simt_lse_kernel<__nv_bfloat16><<<grid, NT, 0, L.st>>>(a, sc.lse, nullptr, nullptr, nullptr, sc.tc_tile_flag);
   L.end();
   return cudaGetLastError();
 }
@@ -333,7 +330,8 @@ cudaError_t simt_repair_dh(const StepArgs& a, const Scratch& sc, Launch& L) {
   cudaFuncSetAttribute(kdh, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   L.begin(K_DH);
   const unsigned ntiles = (unsigned)((a.N + TC_TILE_ROWS - 1) / TC_TILE_ROWS);
-  kdh<<<ntiles, NT, smem, L.st>>>(a, sc.lse, sc.acc, sc.tc_tile_flag);
+  const dim3 grid(ntiles, TC_TILE_ROWS / R);
+  kdh<<<grid, NT, smem, L.st>>>(a, sc.lse, sc.acc, sc.tc_tile_flag);
   L.end();
   return cudaGetLastError();
 }

@@ -340,14 +340,15 @@ __global__ void __launch_bounds__(256) tc_combine_kernel(const float* __restrict
 // rows of a warp, kept in two registers per lane), so at the end of the range
 //   acc^T[c][n] = sum_v W[v][c] p[n][v],   l_n = sum_v p[n][v],
 //   dh_n = s (acc^T[.][n] / l_n - W[y_n]),   lse_n = (m_n + log2 l_n) ln 2.
-// An element above m_n + 80 (p > 2^80, where fp32 sums could start to lose range) flags its
-// 128-token tile; the host then runs the exact two-pass repair on flagged tiles only.
+// An element above m_n + fl_limit flags its 128-token tile, and the host then runs the exact
+// two-pass repair on flagged tiles only.  fl_limit = 115 - ceil(log2 V) keeps every sum finite:
+// l_n <= V 2^fl_limit <= 2^115 and |acc^T| <= 2^115 max|W| < 2^128 for any |W| < 8192 (99 at
+// V = 50304).  A tighter guard would send ordinary wide-logit rows through the repair.
 constexpr int G_XT = 128;                  // X rows per pair (64 per CTA)
 constexpr int G_YB = 256;                  // stream rows per block (128 per CTA)
 constexpr int G_DZ = G_YB * 128;           // one dz buffer: 256 K-rows x 64 bf16 = 32 KB
 constexpr int G_EPI_WARPS = 8;
 constexpr int G_THREADS = 96 + 32 * G_EPI_WARPS;   // warps 0 and 10 TMA, 1 MMA, 2-9 epilogue
-constexpr float FL_LIMIT = 80.f;           // lse+dh pass: largest exponent of p kept
 
 enum GradMode { GM_DW = 0, GM_DH = 1, GM_FL = 2 };
 
@@ -384,6 +385,7 @@ struct GradParams {
   int N, V, C;
   int ch0, nch;          // 256-row C chunks [ch0, ch0 + nch) of acc^T handled by this launch (nch <= 3)
   int beta;              // dW pass: 0 writes, 1 adds
+  float fl_limit;        // lse+dh pass: largest base-2 exponent of p kept (115 - ceil(log2 V))
 };
 
 __device__ __forceinline__ float grad_scale(const GradParams& p) {
@@ -786,7 +788,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             else ps3 += pv;
           }
           lacc += (ps0 + ps1) + (ps2 + ps3);
-          if (tmax > FL_LIMIT) atomicOr(p.tile_flag + t, 1u);
+          if (tmax > p.fl_limit) atomicOr(p.tile_flag + t, 1u);
         } else if (DW) {
           // my columns whose token targets my row: dz there is s (p - 1)
           uint64_t fix = 0;
@@ -1371,6 +1373,11 @@ cudaError_t tc_grad_range(const StepArgs& a, const Scratch& sc, Launch& L, int c
   p.zt_out = sc.tc_zt;
   p.acc = sc.acc;
   p.scale_fixed = a.norm == 0 ? (float)(1.0 / (double)a.global_valid) : -1.f;   // 0: global normalisation
+  {
+    int lg = 0;   // ceil(log2 V)
+    while ((1LL << lg) < a.V) ++lg;
+    p.fl_limit = (float)(115 - lg);
+  }
   p.err = &sc.acc->err;
   p.Wt = static_cast<const __nv_bfloat16*>(a.W);
   p.dW = a.dW;
