@@ -91,3 +91,16 @@ def test_header_compiles_as_c_and_links(lib, tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.strip() == "ok"
+
+
+def test_binding_fails_loudly_without_the_library_or_a_device(tmp_path):
+    # no CPU fallback: a missing library is an error, and so is a handle on host memory
+    import torch
+    with pytest.raises(RuntimeError):
+        saved, M._lib = M._lib, None
+        try:
+            M.load(str(tmp_path / "missing.so"))
+        finally:
+            M._lib = saved
+    with pytest.raises(ValueError):
+        M.Lmce(64, 65, 16, torch.zeros(65, 64), "fp32")
