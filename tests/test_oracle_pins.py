@@ -477,3 +477,19 @@ def test_step_ln_finite_differences(kind):
                 mm = list(xs); mm[k] = (xm, y)
                 num[n, c] = (J(mp, gamma, beta) - J(mm, gamma, beta)) / (2 * e)
         assert np.abs(num - r.dx[k]).max() <= 1e-6 * max(1.0, np.abs(r.dx[k]).max())
+
+
+def test_optimizer_defaults_are_the_pages():
+    # the printed hyperparameters (tests/golden/optimizer_hyperparameters.json, with citations)
+    # are the defaults of the oracle's AdamW and clip and of the binding's adamw
+    import inspect
+    g = json.load(open(os.path.join(GOLDEN, "optimizer_hyperparameters.json")))
+    sig = inspect.signature(O.adamw_step).parameters
+    assert tuple(sig["betas"].default) == tuple(g["betas"])
+    assert sig["eps"].default == g["eps"] and sig["weight_decay"].default == g["weight_decay"]
+    assert inspect.signature(O.clip_coef).parameters["max_norm"].default == g["grad_norm_clip"]
+    from grad_lmce_microstep_gb300 import lmce as M
+    bs = inspect.signature(M.Lmce.adamw).parameters
+    assert tuple(bs["betas"].default) == tuple(g["betas"])
+    assert bs["eps"].default == g["eps"] and bs["weight_decay"].default == g["weight_decay"]
+    assert inspect.signature(M.clip_coef).parameters["max_norm"].default == g["grad_norm_clip"]
