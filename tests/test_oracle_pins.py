@@ -493,3 +493,66 @@ def test_optimizer_defaults_are_the_pages():
     assert tuple(bs["betas"].default) == tuple(g["betas"])
     assert bs["eps"].default == g["eps"] and bs["weight_decay"].default == g["weight_decay"]
     assert inspect.signature(M.clip_coef).parameters["max_norm"].default == g["grad_norm_clip"]
+
+
+def test_adamw_gradient_scale_invariance():
+    # with eps = 0 and no decay, Adam's step does not change when every gradient is multiplied by
+    # the same positive constant (m scales by c, sqrt(v) by c); a moment update that mixes the
+    # two moments, or a bias correction applied to one side only, breaks this
+    rng = np.random.default_rng(15)
+    shape = (5, 6)
+    p0 = rng.standard_normal(shape)
+    gs = [rng.standard_normal(shape) for _ in range(4)]
+    out = []
+    for c in (1.0, 37.0, 1e-3):
+        p, m, v = p0.copy(), np.zeros(shape), np.zeros(shape)
+        for t, g in enumerate(gs, start=1):
+            p, m, v = O.adamw_step(p, m, v, c * g, t, 1e-2, (0.9, 0.95), 0.0, 0.0)
+        out.append(p)
+    np.testing.assert_allclose(out[1], out[0], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(out[2], out[0], rtol=1e-12, atol=1e-14)
+
+
+def test_adamw_clip_equals_prescaled_gradient():
+    # the clip coefficient multiplies the gradient before both moments
+    rng = np.random.default_rng(16)
+    p, m, v, g = (rng.standard_normal((4, 3)) for _ in range(4))
+    v = np.abs(v)
+    a = O.adamw_step(p, m, v, g, 3, 1e-3, clip=0.25)
+    b = O.adamw_step(p, m, v, 0.25 * g, 3, 1e-3, clip=1.0)
+    for x, y in zip(a, b):
+        np.testing.assert_allclose(x, y, rtol=1e-15, atol=0)
+
+
+def test_head_invariants_property():
+    # random small problems: shifting every vocabulary row of W by one vector u moves each row's
+    # logits by a constant, so the loss and dh do not move; the vocabulary rows of dW add up to
+    # the zero vector (softmax-minus-one-hot rows sum to zero); both normalisations
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+
+    @hyp.settings(max_examples=25, deadline=None)
+    @hyp.given(C=st.integers(1, 6), V=st.integers(2, 9), n1=st.integers(1, 7), n2=st.integers(0, 5),
+               seed=st.integers(0, 10 ** 6), micro=st.booleans())
+    def check(C, V, n1, n2, seed, micro):
+        rng = np.random.default_rng(seed)
+        W = rng.standard_normal((V, C))
+        mbs = []
+        for n in (n1, n2):
+            h = rng.standard_normal((n, C))
+            y = rng.integers(0, V, n)
+            if n > 1:
+                y[rng.integers(0, n)] = O.IGNORE_ID
+            mbs.append((h, y))
+        if all(O.count_valid(y, V) == 0 for _, y in mbs):
+            return
+        norm = "micro_mean" if micro else "global"
+        r = O.step(mbs, W, norm=norm)
+        u = rng.standard_normal(C)
+        r2 = O.step(mbs, W + u, norm=norm)
+        assert abs(r2.loss_sum - r.loss_sum) <= 1e-9 * max(1.0, abs(r.loss_sum))
+        for a, b in zip(r.micro, r2.micro):
+            np.testing.assert_allclose(b.dh, a.dh, rtol=1e-9, atol=1e-11)
+        np.testing.assert_allclose(r.dW.sum(axis=0), 0.0, atol=1e-12)
+
+    check()
