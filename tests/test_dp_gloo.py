@@ -1,4 +1,4 @@
-"""Data-parallel host logic on two CPU ranks (gloo, world size 2).
+"""Data-parallel host logic on CPU ranks (gloo, world size 2 and 3).
 
 Each rank runs the float64 oracle on its shard of rows with the globally reduced
 valid count, then SUM-reduces dW and (loss_sum, count) through the library's dp
@@ -77,28 +77,31 @@ def _worker(rank, world, port, out):
         dW2, dg, db = torch.tensor(rl.head.dW), torch.tensor(rl.dgamma), torch.tensor(rl.dbeta)
         dp.reduce_step(dW2, rl.head.loss_sum, rl.head.count, extra=(dg, db))
         res["ln"] = (dW2.numpy(), dg.numpy(), db.numpy())
-        # the two-GPU worked example: per-rank micro-mean objectives, averaged
-        g = json.load(open(os.path.join(GOLDEN, "p5_worked_examples.json")))["two_gpu"]
-        W2 = np.array([[1.0], [0.0]])
-        rows = []
-        for l in g["rank_token_losses_per_micro_step"][rank]:
-            d = np.array([math.log(math.exp(L) - 1.0) for L in l])
-            rows.append((d[:, None], np.ones(len(l), dtype=np.int64)))
-        obj = O.step(rows, W2, norm="micro_mean").objective
-        t = torch.tensor([obj], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.SUM)
-        res["p5_avg"] = t.item() / world
+        if world == 2:
+            # the two-GPU worked example: per-rank micro-mean objectives, averaged
+            g = json.load(open(os.path.join(GOLDEN, "p5_worked_examples.json")))["two_gpu"]
+            W2 = np.array([[1.0], [0.0]])
+            rows = []
+            for l in g["rank_token_losses_per_micro_step"][rank]:
+                d = np.array([math.log(math.exp(L) - 1.0) for L in l])
+                rows.append((d[:, None], np.ones(len(l), dtype=np.int64)))
+            obj = O.step(rows, W2, norm="micro_mean").objective
+            t = torch.tensor([obj], dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.SUM)
+            res["p5_avg"] = t.item() / world
         out[rank] = res
     finally:
         dist.destroy_process_group()
 
 
-def test_two_rank_sum_reduction_matches_single_process():
+@pytest.mark.parametrize("world", [2, 3])
+def test_sum_reduction_matches_single_process(world):
+    # world 3 shards every 10-row micro-batch unevenly (4, 3, 3 rows)
     ctx = mp.get_context("spawn")
     mgr = ctx.Manager()
     out = mgr.dict()
     port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, 2, port, out)) for r in range(2)]
+    procs = [ctx.Process(target=_worker, args=(r, world, port, out)) for r in range(world)]
     for p in procs:
         p.start()
     for p in procs:
@@ -107,13 +110,14 @@ def test_two_rank_sum_reduction_matches_single_process():
     W, mbs = _problem()
     whole = O.step(mbs, W, norm="global")
     g = json.load(open(os.path.join(GOLDEN, "p5_worked_examples.json")))["two_gpu"]
-    for r in range(2):
+    for r in range(world):
         res = out[r]
         assert np.abs(res["dW"] - whole.dW).max() < 1e-14
         assert res["loss_sum"] == pytest.approx(whole.loss_sum, rel=1e-13)
         assert res["count"] == whole.count
         assert res["objective"] == pytest.approx(whole.objective, rel=1e-13)
-        assert res["p5_avg"] == pytest.approx(g["ddp_average"], rel=1e-12)
+        if world == 2:
+            assert res["p5_avg"] == pytest.approx(g["ddp_average"], rel=1e-12)
         gamma, beta = _ln_params(W.shape[1])
         wl = O.step_ln([(h * 1.3 + 0.2, y) for h, y in mbs], gamma, beta, W, "layernorm", 1e-5)
         dW2, dg, db = res["ln"]
