@@ -104,3 +104,16 @@ def test_binding_fails_loudly_without_the_library_or_a_device(tmp_path):
             M._lib = saved
     with pytest.raises(ValueError):
         M.Lmce(64, 65, 16, torch.zeros(65, 64), "fp32")
+
+
+def test_cuda_failure_reaches_the_caller_as_a_status(lib):
+    # a host-side fault: on a machine without a usable device the runtime call in lmce_create
+    # fails, and the library returns LMCE_ERR_CUDA with no handle instead of crashing
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    cfg = M.Config(768, 50304, 1024, 0, -100, 0, 1, 0, 0)
+    h = ctypes.c_void_p(123)
+    assert lib.lmce_create(ctypes.byref(cfg), ctypes.c_void_p(256), ctypes.byref(h)) == M.ERR_CUDA
+    assert h.value is None
+    assert M.status_string(M.ERR_CUDA) != "unknown status"
