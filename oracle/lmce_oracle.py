@@ -369,11 +369,3 @@ def adamw_step(p, m, v, g, step: int, lr: float, betas=(0.9, 0.95), eps: float =
     p = p * (1.0 - lr * weight_decay) - lr * mhat / (np.sqrt(vhat) + eps)
     return p, m, v
 
-
-# ---------------------------------------------------------------------------
-# Closed forms used as pins
-# ---------------------------------------------------------------------------
-
-def uniform_loss(V: int) -> float:
-    """Loss of a row whose logits are all equal: -log(1/V) = log V (GPT-2 page, section 7)."""
-    return math.log(V)
