@@ -216,6 +216,11 @@ __global__ void __launch_bounds__(AW_T) adamw_kernel(const float* __restrict__ g
 
 }  // namespace
 
+cudaError_t finish_load_kernel() {
+  cudaFuncAttributes fa;
+  return cudaFuncGetAttributes(&fa, finish_kernel);
+}
+
 cudaError_t launch_finish(const StepArgs& a, const Scratch& s, int64_t nparts, Launch& L, int mode) {
   L.begin(K_FINISH);
   finish_kernel<<<1, FIN_T, 0, L.st>>>(s.part_loss, s.part_cnt, s.part_err, nparts, a.norm, a.G,
@@ -245,6 +250,7 @@ struct lmce_handle {
     float* rstd;       // [max_N]
     float* part;       // [2][ln_part_rows()][C]
   } ln;
+  int64_t test_stall_ns;  // lmce_test_stall_next_microstep: armed for the next micro-step, then cleared
   int attempted;       // micro-steps accepted since create/finalize
   int64_t launches;
   Prof prof;
@@ -419,6 +425,8 @@ int run_microstep(lmce_handle* h, const void* hidden, const void* W, const int32
   a.beta = write_dW ? 0 : 1;
   a.bf16 = c.dtype == LMCE_BF16;
   a.tc_two_pass = h->path == LMCE_PATH_TCGEN05_TWO_PASS;
+  a.test_stall_ns = h->test_stall_ns;
+  h->test_stall_ns = 0;
   if (N == 0) {
     // An empty micro-step still counts; the first one of a step leaves dW = 0.
     if (write_dW && cudaMemsetAsync(h->dW, 0, sizeof(float) * (size_t)c.V * c.C, st) != cudaSuccess)
@@ -735,6 +743,13 @@ extern "C" const char* lmce_status_string(int s) {
     case LMCE_ERR_STATE: return "call out of order";
     default: return "unknown status";
   }
+}
+
+extern "C" int lmce_test_stall_next_microstep(lmce_handle* h, int64_t wait_ns) {
+  if (!h || wait_ns <= 0 || wait_ns > 1000000000LL) return LMCE_ERR_ARG;
+  if (h->path == LMCE_PATH_SIMT) return LMCE_ERR_STATE;
+  h->test_stall_ns = wait_ns;
+  return LMCE_OK;
 }
 
 extern "C" int64_t lmce_launch_count(const lmce_handle* h) { return h ? h->launches : 0; }

@@ -90,6 +90,8 @@ struct StepArgs {
   int32_t beta;           // 0: dW = grad, 1: dW += grad
   int32_t bf16;           // 1: dtype bf16, 0: fp32
   int32_t tc_two_pass;    // tensor-core path: 1 = separate logsumexp pass, 0 = one-pass lse + dh
+  int64_t test_stall_ns = 0;  // failure-detection test: > 0 makes the tensor-core gradient launches
+                              // start no operand load and bounds their waits by this many ns
 };
 
 // Library-owned device scratch.
@@ -167,6 +169,8 @@ cudaError_t ln_backward(const LnArgs& a, Launch& L);
 //   FIN_LOSS : loss and error partials, with the scale FIN_COUNT set
 enum FinMode { FIN_ALL = 0, FIN_COUNT = 1, FIN_LOSS = 2 };
 cudaError_t launch_finish(const StepArgs& a, const Scratch& s, int64_t nparts, Launch& L, int mode = FIN_ALL);
+// Loads the module that holds the reduction kernel (no launch).
+cudaError_t finish_load_kernel();
 
 // SIMT path (fp32 FFMA).
 int64_t simt_parts(int64_t N);
@@ -174,6 +178,8 @@ size_t simt_grad_smem(int64_t C);
 cudaError_t simt_microstep(const StepArgs& a, const Scratch& s, Launch& L);
 // The two gradient passes alone (lse and the scale already on the device).
 cudaError_t simt_grads(const StepArgs& a, const Scratch& s, Launch& L);
+// Loads the module of every SIMT kernel for both dtypes (no launch).
+cudaError_t simt_load_kernels();
 // Exact logsumexp and dh of the rows of the 128-token tiles whose flag is set (every other
 // block returns at once): the repair of the one-pass logsumexp + dh kernel.
 constexpr int TC_TILE_ROWS = 128;

@@ -7,6 +7,8 @@
 // with the SIMT kernels, taking the per-row logsumexp, the per-block loss/count partials
 // and the step accumulators from a fixed array compiled into this library instead of from
 // lmce_create's allocations.  The caller still passes every input and output buffer.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <mutex>
 
 #include "lmce.h"
@@ -31,26 +33,58 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[NA_BYTES];
 
 constexpr int NA_MAX_DEV = 64;
 std::mutex g_mu;
-unsigned char* g_addr[NA_MAX_DEV] = {};
+// Per device: the context whose modules were loaded for this entry point (see setup()).
+struct DevState {
+  bool arch_ok;
+  bool loaded;
+  CUcontext ctx;
+};
+DevState g_dev[NA_MAX_DEV] = {};
 
-// Once per device, with that device current: check the architecture and look up the
-// device address of the scratch array (its name in host code is only a stand-in).
+PFN_cuCtxGetCurrent_v4000 ctx_fn() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+  });
+  return fn;
+}
+
+// With the caller's device current: check its architecture once, look up the device address
+// of the scratch array (its name in host code is only a stand-in) on every call, so a device
+// reset that moves the array is followed, and load every module this entry point launches
+// from once per context.  With lazy module loading a module is loaded, and device memory
+// allocated for its code, at the first launch of one of its kernels; loading them here keeps
+// every later call free of allocations, whatever dtype or size it has.
 int setup(unsigned char** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return LMCE_ERR_CUDA;
   if (dev < 0 || dev >= NA_MAX_DEV) return LMCE_ERR_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_addr[dev]) {
+  DevState& d = g_dev[dev];
+  if (!d.arch_ok) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return LMCE_ERR_CUDA;
     if (major != 10 || minor != 3) return LMCE_ERR_ARCH;
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return LMCE_ERR_CUDA;
-    g_addr[dev] = static_cast<unsigned char*>(p);
+    d.arch_ok = true;
   }
-  *out = g_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return LMCE_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  PFN_cuCtxGetCurrent_v4000 f = ctx_fn();
+  if (!f || f(&ctx) != CUDA_SUCCESS || !ctx) return LMCE_ERR_CUDA;
+  if (!d.loaded || d.ctx != ctx) {
+    if (simt_load_kernels() != cudaSuccess || finish_load_kernel() != cudaSuccess) return LMCE_ERR_CUDA;
+    d.loaded = true;
+    d.ctx = ctx;
+  }
+  *out = static_cast<unsigned char*>(p);
   return LMCE_OK;
 }
 
@@ -71,11 +105,14 @@ extern "C" int lmce_microstep_noalloc(const lmce_config* cfg, const void* hidden
   if (cfg->path != LMCE_PATH_AUTO && cfg->path != LMCE_PATH_SIMT) return LMCE_ERR_ARG;
   if (N < 0 || N > NA_MAX_N || simt_parts(N) > NA_PARTS) return LMCE_ERR_ARG;
   if (N > 0 && (!hidden || !W || !targets || !dh)) return LMCE_ERR_ARG;
+  const size_t esz = cfg->dtype == LMCE_BF16 ? 2 : 4;
+  if (N > 0 && (((uintptr_t)hidden | (uintptr_t)W | (uintptr_t)dh) & (esz - 1))) return LMCE_ERR_ARG;
+  if (((uintptr_t)dW & 3) || ((uintptr_t)targets & 3) || ((uintptr_t)row_loss & 3)) return LMCE_ERR_ARG;
+  if (((uintptr_t)loss_sum_out & 7) || ((uintptr_t)valid_count_out & 7)) return LMCE_ERR_ARG;
   unsigned char* base = nullptr;
   int st = setup(&base);
   if (st != LMCE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  const size_t esz = cfg->dtype == LMCE_BF16 ? 2 : 4;
   Scratch sc;
   sc.lse = reinterpret_cast<float*>(base + OFF_LSE);
   sc.part_loss = reinterpret_cast<double*>(base + OFF_PLOSS);

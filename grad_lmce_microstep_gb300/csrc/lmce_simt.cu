@@ -336,4 +336,17 @@ cudaError_t simt_repair_dh(const StepArgs& a, const Scratch& sc, Launch& L) {
   return cudaGetLastError();
 }
 
+// Loads the module of every SIMT kernel, both dtypes (with lazy module loading a module is
+// otherwise loaded, and its device memory allocated, at the first launch of one of its kernels).
+cudaError_t simt_load_kernels() {
+  cudaFuncAttributes fa;
+  cudaError_t e;
+  if ((e = cudaFuncGetAttributes(&fa, simt_lse_kernel<float>)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, simt_lse_kernel<__nv_bfloat16>)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, simt_grad_kernel<float, true>)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, simt_grad_kernel<float, false>)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, simt_grad_kernel<__nv_bfloat16, true>)) != cudaSuccess) return e;
+  return cudaFuncGetAttributes(&fa, simt_grad_kernel<__nv_bfloat16, false>);
+}
+
 }  // namespace lmce

@@ -25,6 +25,9 @@ namespace {
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s: any wait longer than this is an error
+// A gradient kernel that gave up waits this long for the MMAs it already issued before it
+// releases TMEM, whatever its own wait limit.
+constexpr uint64_t DRAIN_NS = 2000000000ull;
 
 
 // ---- pass 1 geometry -----------------------------------------------------------------
@@ -334,16 +337,20 @@ __global__ void __launch_bounds__(256) tc_combine_kernel(const float* __restrict
 //
 // The lse+dh pass needs no logsumexp beforehand.  It is the online softmax of flash
 // attention with the stale-maximum rule of FlashAttention-4 taken to its end: each token
-// column's base-2 reference m_n is fixed once, as the exact maximum over the first block of
-// the pair's range (agreed between the two CTAs over DSMEM), and never moved.  The operand
-// is p = 2^(z log2 e - m_n) and the epilogue also sums p per column (a butterfly over the 32
-// rows of a warp, kept in two registers per lane), so at the end of the range
+// column's base-2 reference m_n is fixed once, FL_HEADROOM above the exact maximum over the
+// first block of the pair's range (agreed between the two CTAs over DSMEM), and never moved.
+// The operand is p = 2^(z log2 e - m_n) and the epilogue also sums p per column (a butterfly
+// over the 32 rows of a warp, kept in two registers per lane), so at the end of the range
 //   acc^T[c][n] = sum_v W[v][c] p[n][v],   l_n = sum_v p[n][v],
 //   dh_n = s (acc^T[.][n] / l_n - W[y_n]),   lse_n = (m_n + log2 l_n) ln 2.
 // An element above m_n + fl_limit flags its 128-token tile, and the host then runs the exact
 // two-pass repair on flagged tiles only.  fl_limit = 115 - ceil(log2 V) keeps every sum finite:
 // l_n <= V 2^fl_limit <= 2^115 and |acc^T| <= 2^115 max|W| < 2^128 for any |W| < 8192 (99 at
-// V = 50304).  A tighter guard would send ordinary wide-logit rows through the repair.
+// V = 50304).  The headroom moves the guard to FL_HEADROOM + fl_limit above the first block's
+// maximum (131 at V = 50304; the widest rows of the logit-stress workload, 1 % of tokens x40,
+// reach 100 above it).  It costs nothing in precision: p of the block maximum is 2^-FL_HEADROOM,
+// far inside fp32 and bf16 range, and the terms that underflow (p < 2^-126) lie more than
+// 126 - FL_HEADROOM = 94 below that maximum, a relative weight under 2^-94.
 constexpr int G_XT = 128;                  // X rows per pair (64 per CTA)
 constexpr int G_YB = 256;                  // stream rows per block (128 per CTA)
 constexpr int G_DZ = G_YB * 128;           // one dz buffer: 256 K-rows x 64 bf16 = 32 KB
@@ -351,6 +358,7 @@ constexpr int G_EPI_WARPS = 8;
 constexpr int G_THREADS = 96 + 32 * G_EPI_WARPS;   // warps 0 and 10 TMA, 1 MMA, 2-9 epilogue
 
 enum GradMode { GM_DW = 0, GM_DH = 1, GM_FL = 2 };
+constexpr float FL_HEADROOM = 32.f;        // lse+dh pass: reference above the first block's maximum (base 2)
 
 // Ring geometry per mode: NST slots of SLOT bytes.  An S stage carries SK 64-column atoms of
 // K = C (per CTA: 128 stream rows, then 64 X rows at SK * 16 KB); an accumulation stage
@@ -386,6 +394,8 @@ struct GradParams {
   int ch0, nch;          // 256-row C chunks [ch0, ch0 + nch) of acc^T handled by this launch (nch <= 3)
   int beta;              // dW pass: 0 writes, 1 adds
   float fl_limit;        // lse+dh pass: largest base-2 exponent of p kept (115 - ceil(log2 V))
+  uint64_t wait_ns;      // limit of every bounded wait (WAIT_NS; shorter in the failure-detection test)
+  int stall;             // failure-detection test: the producers start no load
 };
 
 __device__ __forceinline__ float grad_scale(const GradParams& p) {
@@ -453,6 +463,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
+  const uint64_t wait_ns = p.wait_ns;
   const int nX = DW ? p.V : p.N;
   const int nY = DW ? p.N : p.V;
   const int nblk = (nY + G_YB - 1) / G_YB;
@@ -519,14 +530,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           const bool sphase = j < nb && u < KC;
           bool w = true;
           if (lane == 0) {
-            w = mbar_wait(smem_u32(&empty[st]), ((it / NST) & 1) ^ 1, WAIT_NS);
+            w = mbar_wait(smem_u32(&empty[st]), ((it / NST) & 1) ^ 1, wait_ns);
             if (!w) record_timeout(p.err, 17);
             else if (rank == 0) mbar_expect_tx(smem_u32(&full[st]), sphase ? 2 * SK * 24576 : 2 * AQ * 16384 * NCH);
           }
           if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
           const uint32_t dst = smem_u32(sY) + st * SLOT;
           const uint32_t bar = lead_full + st * 8;
-          if (sphase) {
+          if (p.stall) {
+            // failure-detection test: no load starts, so every wait on this stage runs out
+          } else if (sphase) {
             // S phase of block b0+j: my 128 stream rows and my 64 X rows, SK atoms of K from 64 SK u
             if (lane == 0) tma_load_3d_cg2(dst, &tmYs, bar, 0, (b0 + j) * G_YB + (int)rank * 128, u * SK);
             else if (lane == 1) tma_load_3d_cg2(dst + SK * 16384, &tmX, bar, 0, x0 + (int)rank * 64, u * SK);
@@ -547,7 +560,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       // The whole warp runs the loop (warp-uniform descriptors); every wait is polled by all
       // lanes and decided together; elect.sync picks the one lane that issues MMAs and commits.
       auto wait_w = [&](uint32_t bar, uint32_t parity, bool cluster, unsigned where) -> bool {
-        const bool w = cluster ? mbar_wait_cluster(bar, parity, WAIT_NS) : mbar_wait(bar, parity, WAIT_NS);
+        const bool w = cluster ? mbar_wait_cluster(bar, parity, wait_ns) : mbar_wait(bar, parity, wait_ns);
         const bool all = __all_sync(0xffffffffu, w);
         if (!all && lane == 0) record_timeout(p.err, where);
         return all;
@@ -641,7 +654,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       if (!ok) {
         // give up: wait (bounded) for the MMAs already issued before TMEM is released
         mma_commit2_elect(smem_u32(&drain_bar));
-        mbar_wait(smem_u32(&drain_bar), 0, WAIT_NS);
+        mbar_wait(smem_u32(&drain_bar), 0, DRAIN_NS);
       }
     }
   } else if (warp <= 9) {
@@ -724,7 +737,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             }
           }
         }
-        if (!mbar_wait(smem_u32(&s_full), gb & 1, WAIT_NS)) {
+        if (!mbar_wait(smem_u32(&s_full), gb & 1, wait_ns)) {
           record_timeout(p.err, 25);
           epi_abort = 1;
         }
@@ -757,14 +770,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           // columns past the vocabulary (last block only) carry no term
           const int nvalid = min(64, p.V - (ys0 + ks * 64));
           if (j == 0) {
-            // reference m: the exact maximum of my row over this first block (four quarters)
+            // reference m: FL_HEADROOM above the exact maximum of my row over this first block
+            // (four quarters)
             float mx = -INFINITY;
 #pragma unroll
             for (int e = 0; e < 64; ++e)
               if (e < nvalid) mx = fmaxf(mx, z[e]);
             fl_red[ks][xr] = mx;
             asm volatile("bar.sync 1, 256;" ::: "memory");
-            m2 = fmaxf(fmaxf(fl_red[0][xr], fl_red[1][xr]), fmaxf(fl_red[2][xr], fl_red[3][xr])) * LOG2E;
+            m2 = fmaf(fmaxf(fmaxf(fl_red[0][xr], fl_red[1][xr]), fmaxf(fl_red[2][xr], fl_red[3][xr])), LOG2E,
+                      FL_HEADROOM);
           }
           // my row's target logit, when its column falls in my quarter of this block
           const int tq = yrow - (ys0 + ks * 64);
@@ -819,7 +834,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         }
         // dz buffer db is free once the accumulation NDZ blocks back has completed
         const int db = gb % NDZ;
-        if (!mbar_wait(smem_u32(&dz_empty[db]), ((gb / NDZ) & 1) ^ 1, WAIT_NS)) {
+        if (!mbar_wait(smem_u32(&dz_empty[db]), ((gb / NDZ) & 1) ^ 1, wait_ns)) {
           record_timeout(p.err, 26);
           epi_abort = 1;
         }
@@ -842,7 +857,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       // acted on only right after a barrier, so every epilogue thread takes the same branch
       const bool whole = b0 == 0 && nb == nblk;
       if (!DW && whole) wload(0);   // in flight while the last accumulation completes
-      if (!mbar_wait(smem_u32(&acc_full), sg & 1, WAIT_NS)) {
+      if (!mbar_wait(smem_u32(&acc_full), sg & 1, wait_ns)) {
         record_timeout(p.err, 27);
         epi_abort = 1;
       }
@@ -870,7 +885,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         asm volatile("bar.sync 1, 256;" ::: "memory");
         if (et == 0) {
           mbar_arrive_cluster(mapa(smem_u32(&lx_full), peer));
-          if (!mbar_wait_cluster(smem_u32(&lx_full), sg & 1, WAIT_NS)) {
+          if (!mbar_wait_cluster(smem_u32(&lx_full), sg & 1, wait_ns)) {
             record_timeout(p.err, 30);
             epi_abort = 1;
           }
@@ -1392,6 +1407,8 @@ cudaError_t tc_grad_range(const StepArgs& a, const Scratch& sc, Launch& L, int c
   p.ch0 = ch0;
   p.nch = nch;
   p.beta = a.beta;
+  p.wait_ns = a.test_stall_ns > 0 ? (uint64_t)a.test_stall_ns : WAIT_NS;
+  p.stall = a.test_stall_ns > 0 ? 1 : 0;
   const int nblk = (int)((nY + G_YB - 1) / G_YB);
   const int T = (int)((nX + G_XT - 1) / G_XT);
   const long long U = (long long)T * nblk;

@@ -34,7 +34,7 @@ TORCH_DTYPES = {"bf16": torch.bfloat16, "fp32": torch.float32}
 EXPORTS = ("lmce_create", "lmce_microstep", "lmce_finalize", "lmce_destroy", "lmce_status_string",
            "lmce_launch_count", "lmce_selected_path", "lmce_profile", "lmce_profile_read",
            "lmce_microstep_noalloc", "lmce_dw_sumsq", "lmce_adamw", "lmce_microstep_compact",
-           "lmce_microstep_ln", "lmce_microstep_ln_compact")
+           "lmce_microstep_ln", "lmce_microstep_ln_compact", "lmce_test_stall_next_microstep")
 
 NOALLOC_MAX_N = 65536
 
@@ -104,6 +104,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.lmce_profile_read.restype = i32
     L.lmce_microstep_noalloc.argtypes = [ctypes.POINTER(Config), vp, vp, vp, i64, i64, vp, vp, i32, vp, vp, vp, vp]
     L.lmce_microstep_noalloc.restype = i32
+    L.lmce_test_stall_next_microstep.argtypes = [vp, i64]
+    L.lmce_test_stall_next_microstep.restype = i32
     _lib = L
     return L
 
@@ -296,6 +298,11 @@ class Lmce:
                                  float(clip), _stream(stream))
         if st != OK:
             raise LmceError(st, "lmce_adamw")
+
+    def test_stall_next_microstep(self, wait_ns: int) -> int:
+        """Failure-detection test hook: the next micro-step's tensor-core gradient launches start
+        no load and give up after wait_ns (lmce_finalize then reports LMCE_ERR_CUDA)."""
+        return int(self.lib.lmce_test_stall_next_microstep(self.handle, int(wait_ns)))
 
     def profile(self, enable: bool):
         """Record CUDA events around every kernel launch (enable=True clears old records)."""

@@ -271,6 +271,19 @@ LMCE_API int64_t lmce_launch_count(const lmce_handle* h);
  * the path micro-steps run. */
 LMCE_API int lmce_selected_path(const lmce_handle* h);
 
+/*
+ * lmce_test_stall_next_microstep -- failure-detection test hook (not part of a training
+ * step).  Arms the next micro-step of this handle so that its tensor-core gradient launches
+ * start no operand load and bound every wait by `wait_ns` nanoseconds (0 < wait_ns <= 1 s)
+ * instead of the normal 2 s.  Their waits then run out: each kernel records a timeout in the
+ * step's error word, waits for the MMAs it issued, releases its tensor memory and returns,
+ * and the context stays usable.  lmce_finalize reports the step as LMCE_ERR_CUDA; the
+ * step's outputs are undefined.  One micro-step only; the hook then disarms itself.
+ * Errors: LMCE_ERR_ARG (null handle, wait_ns out of range), LMCE_ERR_STATE (the handle runs
+ *         the SIMT path, whose kernels have no such waits).
+ */
+LMCE_API int lmce_test_stall_next_microstep(lmce_handle* h, int64_t wait_ns);
+
 /* ---- kernel timing (benchmark instrumentation) --------------------------------------
  * When enabled, the library records a CUDA event pair around every kernel it launches
  * (on the stream the kernel runs on) so that per-kernel device time can be read back.
@@ -314,12 +327,20 @@ LMCE_API int lmce_profile_read(lmce_handle* h, int kind, double* total_ms, int64
  *   loss_sum_out    : device double, or NULL: this micro-step's summed loss
  *   valid_count_out : device int64, or NULL: this micro-step's valid targets
  * Limits: N <= LMCE_NOALLOC_MAX_N; a larger N returns LMCE_ERR_ARG before anything is
- * enqueued.  Out-of-range targets are treated as ignored but not reported here.
- * The first call on a device sets up that device (looks up the array's device address
- * with that device current), so make it before any stream capture.  Every call on a device
- * shares the one array and it keeps the last call's contents (the accumulators are cleared
- * by each call); calls whose work overlaps on the GPU -- on different streams, or from
- * different host threads -- race on it and must be serialised by the caller.
+ * enqueued.  hidden, W and dh must be aligned to their element size, the other pointers to
+ * theirs (LMCE_ERR_ARG otherwise).
+ * Errors found on the device are not returned by this call: an out-of-range target is
+ * treated as ignored (it is left out of *valid_count_out, so a caller that knows its own
+ * count can compare), and a non-finite loss shows as a non-finite *loss_sum_out.
+ * Set-up: the first call on a device (more exactly, on a CUDA context: again after a device
+ * reset) loads the code of every kernel this entry point launches, for both dtypes.  It is
+ * the only call that may load code; later calls allocate nothing, whatever their dtype or
+ * size.  Make it before any stream capture.  Each call looks the array's device address up
+ * again with the device current, so a reset that moves the array is followed.
+ * Every call on a device shares the one array and it keeps the last call's contents (the
+ * accumulators are cleared by each call); calls whose work overlaps on the GPU -- on
+ * different streams, or from different host threads -- race on it and must be serialised
+ * by the caller.
  * Errors: LMCE_ERR_ARG, LMCE_ERR_ARCH, LMCE_ERR_NO_VALID (GLOBAL norm with
  *         global_valid <= 0: dh zeroed, dW untouched), LMCE_ERR_CUDA.
  */

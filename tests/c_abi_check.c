@@ -39,6 +39,7 @@ int main(void) {
   expect("adamw", lmce_adamw(NULL, NULL, NULL, NULL, NULL, 1, 1e-3f, 0.9f, 0.95f, 1e-8f, 0.1f, 1.0f, NULL),
          LMCE_ERR_ARG);
   expect("profile", lmce_profile(NULL, 1), LMCE_ERR_ARG);
+  expect("test_stall_next_microstep", lmce_test_stall_next_microstep(NULL, 1000000), LMCE_ERR_ARG);
   expect("destroy(NULL)", lmce_destroy(NULL), LMCE_OK);
   if (lmce_status_string(LMCE_OK) == NULL || lmce_launch_count(NULL) != 0 || lmce_selected_path(NULL) != -1) {
     printf("status / count / path queries\n");

@@ -68,9 +68,10 @@ def test_logit_stress_small(path):
 
 def test_lse_dh_repair_of_out_of_range_tiles():
     # One vocabulary row aligned with one token's hidden state: that token's logit there is
-    # ~0.5 |h|^2 ~ 128 nats above its first-block maximum, beyond the one-pass kernel's range
-    # (2^(115 - ceil(log2 V)) = 2^105 at V = 1000), so its 128-token tile is flagged and
-    # recomputed by the exact repair; without the repair that row's dh and loss would be inf.
+    # ~0.5 |h|^2 ~ 128 nats (~185 in base 2) above its first-block maximum, beyond the one-pass
+    # kernel's range (a headroom of 32 plus 115 - ceil(log2 V) = 105 at V = 1000, so 137 in
+    # base 2), so its 128-token tile is flagged and recomputed by the exact repair; without the
+    # repair that row's dh and loss would be inf.
     w = I.custom([300, 173], 256, 1000, "bf16", seed=11)
     h5 = w.micro[0][0][5].float()
     w.W[700] = (0.5 * h5).to(w.W.dtype)
@@ -83,15 +84,18 @@ def test_lse_dh_repair_of_out_of_range_tiles():
         assert_parity(got, ref, "bf16")
 
 
-def test_lse_dh_wide_logit_within_range():
-    # a logit ~60 nats (~87 in base 2) above the token's first-block maximum: inside the one-pass
-    # kernel's range at V = 1000 (105), so no repair runs and the one-pass sums must hold it
+@pytest.mark.parametrize("nats", [60.0, 88.0])
+def test_lse_dh_wide_logit_within_range(nats):
+    # a logit ~60 nats (~87 in base 2) or ~88 nats (~127) above the token's first-block maximum:
+    # inside the one-pass kernel's range at V = 1000 (137 in base 2 with the headroom), so no
+    # repair runs and the one-pass sums must hold it; 88 nats lies beyond the range the kernel
+    # had without the headroom (105)
     w = I.custom([300, 173], 256, 1000, "bf16", seed=13)
     h5 = w.micro[0][0][5].float()
-    w.W[700] = (60.0 / float(h5 @ h5) * h5).to(w.W.dtype)
+    w.W[700] = (nats / float(h5 @ h5) * h5).to(w.W.dtype)
     w.micro[0][1][5] = 700
     ref = run_oracle(w)
-    assert 55.0 < ref.micro[0].lse[5] < 65.0
+    assert nats - 5.0 < ref.micro[0].lse[5] < nats + 5.0
     for path in ("tcgen05", "tcgen05_two_pass"):
         got = run_lib(w, path=path)
         assert got["status"] == M.OK
