@@ -17,6 +17,7 @@ from grad_lmce_microstep_gb300 import inputs as I
 from grad_lmce_microstep_gb300 import lmce as M
 from oracle import lmce_oracle as O
 
+import sched_util as S
 from gpu_util import GRAD_REL, LOSS_REL
 
 pytestmark = pytest.mark.gpu
@@ -62,6 +63,20 @@ def _check_dW_rows(w, dW, scales, rng, lses, extra=()):
     assert np.abs(got - want).max() <= tol, np.abs(got - want).max() / np.abs(want).max()
 
 
+def _split_rows(w, compact=False):
+    """Per micro-step, the token rows at the edges of the lse+dh pass's split tiles (in the
+    input's row numbering), and the vocabulary rows at the edges of the dW pass's split tiles."""
+    pairs = S.pairs_on_device()
+    tok, voc = [], set()
+    for h, y in w.micro:
+        valid = np.nonzero(O.target_status(y, w.V, w.ignore_id)[0])[0]
+        n = len(valid) if compact else y.numel()
+        rows = S.split_tile_edge_rows(n, w.V, pairs)
+        tok.append([int(valid[r]) for r in rows] if compact else rows)
+        voc.update(S.split_tile_edge_rows(w.V, n, pairs))
+    return tok, sorted(voc)
+
+
 def _oracle_totals(w):
     lses = [O.lse_all(h, w.W) for h, _ in w.micro]
     loss = 0.0
@@ -88,15 +103,18 @@ def test_full_size_head(name, compact):
     lses, loss = _oracle_totals(w)
     assert abs(ls - loss) <= LOSS_REL * abs(loss)
     assert abs(mean - loss / sum(counts)) <= LOSS_REL * abs(loss / sum(counts))
-    # rows from each micro-step, incl. the masked tail of the masked workload
+    # rows from each micro-step, incl. the masked tail of the masked workload, and the first and
+    # last row of every split tile of the lse+dh pass
+    tok, voc = _split_rows(w, compact)
     extra = (lambda k: [16383, 1023, 1024 * 16 - 1]) if name == "masked_unequal" else (lambda k: [0])
     if name == "padded_docs":   # the last token of a document and the first pad after it
         extra = lambda k: [r * 2048 + L + d for r, L in enumerate(w.meta["doc_lengths"][k][:3]) for d in (-1, 0)]
-    _check_rows(w, dhs, rls, scales, rng, extra)
-    # dW rows: random ones, the padded vocabulary tail and frequent targets
+    _check_rows(w, dhs, rls, scales, rng, lambda k: list(extra(k)) + tok[k])
+    # dW rows: random ones, the padded vocabulary tail, frequent targets and the edges of the dW
+    # pass's split tiles
     ys = np.concatenate([O.i64(y) for _, y in w.micro])
     top = np.bincount(ys[ys >= 0], minlength=w.V).argsort()[-4:].tolist()
-    _check_dW_rows(w, dW, scales, rng, lses, extra=top + [w.V - 1, 50257])
+    _check_dW_rows(w, dW, scales, rng, lses, extra=top + [w.V - 1, 50257] + voc)
 
 
 def test_full_batch_524k_sampled_and_closed_form():
@@ -105,7 +123,8 @@ def test_full_batch_524k_sampled_and_closed_form():
     dW, dhs, rls, (ls, cnt, mean, st) = _run(w)
     assert st == M.OK and cnt == 524288
     scales = O.micro_scales(w.valid_counts(), "global", w.G)
-    _check_rows(w, dhs, rls, scales, rng)
+    tok, voc = _split_rows(w)
+    _check_rows(w, dhs, rls, scales, rng, lambda k: tok[k])
     # the summed loss equals the sum of the per-row losses the library returned
     assert abs(ls - sum(float(r.double().sum()) for r in rls)) <= 1e-6 * abs(ls)
     del dhs, rls
@@ -120,7 +139,7 @@ def test_full_batch_524k_sampled_and_closed_form():
     hsum = np.zeros(w.C)
     for h, _ in w.micro:
         hsum += h.double().sum(0).numpy()
-    vs = np.array(sorted(set(rng.choice(w.V, 64, replace=False).tolist())))
+    vs = np.array(sorted(set(rng.choice(w.V, 64, replace=False).tolist()) | set(voc)))
     want = np.tile(s * hsum / w.V, (len(vs), 1))
     for h, y in w.micro:
         yy = O.i64(y)
@@ -142,8 +161,24 @@ def test_full_logit_stress():
     lses, loss = _oracle_totals(w)
     assert max(float(l.max()) for l in lses) > 60.0
     assert abs(ls - loss) <= LOSS_REL * abs(loss)
-    # include the x40 rows (largest norms) of every micro-step
-    norms = [h.float().norm(dim=1) for h, _ in w.micro]
-    big = [n.argsort(descending=True)[:8].tolist() for n in norms]
-    _check_rows(w, dhs, rls, scales, rng, extra=lambda k: big[k])
-    _check_dW_rows(w, dW, scales, rng, lses)
+    # The x40 rows of every micro-step, ranked by how far a logit rises above the one-pass
+    # kernel's reference (the first-block maximum of the segment that holds it): the eight
+    # closest to the kernel's range guard (32 + 115 - ceil(log2 V) in base 2), and every row of
+    # a tile that crosses it (flagged and recomputed by the exact repair).  Plus the edges of
+    # every split tile of both gradient passes.
+    pairs = S.pairs_on_device()
+    guard = 32 + 115 - math.ceil(math.log2(w.V))
+    near = []
+    for h, y in w.micro:
+        big = h.float().norm(dim=1).argsort(descending=True)[:w.meta["scaled_rows"]].numpy()
+        z = O.f64(h[torch.as_tensor(big)]) @ O.f64(w.W).T
+        ex = np.array([S.guard_excess(z[i], S.segment_first_blocks(h.shape[0], w.V, pairs, int(n) // S.XT))
+                       for i, n in enumerate(big)])
+        rows = big[np.argsort(-ex)[:8]].tolist()
+        for n in big[ex > guard]:
+            t0 = int(n) // S.XT * S.XT
+            rows += list(range(t0, min(t0 + S.XT, h.shape[0])))
+        near.append(rows)
+    tok, voc = _split_rows(w)
+    _check_rows(w, dhs, rls, scales, rng, extra=lambda k: near[k] + tok[k])
+    _check_dW_rows(w, dW, scales, rng, lses, extra=voc)
