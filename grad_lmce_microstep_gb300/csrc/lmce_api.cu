@@ -687,6 +687,13 @@ extern "C" int lmce_dw_sumsq(lmce_handle* h, double* sumsq, void* stream) {
   return LMCE_OK;
 }
 
+extern "C" int lmce_clip_coef(double sumsq, double max_norm, float* coef) {
+  if (!coef || !(sumsq >= 0.0) || !isfinite(sumsq) || !(max_norm > 0.0) || !isfinite(max_norm)) return LMCE_ERR_ARG;
+  const double c = max_norm / (sqrt(sumsq) + 1e-6);   // clip_grad_norm_'s guard against a zero norm
+  *coef = (float)(c < 1.0 ? c : 1.0);
+  return LMCE_OK;
+}
+
 extern "C" int lmce_adamw(lmce_handle* h, float* p, float* m, float* v, void* W_out, int64_t step, float lr,
                           float beta1, float beta2, float eps, float weight_decay, float clip, void* stream) {
   if (!h || !p || !m || !v || step < 1) return LMCE_ERR_ARG;

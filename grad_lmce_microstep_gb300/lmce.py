@@ -8,7 +8,6 @@ missing this module raises; there is no CPU fallback.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 
 import torch
@@ -34,7 +33,7 @@ TORCH_DTYPES = {"bf16": torch.bfloat16, "fp32": torch.float32}
 EXPORTS = ("lmce_create", "lmce_microstep", "lmce_finalize", "lmce_destroy", "lmce_status_string",
            "lmce_launch_count", "lmce_selected_path", "lmce_profile", "lmce_profile_read",
            "lmce_microstep_noalloc", "lmce_dw_sumsq", "lmce_adamw", "lmce_microstep_compact",
-           "lmce_microstep_ln", "lmce_microstep_ln_compact", "lmce_test_stall_next_microstep")
+           "lmce_microstep_ln", "lmce_microstep_ln_compact", "lmce_test_stall_next_microstep", "lmce_clip_coef")
 
 NOALLOC_MAX_N = 65536
 
@@ -104,6 +103,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.lmce_profile_read.restype = i32
     L.lmce_microstep_noalloc.argtypes = [ctypes.POINTER(Config), vp, vp, vp, i64, i64, vp, vp, i32, vp, vp, vp, vp]
     L.lmce_microstep_noalloc.restype = i32
+    L.lmce_clip_coef.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.POINTER(ctypes.c_float)]
+    L.lmce_clip_coef.restype = i32
     L.lmce_test_stall_next_microstep.argtypes = [vp, i64]
     L.lmce_test_stall_next_microstep.restype = i32
     _lib = L
@@ -111,12 +112,16 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
 
 
 def clip_coef(sumsq: float, max_norm: float = 1.0) -> float:
-    """Global-norm clip coefficient for lmce_adamw's `clip`: max_norm / (sqrt(sumsq) + 1e-6), at most 1.
+    """Global-norm clip coefficient for lmce_adamw's `clip` (lmce_clip_coef).
 
     sumsq is the sum of squares over every gradient of the model (lmce_dw_sumsq gives the tied
     matrix's share), as torch.nn.utils.clip_grad_norm_ computes it.
     """
-    return min(1.0, float(max_norm) / (math.sqrt(float(sumsq)) + 1e-6))
+    out = ctypes.c_float()
+    st = load().lmce_clip_coef(float(sumsq), float(max_norm), ctypes.byref(out))
+    if st != OK:
+        raise LmceError(st, "lmce_clip_coef")
+    return float(out.value)
 
 
 def status_string(status: int) -> str:

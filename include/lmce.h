@@ -123,7 +123,12 @@ LMCE_API int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out);
 
 /*
  * lmce_microstep -- enqueue one micro-step on `stream` (a cudaStream_t; NULL = legacy
- * default stream) and return without waiting.
+ * default stream) and return without waiting.  It computes, for this micro-batch, the
+ * logits of the tied head, each row's softmax cross-entropy and its gradient ("How I
+ * trained my own GPT-2 124M on FineWeb-Edu", section 4 "Implementing Loss Calculation"),
+ * scaled by s_k and added into dW as backward adds into .grad between optimizer steps
+ * (section 8.1 "Gradient Accumulation"; s_k as "Multi-GPU calculation of gradients for
+ * accelerated training", section "Gradient accumulation averages across micro-steps").
  *   hidden      : device, dtype [N, C]  -- h, the final hidden states of N rows
  *   W           : device, dtype [V, C]  -- the tied wte / lm_head weight
  *   targets     : device, int32 [N]     -- next-token ids, or ignore_id
@@ -207,7 +212,11 @@ LMCE_API int lmce_microstep_ln_compact(lmce_handle* h, const void* x, const floa
 
 /*
  * lmce_finalize -- synchronise `stream`, read the step's results and reset the handle
- * for the next optimizer step (the next micro-step writes dW again).
+ * for the next optimizer step (the next micro-step writes dW again).  It is the loss a
+ * training loop reads once per step: the pages accumulate loss / G over the micro-steps
+ * and read it after the last one ("How I trained my own GPT-2 124M", section 9, training
+ * loop; "Multi-GPU calculation of gradients for accelerated training", section "Gradient
+ * accumulation averages across micro-steps"), here as the objective sum_k s_k loss_k.
  *   loss_sum    : host, may be NULL -- sum of the valid rows' losses over the step
  *   valid_count : host, may be NULL -- valid targets seen over the step
  *   loss_mean   : host, may be NULL -- sum_k s_k * loss_sum_k, the objective whose gradient
@@ -233,6 +242,19 @@ LMCE_API int lmce_finalize(lmce_handle* h, double* loss_sum, int64_t* valid_coun
 LMCE_API int lmce_dw_sumsq(lmce_handle* h, double* sumsq, void* stream);
 
 /*
+ * lmce_clip_coef -- the global-norm clip coefficient that torch.nn.utils.clip_grad_norm_
+ * applies ("Reproduce GPT-2 124M", training configuration: grad_norm_clip = 1.0):
+ *   *coef = min(1, max_norm / (sqrt(sumsq) + 1e-6))   (float64, then rounded to float32)
+ *   sumsq    : the sum of squares over every gradient of the model (lmce_dw_sumsq gives the
+ *              tied matrix's share; add the other tensors' shares), finite and >= 0
+ *   max_norm : > 0 and finite
+ *   coef     : host -- the value lmce_adamw's `clip` takes
+ * Host only: touches no device and no handle.
+ * Errors: LMCE_ERR_ARG (null coef, sumsq < 0 or not finite, max_norm <= 0 or not finite).
+ */
+LMCE_API int lmce_clip_coef(double sumsq, double max_norm, float* coef);
+
+/*
  * lmce_adamw -- one AdamW step on the tied matrix, after lmce_finalize, in one pass over the
  * elements (decoupled weight decay and Adam's bias correction, as torch.optim.AdamW):
  *   g = clip * dW
@@ -247,7 +269,7 @@ LMCE_API int lmce_dw_sumsq(lmce_handle* h, double* sumsq, void* stream);
  *                  Any alignment; when dW, p, m, v and W_out are all 16-byte aligned the kernel
  *                  moves 16-byte vectors
  *   step         : t >= 1, the step being taken
- *   clip         : the global-norm clip coefficient, min(1, max_norm / (norm + 1e-6)) (1 for none)
+ *   clip         : the global-norm clip coefficient, from lmce_clip_coef (1 for none)
  *   lr, beta1, beta2, eps, weight_decay : as torch.optim.AdamW; "How I trained my own GPT-2 124M",
  *                  section 6 "Implementing the Optimizer", uses 0.9, 0.95, 1e-8 and 0.1, with
  *                  decay on every tensor of two or more dimensions (W is one)

@@ -40,6 +40,15 @@ int main(void) {
          LMCE_ERR_ARG);
   expect("profile", lmce_profile(NULL, 1), LMCE_ERR_ARG);
   expect("test_stall_next_microstep", lmce_test_stall_next_microstep(NULL, 1000000), LMCE_ERR_ARG);
+  expect("clip_coef(NULL)", lmce_clip_coef(1.0, 1.0, NULL), LMCE_ERR_ARG);
+  {
+    float c = 0.f;
+    expect("clip_coef(4, 1)", lmce_clip_coef(4.0, 1.0, &c), LMCE_OK);
+    if (!(c > 0.4999f && c < 0.5f)) {
+      printf("clip_coef(4, 1) = %g\n", (double)c);
+      ++failures;
+    }
+  }
   expect("destroy(NULL)", lmce_destroy(NULL), LMCE_OK);
   if (lmce_status_string(LMCE_OK) == NULL || lmce_launch_count(NULL) != 0 || lmce_selected_path(NULL) != -1) {
     printf("status / count / path queries\n");

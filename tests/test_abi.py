@@ -68,11 +68,17 @@ def test_argument_errors_before_any_device_call(lib):
     assert lib.lmce_launch_count(None) == 0
 
 
-def test_clip_coef_host_helper():
-    # the binding's clip coefficient is the oracle's global-norm clip rule
+def test_clip_coef_behind_the_c_abi():
+    # lmce_clip_coef (host only) is the oracle's global-norm clip rule, rounded to float32
+    import numpy as np
     from oracle import lmce_oracle as O
-    for sumsq, mx in ((4.0, 1.0), (0.25, 1.0), (0.0, 1.0), (1e6, 0.5), (1.0, 1.0)):
-        assert M.clip_coef(sumsq, mx) == O.clip_coef(sumsq, mx)
+    for sumsq, mx in ((4.0, 1.0), (0.25, 1.0), (0.0, 1.0), (1e6, 0.5), (1.0, 1.0), (3.7e-3, 0.05)):
+        assert M.clip_coef(sumsq, mx) == float(np.float32(O.clip_coef(sumsq, mx)))
+    lib = M.load()
+    c = ctypes.c_float()
+    for sumsq, mx in ((-1.0, 1.0), (float("nan"), 1.0), (1.0, 0.0), (1.0, float("inf")), (float("inf"), 1.0)):
+        assert lib.lmce_clip_coef(sumsq, mx, ctypes.byref(c)) == M.ERR_ARG
+    assert lib.lmce_clip_coef(1.0, 1.0, None) == M.ERR_ARG
 
 
 def test_header_compiles_as_c_and_links(lib, tmp_path):
