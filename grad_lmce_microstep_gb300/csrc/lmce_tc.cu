@@ -407,6 +407,14 @@ __device__ __forceinline__ float grad_scale(const GradParams& p) {
 // that covers a whole tile writes the output directly, a segment that covers part of a tile
 // (at most the pair's first and last) writes fp32 partial sums to slot 2 pi (first segment) or
 // 2 pi + 1, and the split-combine kernels add the partials of each split tile in pair order.
+//
+// The passes whose stream is the vocabulary (dh, lse+dh) visit the blocks of X tile t in the
+// rotated order (j + rot(t)) mod nblk, j = 0, 1, ...: rot(t) is chosen so that the pair holding
+// most of tile t reaches vocabulary block (tau mod nblk) at its tau-th unit.  All pairs then sweep
+// W roughly in phase, and the part of W being read at any time is a few blocks instead of the
+// whole matrix (every pair at its own offset), so W is read from DRAM about once per sweep.  The
+// order of the blocks within a segment changes no sum's definition: dh and the (max, sum) merge
+// are order-free, and the order is a fixed function of the schedule (bitwise reproducible).
 struct Sched {
   long long U;  // tiles * blocks per tile
   int P;        // pairs
@@ -417,6 +425,20 @@ struct Sched {
     while (p + 1 < P && u0(p + 1) <= u) ++p;
     while (p > 0 && u0(p) > u) --p;
     return p;
+  }
+  __host__ __device__ int rot(int t) const {
+    const long long tb = (long long)t * nblk, te = tb + nblk;
+    const int pa = pair_of(tb), pz = pair_of(te - 1);
+    long long best = -1, tau = 0, j = 0;
+    for (int q = pa; q <= pz; ++q) {
+      const long long a = u0(q) > tb ? u0(q) : tb, b = u0(q + 1) < te ? u0(q + 1) : te;
+      if (b - a > best) {
+        best = b - a;
+        tau = a - u0(q);
+        j = a - tb;
+      }
+    }
+    return (int)(((tau - j) % nblk + nblk) % nblk);
   }
 };
 
@@ -460,6 +482,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
   __shared__ float fl_red[4][64];           // lse+dh: row max / sum over each 64-column quarter
   __shared__ float fl_f[G_XT];              // lse+dh: s / l_x for a valid target, else 0 (both CTAs' rows)
   __shared__ int col_y[G_XT];               // dh, lse+dh: target of each X row (token) of the tile, or -1
+  __shared__ int s_rot;                     // dh, lse+dh: the tile's vocabulary rotation
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -522,6 +545,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       const int b0 = (int)(max(ub, (long long)t * nblk) - (long long)t * nblk);
       const int nb = (int)(min(ue, (long long)(t + 1) * nblk) - (long long)t * nblk) - b0;
       const int x0 = t * G_XT;
+      const int rt = DW ? 0 : sch.rot(t);
       for (int j = 0; j <= nb && ok; ++j) {
         const int nst = (j < nb ? KC : 0) + (j >= 1 ? 4 / AQ : 0);
         for (int u = 0; u < nst; ++u, ++it) {
@@ -541,13 +565,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             // failure-detection test: no load starts, so every wait on this stage runs out
           } else if (sphase) {
             // S phase of block b0+j: my 128 stream rows and my 64 X rows, SK atoms of K from 64 SK u
-            if (lane == 0) tma_load_3d_cg2(dst, &tmYs, bar, 0, (b0 + j) * G_YB + (int)rank * 128, u * SK);
+            const int bj = b0 + j + rt;   // < 2 nblk
+            if (lane == 0) tma_load_3d_cg2(dst, &tmYs, bar, 0, (bj < nblk ? bj : bj - nblk) * G_YB + (int)rank * 128, u * SK);
             else if (lane == 1) tma_load_3d_cg2(dst + SK * 16384, &tmX, bar, 0, x0 + (int)rank * 64, u * SK);
           } else if (lane == 0) {
             // accumulation phase of block b0+j-1, quarters AQ q .. AQ q + AQ - 1 (64 AQ stream rows):
             // my 128 C of every chunk, one 4D box [chunk][atom][64 AQ rows][64]
             const int q = u - (j < nb ? KC : 0);
-            const int row = (b0 + j - 1) * G_YB + q * 64 * AQ;
+            const int bj = b0 + j - 1 + rt;   // < 2 nblk
+            const int row = (bj < nblk ? bj : bj - nblk) * G_YB + q * 64 * AQ;
             tma_load_4d_cg2(dst, &tmYa, bar, 0, row, 2 * (int)rank, p.ch0);
           }
           __syncwarp();
@@ -698,6 +724,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       const int nb = (int)(min(ue, (long long)(t + 1) * nblk) - (long long)t * nblk) - b0;
       const int x0 = t * G_XT;
       const int xg = x0 + xl;                     // my X row
+      // the tile's vocabulary rotation, found by one thread; read after the block loop's first
+      // barrier (the previous tile's readers are past the flush's barriers)
+      if (!DW && et == 0) s_rot = sch.rot(t);
       // dh / lse+dh: my token's target and (dh) log2(s) - lse log2(e); the targets of all 128
       // rows of the tile for the flush
       float crow = -INFINITY;
@@ -723,7 +752,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       float m2 = 0.f, lacc = 0.f;                 // lse+dh: my row's reference (base 2) and sum of p
       for (int j = 0; j < nb; ++j) {
         const int gb = g + j;
-        const int ys0 = (b0 + j) * G_YB;          // first stream row of the block
+        // first stream row of the block (dh passes: rotated; read after the barrier below)
+        const int ys0 = DW ? (b0 + j) * G_YB : 0;
         // dW: stream token et's constant and one-hot hit, loaded while S is computed
         float cc = -INFINITY;
         int hr = -1;
@@ -767,6 +797,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           else mbar_arrive_cluster(leader_s_empty);
         }
         if (FL) {
+          const int bj = b0 + j + s_rot;   // < 2 nblk
+          const int ys0 = (bj < nblk ? bj : bj - nblk) * G_YB;
           // columns past the vocabulary (last block only) carry no term
           const int nvalid = min(64, p.V - (ys0 + ks * 64));
           if (j == 0) {

@@ -49,24 +49,39 @@ def split_tile_edge_rows(nX: int, nY: int, pairs: int):
     return rows
 
 
-def segment_first_blocks(nX: int, nY: int, pairs: int, t: int):
-    """[(b0, b1)] stream-block ranges of the segments that cover X tile t (one per pair)."""
+def rotation(nX: int, nY: int, pairs: int, t: int) -> int:
+    """The vocabulary rotation of X tile t in the dh passes: the pair with the most units of the
+    tile (the lowest on a tie) reaches block (tau mod nblk) at its tau-th unit."""
     U, P, nblk = schedule(nX, nY, pairs)
+    best, tau, j = -1, 0, 0
+    for q in range(P):
+        a, b = max(U * q // P, t * nblk), min(U * (q + 1) // P, (t + 1) * nblk)
+        if b - a > best:
+            best, tau, j = b - a, a - U * q // P, a - t * nblk
+    return (tau - j) % nblk
+
+
+def segment_blocks(nX: int, nY: int, pairs: int, t: int):
+    """For every segment covering X tile t in a dh pass: its vocabulary blocks in the order the
+    pair processes them (the first one sets the one-pass reference)."""
+    U, P, nblk = schedule(nX, nY, pairs)
+    r = rotation(nX, nY, pairs, t)
     out = []
     for q in range(P):
         a, b = max(U * q // P, t * nblk), min(U * (q + 1) // P, (t + 1) * nblk)
         if a < b:
-            out.append((a - t * nblk, b - t * nblk))
+            out.append([(j - t * nblk + r) % nblk for j in range(a, b)])
     return out
 
 
 def guard_excess(z_row: np.ndarray, segs):
-    """Largest excess (base 2) of a token row's logits over the first-block maximum of the
-    segment that holds them, over every segment of the row's tile."""
+    """Largest excess (base 2) of a token row's logits over the maximum of the first block its
+    segment processes, over every segment of the row's tile."""
     zb = z_row / math.log(2.0)
     V = zb.shape[0]
     ex = -np.inf
-    for b0, b1 in segs:
-        m = zb[b0 * YB:min(V, b0 * YB + YB)].max()
-        ex = max(ex, zb[b0 * YB:min(V, b1 * YB)].max() - m)
+    for blocks in segs:
+        m = zb[blocks[0] * YB:min(V, blocks[0] * YB + YB)].max()
+        for b in blocks:
+            ex = max(ex, zb[b * YB:min(V, b * YB + YB)].max() - m)
     return ex

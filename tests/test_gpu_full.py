@@ -162,7 +162,7 @@ def test_full_logit_stress():
     assert max(float(l.max()) for l in lses) > 60.0
     assert abs(ls - loss) <= LOSS_REL * abs(loss)
     # The x40 rows of every micro-step, ranked by how far a logit rises above the one-pass
-    # kernel's reference (the first-block maximum of the segment that holds it): the eight
+    # kernel's reference (the maximum of the first block its segment processes): the eight
     # closest to the kernel's range guard (32 + 115 - ceil(log2 V) in base 2), and every row of
     # a tile that crosses it (flagged and recomputed by the exact repair).  Plus the edges of
     # every split tile of both gradient passes.
@@ -172,7 +172,7 @@ def test_full_logit_stress():
     for h, y in w.micro:
         big = h.float().norm(dim=1).argsort(descending=True)[:w.meta["scaled_rows"]].numpy()
         z = O.f64(h[torch.as_tensor(big)]) @ O.f64(w.W).T
-        ex = np.array([S.guard_excess(z[i], S.segment_first_blocks(h.shape[0], w.V, pairs, int(n) // S.XT))
+        ex = np.array([S.guard_excess(z[i], S.segment_blocks(h.shape[0], w.V, pairs, int(n) // S.XT))
                        for i, n in enumerate(big)])
         rows = big[np.argsort(-ex)[:8]].tolist()
         for n in big[ex > guard]:
