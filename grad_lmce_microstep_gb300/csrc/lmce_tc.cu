@@ -355,7 +355,7 @@ constexpr int G_XT = 128;                  // X rows per pair (64 per CTA)
 constexpr int G_YB = 256;                  // stream rows per block (128 per CTA)
 constexpr int G_DZ = G_YB * 128;           // one dz buffer: 256 K-rows x 64 bf16 = 32 KB
 constexpr int G_EPI_WARPS = 8;
-constexpr int G_THREADS = 96 + 32 * G_EPI_WARPS;   // warps 0 and 10 TMA, 1 MMA, 2-9 epilogue
+constexpr int G_THREADS = 128 + 32 * G_EPI_WARPS;  // warps 0 and 10 TMA, 1 MMA, 2-9 epilogue, 11 ring waiter
 
 enum GradMode { GM_DW = 0, GM_DH = 1, GM_FL = 2 };
 constexpr float FL_HEADROOM = 32.f;        // lse+dh pass: reference above the first block's maximum (base 2)
@@ -476,6 +476,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
   __shared__ __align__(8) uint64_t lx_full;   // lse+dh pass: the peer's s / l_x arrived
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int epi_abort;
+  __shared__ volatile int wt_abort;         // the ring waiter gave up on a stage
   __shared__ __align__(16) float col_c[G_YB];  // dW: per stream token log2(s) - lse log2(e), or -inf (read as float4)
   __shared__ int hit_cnt[2];                // dW: one-hot hits of the block (by block parity)
   __shared__ uint16_t hit[2][G_YB];         // dW: (token in block) << 8 | X row in tile
@@ -516,6 +517,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     hit_cnt[0] = 0;
     hit_cnt[1] = 0;
     epi_abort = 0;
+    wt_abort = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -591,6 +593,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         if (!all && lane == 0) record_timeout(p.err, where);
         return all;
       };
+      // A ring stage is taken from the waiter warp through its slot's named barrier (below).
+      auto ring_take = [&](int st) { asm volatile("bar.sync %0, 64;" ::"r"(2 + st) : "memory"); };
       // S = X . Y_blk^T: M = 128 X rows (64 per CTA), N = 256 stream rows (128 per CTA), K-major
       const uint32_t idS = idesc_bf16(128, G_YB, 0, 0);
       // acc^T += Y_blk^T . dz: M = 256 C rows per chunk (MN-major), N = 128 X rows (K-major dz)
@@ -617,7 +621,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             tc_fence_after();
             for (int kc = 0; kc < KC; ++kc, ++it) {
               const int st = it % NST;
-              if (!wait_w(smem_u32(&full[st]), (it / NST) & 1, false, 22)) {
+              ring_take(st);
+              if (wt_abort) {
                 ok = false;
                 break;
               }
@@ -652,7 +657,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
                 break;
               }
               const int st = it % NST;
-              if (!wait_w(smem_u32(&full[st]), (it / NST) & 1, false, 24)) {
+              ring_take(st);
+              if (wt_abort) {
                 ok = false;
                 break;
               }
@@ -681,6 +687,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         // give up: wait (bounded) for the MMAs already issued before TMEM is released
         mma_commit2_elect(smem_u32(&drain_bar));
         mbar_wait(smem_u32(&drain_bar), 0, DRAIN_NS);
+      }
+    }
+  } else if (warp == 11) {
+    // ---------------- ring waiter (leader CTA) ----------------
+    // Waits on each ring stage's full barrier in the MMA warp's order and hands the stage over
+    // through named barrier 2 + slot.  An mbarrier wait in the MMA warp itself sits behind the
+    // MMAs it has just issued and took ~190 cycles even on a completed phase, long enough for the
+    // tensor pipe to run dry after every stage; a named barrier does not.  The waiter is at most
+    // NST stages ahead (a slot refills only after the MMA warp took it), so every slot's barrier
+    // sees one arrival per use.  A wait that runs out sets wt_abort, which the MMA warp reads
+    // after its barrier.
+    if (rank == 0) {
+      bool ok = true;
+      int it = 0;
+      for (int t = t_first; t <= t_last && ok; ++t) {
+        const int b0 = (int)(max(ub, (long long)t * nblk) - (long long)t * nblk);
+        const int nb = (int)(min(ue, (long long)(t + 1) * nblk) - (long long)t * nblk) - b0;
+        for (int j = 0; j <= nb && ok; ++j) {
+          const int nst = (j < nb ? KC : 0) + (j >= 1 ? 4 / AQ : 0);
+          for (int u = 0; u < nst; ++u, ++it) {
+            const int st = it % NST;
+            const bool w = __all_sync(0xffffffffu, mbar_wait(smem_u32(&full[st]), (it / NST) & 1, wait_ns));
+            if (!w) {
+              if (lane == 0) record_timeout(p.err, 29);
+              wt_abort = 1;
+              ok = false;
+            }
+            __syncwarp();
+            asm volatile("bar.arrive %0, 64;" ::"r"(2 + st) : "memory");
+            if (!ok) break;
+          }
+        }
       }
     }
   } else if (warp <= 9) {
