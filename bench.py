@@ -365,19 +365,33 @@ def run_lmce(args, rank, world, local_rank):
     aw_gbs = aw_bytes / (aw_ms * 1e-3) / 1e9 if aw_ms > 0 else None
     final_norm = None
     if args.final_norm and "ln" in prof and prof["ln"][1] > 0:
-        # per micro-step: forward reads x and writes h, backward reads dh and x and writes dx (5
-        # row tensors), plus the dgamma / dbeta partials (fp32, one row per backward block) written
-        # and read once
+        # Per micro-step, plain: the forward reads x and writes h, the backward reads dh and x and
+        # writes dx (5 row tensors over all rows).  Compacted (ln_f fused with the compaction):
+        # the forward reads the valid rows of x and writes them normalised, the backward reads dh
+        # and x of the valid rows and writes dx of every row (4 valid-row tensors + 1 full one),
+        # and the compaction's count and scan read the targets; the compaction launches are
+        # timed with ln_f's.  Both: the dgamma / dbeta partials (fp32, one row per backward block
+        # of at most one per SM) written and read once.
         esz = 2 if w.dtype == "bf16" else 4
         nmicro = args.steps * w.G
         ln_ms = prof["ln"][0] / nmicro
-        rows = (sum(nvs) if args.compact else tokens_rank) // w.G   # rows one ln_f launch covers (mean)
-        rpb = -(-rows // 304)   # the backward's row range per block: at most 304 blocks
-        ln_bytes = 5 * rows * w.C * esz + 2 * 2 * 4 * w.C * (-(-rows // rpb))
+        n_ln = prof["ln"][1]
+        rows_all = tokens_rank // w.G
+        rows_valid = sum(nvs) // w.G
+        rows = rows_all
+        rpb = -(-rows // N_SM)
+        part_bytes = 2 * 2 * 4 * w.C * (-(-rows // rpb))
+        if args.compact:
+            ln_ms += prof.get("compact", (0.0, 0))[0] / nmicro
+            n_ln += prof.get("compact", (0.0, 0))[1]
+            ln_bytes = (4 * rows_valid + rows_all) * w.C * esz + 4 * rows_all + part_bytes
+        else:
+            ln_bytes = 5 * rows_all * w.C * esz + part_bytes
         ln_gbs = ln_bytes / (ln_ms * 1e-3) / 1e9
         final_norm = {"kind": args.final_norm, "ms_per_micro_step": ln_ms, "launches_per_micro_step":
-                      prof["ln"][1] / nmicro, "bytes_per_micro_step": int(ln_bytes), "achieved_gbs": ln_gbs,
-                      "peak_gbs": pk["hbm_gbs"], "frac": ln_gbs / pk["hbm_gbs"], "bound": "hbm"}
+                      n_ln / nmicro, "bytes_per_micro_step": int(ln_bytes), "achieved_gbs": ln_gbs,
+                      "peak_gbs": pk["hbm_gbs"], "frac": ln_gbs / pk["hbm_gbs"], "bound": "hbm",
+                      "with_compaction": bool(args.compact)}
     adamw = {"ms": aw_ms, "launches": aw_n, "bytes": int(aw_bytes), "achieved_gbs": aw_gbs,
              "peak_gbs": pk["hbm_gbs"], "frac": aw_gbs / pk["hbm_gbs"] if aw_gbs else None, "bound": "hbm",
              "hyper": {"lr": 6e-4, "betas": [0.9, 0.95], "eps": 1e-8, "weight_decay": 0.1, "clip": clip}}

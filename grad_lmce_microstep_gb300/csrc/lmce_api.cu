@@ -606,7 +606,6 @@ extern "C" int lmce_microstep_ln_compact(lmce_handle* h, const void* x, const fl
   const lmce_config& c = h->cfg;
   cudaStream_t st = (cudaStream_t)stream;
   if (c.norm == LMCE_NORM_GLOBAL && global_valid <= 0) return refuse_no_valid(h, N, dx, row_loss, st);
-  // gather the valid rows of x (and their targets), run ln_f and the head on them, scatter dx
   StepArgs a{};
   a.hidden = x;
   a.targets = targets;
@@ -617,10 +616,33 @@ extern "C" int lmce_microstep_ln_compact(lmce_handle* h, const void* x, const fl
   a.V = c.V;
   a.ignore_id = c.ignore_id;
   a.bf16 = c.dtype == LMCE_BF16;
+  // Fused form (rows that fit ln_f's register layout): ln_f's forward reads the valid rows of x
+  // in place and writes the head's compact input, its backward writes dx of every row; x is not
+  // copied and dx needs no separate scatter.
+  LnArgs la{};
+  la.x = x;
+  la.gamma = gamma;
+  la.beta = beta;
+  la.h = h->ln.h;
+  la.dh = h->ln.dh;
+  la.dx = dx;
+  la.mean = h->ln.mean;
+  la.rstd = h->ln.rstd;
+  la.part_g = h->ln.part;
+  la.part_b = h->ln.part + (size_t)ln_part_rows() * (size_t)c.C;
+  la.dgamma = dgamma;
+  la.dbeta = dbeta;
+  la.N = N;
+  la.C = c.C;
+  la.rms = ln_kind == LMCE_LN_RMSNORM;
+  la.eps = eps;
+  la.bf16 = a.bf16;
+  const bool fused = N > 0 && ln_compact_fusable(la);
   Launch L;
   L.st = st;
   L.prof = &h->prof;
-  cudaError_t e = compact_rows(a, h->cs, h->sc.acc, n_valid, L);
+  cudaError_t e = fused ? compact_count_scan(a, h->cs, h->sc.acc, n_valid, L) : compact_rows(a, h->cs, h->sc.acc, n_valid, L);
+  if (e == cudaSuccess && fused) e = ln_gather_forward(la, targets, c.V, h->cs, L);
   h->launches += L.n;
   if (e != cudaSuccess) return LMCE_ERR_CUDA;
   if (n_valid < 0) {
@@ -629,6 +651,20 @@ extern "C" int lmce_microstep_ln_compact(lmce_handle* h, const void* x, const fl
       return LMCE_ERR_CUDA;
     n_valid = *h->cs.host_total;
   }
+  if (fused) {
+    // the parameter gradients follow dW: written by the first micro-step of a step, then added
+    la.accumulate = h->first && !(c.flags & LMCE_ACCUMULATE_FROM_START) ? 0 : 1;
+    const int s = run_microstep(h, h->ln.h, W, h->cs.y_c, n_valid, global_valid, h->ln.dh,
+                                row_loss ? h->cs.rl_c : nullptr, st);
+    if (s != LMCE_OK) return s;
+    Launch L2;
+    L2.st = st;
+    L2.prof = &h->prof;
+    e = ln_backward_scatter(la, h->cs, n_valid, row_loss, L2);
+    h->launches += L2.n;
+    return e == cudaSuccess ? LMCE_OK : LMCE_ERR_CUDA;
+  }
+  // otherwise: x gathered into the compact rows, ln_f and the head on them, dx scattered
   const int s = run_ln_step(h, h->cs.h_c, gamma, beta, ln_kind, eps, W, h->cs.y_c, n_valid, global_valid,
                             h->cs.dh_c, dgamma, dbeta, row_loss ? h->cs.rl_c : nullptr, st);
   if (s != LMCE_OK) return s;

@@ -207,8 +207,8 @@ void launch_scatter(const StepArgs& a, const CompactScratch& cs, int64_t n_valid
 
 int64_t compact_blocks(int64_t N) { return (N + CP_ROWS - 1) / CP_ROWS; }
 
-cudaError_t compact_rows(const StepArgs& a, const CompactScratch& cs, DevAcc* acc, int64_t n_valid,
-                         Launch& L) {
+cudaError_t compact_count_scan(const StepArgs& a, const CompactScratch& cs, DevAcc* acc, int64_t n_valid,
+                               Launch& L) {
   const int64_t nblk = compact_blocks(a.N);
   if (nblk > 0) {
     L.begin(K_COMPACT);
@@ -219,7 +219,13 @@ cudaError_t compact_rows(const StepArgs& a, const CompactScratch& cs, DevAcc* ac
   L.begin(K_COMPACT);
   compact_scan_kernel<<<1, SCAN_T, 0, L.st>>>(cs.blk_cnt, cs.blk_err, nblk, cs.blk_off, cs.total, n_valid, acc);
   L.end();
-  cudaError_t e = cudaGetLastError();
+  return cudaGetLastError();
+}
+
+cudaError_t compact_rows(const StepArgs& a, const CompactScratch& cs, DevAcc* acc, int64_t n_valid,
+                         Launch& L) {
+  const int64_t nblk = compact_blocks(a.N);
+  cudaError_t e = compact_count_scan(a, cs, acc, n_valid, L);
   if (e != cudaSuccess || nblk == 0) return e;
   const int64_t esz = a.bf16 ? 2 : 4;
   const int64_t rb = a.C * esz;

@@ -132,6 +132,8 @@ int64_t compact_blocks(int64_t N);
 // count + scan + gather of a.hidden / a.targets (a.N rows) into the compact buffers; the
 // valid total is checked against n_valid (>= 0) and bad targets are flagged in acc->err
 cudaError_t compact_rows(const StepArgs& a, const CompactScratch& cs, DevAcc* acc, int64_t n_valid, Launch& L);
+// the count and scan alone (block offsets and the valid total, with the same checks)
+cudaError_t compact_count_scan(const StepArgs& a, const CompactScratch& cs, DevAcc* acc, int64_t n_valid, Launch& L);
 // dh / row_loss of a.N rows from the first n_valid compact rows, zero for the ignored rows
 cudaError_t compact_scatter(const StepArgs& a, const CompactScratch& cs, int64_t n_valid, Launch& L);
 
@@ -161,6 +163,15 @@ int64_t ln_rows_per_block(int64_t N);
 int64_t ln_part_rows();                 // the most ln_blocks(N) can be, for any N
 cudaError_t ln_forward(const LnArgs& a, Launch& L);
 cudaError_t ln_backward(const LnArgs& a, Launch& L);
+// ln_f fused with the valid-row compaction, for rows that fit the register layout
+// (ln_compact_fusable).  a.x, a.dx and a.N are the caller's rows; a.h, a.dh, a.mean and a.rstd
+// hold the compact rows.  The forward (after compact_count_scan) normalises the valid rows of x
+// straight into the compact head input and records their targets and positions; the backward
+// writes dx of every row (zero for the rows without a compact position below n_valid), the row
+// losses when row_loss is given, and the parameter gradients.
+bool ln_compact_fusable(const LnArgs& a);
+cudaError_t ln_gather_forward(const LnArgs& a, const int32_t* targets, int64_t V, const CompactScratch& cs, Launch& L);
+cudaError_t ln_backward_scatter(const LnArgs& a, const CompactScratch& cs, int64_t n_valid, float* row_loss, Launch& L);
 
 // Fixed-order reduction of the per-block partials of one micro-step into the step
 // accumulators; also computes this micro-step's gradient scale.  One launch.

@@ -33,7 +33,7 @@ def _xs(w):
     return [((h.float() * 1.7 + 0.4).to(TDT[w.dtype]), y) for h, y in w.micro]
 
 
-def _run(w, xs, gamma, beta, kind, eps, path="auto", steps=1, compact=False):
+def _run(w, xs, gamma, beta, kind, eps, path="auto", steps=1, compact=False, count_on_device=False):
     C, V = w.C, w.V
     W = w.W.cuda()
     dW = torch.empty(V, C, device="cuda")
@@ -49,7 +49,7 @@ def _run(w, xs, gamma, beta, kind, eps, path="auto", steps=1, compact=False):
             xd, yd = x.cuda(), y.cuda()
             dx = torch.full_like(xd, 5.0)
             rl = torch.empty(yd.numel(), device="cuda")
-            nv = int(((y >= 0) & (y < V)).sum()) if compact else None
+            nv = (-1 if count_on_device else int(((y >= 0) & (y < V)).sum())) if compact else None
             L.microstep_ln(xd, g, b, W, yd, gv, dx, dgamma, dbeta, kind, eps, rl, n_valid=nv)
             dxs.append(dx)
             rls.append(rl)
@@ -129,6 +129,49 @@ def test_ln_compact_masked_tails(path, kind):
     for (_, y), dx in zip(xs, got[1]):
         ign = ~((y >= 0) & (y < w.V))
         assert float(dx.cpu()[ign].abs().max()) == 0.0
+
+
+@pytest.mark.parametrize("C,dtype", [(768, "bf16"), (1024, "bf16"), (520, "fp32"), (67, "fp32"), (2048, "bf16")])
+def test_ln_compact_widths(C, dtype):
+    # ln_f fused with the compaction for rows that fit its register layout (768 and 1024 bf16, 520
+    # floats), the gather / separate ln_f / scatter sequence for rows that do not (67 floats, 2048
+    # bf16); ragged micro-steps (N not a multiple of 32) with a whole 32-row block ignored
+    w = I.custom([96, 45], C, 301, dtype, seed=47, ignore_frac=0.3)
+    w.micro[0][1][32:64] = I.IGNORE_ID
+    xs = _xs(w)
+    gamma, beta = _params(C, "layernorm", 47)
+    got = _run(w, xs, gamma, beta, "layernorm", 1e-5, steps=2, compact=True)
+    _check(w, xs, gamma, beta, "layernorm", 1e-5, got)
+    for (_, y), dx in zip(xs, got[1]):
+        ign = ~((y >= 0) & (y < w.V))
+        assert float(dx.cpu()[ign].abs().max()) == 0.0
+
+
+@pytest.mark.parametrize("kind", ["layernorm", "rmsnorm"])
+def test_ln_compact_count_on_device_and_empty_micro_step(kind):
+    # n_valid = -1: the library reads the valid count back; the second micro-step has no valid
+    # target at all (its dx is zero and it adds nothing to dgamma / dbeta)
+    w = I.custom([200, 77], 256, 1000, "bf16", seed=48, ignore_frac=0.2)
+    w.micro[1][1][:] = I.IGNORE_ID
+    xs = _xs(w)
+    gamma, beta = _params(w.C, kind, 48)
+    got = _run(w, xs, gamma, beta, kind, 1e-5, steps=2, compact=True, count_on_device=True)
+    _check(w, xs, gamma, beta, kind, 1e-5, got)
+    assert float(got[1][1].abs().max()) == 0.0
+
+
+def test_ln_compact_bitwise_reproducible():
+    w = I.custom([300, 173], 768, 1000, "bf16", seed=49, ignore_frac=0.4)
+    xs = _xs(w)
+    gamma, beta = _params(w.C, "layernorm", 49)
+    a = _run(w, xs, gamma, beta, "layernorm", 1e-5, path="tcgen05", compact=True)
+    b = _run(w, xs, gamma, beta, "layernorm", 1e-5, path="tcgen05", compact=True)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[3], b[3]) and torch.equal(a[4], b[4])
+    for x, y in zip(a[1], b[1]):
+        assert torch.equal(x, y)
+    for x, y in zip(a[2], b[2]):
+        assert torch.equal(x, y)
+    assert a[5] == b[5]
 
 
 def test_ln_argument_errors_and_no_valid():
