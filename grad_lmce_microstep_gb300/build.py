@@ -18,6 +18,10 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "liblmce.so")
+# The debug build: every kernel's bounds checks compiled in (LMCE_DEBUG_BOUNDS=1); a failed check
+# is reported by lmce_finalize as LMCE_ERR_INTERNAL instead of trapping.
+BUILD_DBG = os.path.join(ROOT, "_build_dbg")
+LIB_DBG = os.path.join(HERE, "liblmce_dbg.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -35,13 +39,18 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def build(verbose: bool = False, extra_flags=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, extra_flags=(), debug_bounds: bool = False) -> str:
+    """Compile every translation unit and link the library; debug_bounds=True makes the debug
+    build (liblmce_dbg.so) instead of the release one."""
+    bdir, lib = (BUILD_DBG, LIB_DBG) if debug_bounds else (BUILD, LIB)
+    if debug_bounds:
+        extra_flags = (*extra_flags, "-DLMCE_DEBUG_BOUNDS=1")
+    os.makedirs(bdir, exist_ok=True)
     cc = nvcc()
     procs = []
     objs = []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         cmd = [cc, *ARCH, *CFLAGS, *extra_flags, "-c", src, "-o", obj]
         if verbose:
@@ -56,15 +65,15 @@ def build(verbose: bool = False, extra_flags=()) -> str:
             failed.append(src)
     if failed:
         raise RuntimeError("nvcc failed on " + ", ".join(os.path.basename(f) for f in failed))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static", "-Xlinker", "--no-undefined",
            "-lpthread", "-ldl", "-lrt"]
     if verbose:
         print(" ".join(cmd), flush=True)
     subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv))
+    print(build(verbose="-v" in sys.argv, debug_bounds="--debug-bounds" in sys.argv))

@@ -373,6 +373,8 @@ extern "C" int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out)
          cudaMallocHost(&q.host_total, sizeof(int64_t)) == cudaSuccess &&
          // defined contents for rows a wrong n_valid would read: zero rows, targets -1
          cudaMemset(q.h_c, 0, rows) == cudaSuccess && cudaMemset(q.y_c, 0xff, sizeof(int32_t) * maxN) == cudaSuccess;
+    q.rows = maxN;
+    q.err = &h->sc.acc->err;
   }
   if (ok && (cfg->flags & LMCE_FINAL_NORM)) {
     const size_t rows = (size_t)maxN * (size_t)cfg->C * (cfg->dtype == LMCE_BF16 ? 2 : 4);
@@ -561,6 +563,7 @@ int run_ln_step(lmce_handle* h, const void* x, const float* gamma, const float* 
   a.eps = eps;
   a.bf16 = c.dtype == LMCE_BF16;
   a.accumulate = write ? 0 : 1;
+  a.err = &h->sc.acc->err;
   Launch L;
   L.st = st;
   L.prof = &h->prof;
@@ -637,6 +640,7 @@ extern "C" int lmce_microstep_ln_compact(lmce_handle* h, const void* x, const fl
   la.rms = ln_kind == LMCE_LN_RMSNORM;
   la.eps = eps;
   la.bf16 = a.bf16;
+  la.err = &h->sc.acc->err;
   const bool fused = N > 0 && ln_compact_fusable(la);
   Launch L;
   L.st = st;
@@ -691,6 +695,7 @@ extern "C" int lmce_finalize(lmce_handle* h, double* loss_sum, int64_t* valid_co
   h->first = true;
   h->attempted = 0;
   if (cudaMemsetAsync(h->sc.acc, 0, sizeof(DevAcc), st) != cudaSuccess) return LMCE_ERR_CUDA;
+  if (r.err & ERR_BIT_BOUNDS) return LMCE_ERR_INTERNAL;  // a debug-build bounds check failed
   if (r.err & ERR_BIT_TIMEOUT) return LMCE_ERR_CUDA;  // a bounded device wait ran out
   if (r.err & ERR_BIT_COUNT) return LMCE_ERR_ARG;     // a compacted micro-step's n_valid was wrong
   if (r.err & ERR_BIT_BAD_TARGET) return LMCE_ERR_BAD_TARGET;
@@ -784,8 +789,19 @@ extern "C" const char* lmce_status_string(int s) {
     case LMCE_ERR_NO_VALID: return "no valid target in the step";
     case LMCE_ERR_NONFINITE: return "loss is not finite";
     case LMCE_ERR_STATE: return "call out of order";
+    case LMCE_ERR_INTERNAL: return "a bounds check of the debug build failed (library bug)";
     default: return "unknown status";
   }
+}
+
+extern "C" int lmce_debug_bounds(void) { return LMCE_DEBUG_BOUNDS ? 1 : 0; }
+
+extern "C" int lmce_test_bounds_limit(lmce_handle* h, int64_t rows) {
+  if (!h) return LMCE_ERR_ARG;
+  if (!LMCE_DEBUG_BOUNDS || !h->cs.h_c) return LMCE_ERR_STATE;
+  if (rows < 0 || rows > h->cfg.max_N) return LMCE_ERR_ARG;
+  h->cs.rows = rows;
+  return LMCE_OK;
 }
 
 extern "C" int lmce_test_stall_next_microstep(lmce_handle* h, int64_t wait_ns) {

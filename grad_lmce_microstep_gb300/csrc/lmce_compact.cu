@@ -104,7 +104,8 @@ __global__ void __launch_bounds__(MV_T) compact_gather_kernel(const U* __restric
                                                              const int32_t* __restrict__ y, int64_t N, int64_t V,
                                                              unsigned w, const int64_t* __restrict__ blk_off,
                                                              U* __restrict__ h_c, int32_t* __restrict__ y_c,
-                                                             int32_t* __restrict__ pos) {
+                                                             int32_t* __restrict__ pos, int64_t rows,
+                                                             unsigned* err) {
   __shared__ int64_t rowpos[CP_ROWS];
   const int t = threadIdx.x;
   const int64_t r0 = (int64_t)blockIdx.x * CP_ROWS;
@@ -113,7 +114,8 @@ __global__ void __launch_bounds__(MV_T) compact_gather_kernel(const U* __restric
     const int yt = n < N ? y[n] : -1;
     const bool v = n < N && valid_target(yt, V);
     const unsigned bal = __ballot_sync(0xffffffffu, v);
-    const int64_t p = v ? blk_off[blockIdx.x] + __popc(bal & ((1u << t) - 1u)) : -1;
+    int64_t p = v ? blk_off[blockIdx.x] + __popc(bal & ((1u << t) - 1u)) : -1;
+    if (p >= 0 && !dcheck(p < rows, err, BS_COMPACT_POS)) p = -1;
     if (n < N) {
       pos[n] = (int32_t)p;
       if (v) y_c[p] = yt;
@@ -150,14 +152,15 @@ template <typename U>
 __global__ void __launch_bounds__(MV_T) compact_scatter_kernel(const int32_t* __restrict__ pos, int64_t N,
                                                               int64_t n_valid, unsigned w, const U* __restrict__ dh_c,
                                                               U* __restrict__ dh, const float* __restrict__ rl_c,
-                                                              float* __restrict__ row_loss) {
+                                                              float* __restrict__ row_loss, int64_t cap,
+                                                              unsigned* err) {
   __shared__ int64_t rowpos[CP_ROWS];
   const int t = threadIdx.x;
   const int64_t r0 = (int64_t)blockIdx.x * CP_ROWS;
   const int rows = (int)(N - r0 < CP_ROWS ? N - r0 : CP_ROWS);
   if (t < rows) {
     const int64_t q = pos[r0 + t];
-    const bool ok = q >= 0 && q < n_valid;
+    const bool ok = q >= 0 && q < n_valid && dcheck(q < cap, err, BS_SCATTER_POS);
     rowpos[t] = ok ? q : -1;
     if (row_loss) row_loss[r0 + t] = ok ? rl_c[q] : 0.f;
   }
@@ -194,13 +197,14 @@ template <typename U>
 void launch_gather(const StepArgs& a, const CompactScratch& cs, int64_t nblk, int64_t rb, cudaStream_t st) {
   compact_gather_kernel<U><<<(unsigned)nblk, MV_T, 0, st>>>((const U*)a.hidden, a.targets, a.N, a.V,
                                                             (unsigned)(rb / (int64_t)sizeof(U)), cs.blk_off,
-                                                            (U*)cs.h_c, cs.y_c, cs.pos);
+                                                            (U*)cs.h_c, cs.y_c, cs.pos, cs.rows, cs.err);
 }
 
 template <typename U>
 void launch_scatter(const StepArgs& a, const CompactScratch& cs, int64_t n_valid, int64_t rb, cudaStream_t st) {
   compact_scatter_kernel<U><<<(unsigned)compact_blocks(a.N), MV_T, 0, st>>>(
-      cs.pos, a.N, n_valid, (unsigned)(rb / (int64_t)sizeof(U)), (const U*)cs.dh_c, (U*)a.dh, cs.rl_c, a.row_loss);
+      cs.pos, a.N, n_valid, (unsigned)(rb / (int64_t)sizeof(U)), (const U*)cs.dh_c, (U*)a.dh, cs.rl_c, a.row_loss,
+      cs.rows, cs.err);
 }
 
 }  // namespace

@@ -73,6 +73,36 @@ constexpr unsigned ERR_BIT_NONFINITE = 2u;
 // A bounded device wait ran out (tensor-core path); bits 8..15 say which wait.
 constexpr unsigned ERR_BIT_TIMEOUT = 4u;
 constexpr unsigned ERR_BIT_COUNT = 8u;      // a compacted micro-step's valid count was not the caller's
+// A bounds check of the debug build failed (bits 16..23 say which site); the access was skipped.
+constexpr unsigned ERR_BIT_BOUNDS = 16u;
+
+// Bounds checks of the debug build (LMCE_DEBUG_BOUNDS=1, built as liblmce_dbg.so): a check that
+// fails records ERR_BIT_BOUNDS and its site in the step's error word, and the caller skips the
+// access; lmce_finalize then returns LMCE_ERR_INTERNAL.  Nothing traps.  In the release build a
+// check always passes and compiles to nothing.
+#ifndef LMCE_DEBUG_BOUNDS
+#define LMCE_DEBUG_BOUNDS 0
+#endif
+enum BoundsSite : unsigned {
+  BS_TMA_ROW = 1,       // gradient kernels: a TMA box's row coordinate past its tensor
+  BS_HIT = 2,           // dW pass: one-hot hits of a block past the list
+  BS_SLOT = 3,          // gradient kernels / split combine: a partial slot past the pairs' slots
+  BS_TILE_FLAG = 4,     // lse+dh pass / row post: a 128-token tile index past the flags
+  BS_W_ROW = 5,         // dh passes: a one-hot row of W past V
+  BS_COMPACT_POS = 6,   // compaction / fused ln_f forward: a compact position past the buffer
+  BS_SCATTER_POS = 7,   // scatter / fused ln_f backward: a compact position past the valid rows
+};
+__device__ __forceinline__ bool dcheck(bool ok, unsigned* err, unsigned site) {
+#if LMCE_DEBUG_BOUNDS
+  if (!ok) atomicOr(err, ERR_BIT_BOUNDS | (site << 16));
+  return ok;
+#else
+  (void)ok;
+  (void)err;
+  (void)site;
+  return true;
+#endif
+}
 
 // Arguments of one micro-step as the kernels see them.
 struct StepArgs {
@@ -127,6 +157,9 @@ struct CompactScratch {
   int64_t* blk_off;    // [compact_blocks(max_N)]
   int64_t* total;      // [1] valid rows found
   int64_t* host_total; // pinned [1]
+  int64_t rows;        // the compact buffers' rows as the debug checks see them (max_N; lowered
+                       // by the debug build's test hook)
+  unsigned* err;       // the step's error word (debug bounds checks)
 };
 int64_t compact_blocks(int64_t N);
 // count + scan + gather of a.hidden / a.targets (a.N rows) into the compact buffers; the
@@ -157,6 +190,7 @@ struct LnArgs {
   float eps;
   int32_t bf16;
   int32_t accumulate;   // 1: dgamma / dbeta +=, 0: =
+  unsigned* err;        // the step's error word (debug bounds checks)
 };
 int64_t ln_blocks(int64_t N);           // backward blocks (parameter-gradient partials) for N rows
 int64_t ln_rows_per_block(int64_t N);

@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(LN_T, KV <= 3 ? 3 : 2) ln_gather_fwd_kernel(
     const T* __restrict__ x, const int32_t* __restrict__ y, int64_t V, const int64_t* __restrict__ blk_off,
     const float* __restrict__ gamma, const float* __restrict__ beta, int64_t N, int64_t C, int rms, float eps,
     T* __restrict__ h, float* __restrict__ mean_out, float* __restrict__ rstd_out, int32_t* __restrict__ y_c,
-    int32_t* __restrict__ pos) {
+    int32_t* __restrict__ pos, int64_t rows, unsigned* err) {
   constexpr int VN = Vec<T>::N;
   const int lane = threadIdx.x & 31;
   const int64_t stride = (int64_t)gridDim.x * (LN_T / 32);
@@ -345,12 +345,14 @@ __global__ void __launch_bounds__(LN_T, KV <= 3 ? 3 : 2) ln_gather_fwd_kernel(
   int64_t p = -1, pn = -1;
   if (n < N) {
     p = ln_compact_pos(y, N, V, blk_off, n, &yc);
+    if (p >= 0 && !dcheck(p < rows, err, BS_COMPACT_POS)) p = -1;
     if (p >= 0) load_row<T, KV>(x + n * C, C, lane, cur);
   }
   for (; n < N; n += stride) {
     const int64_t nn = n + stride;
     if (nn < N) {
       pn = ln_compact_pos(y, N, V, blk_off, nn, &yx);
+      if (pn >= 0 && !dcheck(pn < rows, err, BS_COMPACT_POS)) pn = -1;
       if (pn >= 0) load_row<T, KV>(x + nn * C, C, lane, nxt);   // in flight meanwhile
     }
     if (lane == 0) pos[n] = (int32_t)p;
@@ -417,7 +419,8 @@ __global__ void __launch_bounds__(NT, 1) ln_bwd_scatter_kernel(
     const T* __restrict__ dh_c, const T* __restrict__ x, const float* __restrict__ gamma,
     const float* __restrict__ mean_c, const float* __restrict__ rstd_c, const int32_t* __restrict__ pos,
     int64_t n_valid, int64_t N, int64_t C, int rms, T* __restrict__ dx, float* __restrict__ part_g,
-    float* __restrict__ part_b, int64_t rpb, const float* __restrict__ rl_c, float* __restrict__ row_loss) {
+    float* __restrict__ part_b, int64_t rpb, const float* __restrict__ rl_c, float* __restrict__ row_loss,
+    int64_t rows, unsigned* err) {
   constexpr int VN = Vec<T>::N;
   extern __shared__ float ln_slices[];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -428,7 +431,7 @@ __global__ void __launch_bounds__(NT, 1) ln_bwd_scatter_kernel(
   for (int j = 0; j < KV * VN; ++j) ag[j] = ab[j] = 0.f;
   auto qof = [&](int64_t n) -> int64_t {
     const int64_t q = pos[n];
-    return q >= 0 && q < n_valid ? q : -1;
+    return q >= 0 && q < n_valid && dcheck(q < rows, err, BS_SCATTER_POS) ? q : -1;
   };
   uint4 cd[KV], cx[KV], nd[KV], nx[KV];
   int64_t q = -1, qn = -1;
@@ -600,7 +603,7 @@ void launch_gather_fwd(const LnArgs& a, const int32_t* y, int64_t V, const Compa
   if (blocks > 152 * LN_FWD_BLOCKS_PER_SM) blocks = 152 * LN_FWD_BLOCKS_PER_SM;   // warps loop over rows
   ln_gather_fwd_kernel<T, KV><<<(unsigned)blocks, LN_T, 0, st>>>((const T*)a.x, y, V, cs.blk_off, a.gamma, a.beta,
                                                                   a.N, a.C, a.rms, a.eps, (T*)a.h, a.mean, a.rstd,
-                                                                  cs.y_c, cs.pos);
+                                                                  cs.y_c, cs.pos, cs.rows, cs.err);
 }
 
 template <typename T, int KV>
@@ -612,7 +615,7 @@ cudaError_t launch_bwd_scatter(const LnArgs& a, const CompactScratch& cs, int64_
   if (e != cudaSuccess) return e;
   ln_bwd_scatter_kernel<T, KV><<<(unsigned)nblk, lnb_threads<T, KV>(), smem, st>>>(
       (const T*)a.dh, (const T*)a.x, a.gamma, a.mean, a.rstd, cs.pos, n_valid, a.N, a.C, a.rms, (T*)a.dx, a.part_g,
-      a.part_b, rpb, cs.rl_c, row_loss);
+      a.part_b, rpb, cs.rl_c, row_loss, cs.rows, cs.err);
   return cudaSuccess;
 }
 

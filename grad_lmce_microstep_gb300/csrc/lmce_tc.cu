@@ -568,6 +568,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           } else if (sphase) {
             // S phase of block b0+j: my 128 stream rows and my 64 X rows, SK atoms of K from 64 SK u
             const int bj = b0 + j + rt;   // < 2 nblk
+            if (lane == 0) dcheck(bj < 2 * nblk && t < T, p.err, BS_TMA_ROW);
             if (lane == 0) tma_load_3d_cg2(dst, &tmYs, bar, 0, (bj < nblk ? bj : bj - nblk) * G_YB + (int)rank * 128, u * SK);
             else if (lane == 1) tma_load_3d_cg2(dst + SK * 16384, &tmX, bar, 0, x0 + (int)rank * 64, u * SK);
           } else if (lane == 0) {
@@ -575,6 +576,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             // my 128 C of every chunk, one 4D box [chunk][atom][64 AQ rows][64]
             const int q = u - (j < nb ? KC : 0);
             const int bj = b0 + j - 1 + rt;   // < 2 nblk
+            dcheck(bj < 2 * nblk && q < 4 / AQ, p.err, BS_TMA_ROW);
             const int row = (bj < nblk ? bj : bj - nblk) * G_YB + q * 64 * AQ;
             tma_load_4d_cg2(dst, &tmYa, bar, 0, row, 2 * (int)rank, p.ch0);
           }
@@ -753,7 +755,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       const int c0 = (p.ch0 + i) * 256 + (int)rank * 128;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const int y = col_y[wr + 16 * j];   // rows without a target read row 0 and ignore it
+        int y = col_y[wr + 16 * j];   // rows without a target read row 0 and ignore it
+        if (!dcheck(y < p.V, p.err, BS_W_ROW)) y = 0;
         wv[j] = __ldg(reinterpret_cast<const uint4*>(p.Wt + (size_t)(y >= 0 ? y : 0) * p.C + c0) + ws);
       }
     };
@@ -827,7 +830,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           // this block's per-token constants and hits (last block's readers are past the barrier above)
           col_c[et] = cc;
           if (et == 0) hit_cnt[(gb + 1) & 1] = 0;
-          if (hr >= 0) hit[gb & 1][atomicAdd(&hit_cnt[gb & 1], 1)] = (uint16_t)((et << 8) | hr);
+          if (hr >= 0) {
+            const int hi = atomicAdd(&hit_cnt[gb & 1], 1);
+            if (dcheck(hi < G_YB, p.err, BS_HIT)) hit[gb & 1][hi] = (uint16_t)((et << 8) | hr);
+          }
         }
         asm volatile("bar.sync 1, 256;" ::: "memory");
         if (warp == 2 && lane == 0) {
@@ -873,7 +879,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             else ps3 += pv;
           }
           lacc += (ps0 + ps1) + (ps2 + ps3);
-          if (tmax > p.fl_limit) atomicOr(p.tile_flag + t, 1u);
+          if (tmax > p.fl_limit && dcheck(t < T, p.err, BS_TILE_FLAG)) atomicOr(p.tile_flag + t, 1u);
         } else if (DW) {
           // my columns whose token targets my row: dz there is s (p - 1)
           uint64_t fix = 0;
@@ -935,6 +941,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       if (epi_abort) break;
       tc_fence_after();
       const int slot = 2 * pi + (sg == 0 ? 0 : 1);
+      // the launch has at most tc_pairs() pairs: a slot past the partial buffer is reported and
+      // its plain stores skipped (its TMA stores are clipped to the buffer's rows)
+      const bool slot_ok = dcheck(slot < (int)gridDim.x, p.err, BS_SLOT);
       if (FL) {
         // l_x of my rows (four quarters, fixed order); s / l_x for both CTAs' rows via DSMEM
         fl_red[ks][xr] = lacc;
@@ -946,7 +955,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           st_cluster_f32(mapa(smem_u32(&fl_f[xl]), peer), f);
           if (whole) {
             if (xg < p.N) p.lse_out[xg] = (m2 + log2f(l)) * LN2;
-          } else {
+          } else if (slot_ok) {
             p.part_lm[((size_t)slot * 2 + 0) * G_XT + xl] = m2;
             p.part_lm[((size_t)slot * 2 + 1) * G_XT + xl] = l;
           }
@@ -1014,7 +1023,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             float v[32];
             tmem_ld32(tmem + i * 128 + lane_off + hf * 64 + cc * 32, v);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) part[(size_t)(hf * 64 + cc * 32 + e) * p.C + c] = v[e];
+            for (int e = 0; e < 32; ++e)
+              if (slot_ok) part[(size_t)(hf * 64 + cc * 32 + e) * p.C + c] = v[e];
           }
         }
       } else {
@@ -1100,7 +1110,12 @@ __global__ void __launch_bounds__(256) tc_split_combine_kernel(GradParams p, Sch
   __shared__ float fac[G_XT];       // lse+dh: s / l for a valid target, else 0
   __shared__ int rowy[G_XT];        // dh passes: each row's target, or -1
   const int t = sp.t[blockIdx.x];
-  if (threadIdx.x == 0) nslots = split_slots(sch, t, slots);
+  if (threadIdx.x == 0) {
+    int ns = split_slots(sch, t, slots);
+    for (int k = 0; k < ns; ++k)
+      if (!dcheck(slots[k] < 2 * sch.P, p.err, BS_SLOT)) ns = k;
+    nslots = ns;
+  }
   __syncthreads();
   const int nX = DW ? p.V : p.N;
   const float s = grad_scale(p);

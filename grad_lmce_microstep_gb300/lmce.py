@@ -14,6 +14,7 @@ import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "liblmce.so")
+DEBUG_LIB_PATH = os.path.join(HERE, "liblmce_dbg.so")   # built with the device bounds checks
 
 OK = 0
 ERR_ARG = 1
@@ -23,6 +24,7 @@ ERR_BAD_TARGET = 4
 ERR_NO_VALID = 5
 ERR_NONFINITE = 6
 ERR_STATE = 7
+ERR_INTERNAL = 8
 
 DTYPES = {"bf16": 0, "fp32": 1}
 NORMS = {"global": 0, "micro_mean": 1}
@@ -33,7 +35,8 @@ TORCH_DTYPES = {"bf16": torch.bfloat16, "fp32": torch.float32}
 EXPORTS = ("lmce_create", "lmce_microstep", "lmce_finalize", "lmce_destroy", "lmce_status_string",
            "lmce_launch_count", "lmce_selected_path", "lmce_profile", "lmce_profile_read",
            "lmce_microstep_noalloc", "lmce_dw_sumsq", "lmce_adamw", "lmce_microstep_compact",
-           "lmce_microstep_ln", "lmce_microstep_ln_compact", "lmce_test_stall_next_microstep", "lmce_clip_coef")
+           "lmce_microstep_ln", "lmce_microstep_ln_compact", "lmce_test_stall_next_microstep", "lmce_clip_coef",
+           "lmce_debug_bounds", "lmce_test_bounds_limit")
 
 NOALLOC_MAX_N = 65536
 
@@ -107,6 +110,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.lmce_clip_coef.restype = i32
     L.lmce_test_stall_next_microstep.argtypes = [vp, i64]
     L.lmce_test_stall_next_microstep.restype = i32
+    L.lmce_debug_bounds.argtypes = []
+    L.lmce_debug_bounds.restype = i32
+    L.lmce_test_bounds_limit.argtypes = [vp, i64]
+    L.lmce_test_bounds_limit.restype = i32
     _lib = L
     return L
 
@@ -308,6 +315,11 @@ class Lmce:
         """Failure-detection test hook: the next micro-step's tensor-core gradient launches start
         no load and give up after wait_ns (lmce_finalize then reports LMCE_ERR_CUDA)."""
         return int(self.lib.lmce_test_stall_next_microstep(self.handle, int(wait_ns)))
+
+    def test_bounds_limit(self, rows: int) -> int:
+        """Debug-build test hook: the compaction's bounds checks see `rows` compact rows
+        (lmce_test_bounds_limit); the release build returns ERR_STATE."""
+        return int(self.lib.lmce_test_bounds_limit(self.handle, int(rows)))
 
     def profile(self, enable: bool):
         """Record CUDA events around every kernel launch (enable=True clears old records)."""

@@ -58,6 +58,7 @@ extern "C" {
 #define LMCE_ERR_NO_VALID    5  /* the step has no valid target                             */
 #define LMCE_ERR_NONFINITE   6  /* the summed loss is not finite (finalize)                 */
 #define LMCE_ERR_STATE       7  /* call out of order (e.g. finalize before any micro-step)  */
+#define LMCE_ERR_INTERNAL    8  /* a bounds check of the debug build failed (finalize)      */
 
 /* ---- configuration ----------------------------------------------------------------- */
 typedef enum { LMCE_BF16 = 0, LMCE_FP32 = 1 } lmce_dtype;
@@ -305,6 +306,28 @@ LMCE_API int lmce_selected_path(const lmce_handle* h);
  *         the SIMT path, whose kernels have no such waits).
  */
 LMCE_API int lmce_test_stall_next_microstep(lmce_handle* h, int64_t wait_ns);
+
+/*
+ * Debug build (no counterpart in the pages: a checking aid for this library).  Built with
+ * LMCE_DEBUG_BOUNDS=1 (grad_lmce_microstep_gb300.build.build(debug_bounds=True) makes
+ * liblmce_dbg.so beside liblmce.so), the kernels check their computed indices before the
+ * accesses they guard: the row coordinates of the tensor-core passes' TMA boxes, the one-hot
+ * hit list, the split-tile partial slots, the repair flags, the one-hot rows of W, and the
+ * compaction's positions.  A check that fails records the site in the step's error word and
+ * the access is skipped; nothing traps, and lmce_finalize returns LMCE_ERR_INTERNAL.  The
+ * release build compiles the checks away.
+ *
+ * lmce_debug_bounds -- 1 in the debug build, 0 in the release build.  Needs no device.
+ *
+ * lmce_test_bounds_limit -- test hook of the debug build: the compaction's checks treat the
+ * compact buffers as holding `rows` rows (0 <= rows <= max_N; max_N restores them), so a step
+ * with more valid rows than that reports LMCE_ERR_INTERNAL at finalize without any access
+ * outside the real buffers.  That step's outputs are undefined.
+ * Errors: LMCE_ERR_ARG (null handle, rows out of range), LMCE_ERR_STATE (the release build, or
+ *         a handle created without LMCE_COMPACT_VALID_ROWS).
+ */
+LMCE_API int lmce_debug_bounds(void);
+LMCE_API int lmce_test_bounds_limit(lmce_handle* h, int64_t rows);
 
 /* ---- kernel timing (benchmark instrumentation) --------------------------------------
  * When enabled, the library records a CUDA event pair around every kernel it launches

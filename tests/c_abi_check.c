@@ -41,6 +41,11 @@ int main(void) {
   expect("profile", lmce_profile(NULL, 1), LMCE_ERR_ARG);
   expect("test_stall_next_microstep", lmce_test_stall_next_microstep(NULL, 1000000), LMCE_ERR_ARG);
   expect("clip_coef(NULL)", lmce_clip_coef(1.0, 1.0, NULL), LMCE_ERR_ARG);
+  expect("test_bounds_limit", lmce_test_bounds_limit(NULL, 0), LMCE_ERR_ARG);
+  if (lmce_debug_bounds() != 0 && lmce_debug_bounds() != 1) {
+    printf("debug_bounds\n");
+    ++failures;
+  }
   {
     float c = 0.f;
     expect("clip_coef(4, 1)", lmce_clip_coef(4.0, 1.0, &c), LMCE_OK);

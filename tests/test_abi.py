@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(8):
+    for code in range(9):
         assert M.status_string(code) and M.status_string(code) != "unknown status"
     assert M.status_string(99) == "unknown status"
 
@@ -123,3 +123,20 @@ def test_cuda_failure_reaches_the_caller_as_a_status(lib):
     assert lib.lmce_create(ctypes.byref(cfg), ctypes.c_void_p(256), ctypes.byref(h)) == M.ERR_CUDA
     assert h.value is None
     assert M.status_string(M.ERR_CUDA) != "unknown status"
+
+
+def test_release_build_has_no_bounds_checks(lib):
+    assert lib.lmce_debug_bounds() == 0
+    assert lib.lmce_test_bounds_limit(None, 0) == M.ERR_ARG
+
+
+def test_debug_build_compiles_the_bounds_checks():
+    # the debug build (LMCE_DEBUG_BOUNDS=1) cross-compiles here like the release one, exports the
+    # same entry points, and says it is the debug build (a host call: no device needed)
+    path = B.build(debug_bounds=True)
+    assert os.path.basename(path) == "liblmce_dbg.so"
+    dbg = ctypes.CDLL(path)
+    for name in declared():
+        assert hasattr(dbg, name), name
+    assert dbg.lmce_debug_bounds() == 1
+    assert dbg.lmce_test_bounds_limit(None, 0) == M.ERR_ARG
