@@ -4,15 +4,16 @@
 #include <string.h>
 #include <math.h>
 
+#include <mutex>
 #include <new>
 
 #include "lmce.h"
+
 #include "lmce_internal.cuh"
 
 namespace lmce {
 namespace {
 
-constexpr int FIN_T = 256;
 
 // One block sums the per-block partials of a micro-step in a fixed order (each thread a
 // fixed strided subset, then a fixed tree), then updates the step accumulators.
@@ -21,54 +22,14 @@ constexpr int FIN_T = 256;
 //   micro-mean norm: s = 1 / (valid_k * G), 0 for a micro-step without valid targets
 // ("Multi-GPU calculation of gradients for accelerated training", section "Gradient
 // accumulation averages across micro-steps").
+static_assert(LMCE_NORM_GLOBAL == 0 && LMCE_NORM_MICRO_MEAN == 1, "finish_block's norm codes");
+
 __global__ void __launch_bounds__(FIN_T) finish_kernel(const double* __restrict__ part_loss,
                                                        const int* __restrict__ part_cnt,
                                                        const unsigned* __restrict__ part_err,
                                                        int64_t nparts, int norm, int G,
                                                        long long global_valid, DevAcc* acc, int mode) {
-  __shared__ double sl[FIN_T];
-  __shared__ long long sc[FIN_T];
-  __shared__ unsigned se[FIN_T];
-  const int t = threadIdx.x;
-  double l = 0.0;
-  long long c = 0;
-  unsigned e = 0;
-  for (int64_t i = t; i < nparts; i += FIN_T) {
-    if (mode != FIN_COUNT) l += part_loss[i];
-    if (mode != FIN_LOSS) c += part_cnt[i];
-    e |= part_err[i];
-  }
-  sl[t] = l;
-  sc[t] = c;
-  se[t] = e;
-  __syncthreads();
-  for (int o = FIN_T / 2; o > 0; o >>= 1) {
-    if (t < o) {
-      sl[t] += sl[t + o];
-      sc[t] += sc[t + o];
-      se[t] |= se[t + o];
-    }
-    __syncthreads();
-  }
-  if (t == 0) {
-    const double loss_k = sl[0];
-    const long long cnt_k = sc[0];
-    acc->err |= se[0];
-    if (mode != FIN_LOSS) {
-      double s;
-      if (norm == LMCE_NORM_GLOBAL) s = global_valid > 0 ? 1.0 / (double)global_valid : 0.0;
-      else s = cnt_k > 0 ? 1.0 / ((double)cnt_k * (double)G) : 0.0;
-      acc->scale = (float)s;
-      acc->scale64 = s;
-      acc->count += cnt_k;
-    }
-    if (mode != FIN_COUNT) {
-      acc->loss_sum += loss_k;
-      acc->objective += acc->scale64 * loss_k;
-      if (!isfinite(loss_k)) acc->err |= ERR_BIT_NONFINITE;
-      acc->micro += 1;
-    }
-  }
+  finish_block(part_loss, part_cnt, part_err, nparts, norm, G, global_valid, acc, mode);
 }
 
 // Sum of squares of n floats to float64 accuracy without float64 arithmetic per element (a
@@ -231,6 +192,40 @@ cudaError_t launch_finish(const StepArgs& a, const Scratch& s, int64_t nparts, L
 
 }  // namespace lmce
 
+namespace lmce {
+
+cudaError_t max_dyn_smem(const void* func, int bytes) {
+  // a fixed table (no heap use: the allocation-free entry point goes through here too); when it
+  // is full the attribute is simply set on every call
+  struct Entry {
+    int dev;
+    const void* func;
+    int bytes;
+  };
+  constexpr int CAP = 256;
+  static std::mutex mu;
+  static Entry tab[CAP];
+  static int used = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i) {
+    Entry& x = tab[i];
+    if (x.dev == dev && x.func == func) {
+      if (x.bytes >= bytes) return cudaSuccess;
+      e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      if (e == cudaSuccess) x.bytes = bytes;
+      return e;
+    }
+  }
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && used < CAP) tab[used++] = {dev, func, bytes};
+  return e;
+}
+
+}  // namespace lmce
+
 using namespace lmce;
 
 struct lmce_handle {
@@ -272,6 +267,7 @@ static void free_scratch(lmce_handle* h) {
   cudaFree(h->sc.part_cnt);
   cudaFree(h->sc.part_err);
   cudaFree(h->sc.acc);
+  cudaFree(h->sc.ticket);
   cudaFree(h->sc.tc_part_m);
   cudaFree(h->sc.tc_part_l);
   cudaFree(h->sc.tc_zt);
@@ -345,6 +341,8 @@ extern "C" int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out)
             cudaMalloc(&h->sc.part_cnt, sizeof(int) * parts) == cudaSuccess &&
             cudaMalloc(&h->sc.part_err, sizeof(unsigned) * parts) == cudaSuccess &&
             cudaMalloc(&h->sc.acc, sizeof(DevAcc)) == cudaSuccess &&
+            cudaMalloc(&h->sc.ticket, sizeof(unsigned)) == cudaSuccess &&
+            cudaMemset(h->sc.ticket, 0, sizeof(unsigned)) == cudaSuccess &&
             cudaMallocHost(&h->host_acc, sizeof(DevAcc)) == cudaSuccess &&
             cudaMemset(h->sc.acc, 0, sizeof(DevAcc)) == cudaSuccess;
   if (ok && path != LMCE_PATH_SIMT) {

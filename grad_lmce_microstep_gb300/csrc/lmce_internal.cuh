@@ -139,6 +139,7 @@ struct Scratch {
   float* tc_part;      // gradient passes: fp32 partial sums of split tiles, [2 * pairs][128][C]
   float* tc_part_lm;   // logsumexp + dh pass: per-slot (base-2 max, sum) of split tiles, [2 * pairs][2][128]
   unsigned* tc_tile_flag;  // logsumexp + dh pass: per 128-token tile, 1 = recompute exactly
+  unsigned* ticket;    // row passes that reduce their own partials: blocks finished (0 between uses)
 };
 
 constexpr int TC_MAX_SPLIT = 32;
@@ -207,6 +208,11 @@ bool ln_compact_fusable(const LnArgs& a);
 cudaError_t ln_gather_forward(const LnArgs& a, const int32_t* targets, int64_t V, const CompactScratch& cs, Launch& L);
 cudaError_t ln_backward_scatter(const LnArgs& a, const CompactScratch& cs, int64_t n_valid, float* row_loss, Launch& L);
 
+// cudaFuncSetAttribute(func, MaxDynamicSharedMemorySize, bytes), made once per kernel and device
+// for the largest size asked so far (the host cost of the attribute call is otherwise paid on
+// every launch).
+cudaError_t max_dyn_smem(const void* func, int bytes);
+
 // Fixed-order reduction of the per-block partials of one micro-step into the step
 // accumulators; also computes this micro-step's gradient scale.  One launch.
 //   FIN_ALL  : loss, count and error partials (scale from the count)
@@ -214,6 +220,77 @@ cudaError_t ln_backward_scatter(const LnArgs& a, const CompactScratch& cs, int64
 //   FIN_LOSS : loss and error partials, with the scale FIN_COUNT set
 enum FinMode { FIN_ALL = 0, FIN_COUNT = 1, FIN_LOSS = 2 };
 cudaError_t launch_finish(const StepArgs& a, const Scratch& s, int64_t nparts, Launch& L, int mode = FIN_ALL);
+
+// The reduction itself, run by one block of FIN_T threads: thread t sums the partials t, t + FIN_T,
+// ... in order, then a fixed-shape tree adds the threads; thread 0 updates the accumulators.
+// Partials are read past L1 (another block may have just written them).  norm 0 is the global
+// normalisation (s = 1 / global_valid), 1 the micro-step mean (s = 1 / (count * G)).
+constexpr int FIN_T = 256;
+__device__ __forceinline__ void finish_block(const double* part_loss, const int* part_cnt, const unsigned* part_err,
+                                             int64_t nparts, int norm, int G, long long global_valid, DevAcc* acc,
+                                             int mode) {
+  __shared__ double fsl[FIN_T];
+  __shared__ long long fsc[FIN_T];
+  __shared__ unsigned fse[FIN_T];
+  const int t = threadIdx.x;
+  double l = 0.0;
+  long long c = 0;
+  unsigned e = 0;
+  for (int64_t i = t; i < nparts; i += FIN_T) {
+    if (mode != FIN_COUNT) l += __ldcg(part_loss + i);
+    if (mode != FIN_LOSS) c += __ldcg(part_cnt + i);
+    e |= __ldcg(part_err + i);
+  }
+  fsl[t] = l;
+  fsc[t] = c;
+  fse[t] = e;
+  __syncthreads();
+  for (int o = FIN_T / 2; o > 0; o >>= 1) {
+    if (t < o) {
+      fsl[t] += fsl[t + o];
+      fsc[t] += fsc[t + o];
+      fse[t] |= fse[t + o];
+    }
+    __syncthreads();
+  }
+  if (t == 0) {
+    const double loss_k = fsl[0];
+    const long long cnt_k = fsc[0];
+    acc->err |= fse[0];
+    if (mode != FIN_LOSS) {
+      double s;
+      if (norm == 0) s = global_valid > 0 ? 1.0 / (double)global_valid : 0.0;
+      else s = cnt_k > 0 ? 1.0 / ((double)cnt_k * (double)G) : 0.0;
+      acc->scale = (float)s;
+      acc->scale64 = s;
+      acc->count += cnt_k;
+    }
+    if (mode != FIN_COUNT) {
+      acc->loss_sum += loss_k;
+      acc->objective += acc->scale64 * loss_k;
+      if (!isfinite(loss_k)) acc->err |= ERR_BIT_NONFINITE;
+      acc->micro += 1;
+    }
+  }
+}
+
+// True in the one block of the grid that finishes last, once every block's earlier global writes
+// are visible; the ticket returns to 0 for the next use.  A block-wide call (no thread may skip
+// it); it only counts, it never waits on another block.
+__device__ __forceinline__ bool last_block(unsigned* ticket) {
+  __shared__ int is_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned n = gridDim.x * gridDim.y * gridDim.z;
+    const unsigned k = atomicAdd(ticket, 1u);
+    is_last = k == n - 1;
+    if (is_last) *ticket = 0u;   // every block has counted
+  }
+  __syncthreads();
+  if (is_last) __threadfence();
+  return is_last != 0;
+}
 // Loads the module that holds the reduction kernel (no launch).
 cudaError_t finish_load_kernel();
 

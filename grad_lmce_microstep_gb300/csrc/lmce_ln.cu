@@ -588,8 +588,7 @@ void launch_fwd_vec(const LnArgs& a, cudaStream_t st) {
 template <typename T, int KV>
 cudaError_t launch_bwd_vec(const LnArgs& a, int64_t nblk, int64_t rpb, cudaStream_t st) {
   const size_t smem = sizeof(float) * 2 * (lnb_threads<T, KV>() / 32) * (size_t)KV * 32 * Vec<T>::N;
-  cudaError_t e = cudaFuncSetAttribute(ln_bwd_vec_kernel<T, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  cudaError_t e = max_dyn_smem((const void*)ln_bwd_vec_kernel<T, KV>, (int)smem);
   if (e != cudaSuccess) return e;
   ln_bwd_vec_kernel<T, KV><<<(unsigned)nblk, lnb_threads<T, KV>(), smem, st>>>((const T*)a.dh, (const T*)a.x, a.gamma, a.mean,
                                                                a.rstd, a.N, a.C, a.rms, (T*)a.dx, a.part_g, a.part_b,
@@ -610,8 +609,7 @@ template <typename T, int KV>
 cudaError_t launch_bwd_scatter(const LnArgs& a, const CompactScratch& cs, int64_t n_valid, float* row_loss,
                                int64_t nblk, int64_t rpb, cudaStream_t st) {
   const size_t smem = sizeof(float) * 2 * (lnb_threads<T, KV>() / 32) * (size_t)KV * 32 * Vec<T>::N;
-  cudaError_t e = cudaFuncSetAttribute(ln_bwd_scatter_kernel<T, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  cudaError_t e = max_dyn_smem((const void*)ln_bwd_scatter_kernel<T, KV>, (int)smem);
   if (e != cudaSuccess) return e;
   ln_bwd_scatter_kernel<T, KV><<<(unsigned)nblk, lnb_threads<T, KV>(), smem, st>>>(
       (const T*)a.dh, (const T*)a.x, a.gamma, a.mean, a.rstd, cs.pos, n_valid, a.N, a.C, a.rms, (T*)a.dx, a.part_g,
@@ -685,7 +683,7 @@ cudaError_t ln_backward_t(const LnArgs& a, Launch& L) {
   cudaError_t e = cudaSuccess;
   if (kv == 0) {
     const size_t smem = sizeof(float) * 2 * (LN_T / 32) * (size_t)a.C;
-    e = cudaFuncSetAttribute(ln_bwd_rows_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = max_dyn_smem((const void*)ln_bwd_rows_kernel<T>, (int)smem);
     if (e != cudaSuccess) return e;
     L.begin(K_LN);
     ln_bwd_rows_kernel<T><<<(unsigned)nblk, LN_T, smem, L.st>>>((const T*)a.dh, (const T*)a.x, a.gamma, a.mean,

@@ -278,12 +278,13 @@ static cudaError_t simt_grads_t(const StepArgs& a, const Scratch& sc, Launch& L)
   auto kdw = simt_grad_kernel<T, true>;
   auto kdh = simt_grad_kernel<T, false>;
   // the static tiles (~15 KB) plus R*C floats can exceed the default 48 KB window
-  cudaFuncSetAttribute(kdw, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  cudaFuncSetAttribute(kdh, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = max_dyn_smem((const void*)kdw, (int)smem);
+  if (e == cudaSuccess) e = max_dyn_smem((const void*)kdh, (int)smem);
+  if (e != cudaSuccess) return e;
   L.begin(K_DW);
   kdw<<<(unsigned)((a.V + R - 1) / R), NT, smem, L.st>>>(a, sc.lse, sc.acc, nullptr);
   L.end();
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   L.begin(K_DH);
   kdh<<<(unsigned)simt_parts(a.N), NT, smem, L.st>>>(a, sc.lse, sc.acc, nullptr);
@@ -327,7 +328,8 @@ cudaError_t simt_repair_lse(const StepArgs& a, const Scratch& sc, Launch& L) {
 cudaError_t simt_repair_dh(const StepArgs& a, const Scratch& sc, Launch& L) {
   const size_t smem = simt_grad_smem(a.C);
   auto kdh = simt_grad_kernel<__nv_bfloat16, false>;
-  cudaFuncSetAttribute(kdh, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t e = max_dyn_smem((const void*)kdh, (int)smem);
+  if (e != cudaSuccess) return e;
   L.begin(K_DH);
   const unsigned ntiles = (unsigned)((a.N + TC_TILE_ROWS - 1) / TC_TILE_ROWS);
   const dim3 grid(ntiles, TC_TILE_ROWS / R);

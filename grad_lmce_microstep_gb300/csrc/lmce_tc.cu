@@ -1222,8 +1222,11 @@ __global__ void __launch_bounds__(256) tc_split_combine_kernel(GradParams p, Sch
 // ---- per-row pre / post passes of the lse+dh path -----------------------------------------
 
 // Before the lse+dh pass when the scale depends on this micro-step's valid count
-// (normalisation by the micro-step mean): per-block valid counts and target errors.
-__global__ void __launch_bounds__(256) rows_pre_kernel(StepArgs a, int* __restrict__ part_cnt, unsigned* __restrict__ part_err) {
+// (normalisation by the micro-step mean): per-block valid counts and target errors; the block
+// that finishes last reduces them (count mode), which sets the scale.
+__global__ void __launch_bounds__(256) rows_pre_kernel(StepArgs a, int* __restrict__ part_cnt, unsigned* __restrict__ part_err,
+                                                       const double* __restrict__ part_loss, DevAcc* acc,
+                                                       unsigned* ticket) {
   __shared__ int sc[256];
   __shared__ unsigned se[256];
   const int t = threadIdx.x;
@@ -1249,15 +1252,20 @@ __global__ void __launch_bounds__(256) rows_pre_kernel(StepArgs a, int* __restri
     part_cnt[blockIdx.x] = sc[0];
     part_err[blockIdx.x] = se[0];
   }
+  if (last_block(ticket))
+    finish_block(part_loss, part_cnt, part_err, gridDim.x, a.norm, a.G, (long long)a.global_valid, acc, FIN_COUNT);
 }
 
 // After the lse+dh pass and its repairs: row loss lse - z_t, per-block loss partials for the
 // fixed-order sum, valid counts and target / non-finite errors; the repair flags of this
-// block's two 128-token tiles are cleared for the next micro-step.
+// block's two 128-token tiles are cleared for the next micro-step.  The block that finishes
+// last reduces the partials into the step accumulators (fin_mode: FIN_ALL, or FIN_LOSS after
+// the count pass).
 __global__ void __launch_bounds__(256) rows_post_kernel(StepArgs a, const float* __restrict__ lse,
                                                         const float* __restrict__ zt, double* __restrict__ part_loss,
                                                         int* __restrict__ part_cnt, unsigned* __restrict__ part_err,
-                                                        unsigned* __restrict__ tile_flag, int ntiles) {
+                                                        unsigned* __restrict__ tile_flag, int ntiles, DevAcc* acc,
+                                                        unsigned* ticket, int fin_mode) {
   __shared__ double sl[256];
   __shared__ int sc[256];
   __shared__ unsigned se[256];
@@ -1297,6 +1305,8 @@ __global__ void __launch_bounds__(256) rows_post_kernel(StepArgs a, const float*
     part_cnt[blockIdx.x] = sc[0];
     part_err[blockIdx.x] = se[0];
   }
+  if (last_block(ticket))
+    finish_block(part_loss, part_cnt, part_err, gridDim.x, a.norm, a.G, (long long)a.global_valid, acc, fin_mode);
 }
 
 // ---- host side ------------------------------------------------------------------------
@@ -1313,48 +1323,87 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// Encoded tensor maps, reused across launches: a map is a function of its kind, base address,
+// extents and box alone, so an entry stays right even after its buffer is freed and another is
+// made at the same address.  A fixed table with round-robin replacement (no heap use).
+struct MapKey {
+  int kind;
+  const void* ptr;
+  uint64_t rows, cols;
+  uint32_t a, b;
+  bool operator==(const MapKey& o) const {
+    return kind == o.kind && ptr == o.ptr && rows == o.rows && cols == o.cols && a == o.a && b == o.b;
+  }
+};
+template <typename Enc>
+bool cached_map(const MapKey& k, CUtensorMap* m, Enc encode) {
+  constexpr int CAP = 64;
+  static std::mutex mu;
+  static MapKey keys[CAP];
+  static CUtensorMap maps[CAP];
+  static int used = 0, next = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (keys[i] == k) {
+      *m = maps[i];
+      return true;
+    }
+  if (!encode(m)) return false;
+  const int slot = used < CAP ? used++ : next;
+  if (used == CAP) next = (slot + 1) % CAP;
+  keys[slot] = k;
+  maps[slot] = *m;
+  return true;
+}
+
 // The same matrix seen as [cols/64][rows][64]: box {64, box_rows, box_chunks} loads box_chunks
 // consecutive 64-column swizzle atoms of box_rows rows in one instruction.
 bool make_map3(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_chunks) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {64, rows, cols / 64};
-  cuuint64_t strides[2] = {cols * 2, 128};
-  cuuint32_t box[3] = {64, box_rows, box_chunks};
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return cached_map({3, ptr, rows, cols, box_rows, box_chunks}, m, [&](CUtensorMap* out) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {64, rows, cols / 64};
+    cuuint64_t strides[2] = {cols * 2, 128};
+    cuuint32_t box[3] = {64, box_rows, box_chunks};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  });
 }
 
 // [cols/256][4][rows][64] view: box {64, box_rows, 2, box_chunks} loads, for box_chunks
 // consecutive 256-column chunks, two 64-column atoms (this CTA's half of the chunk) of box_rows
 // rows in one instruction.
 bool make_map4(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_chunks) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[4] = {64, rows, 4, cols / 256};
-  cuuint64_t strides[3] = {cols * 2, 128, 512};
-  cuuint32_t box[4] = {64, box_rows, 2, box_chunks};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return cached_map({4, ptr, rows, cols, box_rows, box_chunks}, m, [&](CUtensorMap* out) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {64, rows, 4, cols / 256};
+    cuuint64_t strides[3] = {cols * 2, 128, 512};
+    cuuint32_t box[4] = {64, box_rows, 2, box_chunks};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  });
 }
 
 // Row-major [rows][cols] fp32 or bf16 matrix, box {128 columns, box_rows rows}, no swizzle: the
 // gradient kernels' flush writes its staged tiles through these (stores and reduce-adds).
 bool make_map_rows(CUtensorMap* m, void* ptr, uint64_t rows, uint64_t cols, bool f32, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const uint64_t es = f32 ? 4 : 2;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * es};
-  cuuint32_t box[2] = {128, box_rows};
-  cuuint32_t el[2] = {1, 1};
-  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, el,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return cached_map({f32 ? 5 : 6, ptr, rows, cols, box_rows, 0}, m, [&](CUtensorMap* out) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const uint64_t es = f32 ? 4 : 2;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * es};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t el[2] = {1, 1};
+    return fn(out, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box,
+              el, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  });
 }
 
 int num_sms() {
@@ -1420,11 +1469,12 @@ cudaError_t tc_lse(const StepArgs& a, const Scratch& sc, Launch& L) {
   p.ignore_id = a.ignore_id;
   p.vtiles = vtiles;
   p.nsplit = nsplit;
-  cudaFuncSetAttribute(tc_lse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L_SMEM);
+  cudaError_t e = max_dyn_smem((const void*)tc_lse_kernel, L_SMEM);
+  if (e != cudaSuccess) return e;
   L.begin(K_LSE);
   tc_lse_kernel<<<dim3(2 * nblocks, nsplit), L_THREADS, L_SMEM, L.st>>>(mh, mw, p);
   L.end();
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t nparts = tc_parts(a.N);
   L.begin(K_FINISH);
@@ -1504,11 +1554,12 @@ cudaError_t tc_grad_range(const StepArgs& a, const Scratch& sc, Launch& L, int c
   if (P < 1) P = 1;
   const Sched sch{U, (int)P, nblk};
   const int smem = geo_smem_bytes<MODE>();
-  cudaFuncSetAttribute(tc_grad_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = max_dyn_smem((const void*)tc_grad_kernel<MODE>, smem);
+  if (e != cudaSuccess) return e;
   L.begin(MODE == GM_DW ? K_DW : MODE == GM_DH ? K_DH : K_LSE_DH);
   tc_grad_kernel<MODE><<<(unsigned)(2 * P), G_THREADS, smem, L.st>>>(mx, mys, mya, mo, mp, p);
   L.end();
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   SplitTiles sp;
   sp.n = 0;
@@ -1539,9 +1590,10 @@ cudaError_t tc_grad(const StepArgs& a, const Scratch& sc, Launch& L) {
 }
 
 // Default order.  With global normalisation the scale is the caller's 1 / global_valid and the
-// one-pass logsumexp + dh runs first; with the micro-step mean, a count pass and its finish set
-// the scale before it.  Then: the exact repair of flagged tiles (two near-empty launches when
-// none is flagged), the row losses and counts, their fixed-order reduction, the dW pass.
+// one-pass logsumexp + dh runs first; with the micro-step mean, a count pass sets the scale
+// before it (its last block to finish reduces the counts).  Then: the exact repair of flagged
+// tiles (two near-empty launches when none is flagged), the row losses and counts with their
+// fixed-order reduction (run by the pass's last block), the dW pass.
 static cudaError_t tc_microstep_fused(const StepArgs& a, const Scratch& sc, Launch& L) {
   const int64_t nparts = tc_parts(a.N);   // 256 rows per partial
   const int ntiles = (int)((a.N + TC_TILE_ROWS - 1) / TC_TILE_ROWS);
@@ -1549,20 +1601,19 @@ static cudaError_t tc_microstep_fused(const StepArgs& a, const Scratch& sc, Laun
   cudaError_t e;
   if (!global) {
     L.begin(K_FINISH);
-    rows_pre_kernel<<<(unsigned)nparts, 256, 0, L.st>>>(a, sc.part_cnt, sc.part_err);
+    rows_pre_kernel<<<(unsigned)nparts, 256, 0, L.st>>>(a, sc.part_cnt, sc.part_err, sc.part_loss, sc.acc, sc.ticket);
     L.end();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = launch_finish(a, sc, nparts, L, FIN_COUNT)) != cudaSuccess) return e;
   }
   if ((e = tc_grad<GM_FL>(a, sc, L)) != cudaSuccess) return e;
   if ((e = simt_repair_lse(a, sc, L)) != cudaSuccess) return e;
   if ((e = simt_repair_dh(a, sc, L)) != cudaSuccess) return e;
   L.begin(K_FINISH);
   rows_post_kernel<<<(unsigned)nparts, 256, 0, L.st>>>(a, sc.lse, sc.tc_zt, sc.part_loss, sc.part_cnt, sc.part_err,
-                                                       sc.tc_tile_flag, ntiles);
+                                                       sc.tc_tile_flag, ntiles, sc.acc, sc.ticket,
+                                                       global ? FIN_ALL : FIN_LOSS);
   L.end();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = launch_finish(a, sc, nparts, L, global ? FIN_ALL : FIN_LOSS)) != cudaSuccess) return e;
   return tc_grad<GM_DW>(a, sc, L);
 }
 
