@@ -240,7 +240,6 @@ def run_lmce(args, rank, world, local_rank):
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if sampler:
         sampler.start()
-    L.profile(True)
     launches0 = L.launches
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
@@ -251,9 +250,16 @@ def run_lmce(args, rank, world, local_rank):
     ev1.record(stream)
     barrier()
     launches = L.launches - launches0
+    clocks = sampler.stop() if sampler else None
+    # per-kernel device times: a second timed pass of the same steps with the library's CUDA-event
+    # records around every kernel (kept out of the pass above: the records sit between the
+    # launches and cost 1-5 % of a step)
+    L.profile(True)
+    for _ in range(args.steps):
+        step()
+    barrier()
     L.profile(False)
     prof = L.profile_read()
-    clocks = sampler.stop() if sampler else None
     # host cost of one micro-step call through the binding (argument checks, cached tensor maps,
     # the launches), timed on the host with no event records; the GPU work runs behind it
     host_ns = []
@@ -468,6 +474,7 @@ def run_lmce(args, rank, world, local_rank):
                      "peak_source": ("bf16_tflops (burst) of " + pk_kind) if bound == "tensor"
                      else "fp32 FFMA: 152 SMs x 128 lanes x 2 flop x max SM clock"},
         "kernels_ms": {k: {"total_ms": v[0], "launches": v[1], "avg_ms": v[0] / v[1]} for k, v in kinds.items()},
+        "kernels_ms_source": "a second timed pass of the same steps with CUDA events around every kernel",
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": int(launches),

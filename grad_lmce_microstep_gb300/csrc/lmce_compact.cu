@@ -23,6 +23,7 @@ __global__ void __launch_bounds__(CP_ROWS) compact_count_kernel(const int32_t* _
                                                                int64_t V, int32_t ignore_id,
                                                                int* __restrict__ blk_cnt,
                                                                unsigned* __restrict__ blk_err) {
+  griddep_wait();
   const int64_t n = (int64_t)blockIdx.x * CP_ROWS + threadIdx.x;
   int v = 0;
   unsigned e = 0;
@@ -46,6 +47,7 @@ __global__ void __launch_bounds__(SCAN_T) compact_scan_kernel(const int* __restr
                                                              int64_t nblk, int64_t* __restrict__ blk_off,
                                                              int64_t* __restrict__ total, int64_t n_valid,
                                                              DevAcc* acc) {
+  griddep_wait();
   __shared__ long long wsum[SCAN_T / 32];
   __shared__ long long carry;
   __shared__ unsigned err_all;
@@ -106,6 +108,7 @@ __global__ void __launch_bounds__(MV_T) compact_gather_kernel(const U* __restric
                                                              U* __restrict__ h_c, int32_t* __restrict__ y_c,
                                                              int32_t* __restrict__ pos, int64_t rows,
                                                              unsigned* err) {
+  griddep_wait();
   __shared__ int64_t rowpos[CP_ROWS];
   const int t = threadIdx.x;
   const int64_t r0 = (int64_t)blockIdx.x * CP_ROWS;
@@ -154,6 +157,7 @@ __global__ void __launch_bounds__(MV_T) compact_scatter_kernel(const int32_t* __
                                                               U* __restrict__ dh, const float* __restrict__ rl_c,
                                                               float* __restrict__ row_loss, int64_t cap,
                                                               unsigned* err) {
+  griddep_wait();
   __shared__ int64_t rowpos[CP_ROWS];
   const int t = threadIdx.x;
   const int64_t r0 = (int64_t)blockIdx.x * CP_ROWS;
@@ -195,16 +199,15 @@ int pick_vec(int64_t row_bytes, const void* a, const void* b) {
 
 template <typename U>
 void launch_gather(const StepArgs& a, const CompactScratch& cs, int64_t nblk, int64_t rb, cudaStream_t st) {
-  compact_gather_kernel<U><<<(unsigned)nblk, MV_T, 0, st>>>((const U*)a.hidden, a.targets, a.N, a.V,
-                                                            (unsigned)(rb / (int64_t)sizeof(U)), cs.blk_off,
-                                                            (U*)cs.h_c, cs.y_c, cs.pos, cs.rows, cs.err);
+  launch_pdl(compact_gather_kernel<U>, dim3((unsigned)nblk), dim3(MV_T), 0, st, (const U*)a.hidden, a.targets, a.N, a.V,
+             (unsigned)(rb / (int64_t)sizeof(U)), (const int64_t*)cs.blk_off, (U*)cs.h_c, cs.y_c, cs.pos, cs.rows, cs.err);
 }
 
 template <typename U>
 void launch_scatter(const StepArgs& a, const CompactScratch& cs, int64_t n_valid, int64_t rb, cudaStream_t st) {
-  compact_scatter_kernel<U><<<(unsigned)compact_blocks(a.N), MV_T, 0, st>>>(
-      cs.pos, a.N, n_valid, (unsigned)(rb / (int64_t)sizeof(U)), (const U*)cs.dh_c, (U*)a.dh, cs.rl_c, a.row_loss,
-      cs.rows, cs.err);
+  launch_pdl(compact_scatter_kernel<U>, dim3((unsigned)compact_blocks(a.N)), dim3(MV_T), 0, st, (const int32_t*)cs.pos,
+             a.N, n_valid, (unsigned)(rb / (int64_t)sizeof(U)), (const U*)cs.dh_c, (U*)a.dh, (const float*)cs.rl_c,
+             a.row_loss, cs.rows, cs.err);
 }
 
 }  // namespace
@@ -216,12 +219,13 @@ cudaError_t compact_count_scan(const StepArgs& a, const CompactScratch& cs, DevA
   const int64_t nblk = compact_blocks(a.N);
   if (nblk > 0) {
     L.begin(K_COMPACT);
-    compact_count_kernel<<<(unsigned)nblk, CP_ROWS, 0, L.st>>>(a.targets, a.N, a.V, a.ignore_id, cs.blk_cnt,
-                                                               cs.blk_err);
+    launch_pdl(compact_count_kernel, dim3((unsigned)nblk), dim3(CP_ROWS), 0, L.st, a.targets, a.N, a.V, a.ignore_id,
+               cs.blk_cnt, cs.blk_err);
     L.end();
   }
   L.begin(K_COMPACT);
-  compact_scan_kernel<<<1, SCAN_T, 0, L.st>>>(cs.blk_cnt, cs.blk_err, nblk, cs.blk_off, cs.total, n_valid, acc);
+  launch_pdl(compact_scan_kernel, dim3(1), dim3(SCAN_T), 0, L.st, (const int*)cs.blk_cnt, (const unsigned*)cs.blk_err, nblk,
+             cs.blk_off, cs.total, n_valid, acc);
   L.end();
   return cudaGetLastError();
 }

@@ -208,6 +208,26 @@ bool ln_compact_fusable(const LnArgs& a);
 cudaError_t ln_gather_forward(const LnArgs& a, const int32_t* targets, int64_t V, const CompactScratch& cs, Launch& L);
 cudaError_t ln_backward_scatter(const LnArgs& a, const CompactScratch& cs, int64_t n_valid, float* row_loss, Launch& L);
 
+// Programmatic dependent launch: the kernels of a micro-step are launched so that each may be
+// scheduled while the one before it on the stream drains; each kernel launched this way first
+// waits (griddep_wait) until the previous grid has completed and its writes are visible, before
+// it reads or writes anything.  Outside such a launch the wait returns at once.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // cudaFuncSetAttribute(func, MaxDynamicSharedMemorySize, bytes), made once per kernel and device
 // for the largest size asked so far (the host cost of the attribute call is otherwise paid on
 // every launch).

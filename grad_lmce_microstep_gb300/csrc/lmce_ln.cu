@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(LN_T, KV <= 3 ? 4 : 2) ln_fwd_vec_kernel(const
                                                          const float* __restrict__ beta, int64_t N, int64_t C,
                                                          int rms, float eps, T* __restrict__ h,
                                                          float* __restrict__ mean_out, float* __restrict__ rstd_out) {
+  griddep_wait();
   constexpr int VN = Vec<T>::N;
   const int lane = threadIdx.x & 31;
   const int64_t stride = (int64_t)gridDim.x * (LN_T / 32);
@@ -170,6 +171,7 @@ __global__ void __launch_bounds__(LN_T) ln_fwd_rows_kernel(const T* __restrict__
                                                           int rms, float eps, T* __restrict__ h,
                                                           float* __restrict__ mean_out,
                                                           float* __restrict__ rstd_out) {
+  griddep_wait();
   const int lane = threadIdx.x & 31;
   const int64_t n = (int64_t)blockIdx.x * (LN_T / 32) + (threadIdx.x >> 5);
   if (n >= N) return;
@@ -281,6 +283,7 @@ __global__ void __launch_bounds__(NT, 1) ln_bwd_vec_kernel(
     const T* __restrict__ dh, const T* __restrict__ x, const float* __restrict__ gamma,
     const float* __restrict__ mean_in, const float* __restrict__ rstd_in, int64_t N, int64_t C, int rms,
     T* __restrict__ dx, float* __restrict__ part_g, float* __restrict__ part_b, int64_t rpb) {
+  griddep_wait();
   constexpr int VN = Vec<T>::N;
   extern __shared__ float ln_slices[];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -335,6 +338,7 @@ __global__ void __launch_bounds__(LN_T, KV <= 3 ? 3 : 2) ln_gather_fwd_kernel(
     const float* __restrict__ gamma, const float* __restrict__ beta, int64_t N, int64_t C, int rms, float eps,
     T* __restrict__ h, float* __restrict__ mean_out, float* __restrict__ rstd_out, int32_t* __restrict__ y_c,
     int32_t* __restrict__ pos, int64_t rows, unsigned* err) {
+  griddep_wait();
   constexpr int VN = Vec<T>::N;
   const int lane = threadIdx.x & 31;
   const int64_t stride = (int64_t)gridDim.x * (LN_T / 32);
@@ -421,6 +425,7 @@ __global__ void __launch_bounds__(NT, 1) ln_bwd_scatter_kernel(
     int64_t n_valid, int64_t N, int64_t C, int rms, T* __restrict__ dx, float* __restrict__ part_g,
     float* __restrict__ part_b, int64_t rpb, const float* __restrict__ rl_c, float* __restrict__ row_loss,
     int64_t rows, unsigned* err) {
+  griddep_wait();
   constexpr int VN = Vec<T>::N;
   extern __shared__ float ln_slices[];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -478,6 +483,7 @@ __global__ void __launch_bounds__(LN_T) ln_bwd_rows_kernel(const T* __restrict__
                                                           const float* __restrict__ rstd_in, int64_t N, int64_t C,
                                                           int rms, T* __restrict__ dx, float* __restrict__ part_g,
                                                           float* __restrict__ part_b, int64_t rpb) {
+  griddep_wait();
   extern __shared__ float ln_slices[];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int64_t r0 = (int64_t)blockIdx.x * rpb, r1 = r0 + rpb < N ? r0 + rpb : N;
@@ -529,6 +535,7 @@ __global__ void __launch_bounds__(LNR_T) ln_param_reduce_kernel(const float* __r
                                                                const float* __restrict__ part_b, int64_t nblk,
                                                                int64_t C, int accumulate, float* __restrict__ dgamma,
                                                                float* __restrict__ dbeta) {
+  griddep_wait();
   constexpr int NW = LNR_T / 32;
   __shared__ float sg[NW][32], sb[NW][32];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -581,8 +588,8 @@ template <typename T, int KV>
 void launch_fwd_vec(const LnArgs& a, cudaStream_t st) {
   int64_t blocks = (a.N + LN_T / 32 - 1) / (LN_T / 32);
   if (blocks > 152 * LN_FWD_BLOCKS_PER_SM) blocks = 152 * LN_FWD_BLOCKS_PER_SM;   // warps loop over rows
-  ln_fwd_vec_kernel<T, KV><<<(unsigned)blocks, LN_T, 0, st>>>((const T*)a.x, a.gamma, a.beta, a.N, a.C, a.rms,
-                                                              a.eps, (T*)a.h, a.mean, a.rstd);
+  launch_pdl(ln_fwd_vec_kernel<T, KV>, dim3((unsigned)blocks), dim3(LN_T), 0, st, (const T*)a.x, a.gamma, a.beta, a.N, a.C,
+             (int)a.rms, a.eps, (T*)a.h, a.mean, a.rstd);
 }
 
 template <typename T, int KV>
@@ -590,19 +597,18 @@ cudaError_t launch_bwd_vec(const LnArgs& a, int64_t nblk, int64_t rpb, cudaStrea
   const size_t smem = sizeof(float) * 2 * (lnb_threads<T, KV>() / 32) * (size_t)KV * 32 * Vec<T>::N;
   cudaError_t e = max_dyn_smem((const void*)ln_bwd_vec_kernel<T, KV>, (int)smem);
   if (e != cudaSuccess) return e;
-  ln_bwd_vec_kernel<T, KV><<<(unsigned)nblk, lnb_threads<T, KV>(), smem, st>>>((const T*)a.dh, (const T*)a.x, a.gamma, a.mean,
-                                                               a.rstd, a.N, a.C, a.rms, (T*)a.dx, a.part_g, a.part_b,
-                                                               rpb);
-  return cudaSuccess;
+  return launch_pdl(ln_bwd_vec_kernel<T, KV>, dim3((unsigned)nblk), dim3(lnb_threads<T, KV>()), smem, st, (const T*)a.dh,
+                    (const T*)a.x, a.gamma, (const float*)a.mean, (const float*)a.rstd, a.N, a.C, (int)a.rms, (T*)a.dx,
+                    a.part_g, a.part_b, rpb);
 }
 
 template <typename T, int KV>
 void launch_gather_fwd(const LnArgs& a, const int32_t* y, int64_t V, const CompactScratch& cs, cudaStream_t st) {
   int64_t blocks = (a.N + LN_T / 32 - 1) / (LN_T / 32);
   if (blocks > 152 * LN_FWD_BLOCKS_PER_SM) blocks = 152 * LN_FWD_BLOCKS_PER_SM;   // warps loop over rows
-  ln_gather_fwd_kernel<T, KV><<<(unsigned)blocks, LN_T, 0, st>>>((const T*)a.x, y, V, cs.blk_off, a.gamma, a.beta,
-                                                                  a.N, a.C, a.rms, a.eps, (T*)a.h, a.mean, a.rstd,
-                                                                  cs.y_c, cs.pos, cs.rows, cs.err);
+  launch_pdl(ln_gather_fwd_kernel<T, KV>, dim3((unsigned)blocks), dim3(LN_T), 0, st, (const T*)a.x, y, V,
+             (const int64_t*)cs.blk_off, a.gamma, a.beta, a.N, a.C, (int)a.rms, a.eps, (T*)a.h, a.mean, a.rstd, cs.y_c,
+             cs.pos, cs.rows, cs.err);
 }
 
 template <typename T, int KV>
@@ -611,10 +617,10 @@ cudaError_t launch_bwd_scatter(const LnArgs& a, const CompactScratch& cs, int64_
   const size_t smem = sizeof(float) * 2 * (lnb_threads<T, KV>() / 32) * (size_t)KV * 32 * Vec<T>::N;
   cudaError_t e = max_dyn_smem((const void*)ln_bwd_scatter_kernel<T, KV>, (int)smem);
   if (e != cudaSuccess) return e;
-  ln_bwd_scatter_kernel<T, KV><<<(unsigned)nblk, lnb_threads<T, KV>(), smem, st>>>(
-      (const T*)a.dh, (const T*)a.x, a.gamma, a.mean, a.rstd, cs.pos, n_valid, a.N, a.C, a.rms, (T*)a.dx, a.part_g,
-      a.part_b, rpb, cs.rl_c, row_loss, cs.rows, cs.err);
-  return cudaSuccess;
+  return launch_pdl(ln_bwd_scatter_kernel<T, KV>, dim3((unsigned)nblk), dim3(lnb_threads<T, KV>()), smem, st,
+                    (const T*)a.dh, (const T*)a.x, a.gamma, (const float*)a.mean, (const float*)a.rstd,
+                    (const int32_t*)cs.pos, n_valid, a.N, a.C, (int)a.rms, (T*)a.dx, a.part_g, a.part_b, rpb,
+                    (const float*)cs.rl_c, row_loss, cs.rows, cs.err);
 }
 
 template <typename T>
@@ -650,8 +656,8 @@ cudaError_t ln_backward_scatter_t(const LnArgs& a, const CompactScratch& cs, int
   L.end();
   if (e != cudaSuccess) return e;
   L.begin(K_LN);
-  ln_param_reduce_kernel<<<(unsigned)((a.C + 31) / 32), LNR_T, 0, L.st>>>(a.part_g, a.part_b, nblk, a.C,
-                                                                          a.accumulate, a.dgamma, a.dbeta);
+  launch_pdl(ln_param_reduce_kernel, dim3((unsigned)((a.C + 31) / 32)), dim3(LNR_T), 0, L.st, (const float*)a.part_g,
+             (const float*)a.part_b, nblk, a.C, (int)a.accumulate, a.dgamma, a.dbeta);
   L.end();
   return cudaGetLastError();
 }
@@ -704,8 +710,8 @@ cudaError_t ln_backward_t(const LnArgs& a, Launch& L) {
     if (e != cudaSuccess) return e;
   }
   L.begin(K_LN);
-  ln_param_reduce_kernel<<<(unsigned)((a.C + 31) / 32), LNR_T, 0, L.st>>>(a.part_g, a.part_b, nblk, a.C,
-                                                                          a.accumulate, a.dgamma, a.dbeta);
+  launch_pdl(ln_param_reduce_kernel, dim3((unsigned)((a.C + 31) / 32)), dim3(LNR_T), 0, L.st, (const float*)a.part_g,
+             (const float*)a.part_b, nblk, a.C, (int)a.accumulate, a.dgamma, a.dbeta);
   L.end();
   return cudaGetLastError();
 }

@@ -161,6 +161,7 @@ __global__ void __launch_bounds__(NT) simt_lse_kernel(StepArgs a, float* __restr
                                                       int* __restrict__ part_cnt,
                                                       unsigned* __restrict__ part_err,
                                                       const unsigned* __restrict__ gate) {
+  griddep_wait();
   if (!gate) {
     simt_lse_rows<T>(a, lse_out, part_loss, part_cnt, part_err, blockIdx.x, false);
     return;
@@ -256,6 +257,7 @@ template <typename T, bool DW>
 __global__ void __launch_bounds__(NT) simt_grad_kernel(StepArgs a, const float* __restrict__ lse,
                                                        const DevAcc* __restrict__ acc_dev,
                                                        const unsigned* __restrict__ gate) {
+  griddep_wait();
   if (DW || !gate) {
     simt_grad_rows<T, DW>(a, lse, acc_dev, blockIdx.x);
     return;
@@ -320,22 +322,23 @@ cudaError_t simt_repair_lse(const StepArgs& a, const Scratch& sc, Launch& L) {
   L.begin(K_LSE);
   const unsigned ntiles = (unsigned)((a.N + TC_TILE_ROWS - 1) / TC_TILE_ROWS);
   const dim3 grid(ntiles, TC_TILE_ROWS / R);
-  simt_lse_kernel<__nv_bfloat16><<<grid, NT, 0, L.st>>>(a, sc.lse, nullptr, nullptr, nullptr, sc.tc_tile_flag);
+  const cudaError_t e = launch_pdl(simt_lse_kernel<__nv_bfloat16>, grid, dim3(NT), 0, L.st, a, sc.lse, nullptr, nullptr,
+                                   nullptr, sc.tc_tile_flag);
   L.end();
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t simt_repair_dh(const StepArgs& a, const Scratch& sc, Launch& L) {
   const size_t smem = simt_grad_smem(a.C);
   auto kdh = simt_grad_kernel<__nv_bfloat16, false>;
-  const cudaError_t e = max_dyn_smem((const void*)kdh, (int)smem);
+  cudaError_t e = max_dyn_smem((const void*)kdh, (int)smem);
   if (e != cudaSuccess) return e;
   L.begin(K_DH);
   const unsigned ntiles = (unsigned)((a.N + TC_TILE_ROWS - 1) / TC_TILE_ROWS);
   const dim3 grid(ntiles, TC_TILE_ROWS / R);
-  kdh<<<grid, NT, smem, L.st>>>(a, sc.lse, sc.acc, sc.tc_tile_flag);
+  e = launch_pdl(kdh, grid, dim3(NT), smem, L.st, a, sc.lse, sc.acc, sc.tc_tile_flag);
   L.end();
-  return cudaGetLastError();
+  return e;
 }
 
 // Loads the module of every SIMT kernel, both dtypes (with lazy module loading a module is

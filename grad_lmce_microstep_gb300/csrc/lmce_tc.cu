@@ -458,6 +458,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
   constexpr int NST = Geo<MODE>::NST, SLOT = Geo<MODE>::SLOT, SK = Geo<MODE>::SK, AQ = Geo<MODE>::AQ;
   constexpr int NDZ = Geo<MODE>::NDZ;
   static_assert(SK * 24576 <= SLOT && AQ * 16384 * 3 <= SLOT && 4 % AQ == 0, "stage does not fit its slot");
+  griddep_wait();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 128-byte-swizzled operands need 1024-byte alignment; the launch reserves no slack for
   // realigning, so a misaligned buffer is reported (both CTAs of the pair see the same layout
@@ -1109,6 +1110,7 @@ __global__ void __launch_bounds__(256) tc_split_combine_kernel(GradParams p, Sch
   __shared__ float wts[16][G_XT];   // lse+dh: 2^(m_k - M) per slot and row
   __shared__ float fac[G_XT];       // lse+dh: s / l for a valid target, else 0
   __shared__ int rowy[G_XT];        // dh passes: each row's target, or -1
+  griddep_wait();
   const int t = sp.t[blockIdx.x];
   if (threadIdx.x == 0) {
     int ns = split_slots(sch, t, slots);
@@ -1227,6 +1229,7 @@ __global__ void __launch_bounds__(256) tc_split_combine_kernel(GradParams p, Sch
 __global__ void __launch_bounds__(256) rows_pre_kernel(StepArgs a, int* __restrict__ part_cnt, unsigned* __restrict__ part_err,
                                                        const double* __restrict__ part_loss, DevAcc* acc,
                                                        unsigned* ticket) {
+  griddep_wait();
   __shared__ int sc[256];
   __shared__ unsigned se[256];
   const int t = threadIdx.x;
@@ -1266,6 +1269,7 @@ __global__ void __launch_bounds__(256) rows_post_kernel(StepArgs a, const float*
                                                         int* __restrict__ part_cnt, unsigned* __restrict__ part_err,
                                                         unsigned* __restrict__ tile_flag, int ntiles, DevAcc* acc,
                                                         unsigned* ticket, int fin_mode) {
+  griddep_wait();
   __shared__ double sl[256];
   __shared__ int sc[256];
   __shared__ unsigned se[256];
@@ -1557,9 +1561,10 @@ cudaError_t tc_grad_range(const StepArgs& a, const Scratch& sc, Launch& L, int c
   cudaError_t e = max_dyn_smem((const void*)tc_grad_kernel<MODE>, smem);
   if (e != cudaSuccess) return e;
   L.begin(MODE == GM_DW ? K_DW : MODE == GM_DH ? K_DH : K_LSE_DH);
-  tc_grad_kernel<MODE><<<(unsigned)(2 * P), G_THREADS, smem, L.st>>>(mx, mys, mya, mo, mp, p);
+  e = launch_pdl(tc_grad_kernel<MODE>, dim3((unsigned)(2 * P)), dim3(G_THREADS), (size_t)smem, L.st, mx, mys, mya, mo,
+                 mp, p);
   L.end();
-  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   if (e != cudaSuccess) return e;
   SplitTiles sp;
   sp.n = 0;
@@ -1573,9 +1578,10 @@ cudaError_t tc_grad_range(const StepArgs& a, const Scratch& sc, Launch& L, int c
   }
   if (sp.n == 0) return cudaSuccess;
   L.begin(K_FINISH);
-  tc_split_combine_kernel<MODE><<<dim3((unsigned)sp.n, (unsigned)COMB_BLOCKS), 256, 0, L.st>>>(p, sch, sp);
+  e = launch_pdl(tc_split_combine_kernel<MODE>, dim3((unsigned)sp.n, (unsigned)COMB_BLOCKS), dim3(256), 0, L.st, p, sch,
+                 sp);
   L.end();
-  return cudaGetLastError();
+  return e;
 }
 
 template <int MODE>
@@ -1601,19 +1607,19 @@ static cudaError_t tc_microstep_fused(const StepArgs& a, const Scratch& sc, Laun
   cudaError_t e;
   if (!global) {
     L.begin(K_FINISH);
-    rows_pre_kernel<<<(unsigned)nparts, 256, 0, L.st>>>(a, sc.part_cnt, sc.part_err, sc.part_loss, sc.acc, sc.ticket);
+    e = launch_pdl(rows_pre_kernel, dim3((unsigned)nparts), dim3(256), 0, L.st, a, sc.part_cnt, sc.part_err, sc.part_loss,
+                   sc.acc, sc.ticket);
     L.end();
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (e != cudaSuccess) return e;
   }
   if ((e = tc_grad<GM_FL>(a, sc, L)) != cudaSuccess) return e;
   if ((e = simt_repair_lse(a, sc, L)) != cudaSuccess) return e;
   if ((e = simt_repair_dh(a, sc, L)) != cudaSuccess) return e;
   L.begin(K_FINISH);
-  rows_post_kernel<<<(unsigned)nparts, 256, 0, L.st>>>(a, sc.lse, sc.tc_zt, sc.part_loss, sc.part_cnt, sc.part_err,
-                                                       sc.tc_tile_flag, ntiles, sc.acc, sc.ticket,
-                                                       global ? FIN_ALL : FIN_LOSS);
+  e = launch_pdl(rows_post_kernel, dim3((unsigned)nparts), dim3(256), 0, L.st, a, sc.lse, sc.tc_zt, sc.part_loss,
+                 sc.part_cnt, sc.part_err, sc.tc_tile_flag, ntiles, sc.acc, sc.ticket, (int)(global ? FIN_ALL : FIN_LOSS));
   L.end();
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (e != cudaSuccess) return e;
   return tc_grad<GM_DW>(a, sc, L);
 }
 
