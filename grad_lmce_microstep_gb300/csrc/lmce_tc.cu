@@ -358,6 +358,9 @@ constexpr int G_EPI_WARPS = 8;
 constexpr int G_THREADS = 128 + 32 * G_EPI_WARPS;  // warps 0 and 10 TMA, 1 MMA, 2-9 epilogue, 11 ring waiter
 
 enum GradMode { GM_DW = 0, GM_DH = 1, GM_FL = 2 };
+// Named barriers of the gradient kernels: 1 the epilogue warps, 2 .. 2 + NST - 1 the ring slots'
+// hand-offs from the waiter warp to the MMA warp, then the dz tile's hand-off.
+constexpr int HB_DZ_FULL = 6;
 constexpr float FL_HEADROOM = 32.f;        // lse+dh pass: reference above the first block's maximum (base 2)
 
 // Ring geometry per mode: NST slots of SLOT bytes.  An S stage carries SK 64-column atoms of
@@ -370,6 +373,7 @@ constexpr float FL_HEADROOM = 32.f;        // lse+dh pass: reference above the f
 template <int MODE>
 struct Geo {
   static constexpr int NST = 4, SLOT = 49152, SK = 2, AQ = 1, NDZ = 1;
+  static_assert(2 + NST <= HB_DZ_FULL, "ring hand-off barriers overlap the dz tile's");
 };
 template <int MODE>
 constexpr int geo_smem_bytes() {
@@ -608,6 +612,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       const uint64_t dXs = sdesc_sw128(smem_u32(sY) + SK * 16384, 16, 1024);
       const uint64_t dYa = sdesc_sw128(smem_u32(sY), AQ * 8192, 1024);      // accumulation, MN-major
       const uint64_t dDZ = sdesc_sw128(smem_u32(sDZ), 16, 1024);            // dz, K-major
+      // the block's dz tile, handed over by the waiter warp through named barrier HB_DZ_FULL
+      auto dz_take = [&]() -> bool {
+        asm volatile("bar.sync %0, 64;" ::"n"(HB_DZ_FULL) : "memory");
+        return !wt_abort;
+      };
       bool ok = true;
       int it = 0, g = 0, sg = 0;              // stage counter, global block counter, segment counter
       for (int t = t_first; t <= t_last && ok; ++t, ++sg) {
@@ -655,7 +664,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             }
             for (int q = 0; q < 4 / AQ && ok; ++q) {
               // the whole dz tile of the block (one wait per block: the epilogue is far ahead)
-              if (q == 0 && !wait_w(smem_u32(&dz_full[db]), (gb / NDZ) & 1, true, 23)) {
+              if (q == 0 && !dz_take()) {
                 ok = false;
                 break;
               }
@@ -695,21 +704,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
   } else if (warp == 11) {
     // ---------------- ring waiter (leader CTA) ----------------
     // Waits on each ring stage's full barrier in the MMA warp's order and hands the stage over
-    // through named barrier 2 + slot.  An mbarrier wait in the MMA warp itself sits behind the
-    // MMAs it has just issued and took ~190 cycles even on a completed phase, long enough for the
-    // tensor pipe to run dry after every stage; a named barrier does not.  The waiter is at most
-    // NST stages ahead (a slot refills only after the MMA warp took it), so every slot's barrier
-    // sees one arrival per use.  A wait that runs out sets wt_abort, which the MMA warp reads
-    // after its barrier.
+    // through named barrier 2 + slot; before a block's accumulation stages it also waits for
+    // that block's dz tile and hands it over through HB_DZ_FULL.  An mbarrier wait in the MMA warp
+    // itself sits behind the MMAs it has just issued and took ~190 cycles even on a completed
+    // phase, long enough for the tensor pipe to run dry after every stage; a named barrier does
+    // not.  The waiter is at most NST stages ahead (a slot refills only after the MMA warp took
+    // it) and one dz tile ahead (the next one is written only after the accumulation that the MMA
+    // warp issues after taking this one), so every barrier sees one arrival per use.  (The S
+    // tile's release stays an mbarrier wait of the MMA warp: handed over too, it measured slower,
+    // since the waiter then stalls on it before the ring stages behind it.)  A wait that runs out
+    // sets wt_abort, which the MMA warp reads after its barrier.
     if (rank == 0) {
       bool ok = true;
-      int it = 0;
+      int it = 0, g = 0;
       for (int t = t_first; t <= t_last && ok; ++t) {
         const int b0 = (int)(max(ub, (long long)t * nblk) - (long long)t * nblk);
         const int nb = (int)(min(ue, (long long)(t + 1) * nblk) - (long long)t * nblk) - b0;
         for (int j = 0; j <= nb && ok; ++j) {
           const int nst = (j < nb ? KC : 0) + (j >= 1 ? 4 / AQ : 0);
           for (int u = 0; u < nst; ++u, ++it) {
+            if (j >= 1 && u == (j < nb ? KC : 0)) {
+              // block j - 1's dz tile, before its first accumulation stage
+              const int gb = g + j - 1;
+              const bool wd =
+                  __all_sync(0xffffffffu, mbar_wait_cluster(smem_u32(&dz_full[gb % NDZ]), (gb / NDZ) & 1, wait_ns));
+              if (!wd) {
+                if (lane == 0) record_timeout(p.err, 23);
+                wt_abort = 1;
+                ok = false;
+              }
+              __syncwarp();
+              asm volatile("bar.arrive %0, 64;" ::"n"(HB_DZ_FULL) : "memory");
+              if (!ok) break;
+            }
             const int st = it % NST;
             const bool w = __all_sync(0xffffffffu, mbar_wait(smem_u32(&full[st]), (it / NST) & 1, wait_ns));
             if (!w) {
@@ -722,6 +749,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             if (!ok) break;
           }
         }
+        g += nb;
       }
     }
   } else if (warp <= 9) {
