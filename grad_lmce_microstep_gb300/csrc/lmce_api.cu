@@ -37,8 +37,9 @@ __global__ void __launch_bounds__(FIN_T) finish_kernel(const double* __restrict_
 // into x*x + fma(x, x, -x*x), and a thread accumulates its terms as a double-single pair (S, E)
 // with Knuth's TwoSum, in round-to-nearest intrinsics the compiler may not contract.  Block b
 // takes the fixed range [b*per, (b+1)*per) in 16-byte steps, each thread a fixed strided subset
-// in order; the threads' S + E are added in float64 in a fixed-shape tree, and one block adds
-// the blocks' partials in block order.  The same order on every call.
+// in order; the threads' S + E are added in float64 in a fixed-shape tree, and the block that
+// finishes last (a ticket, no waiting) adds the blocks' partials in block order.  The same order
+// on every call.
 struct DSum {
   float S = 0.f, E = 0.f;
   __device__ __forceinline__ void add_sq(float x) {
@@ -53,7 +54,7 @@ struct DSum {
 };
 constexpr int SQ_T = 256, SQ_BLOCKS = 608;   // 4 blocks per SM of a 152-SM GB300
 __global__ void __launch_bounds__(SQ_T) sumsq_part_kernel(const float* __restrict__ x, int64_t n, int64_t per,
-                                                         double* __restrict__ part) {
+                                                         double* __restrict__ part, unsigned* ticket) {
   __shared__ double sh[SQ_T];
   const int64_t b0 = (int64_t)blockIdx.x * per, b1 = b0 + per < n ? b0 + per : n;
   DSum d;
@@ -92,20 +93,17 @@ __global__ void __launch_bounds__(SQ_T) sumsq_part_kernel(const float* __restric
     __syncthreads();
   }
   if (threadIdx.x == 0) part[blockIdx.x] = sh[0];
-}
-
-__global__ void __launch_bounds__(SQ_T) sumsq_final_kernel(const double* __restrict__ part, int nparts,
-                                                          double* __restrict__ out) {
-  __shared__ double sh[SQ_T];
+  // the block that finishes last adds the blocks' partials in block order into part[gridDim.x]
+  if (!last_block(ticket)) return;
   double acc = 0.0;
-  for (int i = threadIdx.x; i < nparts; i += SQ_T) acc += part[i];
+  for (int i = threadIdx.x; i < (int)gridDim.x; i += SQ_T) acc += __ldcg(part + i);
   sh[threadIdx.x] = acc;
   __syncthreads();
   for (int o = SQ_T / 2; o > 0; o >>= 1) {
     if (threadIdx.x < o) sh[threadIdx.x] += sh[threadIdx.x + o];
     __syncthreads();
   }
-  if (threadIdx.x == 0) *out = sh[0];
+  if (threadIdx.x == 0) part[gridDim.x] = sh[0];
 }
 
 // One AdamW step over the tied matrix, each element read and written once (30 bytes: dW, p, m, v
@@ -341,8 +339,8 @@ extern "C" int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out)
             cudaMalloc(&h->sc.part_cnt, sizeof(int) * parts) == cudaSuccess &&
             cudaMalloc(&h->sc.part_err, sizeof(unsigned) * parts) == cudaSuccess &&
             cudaMalloc(&h->sc.acc, sizeof(DevAcc)) == cudaSuccess &&
-            cudaMalloc(&h->sc.ticket, sizeof(unsigned)) == cudaSuccess &&
-            cudaMemset(h->sc.ticket, 0, sizeof(unsigned)) == cudaSuccess &&
+            cudaMalloc(&h->sc.ticket, 2 * sizeof(unsigned)) == cudaSuccess &&
+            cudaMemset(h->sc.ticket, 0, 2 * sizeof(unsigned)) == cudaSuccess &&
             cudaMallocHost(&h->host_acc, sizeof(DevAcc)) == cudaSuccess &&
             cudaMemset(h->sc.acc, 0, sizeof(DevAcc)) == cudaSuccess;
   if (ok && path != LMCE_PATH_SIMT) {
@@ -711,10 +709,7 @@ extern "C" int lmce_dw_sumsq(lmce_handle* h, double* sumsq, void* stream) {
   L.st = st;
   L.prof = &h->prof;
   L.begin(K_FINISH);
-  sumsq_part_kernel<<<SQ_BLOCKS, SQ_T, 0, st>>>(h->dW, n, per, h->sumsq_part);
-  L.end();
-  L.begin(K_FINISH);
-  sumsq_final_kernel<<<1, SQ_T, 0, st>>>(h->sumsq_part, SQ_BLOCKS, h->sumsq_part + SQ_BLOCKS);
+  sumsq_part_kernel<<<SQ_BLOCKS, SQ_T, 0, st>>>(h->dW, n, per, h->sumsq_part, h->sc.ticket + 1);
   L.end();
   h->launches += L.n;
   if (cudaGetLastError() != cudaSuccess) return LMCE_ERR_CUDA;

@@ -139,7 +139,8 @@ struct Scratch {
   float* tc_part;      // gradient passes: fp32 partial sums of split tiles, [2 * pairs][128][C]
   float* tc_part_lm;   // logsumexp + dh pass: per-slot (base-2 max, sum) of split tiles, [2 * pairs][2][128]
   unsigned* tc_tile_flag;  // logsumexp + dh pass: per 128-token tile, 1 = recompute exactly
-  unsigned* ticket;    // row passes that reduce their own partials: blocks finished (0 between uses)
+  unsigned* ticket;    // [2] blocks finished, 0 between uses: [0] the row passes that reduce their
+                       // own partials, [1] the squared dW norm
 };
 
 constexpr int TC_MAX_SPLIT = 32;
