@@ -273,3 +273,30 @@ def test_launch_count_and_kernel_timing():
     L.close()
     assert n == sum(v[1] for v in prof.values()) and n >= 2 * 3
     assert all(v[0] > 0 for v in prof.values() if v[1] > 0)
+
+
+def test_tensor_map_cache_eviction_keeps_results_exact():
+    # The tensor-core path reuses encoded TMA maps from a 64-entry table keyed by address, extents
+    # and box.  Forty micro-steps, each with its own input and output buffers (about five new maps
+    # per launch), cycle that table several times over; every micro-step must still equal a run
+    # on the original buffers, bit for bit.
+    w = I.custom([200], 256, 1000, "bf16", seed=7)
+    W, mbs = to_dev(w)
+    (h, y), = mbs
+    gv = int(((y >= 0) & (y < w.V)).sum())
+    dW = torch.empty(w.V, w.C, device="cuda")
+    L = M.Lmce(w.C, w.V, 200, dW, "bf16", path="tcgen05")
+    ref_dh = torch.empty_like(h)
+    L.microstep(h, W, y, gv, ref_dh)
+    L.finalize()
+    ref_dW = dW.clone()
+    keep = []   # every buffer stays alive, so no address is handed out twice
+    for k in range(40):
+        hk, yk, Wk = h.clone(), y.clone(), W.clone()
+        dh = torch.empty_like(hk)
+        keep.append((hk, yk, Wk, dh))
+        L.microstep(hk, Wk, yk, gv, dh)
+        L.finalize()
+        assert torch.equal(dh, ref_dh), k
+        assert torch.equal(dW, ref_dW), k
+    L.close()
