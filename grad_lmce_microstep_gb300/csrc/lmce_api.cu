@@ -272,6 +272,8 @@ static void free_scratch(lmce_handle* h) {
   cudaFree(h->sc.tc_part);
   cudaFree(h->sc.tc_part_lm);
   cudaFree(h->sc.tc_tile_flag);
+  cudaFree(h->sc.rep_part);
+  cudaFree(h->sc.rep_ticket);
   cudaFree(h->sumsq_part);
   h->sumsq_part = nullptr;
   cudaFree(h->cs.h_c);
@@ -351,7 +353,10 @@ extern "C" int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out)
          cudaMalloc(&h->sc.tc_part, tc_part_bytes(cfg->C)) == cudaSuccess &&
          cudaMalloc(&h->sc.tc_part_lm, tc_part_lm_bytes()) == cudaSuccess &&
          cudaMalloc(&h->sc.tc_tile_flag, sizeof(unsigned) * tiles) == cudaSuccess &&
-         cudaMemset(h->sc.tc_tile_flag, 0, sizeof(unsigned) * tiles) == cudaSuccess;
+         cudaMemset(h->sc.tc_tile_flag, 0, sizeof(unsigned) * tiles) == cudaSuccess &&
+         cudaMalloc(&h->sc.rep_part, sizeof(float) * simt_repair_part_floats(cfg->C)) == cudaSuccess &&
+         cudaMalloc(&h->sc.rep_ticket, sizeof(unsigned) * tiles * (TC_TILE_ROWS / 16)) == cudaSuccess &&
+         cudaMemset(h->sc.rep_ticket, 0, sizeof(unsigned) * tiles * (TC_TILE_ROWS / 16)) == cudaSuccess;
   }
   ok = ok && cudaMalloc(&h->sumsq_part, sizeof(double) * (SQ_BLOCKS + 1)) == cudaSuccess;
   if (ok && (cfg->flags & LMCE_COMPACT_VALID_ROWS)) {

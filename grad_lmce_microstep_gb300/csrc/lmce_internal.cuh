@@ -141,6 +141,9 @@ struct Scratch {
   unsigned* tc_tile_flag;  // logsumexp + dh pass: per 128-token tile, 1 = recompute exactly
   unsigned* ticket;    // [2] blocks finished, 0 between uses: [0] the row passes that reduce their
                        // own partials, [1] the squared dW norm
+  // tensor-core path, exact repair of flagged tiles
+  float* rep_part;     // [simt_repair_part_floats(C)] per-slice (max, sum) and dh partials
+  unsigned* rep_ticket;  // [tiles * 8] per row group: slices finished (0 between uses)
 };
 
 constexpr int TC_MAX_SPLIT = 32;
@@ -323,11 +326,14 @@ cudaError_t simt_microstep(const StepArgs& a, const Scratch& s, Launch& L);
 cudaError_t simt_grads(const StepArgs& a, const Scratch& s, Launch& L);
 // Loads the module of every SIMT kernel for both dtypes (no launch).
 cudaError_t simt_load_kernels();
-// Exact logsumexp and dh of the rows of the 128-token tiles whose flag is set (every other
-// block returns at once): the repair of the one-pass logsumexp + dh kernel.
+// Exact logsumexp and dh of the rows of the 128-token tiles whose flag is set: the repair of the
+// one-pass logsumexp + dh kernel.  Two persistent launches whose blocks find the flagged tiles
+// themselves and return at once when there is none; the work of the flagged tiles' rows is split
+// over every SM by vocabulary slice and merged in slice order.
 constexpr int TC_TILE_ROWS = 128;
 cudaError_t simt_repair_lse(const StepArgs& a, const Scratch& s, Launch& L);
 cudaError_t simt_repair_dh(const StepArgs& a, const Scratch& s, Launch& L);
+size_t simt_repair_part_floats(int64_t C);
 
 // Tensor-core path (tcgen05 + TMA).
 bool tc_supported(int64_t C, int64_t V, int bf16);

@@ -68,11 +68,11 @@ __device__ __forceinline__ void logit_tile(const T* __restrict__ X, int64_t own0
   }
 }
 
-// Rows grp*R .. grp*R + R - 1.  repair == false: the lse pass of the SIMT path (lse, row loss,
-// the group's partials at index grp); repair == true: only the logsumexp.
+// Rows grp*R .. grp*R + R - 1: the lse pass of the SIMT path (lse, row loss, the group's partials
+// at index grp).
 template <typename T>
 __device__ void simt_lse_rows(const StepArgs& a, float* __restrict__ lse_out, double* __restrict__ part_loss,
-                              int* __restrict__ part_cnt, unsigned* __restrict__ part_err, int64_t grp, bool repair) {
+                              int* __restrict__ part_cnt, unsigned* __restrict__ part_err, int64_t grp) {
   __shared__ float Xs[BK][R];
   __shared__ float Ys[BK][BT + 1];
   __shared__ float zt[R];
@@ -113,10 +113,6 @@ __device__ void simt_lse_rows(const StepArgs& a, float* __restrict__ lse_out, do
     m = mn;
   }
   __syncthreads();
-  if (repair) {
-    if (q == 0 && n < a.N) lse_out[n] = m + logf(l);
-    return;
-  }
   if (q == 0) {
     double loss = 0.0;
     int valid = 0;
@@ -151,25 +147,13 @@ __device__ void simt_lse_rows(const StepArgs& a, float* __restrict__ lse_out, do
   }
 }
 
-// gate == nullptr: the lse pass of the SIMT path, one block per R rows.
-// gate != nullptr: repair mode, grid (128-token tiles, R-row groups of a tile): a block of a
-// flagged tile takes the logsumexp of its R rows, so a tile's groups run on separate SMs; the
-// blocks of other tiles return at once.
+// The lse pass of the SIMT path, one block per R rows.
 template <typename T>
 __global__ void __launch_bounds__(NT) simt_lse_kernel(StepArgs a, float* __restrict__ lse_out,
                                                       double* __restrict__ part_loss,
                                                       int* __restrict__ part_cnt,
-                                                      unsigned* __restrict__ part_err,
-                                                      const unsigned* __restrict__ gate) {
-  griddep_wait();
-  if (!gate) {
-    simt_lse_rows<T>(a, lse_out, part_loss, part_cnt, part_err, blockIdx.x, false);
-    return;
-  }
-  if (!gate[blockIdx.x]) return;  // block-uniform
-  const int64_t grp = (int64_t)blockIdx.x * (TC_TILE_ROWS / R) + blockIdx.y;
-  if (grp * R >= a.N) return;
-  simt_lse_rows<T>(a, lse_out, part_loss, part_cnt, part_err, grp, true);
+                                                      unsigned* __restrict__ part_err) {
+  simt_lse_rows<T>(a, lse_out, part_loss, part_cnt, part_err, blockIdx.x);
 }
 
 // Owned rows grp*R .. grp*R + R - 1.
@@ -249,23 +233,223 @@ __device__ void simt_grad_rows(const StepArgs& a, const float* __restrict__ lse,
   }
 }
 
-// gate == nullptr: one block per R owned rows.
-// gate != nullptr (dh pass only): repair mode, grid (128-token tiles, R-row groups of a tile): a
-// block of a flagged tile writes the dh rows of its R rows; the blocks of other tiles return at
-// once.
+// The gradient passes of the SIMT path: one block per R owned rows.
 template <typename T, bool DW>
 __global__ void __launch_bounds__(NT) simt_grad_kernel(StepArgs a, const float* __restrict__ lse,
-                                                       const DevAcc* __restrict__ acc_dev,
-                                                       const unsigned* __restrict__ gate) {
-  griddep_wait();
-  if (DW || !gate) {
-    simt_grad_rows<T, DW>(a, lse, acc_dev, blockIdx.x);
-    return;
+                                                       const DevAcc* __restrict__ acc_dev) {
+  simt_grad_rows<T, DW>(a, lse, acc_dev, blockIdx.x);
+}
+
+// ---- exact repair of the one-pass tensor-core logsumexp + dh kernel -----------------------
+// The rows of the 128-token tiles whose flag is set get their logsumexp and dh recomputed with
+// the exact two-pass arithmetic above.  Both kernels are persistent (one block per SM): every
+// block finds the flagged tiles itself (nothing flagged: every block returns after reading the
+// flags), and the work items (flagged tile, R-row group, vocabulary slice) are spread over the
+// blocks, the slices chosen so that about one item falls on each SM.  A row group's slices are
+// merged by the block that finishes the group's last item (a ticket per group, counted, never
+// waited on), in slice order: deterministic.
+constexpr int REP_BLOCKS = 152;   // one per SM of a 152-SM GB300
+constexpr int REP_VS_MAX = 32;    // most vocabulary slices per row group
+constexpr int REP_GROUPS = TC_TILE_ROWS / R;
+
+// Vocabulary slices per row group for `groups` groups (1 when there are enough groups to go round).
+__device__ __forceinline__ int rep_slices(int groups) {
+  const int nv = REP_BLOCKS / groups;
+  return nv < 1 ? 1 : (nv > REP_VS_MAX ? REP_VS_MAX : nv);
+}
+
+// The flagged tiles in tile order, into list[]; returns how many.  A block-wide call.
+__device__ int rep_flagged(const unsigned* __restrict__ flag, int ntiles, int* list) {
+  __shared__ int wsum[NT / 32];
+  __shared__ int found;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (threadIdx.x == 0) found = 0;
+  __syncthreads();
+  for (int b = 0; b < ntiles; b += NT) {
+    const int i = b + threadIdx.x;
+    const bool f = i < ntiles && flag[i] != 0u;
+    const unsigned bal = __ballot_sync(0xffffffffu, f);
+    if (lane == 0) wsum[w] = __popc(bal);
+    __syncthreads();
+    int off = found;
+    for (int k = 0; k < w; ++k) off += wsum[k];
+    if (f) list[off + __popc(bal & ((1u << lane) - 1u))] = i;
+    __syncthreads();
+    if (threadIdx.x == 0)
+      for (int k = 0; k < NT / 32; ++k) found += wsum[k];
+    __syncthreads();
   }
-  if (!gate[blockIdx.x]) return;  // block-uniform
-  const int64_t grp = (int64_t)blockIdx.x * (TC_TILE_ROWS / R) + blockIdx.y;
-  if (grp * R >= a.N) return;
-  simt_grad_rows<T, DW>(a, lse, acc_dev, grp);
+  return found;
+}
+
+// True in the block that finishes the last of a group's `nv` items (after its writes are visible
+// device-wide); that block then merges the group.  The ticket returns to 0.  A block-wide call.
+__device__ __forceinline__ bool rep_last_item(unsigned* ticket, int nv) {
+  __shared__ int last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    last = atomicAdd(ticket, 1u) == (unsigned)nv - 1u;
+    if (last) *ticket = 0u;
+  }
+  __syncthreads();
+  if (last) __threadfence();
+  return last != 0;
+}
+
+// Logsumexp of rows n0 .. n0 + R - 1 over the vocabulary rows [v0, v1): per-row running
+// (max, sum) with natural-base exponentials, as the SIMT lse pass.  Thread (r, q) holds row r.
+template <typename T>
+__device__ void rep_lse_range(const StepArgs& a, int64_t n0, int64_t v0, int64_t v1, float& m, float& l,
+                              float (*Xs)[R], float (*Ys)[BT + 1]) {
+  const T* H = static_cast<const T*>(a.hidden);
+  const T* W = static_cast<const T*>(a.W);
+  const int q = threadIdx.x & 15;
+  m = -INFINITY;
+  l = 0.f;
+  for (int64_t t0 = v0; t0 < v1; t0 += BT) {
+    float s[4];
+    logit_tile(H, n0, a.N, W, t0, v1, a.C, s, Xs, Ys);
+    float tmax = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (t0 + q + 16 * j < v1) tmax = fmaxf(tmax, s[j]);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+    const float mn = fmaxf(m, tmax);
+    float ts = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (t0 + q + 16 * j < v1) ts += expf(s[j] - mn);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) ts += __shfl_xor_sync(0xffffffffu, ts, o);
+    l = (m == -INFINITY ? 0.f : l * expf(m - mn)) + ts;
+    m = mn;
+  }
+}
+
+// part: [REP_BLOCKS][2][R] (max, sum) of the items of groups split into slices.
+__global__ void __launch_bounds__(NT) repair_lse_kernel(StepArgs a, const unsigned* __restrict__ flag, int ntiles,
+                                                        float* __restrict__ lse_out, float* __restrict__ part,
+                                                        unsigned* __restrict__ ticket) {
+  griddep_wait();
+  __shared__ float Xs[BK][R];
+  __shared__ float Ys[BK][BT + 1];
+  extern __shared__ int rep_list[];
+  const int nf = rep_flagged(flag, ntiles, rep_list);
+  if (nf == 0) return;
+  const int groups = nf * REP_GROUPS, nv = rep_slices(groups);
+  const int64_t vw = ((a.V + nv - 1) / nv + BT - 1) / BT * BT;   // slice width, whole logit tiles
+  const int r = threadIdx.x >> 4, q = threadIdx.x & 15;
+  for (int it = blockIdx.x; it < groups * nv; it += gridDim.x) {
+    const int gi = it / nv, v = it % nv;
+    const int64_t n0 = (int64_t)rep_list[gi / REP_GROUPS] * TC_TILE_ROWS + (gi % REP_GROUPS) * R;
+    if (n0 >= a.N) continue;   // the whole group lies past the rows: none of its items runs
+    const int64_t v0 = (int64_t)v * vw, v1 = v0 + vw < a.V ? v0 + vw : a.V;
+    float m, l;
+    rep_lse_range<__nv_bfloat16>(a, n0, v0, v1, m, l, Xs, Ys);
+    if (nv == 1) {
+      if (q == 0 && n0 + r < a.N) lse_out[n0 + r] = m + logf(l);
+      continue;
+    }
+    if (q == 0) {
+      part[((size_t)it * 2 + 0) * R + r] = m;
+      part[((size_t)it * 2 + 1) * R + r] = l;
+    }
+    if (rep_last_item(ticket + gi, nv) && q == 0 && n0 + r < a.N) {
+      float M = -INFINITY;
+      for (int k = 0; k < nv; ++k) M = fmaxf(M, __ldcg(part + ((size_t)(gi * nv + k) * 2 + 0) * R + r));
+      float L = 0.f;
+      for (int k = 0; k < nv; ++k) {
+        const float mk = __ldcg(part + ((size_t)(gi * nv + k) * 2 + 0) * R + r);
+        if (mk != -INFINITY) L += __ldcg(part + ((size_t)(gi * nv + k) * 2 + 1) * R + r) * expf(mk - M);
+      }
+      lse_out[n0 + r] = M + logf(L);
+    }
+  }
+}
+
+// part: [REP_BLOCKS][R][C] fp32 dh partials of the items of groups split into slices.  Dynamic
+// shared memory: the R x C accumulator, then the flagged-tile list.
+__global__ void __launch_bounds__(NT) repair_dh_kernel(StepArgs a, const unsigned* __restrict__ flag, int ntiles,
+                                                       const float* __restrict__ lse, const DevAcc* __restrict__ acc_dev,
+                                                       float* __restrict__ part, unsigned* __restrict__ ticket) {
+  griddep_wait();
+  __shared__ float Xs[BK][R];
+  __shared__ float Ys[BK][BT + 1];
+  __shared__ float dzs[R][BT];
+  extern __shared__ float accs[];   // [R][C], then the list
+  int* rep_list = reinterpret_cast<int*>(accs + (size_t)R * a.C);
+  const int nf = rep_flagged(flag, ntiles, rep_list);
+  if (nf == 0) return;
+  const int groups = nf * REP_GROUPS, nv = rep_slices(groups);
+  const int64_t vw = ((a.V + nv - 1) / nv + BT - 1) / BT * BT;
+  const __nv_bfloat16* H = static_cast<const __nv_bfloat16*>(a.hidden);
+  const __nv_bfloat16* W = static_cast<const __nv_bfloat16*>(a.W);
+  const int tid = threadIdx.x, r = tid >> 4, q = tid & 15;
+  // global normalisation: the caller's 1 / global_valid; micro-step mean: the count pass's scale
+  const float s = a.norm == 0 ? (float)(1.0 / (double)a.global_valid) : acc_dev->scale;
+  for (int it = blockIdx.x; it < groups * nv; it += gridDim.x) {
+    const int gi = it / nv, v = it % nv;
+    const int64_t n0 = (int64_t)rep_list[gi / REP_GROUPS] * TC_TILE_ROWS + (gi % REP_GROUPS) * R;
+    if (n0 >= a.N) continue;
+    const int64_t v0 = (int64_t)v * vw, v1 = v0 + vw < a.V ? v0 + vw : a.V;
+    for (int64_t i = tid; i < (int64_t)R * a.C; i += NT) accs[i] = 0.f;
+    int y = -1;
+    float ln = 0.f;
+    if (n0 + r < a.N) {
+      const int t = a.targets[n0 + r];
+      if (target_valid(t, a.V)) {
+        y = t;
+        ln = lse[n0 + r];
+      }
+    }
+    __syncthreads();
+    for (int64_t t0 = v0; t0 < v1; t0 += BT) {
+      float sv[4];
+      logit_tile(H, n0, a.N, W, t0, v1, a.C, sv, Xs, Ys);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t vv = t0 + q + 16 * j;
+        dzs[r][q + 16 * j] = (y >= 0 && vv < v1) ? s * (expf(sv[j] - ln) - (vv == y ? 1.f : 0.f)) : 0.f;
+      }
+      __syncthreads();
+      const int64_t tn = v1 - t0 < BT ? v1 - t0 : BT;
+      for (int64_t c = tid; c < a.C; c += NT) {
+        float av[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) av[i] = accs[i * a.C + c];
+        for (int t = 0; t < tn; ++t) {
+          const float wv = to_f(W[(t0 + t) * a.C + c]);
+#pragma unroll
+          for (int i = 0; i < R; ++i) av[i] = fmaf(dzs[i][t], wv, av[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < R; ++i) accs[i * a.C + c] = av[i];
+      }
+      __syncthreads();
+    }
+    __nv_bfloat16* dh = static_cast<__nv_bfloat16*>(a.dh);
+    if (nv == 1) {
+      for (int64_t i = tid; i < (int64_t)R * a.C; i += NT) {
+        const int64_t rr = i / a.C, c = i % a.C;
+        if (n0 + rr < a.N) from_f(accs[i], dh + (n0 + rr) * a.C + c);
+      }
+      __syncthreads();   // accs is reused by the next item
+      continue;
+    }
+    float* mine = part + (size_t)it * R * a.C;
+    for (int64_t i = tid; i < (int64_t)R * a.C; i += NT) mine[i] = accs[i];
+    if (rep_last_item(ticket + gi, nv)) {
+      for (int64_t i = tid; i < (int64_t)R * a.C; i += NT) {
+        const int64_t rr = i / a.C, c = i % a.C;
+        float sum = 0.f;
+        for (int k = 0; k < nv; ++k) sum += __ldcg(part + (size_t)(gi * nv + k) * R * a.C + i);
+        if (n0 + rr < a.N) from_f(sum, dh + (n0 + rr) * a.C + c);
+      }
+    }
+    __syncthreads();
+  }
 }
 
 }  // namespace
@@ -284,12 +468,12 @@ static cudaError_t simt_grads_t(const StepArgs& a, const Scratch& sc, Launch& L)
   if (e == cudaSuccess) e = max_dyn_smem((const void*)kdh, (int)smem);
   if (e != cudaSuccess) return e;
   L.begin(K_DW);
-  kdw<<<(unsigned)((a.V + R - 1) / R), NT, smem, L.st>>>(a, sc.lse, sc.acc, nullptr);
+  kdw<<<(unsigned)((a.V + R - 1) / R), NT, smem, L.st>>>(a, sc.lse, sc.acc);
   L.end();
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   L.begin(K_DH);
-  kdh<<<(unsigned)simt_parts(a.N), NT, smem, L.st>>>(a, sc.lse, sc.acc, nullptr);
+  kdh<<<(unsigned)simt_parts(a.N), NT, smem, L.st>>>(a, sc.lse, sc.acc);
   L.end();
   return cudaGetLastError();
 }
@@ -298,7 +482,7 @@ template <typename T>
 static cudaError_t simt_run(const StepArgs& a, const Scratch& sc, Launch& L) {
   const int64_t nb = simt_parts(a.N);
   L.begin(K_LSE);
-  simt_lse_kernel<T><<<(unsigned)nb, NT, 0, L.st>>>(a, sc.lse, sc.part_loss, sc.part_cnt, sc.part_err, nullptr);
+  simt_lse_kernel<T><<<(unsigned)nb, NT, 0, L.st>>>(a, sc.lse, sc.part_loss, sc.part_cnt, sc.part_err);
   L.end();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -315,28 +499,27 @@ cudaError_t simt_grads(const StepArgs& a, const Scratch& sc, Launch& L) {
   return a.bf16 ? simt_grads_t<__nv_bfloat16>(a, sc, L) : simt_grads_t<float>(a, sc, L);
 }
 
-// Repair of the one-pass tensor-core logsumexp + dh kernel (bf16): the exact two passes,
-// restricted to flagged tiles.  Both launches cover every row block; blocks outside flagged
-// tiles return before touching memory, so the common case costs two near-empty launches.
+// Exact repair of the one-pass tensor-core logsumexp + dh kernel (bf16): two persistent launches
+// of REP_BLOCKS blocks whose blocks return at once when no tile is flagged.
+size_t simt_repair_part_floats(int64_t C) { return (size_t)REP_BLOCKS * R * (size_t)(C > 2 ? C : 2); }
+
 cudaError_t simt_repair_lse(const StepArgs& a, const Scratch& sc, Launch& L) {
+  const int ntiles = (int)((a.N + TC_TILE_ROWS - 1) / TC_TILE_ROWS);
   L.begin(K_LSE);
-  const unsigned ntiles = (unsigned)((a.N + TC_TILE_ROWS - 1) / TC_TILE_ROWS);
-  const dim3 grid(ntiles, TC_TILE_ROWS / R);
-  const cudaError_t e = launch_pdl(simt_lse_kernel<__nv_bfloat16>, grid, dim3(NT), 0, L.st, a, sc.lse, nullptr, nullptr,
-                                   nullptr, sc.tc_tile_flag);
+  const cudaError_t e = launch_pdl(repair_lse_kernel, dim3(REP_BLOCKS), dim3(NT), sizeof(int) * (size_t)ntiles, L.st, a,
+                                   sc.tc_tile_flag, ntiles, sc.lse, sc.rep_part, sc.rep_ticket);
   L.end();
   return e;
 }
 
 cudaError_t simt_repair_dh(const StepArgs& a, const Scratch& sc, Launch& L) {
-  const size_t smem = simt_grad_smem(a.C);
-  auto kdh = simt_grad_kernel<__nv_bfloat16, false>;
-  cudaError_t e = max_dyn_smem((const void*)kdh, (int)smem);
+  const int ntiles = (int)((a.N + TC_TILE_ROWS - 1) / TC_TILE_ROWS);
+  const size_t smem = simt_grad_smem(a.C) + sizeof(int) * (size_t)ntiles;
+  cudaError_t e = max_dyn_smem((const void*)repair_dh_kernel, (int)smem);
   if (e != cudaSuccess) return e;
   L.begin(K_DH);
-  const unsigned ntiles = (unsigned)((a.N + TC_TILE_ROWS - 1) / TC_TILE_ROWS);
-  const dim3 grid(ntiles, TC_TILE_ROWS / R);
-  e = launch_pdl(kdh, grid, dim3(NT), smem, L.st, a, sc.lse, sc.acc, sc.tc_tile_flag);
+  e = launch_pdl(repair_dh_kernel, dim3(REP_BLOCKS), dim3(NT), smem, L.st, a, sc.tc_tile_flag, ntiles, sc.lse, sc.acc,
+                 sc.rep_part, sc.rep_ticket);
   L.end();
   return e;
 }

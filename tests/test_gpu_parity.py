@@ -84,6 +84,38 @@ def test_lse_dh_repair_of_out_of_range_tiles():
         assert_parity(got, ref, "bf16")
 
 
+def _flag_tiles(w, picks):
+    # vocabulary row v aligned with token n's hidden state in micro-step k, for (k, n, v) in picks:
+    # that token's logit there lies far beyond the one-pass range, so n's 128-token tile is
+    # flagged and repaired; the token also targets its row (the one-hot term in the repair)
+    for k, n, v in picks:
+        w.W[v] = (0.5 * w.micro[k][0][n].float()).to(w.W.dtype)
+        w.micro[k][1][n] = v
+
+
+def test_repair_many_flagged_tiles():
+    # twenty flagged tiles over two micro-steps (the last one ragged): more row groups than SMs,
+    # so the repair takes whole rows (no vocabulary slices)
+    w = I.custom([1408, 1310], 256, 1000, "bf16", seed=21, ignore_frac=0.05)
+    picks = [(0, 128 * t + 5, 40 + t) for t in range(11)] + [(1, 128 * t + 77, 80 + t) for t in range(10)]
+    _flag_tiles(w, picks)
+    ref = run_oracle(w)
+    got = run_lib(w, path="tcgen05")
+    assert got["status"] == M.OK
+    assert_parity(got, ref, "bf16")
+
+
+def test_repair_two_flagged_tiles_micro_mean():
+    # two flagged tiles: the repair splits their rows' vocabulary between the SMs and merges the
+    # slices; micro-step-mean normalisation (the scale from the count pass)
+    w = I.custom([600, 260], 512, 3001, "bf16", seed=22, ignore_frac=0.1)
+    _flag_tiles(w, [(0, 3, 100), (0, 450, 2999)])
+    ref = run_oracle(w, norm="micro_mean")
+    got = run_lib(w, path="tcgen05", norm="micro_mean")
+    assert got["status"] == M.OK
+    assert_parity(got, ref, "bf16")
+
+
 @pytest.mark.parametrize("nats", [60.0, 88.0])
 def test_lse_dh_wide_logit_within_range(nats):
     # a logit ~60 nats (~87 in base 2) or ~88 nats (~127) above the token's first-block maximum:
