@@ -39,7 +39,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="lmce", choices=["lmce", "reference"])
     p.add_argument("--workload", default="gpt2_124m_head")
-    p.add_argument("--path", default="auto", choices=["auto", "simt", "tcgen05", "tcgen05_two_pass"])
+    p.add_argument("--path", default="auto", choices=["auto", "simt", "tcgen05", "tcgen05_two_pass", "tcgen05_recompute"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--final-norm", default=None, choices=["layernorm", "rmsnorm"],
                    help="ln_f in front of the head (lmce_microstep_ln); inputs become the rows x before it")

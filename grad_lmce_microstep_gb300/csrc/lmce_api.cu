@@ -274,6 +274,10 @@ static void free_scratch(lmce_handle* h) {
   cudaFree(h->sc.tc_tile_flag);
   cudaFree(h->sc.rep_part);
   cudaFree(h->sc.rep_ticket);
+  cudaFree(h->sc.tc_p);
+  cudaFree(h->sc.tc_mref);
+  cudaFree(h->sc.tc_hs);
+  cudaFree(h->sc.tc_kmap);
   cudaFree(h->sumsq_part);
   h->sumsq_part = nullptr;
   cudaFree(h->cs.h_c);
@@ -305,12 +309,13 @@ extern "C" int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out)
   if (cfg->C > (1 << 20) || cfg->V > (1LL << 31) || cfg->max_N > (1LL << 31)) return LMCE_ERR_ARG;
   if (cfg->dtype != LMCE_BF16 && cfg->dtype != LMCE_FP32) return LMCE_ERR_ARG;
   if (cfg->norm != LMCE_NORM_GLOBAL && cfg->norm != LMCE_NORM_MICRO_MEAN) return LMCE_ERR_ARG;
-  if (cfg->path < LMCE_PATH_AUTO || cfg->path > LMCE_PATH_TCGEN05_TWO_PASS) return LMCE_ERR_ARG;
+  if (cfg->path < LMCE_PATH_AUTO || cfg->path > LMCE_PATH_TCGEN05_RECOMPUTE) return LMCE_ERR_ARG;
   if (cfg->flags & ~(LMCE_ACCUMULATE_FROM_START | LMCE_COMPACT_VALID_ROWS | LMCE_FINAL_NORM)) return LMCE_ERR_ARG;
   const bool tc_ok = tc_supported(cfg->C, cfg->V, cfg->dtype == LMCE_BF16);
   const bool simt_ok = cfg->C <= 2048;
   int path;
-  if (cfg->path == LMCE_PATH_TCGEN05 || cfg->path == LMCE_PATH_TCGEN05_TWO_PASS) {
+  if (cfg->path == LMCE_PATH_TCGEN05 || cfg->path == LMCE_PATH_TCGEN05_TWO_PASS ||
+      cfg->path == LMCE_PATH_TCGEN05_RECOMPUTE) {
     if (!tc_ok) return LMCE_ERR_ARG;
     path = cfg->path;
   } else if (cfg->path == LMCE_PATH_SIMT) {
@@ -357,6 +362,17 @@ extern "C" int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out)
          cudaMalloc(&h->sc.rep_part, sizeof(float) * simt_repair_part_floats(cfg->C)) == cudaSuccess &&
          cudaMalloc(&h->sc.rep_ticket, sizeof(unsigned) * tiles * (TC_TILE_ROWS / 16)) == cudaSuccess &&
          cudaMemset(h->sc.rep_ticket, 0, sizeof(unsigned) * tiles * (TC_TILE_ROWS / 16)) == cudaSuccess;
+  }
+  if (ok && path == LMCE_PATH_TCGEN05) {
+    // the stored exponentials of the dW pass: p [max_N][Vp], and per segment copy the row
+    // references and the scaled rows of h; the per-row pass defines every element it reads
+    const int64_t vp = tc_p_cols(cfg->V), np = tc_ver_rows(maxN);
+    const size_t ttiles = (size_t)(maxN + TC_TILE_ROWS - 1) / TC_TILE_ROWS;
+    ok = cudaMalloc(&h->sc.tc_p, sizeof(uint16_t) * (size_t)maxN * (size_t)vp) == cudaSuccess &&
+         cudaMalloc(&h->sc.tc_mref, sizeof(float) * (size_t)TC_MAX_VER * (size_t)np) == cudaSuccess &&
+         cudaMalloc(&h->sc.tc_hs, sizeof(uint16_t) * (size_t)TC_MAX_VER * (size_t)np * (size_t)cfg->C) == cudaSuccess &&
+         cudaMalloc(&h->sc.tc_kmap, ttiles * (size_t)(vp / 256)) == cudaSuccess;
+    h->sc.tc_p_rows = maxN;
   }
   ok = ok && cudaMalloc(&h->sumsq_part, sizeof(double) * (SQ_BLOCKS + 1)) == cudaSuccess;
   if (ok && (cfg->flags & LMCE_COMPACT_VALID_ROWS)) {
@@ -428,6 +444,7 @@ int run_microstep(lmce_handle* h, const void* hidden, const void* W, const int32
   a.beta = write_dW ? 0 : 1;
   a.bf16 = c.dtype == LMCE_BF16;
   a.tc_two_pass = h->path == LMCE_PATH_TCGEN05_TWO_PASS;
+  a.tc_recompute = h->path == LMCE_PATH_TCGEN05_RECOMPUTE;
   a.test_stall_ns = h->test_stall_ns;
   h->test_stall_ns = 0;
   if (N == 0) {

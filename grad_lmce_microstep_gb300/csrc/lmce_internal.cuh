@@ -120,6 +120,8 @@ struct StepArgs {
   int32_t beta;           // 0: dW = grad, 1: dW += grad
   int32_t bf16;           // 1: dtype bf16, 0: fp32
   int32_t tc_two_pass;    // tensor-core path: 1 = separate logsumexp pass, 0 = one-pass lse + dh
+  int32_t tc_recompute = 0;  // one-pass tensor-core path: 1 = the dW pass recomputes the logits
+                             // (0: it reads the stored exponentials when the scratch has them)
   int64_t test_stall_ns = 0;  // failure-detection test: > 0 makes the tensor-core gradient launches
                               // start no operand load and bounds their waits by this many ns
 };
@@ -144,7 +146,19 @@ struct Scratch {
   // tensor-core path, exact repair of flagged tiles
   float* rep_part;     // [simt_repair_part_floats(C)] per-slice (max, sum) and dh partials
   unsigned* rep_ticket;  // [tiles * 8] per row group: slices finished (0 between uses)
+  // tensor-core path, dW from the stored exponentials (all null: the dW pass recomputes the
+  // logits instead)
+  __nv_bfloat16* tc_p;     // [max_N][Vp] the one-pass kernel's bf16 operand p = 2^(z log2 e - m),
+                           // Vp = V rounded up to 256; the target entry later becomes p_y - 2^(lse log2 e - m)
+  float* tc_mref;          // [TC_MAX_VER][Np] base-2 reference m of each row, per segment of its tile
+  __nv_bfloat16* tc_hs;    // [TC_MAX_VER][Np][C] rows of h scaled by s 2^(m - lse log2 e), per segment
+  uint8_t* tc_kmap;        // [tiles][Vp / 256] segment of (128-token tile, 256-row vocabulary block)
+  int64_t tc_p_rows;       // rows of tc_p (max_N)
 };
+
+// Segments of a 128-token tile (pairs of the one-pass kernel's schedule sharing it) the stored-
+// exponential path keeps a reference for; a schedule with more falls back to recomputing.
+constexpr int TC_MAX_VER = 8;
 
 constexpr int TC_MAX_SPLIT = 32;
 
@@ -332,7 +346,9 @@ cudaError_t simt_load_kernels();
 // over every SM by vocabulary slice and merged in slice order.
 constexpr int TC_TILE_ROWS = 128;
 cudaError_t simt_repair_lse(const StepArgs& a, const Scratch& s, Launch& L);
-cudaError_t simt_repair_dh(const StepArgs& a, const Scratch& s, Launch& L);
+// store_p: also rewrite the flagged tiles' rows of the stored exponentials (normalised p, and
+// the reference m = lse log2 e of every segment)
+cudaError_t simt_repair_dh(const StepArgs& a, const Scratch& s, Launch& L, bool store_p = false);
 size_t simt_repair_part_floats(int64_t C);
 
 // Tensor-core path (tcgen05 + TMA).
@@ -342,5 +358,9 @@ int64_t tc_pairs();
 size_t tc_part_bytes(int64_t C);
 size_t tc_part_lm_bytes();
 cudaError_t tc_microstep(const StepArgs& a, const Scratch& s, Launch& L);
+// Stored-exponential dW pass: columns of the stored operand (V rounded up to 256) and rows per
+// reference segment (N rounded up to 256).
+int64_t tc_p_cols(int64_t V);
+int64_t tc_ver_rows(int64_t N);
 
 }  // namespace lmce

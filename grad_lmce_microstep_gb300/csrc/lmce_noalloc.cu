@@ -113,7 +113,7 @@ extern "C" int lmce_microstep_noalloc(const lmce_config* cfg, const void* hidden
   int st = setup(&base);
   if (st != LMCE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  Scratch sc;
+  Scratch sc{};
   sc.lse = reinterpret_cast<float*>(base + OFF_LSE);
   sc.part_loss = reinterpret_cast<double*>(base + OFF_PLOSS);
   sc.part_cnt = reinterpret_cast<int*>(base + OFF_PCNT);

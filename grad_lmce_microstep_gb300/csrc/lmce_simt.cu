@@ -371,9 +371,13 @@ __global__ void __launch_bounds__(NT) repair_lse_kernel(StepArgs a, const unsign
 
 // part: [REP_BLOCKS][R][C] fp32 dh partials of the items of groups split into slices.  Dynamic
 // shared memory: the R x C accumulator, then the flagged-tile list.
+// pst (null: nothing stored): the stored exponentials [N][vp], whose flagged rows get p = softmax
+// (0 for a row without a valid target), and mref [TC_MAX_VER][np] their reference lse log2 e.
 __global__ void __launch_bounds__(NT) repair_dh_kernel(StepArgs a, const unsigned* __restrict__ flag, int ntiles,
                                                        const float* __restrict__ lse, const DevAcc* __restrict__ acc_dev,
-                                                       float* __restrict__ part, unsigned* __restrict__ ticket) {
+                                                       float* __restrict__ part, unsigned* __restrict__ ticket,
+                                                       __nv_bfloat16* __restrict__ pst, int64_t vp,
+                                                       float* __restrict__ mref, int64_t np) {
   griddep_wait();
   __shared__ float Xs[BK][R];
   __shared__ float Ys[BK][BT + 1];
@@ -404,6 +408,8 @@ __global__ void __launch_bounds__(NT) repair_dh_kernel(StepArgs a, const unsigne
         ln = lse[n0 + r];
       }
     }
+    if (pst && v == 0 && q == 0 && n0 + r < a.N)
+      for (int k = 0; k < TC_MAX_VER; ++k) mref[(size_t)k * np + n0 + r] = ln * 1.4426950408889634f;
     __syncthreads();
     for (int64_t t0 = v0; t0 < v1; t0 += BT) {
       float sv[4];
@@ -411,7 +417,9 @@ __global__ void __launch_bounds__(NT) repair_dh_kernel(StepArgs a, const unsigne
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int64_t vv = t0 + q + 16 * j;
-        dzs[r][q + 16 * j] = (y >= 0 && vv < v1) ? s * (expf(sv[j] - ln) - (vv == y ? 1.f : 0.f)) : 0.f;
+        const float pv = (y >= 0 && vv < v1) ? expf(sv[j] - ln) : 0.f;
+        dzs[r][q + 16 * j] = (y >= 0 && vv < v1) ? s * (pv - (vv == y ? 1.f : 0.f)) : 0.f;
+        if (pst && vv < v1 && n0 + r < a.N) pst[(n0 + r) * vp + vv] = __float2bfloat16_rn(pv);
       }
       __syncthreads();
       const int64_t tn = v1 - t0 < BT ? v1 - t0 : BT;
@@ -512,14 +520,15 @@ cudaError_t simt_repair_lse(const StepArgs& a, const Scratch& sc, Launch& L) {
   return e;
 }
 
-cudaError_t simt_repair_dh(const StepArgs& a, const Scratch& sc, Launch& L) {
+cudaError_t simt_repair_dh(const StepArgs& a, const Scratch& sc, Launch& L, bool store_p) {
   const int ntiles = (int)((a.N + TC_TILE_ROWS - 1) / TC_TILE_ROWS);
   const size_t smem = simt_grad_smem(a.C) + sizeof(int) * (size_t)ntiles;
   cudaError_t e = max_dyn_smem((const void*)repair_dh_kernel, (int)smem);
   if (e != cudaSuccess) return e;
   L.begin(K_DH);
   e = launch_pdl(repair_dh_kernel, dim3(REP_BLOCKS), dim3(NT), smem, L.st, a, sc.tc_tile_flag, ntiles, sc.lse, sc.acc,
-                 sc.rep_part, sc.rep_ticket);
+                 sc.rep_part, sc.rep_ticket, store_p ? sc.tc_p : (__nv_bfloat16*)nullptr, tc_p_cols(a.V), sc.tc_mref,
+                 tc_ver_rows(a.N));
   L.end();
   return e;
 }

@@ -351,17 +351,39 @@ __global__ void __launch_bounds__(256) tc_combine_kernel(const float* __restrict
 // reach 100 above it).  It costs nothing in precision: p of the block maximum is 2^-FL_HEADROOM,
 // far inside fp32 and bf16 range, and the terms that underflow (p < 2^-126) lie more than
 // 126 - FL_HEADROOM = 94 below that maximum, a relative weight under 2^-94.
+//
+// dW from the stored exponentials (the default dW pass).  The lse+dh pass also writes its bf16
+// operand p[n][v] = 2^(z log2 e - m_n) to device memory (one TMA store per epilogue warp and
+// block, from the tile it has just written for the MMA) and each row's reference m_n.  Since
+//   s (softmax(z_n)[v] - [v == y_n]) = f_n (p[n][v] - [v == y_n] 2^(lse_n log2 e - m_n)),
+//   f_n = s 2^(m_n - lse_n log2 e),
+// a per-row pass (tc_hs_kernel) replaces each row's target entry of p by the bracket (computed
+// in fp32 from the target logit, then rounded once) and writes hs_n = f_n h_n in bf16, and
+//   dW^T[c][v] = sum_n hs[n][c] p[n][v]
+// is a plain product: the dW pass streams hs and p by TMA into the same accumulation as above,
+// with no logits tile and no epilogue work per block.  The segments of a split tile were summed
+// with different references (each pair fixes its own), so hs keeps one copy per segment and the
+// dW pass takes, for each 128-token tile and 256-row vocabulary block, the copy of the segment
+// that covered that pair of indices.  f_n and the target's bracket hold only while m_n lies within
+// P_RANGE of lse_n log2 e (the bracket <= 2^P_RANGE, f_n >= s 2^-P_RANGE, far from fp32's
+// limits); a segment whose reference lies further below (its first block's maximum more than
+// P_RANGE + FL_HEADROOM = 96 below, in base 2, a row whose mass lies in other segments) flags its
+// tile too, and the exact repair rewrites the rows of a flagged tile with the normalised p and
+// m_n = lse_n log2 e.  Against recomputing the logits this trades a quarter
+// of the tensor work (6 N C V flop per micro-step instead of 8) for one write and one read of
+// the N x V bf16 operand, which stream at a small fraction of HBM bandwidth beside the products.
 constexpr int G_XT = 128;                  // X rows per pair (64 per CTA)
 constexpr int G_YB = 256;                  // stream rows per block (128 per CTA)
 constexpr int G_DZ = G_YB * 128;           // one dz buffer: 256 K-rows x 64 bf16 = 32 KB
 constexpr int G_EPI_WARPS = 8;
 constexpr int G_THREADS = 128 + 32 * G_EPI_WARPS;  // warps 0 and 10 TMA, 1 MMA, 2-9 epilogue, 11 ring waiter
 
-enum GradMode { GM_DW = 0, GM_DH = 1, GM_FL = 2 };
+enum GradMode { GM_DW = 0, GM_DH = 1, GM_FL = 2, GM_DWP = 3 };
 // Named barriers of the gradient kernels: 1 the epilogue warps, 2 .. 2 + NST - 1 the ring slots'
 // hand-offs from the waiter warp to the MMA warp, then the dz tile's hand-off.
 constexpr int HB_DZ_FULL = 6;
 constexpr float FL_HEADROOM = 32.f;        // lse+dh pass: reference above the first block's maximum (base 2)
+constexpr float P_RANGE = 64.f;            // stored p: largest lse log2 e - m of a row's segment kept
 
 // Ring geometry per mode: NST slots of SLOT bytes.  An S stage carries SK 64-column atoms of
 // K = C (per CTA: 128 stream rows, then 64 X rows at SK * 16 KB); an accumulation stage
@@ -373,6 +395,14 @@ constexpr float FL_HEADROOM = 32.f;        // lse+dh pass: reference above the f
 template <int MODE>
 struct Geo {
   static constexpr int NST = 4, SLOT = 49152, SK = 2, AQ = 1, NDZ = 1;
+  static_assert(2 + NST <= HB_DZ_FULL, "ring hand-off barriers overlap the dz tile's");
+};
+// dW from the stored exponentials: a stage is one 64-token quarter of hs (every C chunk, 48 KB)
+// and of p (this CTA's 64 vocabulary rows, 8 KB at P_OFF); the 32 KB buffer stages the flush.
+constexpr int P_OFF = 3 * 16384;
+template <>
+struct Geo<GM_DWP> {
+  static constexpr int NST = 3, SLOT = P_OFF + 8192, SK = 2, AQ = 1, NDZ = 1;
   static_assert(2 + NST <= HB_DZ_FULL, "ring hand-off barriers overlap the dz tile's");
 };
 template <int MODE>
@@ -400,6 +430,13 @@ struct GradParams {
   float fl_limit;        // lse+dh pass: largest base-2 exponent of p kept (115 - ceil(log2 V))
   uint64_t wait_ns;      // limit of every bounded wait (WAIT_NS; shorter in the failure-detection test)
   int stall;             // failure-detection test: the producers start no load
+  // stored exponentials
+  int store_p;           // lse+dh pass: store p (tmE) and the row references
+  float* mref;           // lse+dh pass: [TC_MAX_VER][np] reference m of each row per tile segment
+  int np;                // rows per segment copy (N rounded up to 256)
+  const uint8_t* kmap;   // dW pass from p: segment of (128-token tile, 256-row vocabulary block)
+  int kmap_nblk;         // vocabulary blocks per kmap row
+  int ttiles;            // 128-token tiles (kmap rows)
 };
 
 __device__ __forceinline__ float grad_scale(const GradParams& p) {
@@ -456,12 +493,15 @@ template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     tc_grad_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmYs,
                    const __grid_constant__ CUtensorMap tmYa, const __grid_constant__ CUtensorMap tmO,
-                   const __grid_constant__ CUtensorMap tmP, GradParams p) {
+                   const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmE, GradParams p) {
   constexpr bool DW = MODE == GM_DW;
   constexpr bool FL = MODE == GM_FL;
+  constexpr bool DWP = MODE == GM_DWP;      // dW from the stored exponentials: no logits tile
+  constexpr bool DWX = DW || DWP;           // X = vocabulary rows, stream = tokens, output dW
   constexpr int NST = Geo<MODE>::NST, SLOT = Geo<MODE>::SLOT, SK = Geo<MODE>::SK, AQ = Geo<MODE>::AQ;
   constexpr int NDZ = Geo<MODE>::NDZ;
   static_assert(SK * 24576 <= SLOT && AQ * 16384 * 3 <= SLOT && 4 % AQ == 0, "stage does not fit its slot");
+  static_assert(!DWP || (AQ == 1 && P_OFF + 8192 <= SLOT), "p quarter does not fit its slot");
   griddep_wait();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 128-byte-swizzled operands need 1024-byte alignment; the launch reserves no slack for
@@ -472,7 +512,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     return;
   }
   uint8_t* smem = smem_raw;
-  const int KC = p.C / (64 * SK);           // S phase stages per block
+  const int KC = DWP ? 0 : p.C / (64 * SK);   // S phase stages per block
   const int NCH = p.nch;                    // 256-row C chunks of acc^T in TMEM (from chunk p.ch0 on)
   uint8_t* sY = smem;                       // ring of NST slots
   uint8_t* sDZ = sY + NST * SLOT;           // [NDZ][4 K atoms][64 X rows][128 B], K-major
@@ -493,8 +533,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const uint64_t wait_ns = p.wait_ns;
-  const int nX = DW ? p.V : p.N;
-  const int nY = DW ? p.N : p.V;
+  const int nX = DWX ? p.V : p.N;
+  const int nY = DWX ? p.N : p.V;
   const int nblk = (nY + G_YB - 1) / G_YB;
   const int T = (nX + G_XT - 1) / G_XT;
   const Sched sch{(long long)T * nblk, (int)(gridDim.x >> 1), nblk};
@@ -548,13 +588,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
     const uint32_t lead_full = mapa(smem_u32(&full[0]), 0);
     int it = 0;
     bool ok = true;
+    // dW from p: the hs copy of each 128-token tile of the block being loaded (lane 0, read one
+    // block ahead so that the table's latency stays off the loads)
+    int kv_cur0 = 0, kv_cur1 = 0, kv_nxt0 = 0, kv_nxt1 = 0;
+    auto kver = [&](int t1, int vb) -> int {
+      if (t1 >= p.ttiles) return 0;   // tokens past the last tile: zero rows of copy 0
+      const int k = __ldg(p.kmap + (size_t)t1 * p.kmap_nblk + vb);
+      return dcheck(k < TC_MAX_VER, p.err, BS_TMA_ROW) ? k : 0;
+    };
     for (int t = t_first; t <= t_last && ok; ++t) {
       const int b0 = (int)(max(ub, (long long)t * nblk) - (long long)t * nblk);
       const int nb = (int)(min(ue, (long long)(t + 1) * nblk) - (long long)t * nblk) - b0;
       const int x0 = t * G_XT;
-      const int rt = DW ? 0 : sch.rot(t);
+      const int rt = DWX ? 0 : sch.rot(t);
+      if (DWP && lane == 0) {
+        kv_nxt0 = kver(2 * b0, t >> 1);
+        kv_nxt1 = kver(2 * b0 + 1, t >> 1);
+      }
       for (int j = 0; j <= nb && ok; ++j) {
         const int nst = (j < nb ? KC : 0) + (j >= 1 ? 4 / AQ : 0);
+        if (DWP && j >= 1 && lane == 0) {
+          kv_cur0 = kv_nxt0;
+          kv_cur1 = kv_nxt1;
+          if (j < nb) {
+            kv_nxt0 = kver(2 * (b0 + j), t >> 1);
+            kv_nxt1 = kver(2 * (b0 + j) + 1, t >> 1);
+          }
+        }
         for (int u = 0; u < nst; ++u, ++it) {
           if ((it & 1) != pw) continue;
           const int st = it % NST;
@@ -563,7 +623,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           if (lane == 0) {
             w = mbar_wait(smem_u32(&empty[st]), ((it / NST) & 1) ^ 1, wait_ns);
             if (!w) record_timeout(p.err, 17);
-            else if (rank == 0) mbar_expect_tx(smem_u32(&full[st]), sphase ? 2 * SK * 24576 : 2 * AQ * 16384 * NCH);
+            else if (rank == 0)
+              mbar_expect_tx(smem_u32(&full[st]), sphase ? 2 * SK * 24576 : DWP ? 2 * (16384 * NCH + 8192) : 2 * AQ * 16384 * NCH);
           }
           if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
           const uint32_t dst = smem_u32(sY) + st * SLOT;
@@ -576,6 +637,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             if (lane == 0) dcheck(bj < 2 * nblk && t < T, p.err, BS_TMA_ROW);
             if (lane == 0) tma_load_3d_cg2(dst, &tmYs, bar, 0, (bj < nblk ? bj : bj - nblk) * G_YB + (int)rank * 128, u * SK);
             else if (lane == 1) tma_load_3d_cg2(dst + SK * 16384, &tmX, bar, 0, x0 + (int)rank * 64, u * SK);
+          } else if (DWP) {
+            // block b0+j-1, quarter q (64 tokens): hs rows of the quarter's segment copy, my 128 C
+            // of every chunk; p rows of the same tokens, my 64 vocabulary rows of the tile
+            const int q = u;
+            const int bj = b0 + j - 1;
+            if (lane == 0) {
+              dcheck(bj < nblk && q < 4, p.err, BS_TMA_ROW);
+              const int kv = (q >> 1) ? kv_cur1 : kv_cur0;
+              tma_load_4d_cg2(dst, &tmYa, bar, 0, kv * p.np + bj * G_YB + q * 64, 2 * (int)rank, p.ch0);
+            } else if (lane == 1) {
+              tma_load_3d_cg2(dst + P_OFF, &tmX, bar, 0, bj * G_YB + q * 64, 2 * t + (int)rank);
+            }
           } else if (lane == 0) {
             // accumulation phase of block b0+j-1, quarters AQ q .. AQ q + AQ - 1 (64 AQ stream rows):
             // my 128 C of every chunk, one 4D box [chunk][atom][64 AQ rows][64]
@@ -612,6 +685,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       const uint64_t dXs = sdesc_sw128(smem_u32(sY) + SK * 16384, 16, 1024);
       const uint64_t dYa = sdesc_sw128(smem_u32(sY), AQ * 8192, 1024);      // accumulation, MN-major
       const uint64_t dDZ = sdesc_sw128(smem_u32(sDZ), 16, 1024);            // dz, K-major
+      // dW from p: B = the quarter's p rows, MN-major (64 vocabulary rows of 128 B per token, one
+      // 64-wide atom per CTA, K groups of 8 tokens 1 KB apart)
+      const uint32_t idP = idesc_bf16(256, G_XT, 1, 1);
+      const uint64_t dP = sdesc_sw128(smem_u32(sY) + P_OFF, 8192, 1024);
       // the block's dz tile, handed over by the waiter warp through named barrier HB_DZ_FULL
       auto dz_take = [&]() -> bool {
         asm volatile("bar.sync %0, 64;" ::"n"(HB_DZ_FULL) : "memory");
@@ -623,7 +700,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         const int b0 = (int)(max(ub, (long long)t * nblk) - (long long)t * nblk);
         const int nb = (int)(min(ue, (long long)(t + 1) * nblk) - (long long)t * nblk) - b0;
         for (int j = 0; j <= nb && ok; ++j) {
-          if (j < nb) {
+          if (!DWP && j < nb) {
             // S of block j (the epilogue must have read the previous block's)
             const int gb = g + j;
             if (!wait_w(smem_u32(&s_empty), (gb & 1) ^ 1, true, 21)) {
@@ -664,7 +741,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             }
             for (int q = 0; q < 4 / AQ && ok; ++q) {
               // the whole dz tile of the block (one wait per block: the epilogue is far ahead)
-              if (q == 0 && !dz_take()) {
+              if (!DWP && q == 0 && !dz_take()) {
                 ok = false;
                 break;
               }
@@ -677,19 +754,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
               ++it;
               tc_fence_after();
               const uint64_t a = dYa + (uint32_t)(st * (SLOT >> 4));
-              const uint64_t b = dDZ + (uint32_t)((db * G_DZ + q * AQ * 8192) >> 4);
-              // chunk i: AQ * 16 KB apart; K steps of 16 rows: A 2 KB apart, dz 32 B within its
-              // 64-row K atom (atoms 8 KB apart)
-              for (int i = 0; i < NCH; ++i) {
+              if (DWP) {
+                // K steps of 16 tokens: A and p both 2 KB apart
+                const uint64_t b = dP + (uint32_t)(st * (SLOT >> 4));
+                for (int i = 0; i < NCH; ++i) {
 #pragma unroll
-                for (int k = 0; k < 4 * AQ; ++k)
-                  mma_ss2_elect(tmem + i * 128, a + (i * AQ * 1024 + k * 128), b + ((k >> 2) * 512 + (k & 3) * 2), idA,
-                                (jb | q | k) != 0);
+                  for (int k = 0; k < 4; ++k)
+                    mma_ss2_elect(tmem + i * 128, a + (i * 1024 + k * 128), b + k * 128, idP, (jb | q | k) != 0);
+                }
+              } else {
+                const uint64_t b = dDZ + (uint32_t)((db * G_DZ + q * AQ * 8192) >> 4);
+                // chunk i: AQ * 16 KB apart; K steps of 16 rows: A 2 KB apart, dz 32 B within its
+                // 64-row K atom (atoms 8 KB apart)
+                for (int i = 0; i < NCH; ++i) {
+#pragma unroll
+                  for (int k = 0; k < 4 * AQ; ++k)
+                    mma_ss2_elect(tmem + i * 128, a + (i * AQ * 1024 + k * 128), b + ((k >> 2) * 512 + (k & 3) * 2),
+                                  idA, (jb | q | k) != 0);
+                }
               }
               mma_commit_mc2_elect(smem_u32(&empty[st]), 3);
             }
             if (!ok) break;
-            mma_commit_mc2_elect(smem_u32(&dz_empty[db]), 3);
+            if (!DWP) mma_commit_mc2_elect(smem_u32(&dz_empty[db]), 3);
             if (jb == nb - 1) mma_commit_mc2_elect(smem_u32(&acc_full), 3);
           }
         }
@@ -723,7 +810,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         for (int j = 0; j <= nb && ok; ++j) {
           const int nst = (j < nb ? KC : 0) + (j >= 1 ? 4 / AQ : 0);
           for (int u = 0; u < nst; ++u, ++it) {
-            if (j >= 1 && u == (j < nb ? KC : 0)) {
+            if (!DWP && j >= 1 && u == (j < nb ? KC : 0)) {
               // block j - 1's dz tile, before its first accumulation stage
               const int gb = g + j - 1;
               const bool wd =
@@ -796,12 +883,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       const int xg = x0 + xl;                     // my X row
       // the tile's vocabulary rotation, found by one thread; read after the block loop's first
       // barrier (the previous tile's readers are past the flush's barriers)
-      if (!DW && et == 0) s_rot = sch.rot(t);
+      if (!DWX && et == 0) s_rot = sch.rot(t);
       // dh / lse+dh: my token's target and (dh) log2(s) - lse log2(e); the targets of all 128
       // rows of the tile for the flush
       float crow = -INFINITY;
       int yrow = -1;
-      if (!DW) {
+      if (!DWX) {
         if (xg < p.N) {
           const int tg = p.targets[xg];
           if (tg >= 0 && tg < p.V) {
@@ -820,7 +907,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         }
       }
       float m2 = 0.f, lacc = 0.f;                 // lse+dh: my row's reference (base 2) and sum of p
-      for (int j = 0; j < nb; ++j) {
+      // dW from p: no logits tile, nothing to do per block
+      for (int j = 0; j < (DWP ? 0 : nb); ++j) {
         const int gb = g + j;
         // first stream row of the block (dh passes: rotated; read after the barrier below)
         const int ys0 = DW ? (b0 + j) * G_YB : 0;
@@ -943,6 +1031,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           record_timeout(p.err, 26);
           epi_abort = 1;
         }
+        if (FL && p.store_p) {
+          // and once this warp's store of the previous block's p rows has read them
+          if (lane == 0) bulk_wait_read0();
+          __syncwarp();
+        }
         // my row of K atom ks, K-major, 128-byte swizzle: all in this CTA's shared memory
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -956,12 +1049,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         if (lane == 0) {
           if (rank == 0) mbar_arrive(smem_u32(&dz_full[db]));
           else mbar_arrive_cluster(dzf + db * 8);
+          const int row0 = x0 + (int)rank * 64 + 32 * (qd & 1);
+          if (FL && p.store_p && row0 < p.N) {
+            // the warp's 32 rows x 64 columns of p, as written for the MMA, to p[tokens][vocabulary]
+            // (a box may reach past row N, clipped, but never starts there)
+            const int bj = b0 + j + s_rot;
+            const int vb = bj < nblk ? bj : bj - nblk;
+            tma_store_3d(&tmE, dz_row + db * G_DZ + (uint32_t)(qd & 1) * 4096, 0, row0, vb * 4 + ks);
+            bulk_commit();
+          }
         }
       }
+      // the dz buffer also stages the flush: every store of p has read it
+      if (FL && p.store_p && lane == 0) bulk_wait_read0();
       // accumulator -> output (whole tile) or partial slot (part of a tile); an abort is
       // acted on only right after a barrier, so every epilogue thread takes the same branch
       const bool whole = b0 == 0 && nb == nblk;
-      if (!DW && whole) wload(0);   // in flight while the last accumulation completes
+      if (!DWX && whole) wload(0);   // in flight while the last accumulation completes
       if (!mbar_wait(smem_u32(&acc_full), sg & 1, wait_ns)) {
         record_timeout(p.err, 27);
         epi_abort = 1;
@@ -982,8 +1086,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           const float f = yrow >= 0 ? s / l : 0.f;
           fl_f[xl] = f;
           st_cluster_f32(mapa(smem_u32(&fl_f[xl]), peer), f);
+          if (p.store_p && xg < p.N) {
+            // the reference of this segment of the tile (segment k = pairs since the tile's first)
+            const int kseg = pi - sch.pair_of((long long)t * nblk);
+            if (dcheck(kseg < TC_MAX_VER, p.err, BS_SLOT)) p.mref[(size_t)kseg * p.np + xg] = m2;
+          }
           if (whole) {
             if (xg < p.N) p.lse_out[xg] = (m2 + log2f(l)) * LN2;
+            // stored p: the row's only reference must lie within P_RANGE of its lse log2 e
+            if (p.store_p && yrow >= 0 && !(log2f(l) <= P_RANGE) && dcheck(t < T, p.err, BS_TILE_FLAG))
+              atomicOr(p.tile_flag + t, 1u);
           } else if (slot_ok) {
             p.part_lm[((size_t)slot * 2 + 0) * G_XT + xl] = m2;
             p.part_lm[((size_t)slot * 2 + 1) * G_XT + xl] = l;
@@ -1011,7 +1123,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       //    term are first stored into the buffer (row x at 256 B x) and dh overwrites them.
       const int kl = qd * 32 + lane;
       const uint32_t stg = smem_u32(sDZ);
-      if (!DW && whole) {
+      if (!DWX && whole) {
         __nv_bfloat16* sw = reinterpret_cast<__nv_bfloat16*>(sDZ);
         for (int i = 0; i < NCH; ++i) {
           const int c0 = (p.ch0 + i) * 256 + (int)rank * 128;
@@ -1041,7 +1153,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           }
           asm volatile("bar.sync 1, 256;" ::: "memory");
         }
-      } else if (!DW) {
+      } else if (!DWX) {
         // partial tile of a dh pass: fp32 partial sums with plain stores (measured faster here
         // than the staged path, whose TMA traffic competes with this pass's operand stream)
         float* part = p.part + (size_t)slot * G_XT * p.C;
@@ -1096,7 +1208,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       }
       g += nb;
     }
-    if (et == 0) bulk_wait0();   // every flush's global writes are performed before the CTA exits
+    // every flush's and every store of p's global writes are performed before the CTA exits
+    if (et == 0 || (FL && p.store_p && lane == 0)) bulk_wait0();
   }
 
   tc_fence_before();
@@ -1131,7 +1244,7 @@ __device__ __forceinline__ int split_slots(const Sched& sch, int t, int* slots) 
 constexpr int COMB_BLOCKS = 8, COMB_U = 4;
 template <int MODE>
 __global__ void __launch_bounds__(256) tc_split_combine_kernel(GradParams p, Sched sch, const __grid_constant__ SplitTiles sp) {
-  constexpr bool DW = MODE == GM_DW;
+  constexpr bool DW = MODE == GM_DW || MODE == GM_DWP;
   constexpr bool FL = MODE == GM_FL;
   __shared__ int slots[16];
   __shared__ int nslots;
@@ -1169,6 +1282,13 @@ __global__ void __launch_bounds__(256) tc_split_combine_kernel(GradParams p, Sch
       }
       fac[xl] = y >= 0 ? s / l : 0.f;
       if (blockIdx.y == 0 && x < p.N) p.lse_out[x] = (M + log2f(l)) * LN2;
+      if (blockIdx.y == 0 && p.store_p && y >= 0) {
+        // stored p: every segment's reference within P_RANGE of the row's lse log2 e
+        const float l2 = M + log2f(l);
+        bool far = false;
+        for (int k = 0; k < nslots; ++k) far |= !(l2 - p.part_lm[((size_t)slots[k] * 2 + 0) * G_XT + xl] <= P_RANGE);
+        if (far && dcheck(t < sch.U / sch.nblk, p.err, BS_TILE_FLAG)) atomicOr(p.tile_flag + t, 1u);
+      }
     }
   }
   if (!DW) __syncthreads();
@@ -1341,6 +1461,95 @@ __global__ void __launch_bounds__(256) rows_post_kernel(StepArgs a, const float*
     finish_block(part_loss, part_cnt, part_err, gridDim.x, a.norm, a.G, (long long)a.global_valid, acc, fin_mode);
 }
 
+// ---- dW from the stored exponentials: per-row pass ------------------------------------------
+// s1 is the lse+dh pass's schedule (X = 128-token tiles, stream = 256-row vocabulary blocks in
+// each tile's rotated order).  The segment of (tile t, block vb) is the number of pairs between
+// the one that holds the tile's first unit and the one that holds that block's unit.
+__device__ __forceinline__ int seg_of(const Sched& s1, int t, int vb, int rot) {
+  const long long tb = (long long)t * s1.nblk;
+  const int pos = ((vb - rot) % s1.nblk + s1.nblk) % s1.nblk;
+  return s1.pair_of(tb + pos) - s1.pair_of(tb);
+}
+__device__ __forceinline__ int segs_of(const Sched& s1, int t) {
+  const long long tb = (long long)t * s1.nblk;
+  return s1.pair_of(tb + s1.nblk - 1) - s1.pair_of(tb) + 1;
+}
+
+constexpr int HS_ROWS = 32;     // rows per block iteration (a 128-token tile holds four)
+constexpr int HS_BLOCKS = 608;  // four per SM
+
+// After the lse+dh pass, its repairs and the final logsumexp of every row:
+//   kmap[t][vb] = segment of (tile t, block vb);
+//   hs[k][n] = f_k h_n in bf16, f_k = s 2^(m_k,n - lse_n log2 e) (0 for a row without a valid
+//              target; zero rows from N to np), for each segment k of row n's tile;
+//   p[n][y_n] = 2^(z_t log2 e - m) - 2^(lse_n log2 e - m) with m the reference of the segment
+//              that covered (tile of n, block of y_n): p - onehot in that segment's scale.
+__global__ void __launch_bounds__(256) tc_hs_kernel(StepArgs a, Sched s1, int ttiles, int np, int64_t vp,
+                                                    const float* __restrict__ lse, const float* __restrict__ zt,
+                                                    const float* __restrict__ mref, float scale_fixed,
+                                                    const DevAcc* __restrict__ acc, __nv_bfloat16* __restrict__ hs,
+                                                    __nv_bfloat16* __restrict__ pst, uint8_t* __restrict__ kmap) {
+  griddep_wait();
+  __shared__ float fs[HS_ROWS][TC_MAX_VER];
+  __shared__ int nseg_sh;
+  const int tid = threadIdx.x;
+  const float s = scale_fixed >= 0.f ? scale_fixed : acc->scale;
+  // the segment table
+  const long long nk = (long long)ttiles * s1.nblk;
+  for (long long i = (long long)blockIdx.x * blockDim.x + tid; i < nk; i += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(i / s1.nblk), vb = (int)(i % s1.nblk);
+    kmap[i] = (uint8_t)seg_of(s1, t, vb, s1.rot(t));
+  }
+  const int vecs = (int)(a.C / 8);   // 16-byte vectors per row
+  const __nv_bfloat16* H = static_cast<const __nv_bfloat16*>(a.hidden);
+  for (int g = blockIdx.x; g * HS_ROWS < np; g += gridDim.x) {
+    const int n0 = g * HS_ROWS;
+    const int t = n0 / TC_TILE_ROWS;
+    if (tid < HS_ROWS) {
+      const int n = n0 + tid;
+      const int ns = t < ttiles ? segs_of(s1, t) : 1;
+      if (tid == 0) nseg_sh = ns;
+      int y = -1;
+      if (n < a.N) {
+        const int tg = a.targets[n];
+        if (tg >= 0 && (int64_t)tg < a.V) y = tg;
+      }
+      const float l2 = y >= 0 ? lse[n] * LOG2E : 0.f;
+      for (int k = 0; k < TC_MAX_VER; ++k)
+        fs[tid][k] = (y >= 0 && k < ns) ? s * exp2f(mref[(size_t)k * np + n] - l2) : 0.f;
+      if (y >= 0) {
+        const int ky = seg_of(s1, t, y / G_YB, s1.rot(t));
+        const float m = mref[(size_t)ky * np + n];
+        pst[(size_t)n * vp + y] = __float2bfloat16_rn(exp2f(fmaf(zt[n], LOG2E, -m)) - exp2f(l2 - m));
+      }
+    }
+    __syncthreads();
+    const int ns = nseg_sh;
+    for (int e = tid; e < HS_ROWS * vecs; e += blockDim.x) {
+      const int r = e / vecs, cv = e % vecs;
+      const int n = n0 + r;
+      uint4 hv = make_uint4(0u, 0u, 0u, 0u);
+      if (n < a.N) hv = __ldg(reinterpret_cast<const uint4*>(H + (size_t)n * a.C) + cv);
+      for (int k = 0; k < ns; ++k) {
+        const float f = fs[r][k];
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+        if (f != 0.f) {
+          const uint32_t* hi = reinterpret_cast<const uint32_t*>(&hv);
+          uint32_t* oo = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hi[w]));
+            __nv_bfloat162 pr = __floats2bfloat162_rn(x.x * f, x.y * f);
+            oo[w] = *reinterpret_cast<uint32_t*>(&pr);
+          }
+        }
+        reinterpret_cast<uint4*>(hs + ((size_t)k * np + n) * a.C)[cv] = o;
+      }
+    }
+    __syncthreads();
+  }
+}
+
 // ---- host side ------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1476,6 +1685,10 @@ int64_t tc_parts(int64_t N) { return (N + 255) / 256; }
 
 int64_t tc_pairs() { return num_sms() / 2; }
 
+int64_t tc_p_cols(int64_t V) { return (V + G_YB - 1) / G_YB * G_YB; }
+
+int64_t tc_ver_rows(int64_t N) { return (N + G_YB - 1) / G_YB * G_YB; }
+
 size_t tc_part_bytes(int64_t C) { return (size_t)2 * (size_t)tc_pairs() * G_XT * (size_t)C * sizeof(float); }
 
 size_t tc_part_lm_bytes() { return (size_t)2 * (size_t)tc_pairs() * 2 * G_XT * sizeof(float); }
@@ -1533,20 +1746,72 @@ int chunk_ranges(int64_t C, int* ch0, int* nch) {
   return runs;
 }
 
+// The balanced schedule of a gradient launch over nX rows in 128-row X tiles and nY stream rows
+// in 256-row blocks.
+Sched grad_sched(int64_t nX, int64_t nY) {
+  const int nblk = (int)((nY + G_YB - 1) / G_YB);
+  const int T = (int)((nX + G_XT - 1) / G_XT);
+  const long long U = (long long)T * nblk;
+  // every pair covers at least a sixth of a tile, so a split tile has a handful of partials
+  long long P = tc_pairs();
+  if (P > U * 6 / nblk) P = U * 6 / nblk;
+  if (P > U) P = U;  // every pair gets at least one unit
+  if (P < 1) P = 1;
+  return Sched{U, (int)P, nblk};
+}
+
+// Most segments (pairs) sharing one X tile of schedule s over T tiles.
+int max_segments(const Sched& s, int T) {
+  int best = 1;
+  for (int t = 0; t < T; ++t) {
+    const long long tb = (long long)t * s.nblk;
+    const int n = s.pair_of(tb + s.nblk - 1) - s.pair_of(tb) + 1;
+    if (n > best) best = n;
+  }
+  return best;
+}
+
+// Stored-exponential dW pass on this micro-step: buffers allocated and large enough, and every
+// tile split over at most TC_MAX_VER pairs.  *nver = copies of hs the per-row pass writes.
+bool use_stored_p(const StepArgs& a, const Scratch& sc, int* nver) {
+  if (!sc.tc_p || a.tc_recompute || a.N <= 0 || a.N > sc.tc_p_rows) return false;
+  const Sched s1 = grad_sched(a.N, a.V);
+  *nver = max_segments(s1, (int)((a.N + G_XT - 1) / G_XT));
+  return *nver <= TC_MAX_VER;
+}
+
 template <int MODE>
-cudaError_t tc_grad_range(const StepArgs& a, const Scratch& sc, Launch& L, int ch0, int nch) {
+cudaError_t tc_grad_range(const StepArgs& a, const Scratch& sc, Launch& L, int ch0, int nch, int nver = 0) {
   constexpr bool DW = MODE == GM_DW;
+  constexpr bool DWP = MODE == GM_DWP;
+  constexpr bool DWX = DW || DWP;
   const void* X = DW ? a.W : a.hidden;
   const void* Y = DW ? a.hidden : a.W;
-  const int64_t nX = DW ? a.V : a.N, nY = DW ? a.N : a.V;
-  CUtensorMap mx, mys, mya, mo, mp;
+  const int64_t nX = DWX ? a.V : a.N, nY = DWX ? a.N : a.V;
+  const int64_t vp = tc_p_cols(a.V), np = tc_ver_rows(a.N);
+  CUtensorMap mx, mys, mya, mo, mp, me;
   constexpr int SK = Geo<MODE>::SK, AQ = Geo<MODE>::AQ;
+  // lse+dh pass: stores p on the first range of C chunks when the dW pass reads it
+  const bool store_p = MODE == GM_FL && nver > 0 && ch0 == 0;
   // flush targets: dW (fp32, 16-row boxes) or dh (bf16, whole 128-row tiles); the fp32 partial slots
-  const bool mo_ok = DW ? make_map_rows(&mo, a.dW, (uint64_t)a.V, (uint64_t)a.C, true, 16)
-                        : make_map_rows(&mo, a.dh, (uint64_t)a.N, (uint64_t)a.C, false, G_XT);
-  if (!make_map3(&mx, X, (uint64_t)nX, (uint64_t)a.C, G_XT / 2, SK) ||
-      !make_map3(&mys, Y, (uint64_t)nY, (uint64_t)a.C, 128, SK) ||
-      !make_map4(&mya, Y, (uint64_t)nY, (uint64_t)a.C, 64 * AQ, (uint32_t)nch) || !mo_ok ||
+  const bool mo_ok = DWX ? make_map_rows(&mo, a.dW, (uint64_t)a.V, (uint64_t)a.C, true, 16)
+                         : make_map_rows(&mo, a.dh, (uint64_t)a.N, (uint64_t)a.C, false, G_XT);
+  bool maps_ok;
+  if (DWP) {
+    // X: p [N][vp] as 64-column atoms, 64-token boxes of one atom; Y: the nver copies of hs
+    maps_ok = make_map3(&mx, sc.tc_p, (uint64_t)a.N, (uint64_t)vp, 64, 1) &&
+              make_map4(&mya, sc.tc_hs, (uint64_t)(nver * np), (uint64_t)a.C, 64, (uint32_t)nch);
+    mys = mx;
+    me = mx;
+  } else {
+    maps_ok = make_map3(&mx, X, (uint64_t)nX, (uint64_t)a.C, G_XT / 2, SK) &&
+              make_map3(&mys, Y, (uint64_t)nY, (uint64_t)a.C, 128, SK) &&
+              make_map4(&mya, Y, (uint64_t)nY, (uint64_t)a.C, 64 * AQ, (uint32_t)nch);
+    // p as the epilogue warps store it: 32 tokens x one 64-column atom
+    me = mx;
+    if (store_p) maps_ok = maps_ok && make_map3(&me, sc.tc_p, (uint64_t)a.N, (uint64_t)vp, 32, 1);
+  }
+  if (!maps_ok || !mo_ok ||
       !make_map_rows(&mp, sc.tc_part, (uint64_t)(2 * tc_pairs() * G_XT), (uint64_t)a.C, true, 16))
     return cudaErrorInvalidValue;
   GradParams p;
@@ -1576,23 +1841,21 @@ cudaError_t tc_grad_range(const StepArgs& a, const Scratch& sc, Launch& L, int c
   p.beta = a.beta;
   p.wait_ns = a.test_stall_ns > 0 ? (uint64_t)a.test_stall_ns : WAIT_NS;
   p.stall = a.test_stall_ns > 0 ? 1 : 0;
-  const int nblk = (int)((nY + G_YB - 1) / G_YB);
-  const int T = (int)((nX + G_XT - 1) / G_XT);
-  const long long U = (long long)T * nblk;
-  // every pair covers at least a sixth of a tile, so a split tile has a handful of partials
-  long long P = tc_pairs();
-  if (P > U * 6 / nblk) P = U * 6 / nblk;
-  if (P > U) P = U;  // every pair gets at least one unit
-  if (P < 1) P = 1;
-  const Sched sch{U, (int)P, nblk};
+  p.store_p = store_p ? 1 : 0;
+  p.mref = sc.tc_mref;
+  p.np = (int)np;
+  p.kmap = sc.tc_kmap;
+  p.kmap_nblk = (int)(vp / G_YB);
+  p.ttiles = (int)((a.N + G_XT - 1) / G_XT);
+  const Sched sch = grad_sched(nX, nY);
+  const int nblk = sch.nblk;
   const int smem = geo_smem_bytes<MODE>();
   cudaError_t e = max_dyn_smem((const void*)tc_grad_kernel<MODE>, smem);
   if (e != cudaSuccess) return e;
-  L.begin(MODE == GM_DW ? K_DW : MODE == GM_DH ? K_DH : K_LSE_DH);
-  e = launch_pdl(tc_grad_kernel<MODE>, dim3((unsigned)(2 * P)), dim3(G_THREADS), (size_t)smem, L.st, mx, mys, mya, mo,
-                 mp, p);
+  L.begin(DWX ? K_DW : MODE == GM_DH ? K_DH : K_LSE_DH);
+  e = launch_pdl(tc_grad_kernel<MODE>, dim3((unsigned)(2 * sch.P)), dim3(G_THREADS), (size_t)smem, L.st, mx, mys, mya,
+                 mo, mp, me, p);
   L.end();
-  if (e != cudaSuccess) return e;
   if (e != cudaSuccess) return e;
   SplitTiles sp;
   sp.n = 0;
@@ -1613,21 +1876,39 @@ cudaError_t tc_grad_range(const StepArgs& a, const Scratch& sc, Launch& L, int c
 }
 
 template <int MODE>
-cudaError_t tc_grad(const StepArgs& a, const Scratch& sc, Launch& L) {
+cudaError_t tc_grad(const StepArgs& a, const Scratch& sc, Launch& L, int nver = 0) {
   int ch0[4], nch[4];
   const int runs = chunk_ranges(a.C, ch0, nch);
   for (int r = 0; r < runs; ++r) {
-    const cudaError_t e = tc_grad_range<MODE>(a, sc, L, ch0[r], nch[r]);
+    const cudaError_t e = tc_grad_range<MODE>(a, sc, L, ch0[r], nch[r], nver);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+// The per-row pass between the lse+dh pass (with its repairs) and the dW pass from p.
+cudaError_t tc_hs(const StepArgs& a, const Scratch& sc, Launch& L) {
+  const int64_t np = tc_ver_rows(a.N);
+  const Sched s1 = grad_sched(a.N, a.V);
+  int blocks = (int)((np / HS_ROWS) < HS_BLOCKS ? np / HS_ROWS : HS_BLOCKS);
+  if (blocks < 1) blocks = 1;
+  L.begin(K_FINISH);
+  const cudaError_t e = launch_pdl(tc_hs_kernel, dim3((unsigned)blocks), dim3(256), 0, L.st, a, s1,
+                                   (int)((a.N + G_XT - 1) / G_XT), (int)np, tc_p_cols(a.V), (const float*)sc.lse,
+                                   (const float*)sc.tc_zt, (const float*)sc.tc_mref,
+                                   a.norm == 0 ? (float)(1.0 / (double)a.global_valid) : -1.f,
+                                   (const DevAcc*)sc.acc, sc.tc_hs, sc.tc_p, sc.tc_kmap);
+  L.end();
+  return e;
 }
 
 // Default order.  With global normalisation the scale is the caller's 1 / global_valid and the
 // one-pass logsumexp + dh runs first; with the micro-step mean, a count pass sets the scale
 // before it (its last block to finish reduces the counts).  Then: the exact repair of flagged
 // tiles (two near-empty launches when none is flagged), the row losses and counts with their
-// fixed-order reduction (run by the pass's last block), the dW pass.
+// fixed-order reduction (run by the pass's last block), then the dW pass: with the stored
+// exponentials, the per-row pass (scaled copies of h, target entries of p) and the product
+// dW += hs^T p; else the pass that recomputes the logits.
 static cudaError_t tc_microstep_fused(const StepArgs& a, const Scratch& sc, Launch& L) {
   const int64_t nparts = tc_parts(a.N);   // 256 rows per partial
   const int ntiles = (int)((a.N + TC_TILE_ROWS - 1) / TC_TILE_ROWS);
@@ -1640,15 +1921,19 @@ static cudaError_t tc_microstep_fused(const StepArgs& a, const Scratch& sc, Laun
     L.end();
     if (e != cudaSuccess) return e;
   }
-  if ((e = tc_grad<GM_FL>(a, sc, L)) != cudaSuccess) return e;
+  int nver = 0;
+  const bool stored = use_stored_p(a, sc, &nver);
+  if ((e = tc_grad<GM_FL>(a, sc, L, stored ? nver : 0)) != cudaSuccess) return e;
   if ((e = simt_repair_lse(a, sc, L)) != cudaSuccess) return e;
-  if ((e = simt_repair_dh(a, sc, L)) != cudaSuccess) return e;
+  if ((e = simt_repair_dh(a, sc, L, stored)) != cudaSuccess) return e;
   L.begin(K_FINISH);
   e = launch_pdl(rows_post_kernel, dim3((unsigned)nparts), dim3(256), 0, L.st, a, sc.lse, sc.tc_zt, sc.part_loss,
                  sc.part_cnt, sc.part_err, sc.tc_tile_flag, ntiles, sc.acc, sc.ticket, (int)(global ? FIN_ALL : FIN_LOSS));
   L.end();
   if (e != cudaSuccess) return e;
-  return tc_grad<GM_DW>(a, sc, L);
+  if (!stored) return tc_grad<GM_DW>(a, sc, L);
+  if ((e = tc_hs(a, sc, L)) != cudaSuccess) return e;
+  return tc_grad<GM_DWP>(a, sc, L, nver);
 }
 
 cudaError_t tc_microstep(const StepArgs& a, const Scratch& sc, Launch& L) {

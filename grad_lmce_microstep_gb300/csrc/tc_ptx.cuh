@@ -153,6 +153,13 @@ __device__ __forceinline__ void tma_store_2d(const void* map, uint32_t src, int 
                "r"(src), "r"(x), "r"(y)
                : "memory");
 }
+// 3D form of the store (box {64 columns, rows, chunks} of a [chunks][rows][64] view).
+__device__ __forceinline__ void tma_store_3d(const void* map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 // Element-wise global += shared (fp32 add performed at L2) over the box.
 __device__ __forceinline__ void tma_reduce_add_2d(const void* map, uint32_t src, int x, int y) {
   asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%2, %3}], [%1];" ::"l"(

@@ -28,7 +28,7 @@ ERR_INTERNAL = 8
 
 DTYPES = {"bf16": 0, "fp32": 1}
 NORMS = {"global": 0, "micro_mean": 1}
-PATHS = {"auto": 0, "simt": 1, "tcgen05": 2, "tcgen05_two_pass": 3}
+PATHS = {"auto": 0, "simt": 1, "tcgen05": 2, "tcgen05_two_pass": 3, "tcgen05_recompute": 4}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 TORCH_DTYPES = {"bf16": torch.bfloat16, "fp32": torch.float32}
 

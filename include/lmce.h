@@ -73,10 +73,17 @@ typedef enum {
   LMCE_PATH_SIMT = 1,       /* fp32 FFMA kernels (any C <= 2048, any V, either dtype)    */
   LMCE_PATH_TCGEN05 = 2,    /* tcgen05/TMA kernels: bf16, C % 256 == 0, 256 <= C <= 1024:
                                one pass for logsumexp and dh (online softmax, exact repair of
-                               rare out-of-range tiles), one pass for dW; C > 768 runs each
-                               pass once per range of at most 768 columns of the gradient */
-  LMCE_PATH_TCGEN05_TWO_PASS = 3  /* tensor cores, shapes as above, always a separate
+                               rare out-of-range tiles) that also stores its bf16
+                               exponentials, then dW as one product with them (no second
+                               logits product); C > 768 runs each pass once per range of at
+                               most 768 columns of the gradient.  Scratch: 2 bytes per
+                               (max_N row, vocabulary entry rounded up to 256) and 16 C + 32
+                               bytes per max_N row (rounded up to 256) beside the rest      */
+  LMCE_PATH_TCGEN05_TWO_PASS = 3,  /* tensor cores, shapes as above, always a separate
                                      logsumexp pass before the dW and dh passes          */
+  LMCE_PATH_TCGEN05_RECOMPUTE = 4  /* as LMCE_PATH_TCGEN05, but the dW pass recomputes the
+                                      logits instead of storing the exponentials (no
+                                      max_N x V scratch; a third more tensor work)        */
 } lmce_path;
 
 typedef struct lmce_config {
@@ -111,7 +118,9 @@ typedef struct lmce_handle lmce_handle;
 /*
  * lmce_create -- validate cfg, check the device, allocate the library scratch
  * (per-row logsumexp, per-block loss/count partials, the step accumulators and the
- * error word: about 12 * max_N + 64 KB of device memory) and return a handle in *out.
+ * error word: about 12 * max_N + 64 KB of device memory, plus the tensor-core path's
+ * buffers, the largest being the stored exponentials of LMCE_PATH_TCGEN05 -- see lmce_path)
+ * and return a handle in *out.
  *   dW : device, fp32 [V, C], owned by the caller and kept by the handle until
  *        lmce_destroy.  The first lmce_microstep after create or finalize WRITES it
  *        (dW = this micro-step's gradient) unless cfg.flags has LMCE_ACCUMULATE_FROM_START;
@@ -290,8 +299,8 @@ LMCE_API const char* lmce_status_string(int status);
 /* lmce_launch_count -- kernels this handle has launched since create (host counter). */
 LMCE_API int64_t lmce_launch_count(const lmce_handle* h);
 
-/* lmce_selected_path -- LMCE_PATH_SIMT, LMCE_PATH_TCGEN05 or LMCE_PATH_TCGEN05_TWO_PASS:
- * the path micro-steps run. */
+/* lmce_selected_path -- LMCE_PATH_SIMT, LMCE_PATH_TCGEN05, LMCE_PATH_TCGEN05_TWO_PASS or
+ * LMCE_PATH_TCGEN05_RECOMPUTE: the path micro-steps run. */
 LMCE_API int lmce_selected_path(const lmce_handle* h);
 
 /*

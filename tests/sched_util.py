@@ -85,3 +85,9 @@ def guard_excess(z_row: np.ndarray, segs):
         for b in blocks:
             ex = max(ex, zb[b * YB:min(V, b * YB + YB)].max() - m)
     return ex
+
+
+def max_segments(nX: int, nY: int, pairs: int) -> int:
+    """Most pairs sharing one X tile: the copies of the scaled rows of h that the dW pass from
+    the stored exponentials keeps, one per segment of a token tile."""
+    return max(len(segment_blocks(nX, nY, pairs, t)) for t in range((nX + XT - 1) // XT))

@@ -14,7 +14,7 @@ from gpu_util import GRAD_REL, assert_parity, max_rel_err, run_lib, run_oracle, 
 
 pytestmark = pytest.mark.gpu
 
-PATHS_BF16 = ["simt", "tcgen05", "tcgen05_two_pass"]
+PATHS_BF16 = ["simt", "tcgen05", "tcgen05_two_pass", "tcgen05_recompute"]
 
 
 def _masked(seed, C=256, V=1000, T=128):

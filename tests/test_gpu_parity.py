@@ -13,7 +13,7 @@ from gpu_util import GRAD_REL, assert_parity, max_rel_err, run_lib, run_oracle, 
 
 pytestmark = pytest.mark.gpu
 
-PATHS_BF16 = ["simt", "tcgen05", "tcgen05_two_pass"]
+PATHS_BF16 = ["simt", "tcgen05", "tcgen05_two_pass", "tcgen05_recompute"]
 
 
 def _need_path(path, C, V, dtype):
@@ -78,7 +78,7 @@ def test_lse_dh_repair_of_out_of_range_tiles():
     w.micro[1][1][17] = 700
     ref = run_oracle(w)
     assert ref.micro[0].lse[5] > 100.0
-    for path in ("tcgen05", "tcgen05_two_pass"):
+    for path in ("tcgen05", "tcgen05_two_pass", "tcgen05_recompute"):
         got = run_lib(w, path=path)
         assert got["status"] == M.OK
         assert_parity(got, ref, "bf16")
@@ -134,7 +134,7 @@ def test_lse_dh_wide_logit_within_range(nats):
         assert_parity(got, ref, "bf16")
 
 
-@pytest.mark.parametrize("path", ["tcgen05", "tcgen05_two_pass"])
+@pytest.mark.parametrize("path", ["tcgen05", "tcgen05_two_pass", "tcgen05_recompute"])
 def test_wide_hidden_c1024(path):
     # C = 1024: TMEM holds three 256-row chunks of the gradient beside the logits tile, so each
     # tensor-core gradient pass runs twice, over C columns [0, 512) and [512, 1024)
