@@ -607,6 +607,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       }
       for (int j = 0; j <= nb && ok; ++j) {
         const int nst = (j < nb ? KC : 0) + (j >= 1 ? 4 / AQ : 0);
+        if (DWP && pw == 0 && lane == 0) {
+          // p of block b0+j+1 (first also of b0+j) into L2 two blocks before its loads: p comes
+          // from DRAM, and the ring covers only a block's worth of load latency
+          for (int jj = (j == 0 ? 0 : j + 1); jj <= j + 1 && jj < nb; ++jj)
+            for (int q = 0; q < 4; ++q) tma_prefetch_3d(&tmX, 0, (b0 + jj) * G_YB + q * 64, 2 * t + (int)rank);
+        }
         if (DWP && j >= 1 && lane == 0) {
           kv_cur0 = kv_nxt0;
           kv_cur1 = kv_nxt1;
@@ -647,7 +653,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
               const int kv = (q >> 1) ? kv_cur1 : kv_cur0;
               tma_load_4d_cg2(dst, &tmYa, bar, 0, kv * p.np + bj * G_YB + q * 64, 2 * (int)rank, p.ch0);
             } else if (lane == 1) {
-              tma_load_3d_cg2(dst + P_OFF, &tmX, bar, 0, bj * G_YB + q * 64, 2 * t + (int)rank);
+              tma_load_3d_cg2_hint(dst + P_OFF, &tmX, bar, 0, bj * G_YB + q * 64, 2 * t + (int)rank, policy_evict_first());
             }
           } else if (lane == 0) {
             // accumulation phase of block b0+j-1, quarters AQ q .. AQ q + AQ - 1 (64 AQ stream rows):
@@ -1055,7 +1061,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             // (a box may reach past row N, clipped, but never starts there)
             const int bj = b0 + j + s_rot;
             const int vb = bj < nblk ? bj : bj - nblk;
-            tma_store_3d(&tmE, dz_row + db * G_DZ + (uint32_t)(qd & 1) * 4096, 0, row0, vb * 4 + ks);
+            tma_store_3d_hint(&tmE, dz_row + db * G_DZ + (uint32_t)(qd & 1) * 4096, 0, row0, vb * 4 + ks,
+                              policy_evict_first());   // read once, by the dW pass
             bulk_commit();
           }
         }

@@ -153,11 +153,41 @@ __device__ __forceinline__ void tma_store_2d(const void* map, uint32_t src, int 
                "r"(src), "r"(x), "r"(y)
                : "memory");
 }
+// 3D form of the pair load with an L2 cache policy (from createpolicy).
+__device__ __forceinline__ void tma_load_3d_cg2_hint(uint32_t dst, const void* map, uint32_t bar_cluster, int x, int y, int z,
+                                                     uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z), "l"(policy)
+      : "memory");
+}
+
+// Brings a box of the tensor into L2 ahead of its load (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_3d(const void* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
+// L2 policy for data touched once: its lines are the first to be evicted.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // 3D form of the store (box {64 columns, rows, chunks} of a [chunks][rows][64] view).
 __device__ __forceinline__ void tma_store_3d(const void* map, uint32_t src, int x, int y, int z) {
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
                "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+// The store with an L2 cache policy.
+__device__ __forceinline__ void tma_store_3d_hint(const void* map, uint32_t src, int x, int y, int z, uint64_t policy) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y), "r"(z), "l"(policy)
                : "memory");
 }
 // Element-wise global += shared (fp32 add performed at L2) over the box.
