@@ -365,11 +365,11 @@ __global__ void __launch_bounds__(256) tc_combine_kernel(const float* __restrict
 // with different references (each pair fixes its own), so hs keeps one copy per segment and the
 // dW pass takes, for each 128-token tile and 256-row vocabulary block, the copy of the segment
 // that covered that pair of indices.  f_n and the target's bracket hold only while m_n lies within
-// P_RANGE of lse_n log2 e (the bracket <= 2^P_RANGE, f_n >= s 2^-P_RANGE, far from fp32's
-// limits); a segment whose reference lies further below (its first block's maximum more than
-// P_RANGE + FL_HEADROOM = 96 below, in base 2, a row whose mass lies in other segments) flags its
-// tile too, and the exact repair rewrites the rows of a flagged tile with the normalised p and
-// m_n = lse_n log2 e.  Against recomputing the logits this trades a quarter
+// p_range(s) = min(96, 118 + log2 s) of lse_n log2 e: the bracket stays <= 2^96 and f_n >= 2^-118,
+// so that f_n h_n stays a normal bf16 for any |h| >= 2^-8 (96 down to s = 2^-22).  A segment whose
+// reference lies further below (its first block's maximum more than p_range + FL_HEADROOM below,
+// in base 2: a row whose mass lies in other segments) flags its tile too, and the exact repair
+// rewrites the rows of a flagged tile with the normalised p and m_n = lse_n log2 e.  Against recomputing the logits this trades a quarter
 // of the tensor work (6 N C V flop per micro-step instead of 8) for one write and one read of
 // the N x V bf16 operand, which stream at a small fraction of HBM bandwidth beside the products.
 constexpr int G_XT = 128;                  // X rows per pair (64 per CTA)
@@ -383,7 +383,8 @@ enum GradMode { GM_DW = 0, GM_DH = 1, GM_FL = 2, GM_DWP = 3 };
 // hand-offs from the waiter warp to the MMA warp, then the dz tile's hand-off.
 constexpr int HB_DZ_FULL = 6;
 constexpr float FL_HEADROOM = 32.f;        // lse+dh pass: reference above the first block's maximum (base 2)
-constexpr float P_RANGE = 64.f;            // stored p: largest lse log2 e - m of a row's segment kept
+// stored p: largest lse log2 e - m of a row's segment kept (s > 0: the scale)
+__host__ __device__ __forceinline__ float p_range(float s) { return s > 0.f ? fminf(96.f, 118.f + log2f(s)) : 96.f; }
 
 // Ring geometry per mode: NST slots of SLOT bytes.  An S stage carries SK 64-column atoms of
 // K = C (per CTA: 128 stream rows, then 64 X rows at SK * 16 KB); an accumulation stage
@@ -1100,8 +1101,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           }
           if (whole) {
             if (xg < p.N) p.lse_out[xg] = (m2 + log2f(l)) * LN2;
-            // stored p: the row's only reference must lie within P_RANGE of its lse log2 e
-            if (p.store_p && yrow >= 0 && !(log2f(l) <= P_RANGE) && dcheck(t < T, p.err, BS_TILE_FLAG))
+            // stored p: the row's only reference must lie within p_range of its lse log2 e
+            if (p.store_p && yrow >= 0 && !(log2f(l) <= p_range(s)) && dcheck(t < T, p.err, BS_TILE_FLAG))
               atomicOr(p.tile_flag + t, 1u);
           } else if (slot_ok) {
             p.part_lm[((size_t)slot * 2 + 0) * G_XT + xl] = m2;
@@ -1290,10 +1291,10 @@ __global__ void __launch_bounds__(256) tc_split_combine_kernel(GradParams p, Sch
       fac[xl] = y >= 0 ? s / l : 0.f;
       if (blockIdx.y == 0 && x < p.N) p.lse_out[x] = (M + log2f(l)) * LN2;
       if (blockIdx.y == 0 && p.store_p && y >= 0) {
-        // stored p: every segment's reference within P_RANGE of the row's lse log2 e
-        const float l2 = M + log2f(l);
+        // stored p: every segment's reference within p_range of the row's lse log2 e
+        const float l2 = M + log2f(l), pr = p_range(s);
         bool far = false;
-        for (int k = 0; k < nslots; ++k) far |= !(l2 - p.part_lm[((size_t)slots[k] * 2 + 0) * G_XT + xl] <= P_RANGE);
+        for (int k = 0; k < nslots; ++k) far |= !(l2 - p.part_lm[((size_t)slots[k] * 2 + 0) * G_XT + xl] <= pr);
         if (far && dcheck(t < sch.U / sch.nblk, p.err, BS_TILE_FLAG)) atomicOr(p.tile_flag + t, 1u);
       }
     }

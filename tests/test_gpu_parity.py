@@ -128,7 +128,10 @@ def test_lse_dh_wide_logit_within_range(nats):
     w.micro[0][1][5] = 700
     ref = run_oracle(w)
     assert nats - 5.0 < ref.micro[0].lse[5] < nats + 5.0
-    for path in ("tcgen05", "tcgen05_two_pass"):
+    # stored exponentials: the token's tile is split into four single-block segments, and the
+    # references of the three without the wide logit lie ~55 / ~95 (base 2) below its lse: inside
+    # the stored path's range (96 at this scale), so no repair runs there either
+    for path in ("tcgen05", "tcgen05_two_pass", "tcgen05_recompute"):
         got = run_lib(w, path=path)
         assert got["status"] == M.OK
         assert_parity(got, ref, "bf16")
