@@ -450,11 +450,12 @@ __device__ __forceinline__ float grad_scale(const GradParams& p) {
 // (at most the pair's first and last) writes fp32 partial sums to slot 2 pi (first segment) or
 // 2 pi + 1, and the split-combine kernels add the partials of each split tile in pair order.
 //
-// The passes whose stream is the vocabulary (dh, lse+dh) visit the blocks of X tile t in the
-// rotated order (j + rot(t)) mod nblk, j = 0, 1, ...: rot(t) is chosen so that the pair holding
-// most of tile t reaches vocabulary block (tau mod nblk) at its tau-th unit.  All pairs then sweep
-// W roughly in phase, and the part of W being read at any time is a few blocks instead of the
-// whole matrix (every pair at its own offset), so W is read from DRAM about once per sweep.  The
+// The passes whose stream is the vocabulary (dh, lse+dh), and the dW pass from p (stream: the
+// tokens), visit the blocks of X tile t in the rotated order (j + rot(t)) mod nblk, j = 0, 1, ...:
+// rot(t) is chosen so that the pair holding most of tile t reaches block (tau mod nblk) at its
+// tau-th unit.  All pairs then sweep the stream roughly in phase, and the part of it being read
+// at any time is a few blocks instead of the whole operand (every pair at its own offset), so W
+// (or the scaled rows of h) is read from DRAM about once per sweep.  The
 // order of the blocks within a segment changes no sum's definition: dh and the (max, sum) merge
 // are order-free, and the order is a fixed function of the schedule (bitwise reproducible).
 struct Sched {
@@ -601,10 +602,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
       const int b0 = (int)(max(ub, (long long)t * nblk) - (long long)t * nblk);
       const int nb = (int)(min(ue, (long long)(t + 1) * nblk) - (long long)t * nblk) - b0;
       const int x0 = t * G_XT;
-      const int rt = DWX ? 0 : sch.rot(t);
+      const int rt = DW ? 0 : sch.rot(t);
+      auto rblk = [&](int jj) { const int b = b0 + jj + rt; return b < nblk ? b : b - nblk; };
       if (DWP && lane == 0) {
-        kv_nxt0 = kver(2 * b0, t >> 1);
-        kv_nxt1 = kver(2 * b0 + 1, t >> 1);
+        kv_nxt0 = kver(2 * rblk(0), t >> 1);
+        kv_nxt1 = kver(2 * rblk(0) + 1, t >> 1);
       }
       for (int j = 0; j <= nb && ok; ++j) {
         const int nst = (j < nb ? KC : 0) + (j >= 1 ? 4 / AQ : 0);
@@ -612,14 +614,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
           // p of block b0+j+1 (first also of b0+j) into L2 two blocks before its loads: p comes
           // from DRAM, and the ring covers only a block's worth of load latency
           for (int jj = (j == 0 ? 0 : j + 1); jj <= j + 1 && jj < nb; ++jj)
-            for (int q = 0; q < 4; ++q) tma_prefetch_3d(&tmX, 0, (b0 + jj) * G_YB + q * 64, 2 * t + (int)rank);
+            for (int q = 0; q < 4; ++q) tma_prefetch_3d(&tmX, 0, rblk(jj) * G_YB + q * 64, 2 * t + (int)rank);
         }
         if (DWP && j >= 1 && lane == 0) {
           kv_cur0 = kv_nxt0;
           kv_cur1 = kv_nxt1;
           if (j < nb) {
-            kv_nxt0 = kver(2 * (b0 + j), t >> 1);
-            kv_nxt1 = kver(2 * (b0 + j) + 1, t >> 1);
+            kv_nxt0 = kver(2 * rblk(j), t >> 1);
+            kv_nxt1 = kver(2 * rblk(j) + 1, t >> 1);
           }
         }
         for (int u = 0; u < nst; ++u, ++it) {
@@ -648,7 +650,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
             // block b0+j-1, quarter q (64 tokens): hs rows of the quarter's segment copy, my 128 C
             // of every chunk; p rows of the same tokens, my 64 vocabulary rows of the tile
             const int q = u;
-            const int bj = b0 + j - 1;
+            const int bj = rblk(j - 1);
             if (lane == 0) {
               dcheck(bj < nblk && q < 4, p.err, BS_TMA_ROW);
               const int kv = (q >> 1) ? kv_cur1 : kv_cur0;
