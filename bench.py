@@ -369,6 +369,34 @@ def run_lmce(args, rank, world, local_rank):
     aw_bytes = p_master.numel() * (4 + 8 + 8 + 8 + (2 if w.dtype == "bf16" else 0))
     del p_master, m_st, v_st, W_next
 
+    # the same steps on the path whose dW pass recomputes the logits (LMCE_PATH_TCGEN05_RECOMPUTE:
+    # logits and dlogits never leave the chip, no N x V scratch), device-timed like the headline
+    recompute = None
+    if L.path == "tcgen05" and not args.compact and not args.final_norm and world == 1:
+        dW_r = torch.empty_like(dW)
+        L_r = M.Lmce(w.C, w.V, max_N, dW_r, w.dtype, norm="global", grad_accum_steps=w.G, path="tcgen05_recompute")
+
+        def step_r():
+            for (h, y), dh in zip(mbs, dhs):
+                L_r.microstep(h, W, y, gv, dh, stream=stream)
+            return L_r.finalize(stream=stream)
+
+        for _ in range(max(3, args.warmup)):
+            step_r()
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step_r()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_r = ev0.elapsed_time(ev1) / args.steps
+        v_r = tokens_rank / (ms_r / 1e3)
+        recompute = {"path": "tcgen05_recompute", "value": v_r, "unit": UNIT, "ms_per_step": ms_r,
+                     "frac_of_peak": v_r * sum(nvs) / tokens_rank * 6.0 * w.C * w.V / 1e12 / peaks()[0]["bf16_tflops"],
+                     "executed_flop_per_token": 8.0 * w.C * w.V}
+        L_r.close()
+        del dW_r
+
     if rank != 0:
         return
 
@@ -482,6 +510,7 @@ def run_lmce(args, rank, world, local_rank):
         "dw_sumsq": dw_sumsq,
         "adamw": adamw,
         "final_norm": final_norm,
+        "recompute_path": recompute,
         "clocks": clocks,
         "check": {"loss_mean": res[2], "valid": res[1]},
     }
