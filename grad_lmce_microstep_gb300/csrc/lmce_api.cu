@@ -230,7 +230,8 @@ struct lmce_handle {
   lmce_config cfg;
   float* dW;
   int device;
-  int path;            // resolved: LMCE_PATH_SIMT, LMCE_PATH_TCGEN05 or LMCE_PATH_TCGEN05_TWO_PASS
+  int path;            // resolved: LMCE_PATH_SIMT, LMCE_PATH_TCGEN05, LMCE_PATH_TCGEN05_TWO_PASS or
+                       // LMCE_PATH_TCGEN05_RECOMPUTE
   Scratch sc;
   DevAcc* host_acc;    // pinned
   bool first;          // next micro-step writes dW instead of adding (unless LMCE_ACCUMULATE_FROM_START)
@@ -368,11 +369,28 @@ extern "C" int lmce_create(const lmce_config* cfg, float* dW, lmce_handle** out)
     // references and the scaled rows of h; the per-row pass defines every element it reads
     const int64_t vp = tc_p_cols(cfg->V), np = tc_ver_rows(maxN);
     const size_t ttiles = (size_t)(maxN + TC_TILE_ROWS - 1) / TC_TILE_ROWS;
-    ok = cudaMalloc(&h->sc.tc_p, sizeof(uint16_t) * (size_t)maxN * (size_t)vp) == cudaSuccess &&
-         cudaMalloc(&h->sc.tc_mref, sizeof(float) * (size_t)TC_MAX_VER * (size_t)np) == cudaSuccess &&
-         cudaMalloc(&h->sc.tc_hs, sizeof(uint16_t) * (size_t)TC_MAX_VER * (size_t)np * (size_t)cfg->C) == cudaSuccess &&
-         cudaMalloc(&h->sc.tc_kmap, ttiles * (size_t)(vp / 256)) == cudaSuccess;
+    const bool got = cudaMalloc(&h->sc.tc_p, sizeof(uint16_t) * (size_t)maxN * (size_t)vp) == cudaSuccess &&
+                     cudaMalloc(&h->sc.tc_mref, sizeof(float) * (size_t)TC_MAX_VER * (size_t)np) == cudaSuccess &&
+                     cudaMalloc(&h->sc.tc_hs, sizeof(uint16_t) * (size_t)TC_MAX_VER * (size_t)np * (size_t)cfg->C) ==
+                         cudaSuccess &&
+                     cudaMalloc(&h->sc.tc_kmap, ttiles * (size_t)(vp / 256)) == cudaSuccess;
     h->sc.tc_p_rows = maxN;
+    if (!got) {
+      // not enough device memory for the N x V scratch: LMCE_PATH_AUTO falls back to recomputing
+      // the logits in the dW pass; an explicit LMCE_PATH_TCGEN05 reports the failure
+      cudaFree(h->sc.tc_p);
+      cudaFree(h->sc.tc_mref);
+      cudaFree(h->sc.tc_hs);
+      cudaFree(h->sc.tc_kmap);
+      h->sc.tc_p = nullptr;
+      h->sc.tc_mref = nullptr;
+      h->sc.tc_hs = nullptr;
+      h->sc.tc_kmap = nullptr;
+      h->sc.tc_p_rows = 0;
+      (void)cudaGetLastError();   // the failed allocation's error is not sticky; clear it
+      if (cfg->path == LMCE_PATH_AUTO) h->path = LMCE_PATH_TCGEN05_RECOMPUTE;
+      else ok = false;
+    }
   }
   ok = ok && cudaMalloc(&h->sumsq_part, sizeof(double) * (SQ_BLOCKS + 1)) == cudaSuccess;
   if (ok && (cfg->flags & LMCE_COMPACT_VALID_ROWS)) {

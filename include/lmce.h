@@ -69,7 +69,9 @@ typedef enum {
 } lmce_norm;
 
 typedef enum {
-  LMCE_PATH_AUTO = 0,       /* tensor-core path when the shape allows it, else SIMT      */
+  LMCE_PATH_AUTO = 0,       /* tensor-core path when the shape allows it, else SIMT; the
+                               stored-exponential dW pass when its scratch fits in device
+                               memory, else the recomputing one                          */
   LMCE_PATH_SIMT = 1,       /* fp32 FFMA kernels (any C <= 2048, any V, either dtype)    */
   LMCE_PATH_TCGEN05 = 2,    /* tcgen05/TMA kernels: bf16, C % 256 == 0, 256 <= C <= 1024:
                                one pass for logsumexp and dh (online softmax, exact repair of

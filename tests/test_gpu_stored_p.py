@@ -94,3 +94,31 @@ def test_far_segment_reference_is_repaired():
     got = run_lib(w, path="tcgen05")
     assert got["status"] == M.OK
     assert_parity(got, ref, "bf16")
+
+
+def test_auto_falls_back_when_p_does_not_fit():
+    # max_N = 4,000,000 rows: the stored exponentials would need ~400 GB (2 bytes x 50,432 per
+    # row), more than the device has, while the rest of the scratch (~1 GB) fits.  LMCE_PATH_AUTO
+    # then takes the recomputing dW pass; an explicit LMCE_PATH_TCGEN05 reports the failure.
+    big = 4_000_000
+    W0 = torch.zeros(50304, 768, dtype=torch.float32, device="cuda")
+    with pytest.raises(M.LmceError) as e:
+        M.Lmce(768, 50304, big, W0, "bf16", path="tcgen05")
+    assert e.value.status == M.ERR_CUDA
+    del W0
+    w = I.custom([300, 173], 256, 50304, "bf16", seed=76, ignore_frac=0.1)
+    W, mbs = (w.W.cuda(), [(h.cuda(), y.cuda()) for h, y in w.micro])
+    dW = torch.empty(w.V, w.C, device="cuda")
+    L = M.Lmce(w.C, w.V, big, dW, "bf16", grad_accum_steps=2, path="auto")
+    assert L.path == "tcgen05_recompute"
+    gv = sum(w.valid_counts())
+    dhs = []
+    for h, y in mbs:
+        dh = torch.empty_like(h)
+        L.microstep(h, W, y, gv, dh)
+        dhs.append(dh)
+    ls, cnt, mean = L.finalize()
+    L.close()
+    got = {"dW": dW.double().cpu().numpy(), "dh": [d.double().cpu().numpy() for d in dhs],
+           "row_loss": [None, None], "loss_sum": ls, "count": cnt, "loss_mean": mean}
+    assert_parity(got, run_oracle(w), "bf16")
