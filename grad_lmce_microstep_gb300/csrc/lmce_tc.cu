@@ -395,20 +395,23 @@ __host__ __device__ __forceinline__ float p_range(float s) { return s > 0.f ? fm
 // pays more than a second dz buffer.
 template <int MODE>
 struct Geo {
-  static constexpr int NST = 4, SLOT = 49152, SK = 2, AQ = 1, NDZ = 1;
+  static constexpr int NST = 4, SLOT = 49152, SK = 2, AQ = 1, NDZ = 1, DZB = G_DZ;
   static_assert(2 + NST <= HB_DZ_FULL, "ring hand-off barriers overlap the dz tile's");
 };
 // dW from the stored exponentials: a stage is one 64-token quarter of hs (every C chunk, 48 KB)
-// and of p (this CTA's 64 vocabulary rows, 8 KB at P_OFF); the 32 KB buffer stages the flush.
+// and of p (this CTA's 64 vocabulary rows, 8 KB at P_OFF).  A stage's loads take 1-1.5 us to
+// land (in-kernel clock stamps) against ~0.5 us of MMA work per stage, so the ring needs four
+// slots; they take all the shared memory, and the flush goes from TMEM straight to global
+// memory instead of through a staging buffer.
 constexpr int P_OFF = 3 * 16384;
 template <>
 struct Geo<GM_DWP> {
-  static constexpr int NST = 3, SLOT = P_OFF + 8192, SK = 2, AQ = 1, NDZ = 1;
+  static constexpr int NST = 4, SLOT = P_OFF + 8192, SK = 2, AQ = 1, NDZ = 1, DZB = 0;
   static_assert(2 + NST <= HB_DZ_FULL, "ring hand-off barriers overlap the dz tile's");
 };
 template <int MODE>
 constexpr int geo_smem_bytes() {
-  return Geo<MODE>::NST * Geo<MODE>::SLOT + Geo<MODE>::NDZ * G_DZ;   // the buffer is declared 1024-aligned
+  return Geo<MODE>::NST * Geo<MODE>::SLOT + Geo<MODE>::DZB;   // the buffer is declared 1024-aligned
 }
 
 struct GradParams {
@@ -1176,6 +1179,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
 #pragma unroll
             for (int e = 0; e < 32; ++e)
               if (slot_ok) part[(size_t)(hf * 64 + cc * 32 + e) * p.C + c] = v[e];
+          }
+        }
+      } else if (DWP) {
+        // straight from TMEM: per 16-column round, for each of its 16 X rows, the warp's 32 C
+        // columns as one 128-byte access (reduce-add into dW, or a store)
+        float* part = p.part + (size_t)slot * G_XT * p.C;
+        for (int i = 0; i < NCH; ++i) {
+          const int c = (p.ch0 + i) * 256 + (int)rank * 128 + kl;
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            float v[16];
+            tmem_ld16(tmem + i * 128 + lane_off + hf * 64 + cc * 16, v);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int xr = hf * 64 + cc * 16 + e;
+              if (!whole) {
+                if (slot_ok) part[(size_t)xr * p.C + c] = v[e];
+              } else if (x0 + xr < nX) {
+                float* d = p.dW + (size_t)(x0 + xr) * p.C + c;
+                if (p.beta) atomicAdd(d, v[e]);
+                else *d = v[e];
+              }
+            }
           }
         }
       } else {
