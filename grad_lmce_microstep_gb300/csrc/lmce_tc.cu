@@ -1127,9 +1127,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
         if (epi_abort) break;
       }
       // acc^T in TMEM: lane = C row, column = X row of the tile; thread: lane quarter qd (C rows
-      // qd*32 + lane of this CTA's 128 per chunk), columns from hf*64.  The dW pass and whole dh
-      // tiles leave through the dz buffer (idle: the segment's accumulation has completed) by
-      // TMA, so the flush is not limited by the rate at which one SM retires scattered stores:
+      // qd*32 + lane of this CTA's 128 per chunk), columns from hf*64.  The recomputing dW pass
+      // and whole dh tiles leave through the dz buffer (idle: the segment's accumulation has
+      // completed) by TMA, so the flush is not limited by the rate at which one SM retires
+      // scattered stores; the dW pass from p has no such buffer (its ring takes all of shared
+      // memory) and writes from registers:
       //  - dW pass: 16-column rounds through two 16 KB halves, each round two boxes of 16 X rows
       //    x 128 C (accumulating into dW: reduce-add at L2; else stores; partial tiles: stores);
       //  - bf16 dh of a whole tile: one 256-column chunk at a time; the rows W[y] of its one-hot
