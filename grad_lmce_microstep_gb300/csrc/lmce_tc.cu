@@ -378,7 +378,8 @@ constexpr int G_DZ = G_YB * 128;           // one dz buffer: 256 K-rows x 64 bf1
 constexpr int G_EPI_WARPS = 8;
 constexpr int G_THREADS = 128 + 32 * G_EPI_WARPS;  // warps 0 and 10 TMA, 1 MMA, 2-9 epilogue, 11 ring waiter
 
-enum GradMode { GM_DW = 0, GM_DH = 1, GM_FL = 2, GM_DWP = 3 };
+// GM_DWP4: the dW pass from p with four 256-row C chunks (C = 1024) in one run
+enum GradMode { GM_DW = 0, GM_DH = 1, GM_FL = 2, GM_DWP = 3, GM_DWP4 = 4 };
 // Named barriers of the gradient kernels: 1 the epilogue warps, 2 .. 2 + NST - 1 the ring slots'
 // hand-offs from the waiter warp to the MMA warp, then the dz tile's hand-off.
 constexpr int HB_DZ_FULL = 6;
@@ -395,18 +396,25 @@ __host__ __device__ __forceinline__ float p_range(float s) { return s > 0.f ? fm
 // pays more than a second dz buffer.
 template <int MODE>
 struct Geo {
-  static constexpr int NST = 4, SLOT = 49152, SK = 2, AQ = 1, NDZ = 1, DZB = G_DZ;
+  static constexpr int NST = 4, SLOT = 49152, SK = 2, AQ = 1, NDZ = 1, DZB = G_DZ, POFF = 0;
   static_assert(2 + NST <= HB_DZ_FULL, "ring hand-off barriers overlap the dz tile's");
 };
 // dW from the stored exponentials: a stage is one 64-token quarter of hs (every C chunk, 48 KB)
-// and of p (this CTA's 64 vocabulary rows, 8 KB at P_OFF).  A stage's loads take 1-1.5 us to
+// and of p (this CTA's 64 vocabulary rows, 8 KB at POFF).  A stage's loads take 1-1.5 us to
 // land (in-kernel clock stamps) against ~0.5 us of MMA work per stage, so the ring needs four
 // slots; they take all the shared memory, and the flush goes from TMEM straight to global
-// memory instead of through a staging buffer.
-constexpr int P_OFF = 3 * 16384;
+// memory instead of through a staging buffer.  With four C chunks (C = 1024: TMEM holds all of
+// acc^T, there being no logits tile) a stage is 72 KB and three slots cover ~1.3 us of MMA work.
 template <>
 struct Geo<GM_DWP> {
-  static constexpr int NST = 4, SLOT = P_OFF + 8192, SK = 2, AQ = 1, NDZ = 1, DZB = 0;
+  static constexpr int POFF = 3 * 16384;
+  static constexpr int NST = 4, SLOT = POFF + 8192, SK = 2, AQ = 1, NDZ = 1, DZB = 0;
+  static_assert(2 + NST <= HB_DZ_FULL, "ring hand-off barriers overlap the dz tile's");
+};
+template <>
+struct Geo<GM_DWP4> {
+  static constexpr int POFF = 4 * 16384;
+  static constexpr int NST = 3, SLOT = POFF + 8192, SK = 2, AQ = 1, NDZ = 1, DZB = 0;
   static_assert(2 + NST <= HB_DZ_FULL, "ring hand-off barriers overlap the dz tile's");
 };
 template <int MODE>
@@ -429,7 +437,8 @@ struct GradParams {
   float* lse_out;        // lse+dh pass: per-row logsumexp
   unsigned* tile_flag;   // lse+dh pass: per 128-token tile, set when the tile needs the repair
   int N, V, C;
-  int ch0, nch;          // 256-row C chunks [ch0, ch0 + nch) of acc^T handled by this launch (nch <= 3)
+  int ch0, nch;          // 256-row C chunks [ch0, ch0 + nch) of acc^T handled by this launch (nch <= 3;
+                         // 4 in the dW pass from p at C = 1024)
   int beta;              // dW pass: 0 writes, 1 adds
   float fl_limit;        // lse+dh pass: largest base-2 exponent of p kept (115 - ceil(log2 V))
   uint64_t wait_ns;      // limit of every bounded wait (WAIT_NS; shorter in the failure-detection test)
@@ -501,12 +510,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(G_THREADS, 1)
                    const __grid_constant__ CUtensorMap tmP, const __grid_constant__ CUtensorMap tmE, GradParams p) {
   constexpr bool DW = MODE == GM_DW;
   constexpr bool FL = MODE == GM_FL;
-  constexpr bool DWP = MODE == GM_DWP;      // dW from the stored exponentials: no logits tile
+  constexpr bool DWP = MODE == GM_DWP || MODE == GM_DWP4;   // dW from the stored exponentials: no logits tile
+  constexpr int P_OFF = Geo<MODE>::POFF;
   constexpr bool DWX = DW || DWP;           // X = vocabulary rows, stream = tokens, output dW
   constexpr int NST = Geo<MODE>::NST, SLOT = Geo<MODE>::SLOT, SK = Geo<MODE>::SK, AQ = Geo<MODE>::AQ;
   constexpr int NDZ = Geo<MODE>::NDZ;
   static_assert(SK * 24576 <= SLOT && AQ * 16384 * 3 <= SLOT && 4 % AQ == 0, "stage does not fit its slot");
   static_assert(!DWP || (AQ == 1 && P_OFF + 8192 <= SLOT), "p quarter does not fit its slot");
+  static_assert(!DWP || P_OFF >= 16384, "hs quarter does not fit before p");
   griddep_wait();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 128-byte-swizzled operands need 1024-byte alignment; the launch reserves no slack for
@@ -1282,7 +1293,7 @@ __device__ __forceinline__ int split_slots(const Sched& sch, int t, int* slots) 
 constexpr int COMB_BLOCKS = 8, COMB_U = 4;
 template <int MODE>
 __global__ void __launch_bounds__(256) tc_split_combine_kernel(GradParams p, Sched sch, const __grid_constant__ SplitTiles sp) {
-  constexpr bool DW = MODE == GM_DW || MODE == GM_DWP;
+  constexpr bool DW = MODE == GM_DW || MODE == GM_DWP || MODE == GM_DWP4;
   constexpr bool FL = MODE == GM_FL;
   __shared__ int slots[16];
   __shared__ int nslots;
@@ -1821,7 +1832,7 @@ bool use_stored_p(const StepArgs& a, const Scratch& sc, int* nver) {
 template <int MODE>
 cudaError_t tc_grad_range(const StepArgs& a, const Scratch& sc, Launch& L, int ch0, int nch, int nver = 0) {
   constexpr bool DW = MODE == GM_DW;
-  constexpr bool DWP = MODE == GM_DWP;
+  constexpr bool DWP = MODE == GM_DWP || MODE == GM_DWP4;
   constexpr bool DWX = DW || DWP;
   const void* X = DW ? a.W : a.hidden;
   const void* Y = DW ? a.hidden : a.W;
@@ -1971,6 +1982,8 @@ static cudaError_t tc_microstep_fused(const StepArgs& a, const Scratch& sc, Laun
   if (e != cudaSuccess) return e;
   if (!stored) return tc_grad<GM_DW>(a, sc, L);
   if ((e = tc_hs(a, sc, L)) != cudaSuccess) return e;
+  // C = 1024: all four chunks in one run (p read once)
+  if (a.C == 4 * 256) return tc_grad_range<GM_DWP4>(a, sc, L, 0, 4, nver);
   return tc_grad<GM_DWP>(a, sc, L, nver);
 }
 
