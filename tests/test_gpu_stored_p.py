@@ -29,6 +29,9 @@ CASES = {
     "c1024": lambda: I.custom([300, 140], 1024, 900, "bf16", seed=73, ignore_frac=0.05),
     # token counts one past a 256-row block, one row, and a vocabulary smaller than one tile
     "one_row_and_tails": lambda: I.custom([257, 1, 129], 512, 100, "bf16", seed=74),
+    # V = 257: the last 256-column block of p holds one valid column, the last 128-row dW tile
+    # one valid row; 17 tokens in the second micro-step
+    "v257": lambda: I.custom([300, 17], 256, 257, "bf16", seed=77, ignore_frac=0.1),
 }
 
 
