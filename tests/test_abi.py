@@ -51,6 +51,7 @@ def test_argument_errors_before_any_device_call(lib):
     assert lib.lmce_create(ctypes.byref(cfg), None, ctypes.byref(h)) == M.ERR_ARG
     assert lib.lmce_create(None, ctypes.c_void_p(16), ctypes.byref(h)) == M.ERR_ARG
     for bad in (dict(C=0), dict(V=-1), dict(max_N=-5), dict(dtype=7), dict(norm=3), dict(path=9),
+                dict(path=5), dict(C=100, path=4), dict(dtype=1, path=2),
                 dict(grad_accum_steps=0), dict(flags=8), dict(C=4096, path=1)):
         c = M.Config(768, 50304, 1024, 0, -100, 0, 1, 0, 0)
         for k, v in bad.items():
@@ -122,6 +123,10 @@ def test_cuda_failure_reaches_the_caller_as_a_status(lib):
     h = ctypes.c_void_p(123)
     assert lib.lmce_create(ctypes.byref(cfg), ctypes.c_void_p(256), ctypes.byref(h)) == M.ERR_CUDA
     assert h.value is None
+    # every valid path, the recompute path (4) included, gets past the argument checks
+    for path in (1, 2, 3, 4):
+        cfg = M.Config(768, 50304, 1024, 0, -100, 0, 1, path, 0)
+        assert lib.lmce_create(ctypes.byref(cfg), ctypes.c_void_p(256), ctypes.byref(h)) == M.ERR_CUDA, path
     assert M.status_string(M.ERR_CUDA) != "unknown status"
 
 
