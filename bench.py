@@ -456,6 +456,13 @@ def run_lmce(args, rank, world, local_rank):
     alg_flop_launch = {"lse": 2.0, "dW": 2.0, "dh": 2.0, "lse_dh": 4.0}.get(dom, 0.0) * w.C * w.V * rows_per_launch \
         / max(runs, 1.0)
     achieved = alg_flop_launch / (dom_ms / dom_n / 1e3) / 1e12
+    # the same figure for each heavy kernel (algorithmic flops per launch / its average launch time)
+    per_kernel = {}
+    for k in ("lse_dh", "dW", "dh", "lse"):
+        if k in kinds and kinds[k][1] > 0:
+            runs_k = kinds[k][1] / (args.steps * w.G)
+            flop_k = {"lse": 2.0, "dW": 2.0, "dh": 2.0, "lse_dh": 4.0}[k] * w.C * w.V * rows_per_launch / max(runs_k, 1.0)
+            per_kernel[k] = flop_k / (kinds[k][0] / kinds[k][1] / 1e3) / 1e12
     if L.path.startswith("tcgen05"):
         # the burst cuBLAS figure: the kernels run at the clocks of a short timed region (the
         # sustained figure was taken over seconds at a lower, power-capped clock)
@@ -501,6 +508,10 @@ def run_lmce(args, rank, world, local_rank):
                      "frac_of_sustained": achieved / sustained if (sustained and bound == "tensor") else None,
                      "peak_source": ("bf16_tflops (burst) of " + pk_kind) if bound == "tensor"
                      else "fp32 FFMA: 152 SMs x 128 lanes x 2 flop x max SM clock"},
+        "roofline_kernels": {k: {"achieved": v, "peak": peak, "unit": "TFLOP/s", "frac": v / peak,
+                                 "traffic": ncu_traffic(k) if L.path.startswith("tcgen05") else None}
+                             for k, v in per_kernel.items()
+                             if bound == "tensor" and kinds[k][0] / kinds[k][1] > 0.05},
         "kernels_ms": {k: {"total_ms": v[0], "launches": v[1], "avg_ms": v[0] / v[1]} for k, v in kinds.items()},
         "kernels_ms_source": "a second timed pass of the same steps with CUDA events around every kernel",
         "cpu_baseline": cpu,
