@@ -456,6 +456,9 @@ def run_lmce(args, rank, world, local_rank):
     alg_flop_launch = {"lse": 2.0, "dW": 2.0, "dh": 2.0, "lse_dh": 4.0}.get(dom, 0.0) * w.C * w.V * rows_per_launch \
         / max(runs, 1.0)
     achieved = alg_flop_launch / (dom_ms / dom_n / 1e3) / 1e12
+    # the ncu traffic figures in profiles/ were taken on the 124M head on the default path
+    traffic_of = (lambda k: ncu_traffic(k)) if (args.workload == "gpt2_124m_head" and L.path == "tcgen05" and
+                                               not args.compact and not args.final_norm) else (lambda k: None)
     # the same figure for each heavy kernel (algorithmic flops per launch / its average launch time)
     per_kernel = {}
     for k in ("lse_dh", "dW", "dh", "lse"):
@@ -504,12 +507,12 @@ def run_lmce(args, rank, world, local_rank):
                          "sustained_tflops": sustained, "of_nominal_dense": achieved_step / NOMINAL_BF16_TFLOPS,
                          "nominal_dense_tflops": NOMINAL_BF16_TFLOPS},
         "roofline": {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": ncu_traffic(dom) if L.path.startswith("tcgen05") else None,
+                     "frac": achieved / peak, "traffic": traffic_of(dom),
                      "frac_of_sustained": achieved / sustained if (sustained and bound == "tensor") else None,
                      "peak_source": ("bf16_tflops (burst) of " + pk_kind) if bound == "tensor"
                      else "fp32 FFMA: 152 SMs x 128 lanes x 2 flop x max SM clock"},
         "roofline_kernels": {k: {"achieved": v, "peak": peak, "unit": "TFLOP/s", "frac": v / peak,
-                                 "traffic": ncu_traffic(k) if L.path.startswith("tcgen05") else None}
+                                 "traffic": traffic_of(k)}
                              for k, v in per_kernel.items()
                              if bound == "tensor" and kinds[k][0] / kinds[k][1] > 0.05},
         "kernels_ms": {k: {"total_ms": v[0], "launches": v[1], "avg_ms": v[0] / v[1]} for k, v in kinds.items()},
