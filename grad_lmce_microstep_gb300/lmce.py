@@ -162,6 +162,11 @@ class Lmce:
     >>> L = Lmce(C, V, max_N, dW, dtype="bf16")           # dW: CUDA fp32 [V, C]
     >>> for h, y in micro_batches: L.microstep(h, W, y, global_valid=n_valid, dh=dh)
     >>> loss_sum, count, loss_mean = L.finalize()
+
+    path: "auto" (tensor cores when the shape allows, with the stored-exponential dW pass when
+    its max_N x V bf16 scratch fits, else the recomputing one), "tcgen05" (stored exponentials,
+    an error if they do not fit), "tcgen05_recompute" (logits recomputed for dW, no N x V
+    scratch), "tcgen05_two_pass" (a separate logsumexp pass) or "simt" (fp32 FFMA kernels).
     """
 
     def __init__(self, C: int, V: int, max_N: int, dW: torch.Tensor, dtype: str = "bf16",
