@@ -16,8 +16,11 @@
  *   Pad targets are ignored by the loss (zerotofrontier "GPT", section "Document
  *   boundaries, packing and masking"); the ignore id is configurable, -100 by default.
  *
- * The N x V logits never reach device memory: every pass recomputes its logit
- * tiles on chip.
+ * The N x V logits and dlogits never reach device memory.  On the default
+ * tensor-core path (LMCE_PATH_TCGEN05) the first pass does store its bf16
+ * exponentials 2^(z log2 e - m) -- one N x V array per micro-step, in the handle's
+ * scratch -- so that dW is a single product; LMCE_PATH_TCGEN05_RECOMPUTE keeps every
+ * N x V quantity on chip and recomputes the logit tiles for dW instead.
  *
  * Conventions for every function below:
  *   - Device pointers are CUDA device addresses on the current device; host pointers
